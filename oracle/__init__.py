@@ -1,0 +1,145 @@
+"""fp64 CPU oracle for the KDA forward, decode step and replay.
+
+TEST INFRASTRUCTURE ONLY: the tests, ``__graft_entry__.smoke()`` and the
+benchmark's CPU-baseline leg use this package.  It shares no code with the CUDA
+library and never imports it.
+
+The arithmetic lives in ``kda_oracle.c`` (plain C, double precision, token by
+token).  This module compiles it with gcc on first use, converts inputs to
+float64 (an exact upcast of bf16/fp32 data) and exposes:
+
+* ``forward``  -- packed varlen prefill: o and final state.
+* ``decode``   -- one token per sequence on a slot-indexed state pool.
+* ``replay``   -- accepted tokens re-applied to committed states (no output).
+
+Decode and replay are the same recurrence as ``forward`` (the speculative-
+decoding paragraph of "Kimi K3 on Fireworks: Fast RL at frontier scale" replays
+the accepted tokens' update inputs from a committed checkpoint), so they are
+written as calls of ``forward`` on the gathered states.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+from typing import Optional
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "kda_oracle.c")
+_BUILD_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD_DIR, "libkda_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile ``kda_oracle.c`` into ``_build/libkda_oracle.so`` (gcc, OpenMP)."""
+    os.makedirs(_BUILD_DIR, exist_ok=True)
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp", _SRC, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            dp = ctypes.POINTER(ctypes.c_double)
+            lib.kda_oracle_forward.restype = ctypes.c_int
+            lib.kda_oracle_forward.argtypes = [dp, dp, dp, dp, dp, dp, ctypes.POINTER(ctypes.c_int64),
+                                               ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                                               ctypes.c_int64, ctypes.c_double, ctypes.c_int, dp, dp,
+                                               ctypes.c_int]
+            lib.kda_oracle_max_threads.restype = ctypes.c_int
+            _lib = lib
+    return _lib
+
+
+def max_threads() -> int:
+    return int(_load().kda_oracle_max_threads())
+
+
+def _f64(x) -> Optional[np.ndarray]:
+    if x is None:
+        return None
+    try:
+        import torch
+        if isinstance(x, torch.Tensor):
+            return np.ascontiguousarray(x.detach().to("cpu", torch.float64).numpy())
+    except ImportError:  # pragma: no cover
+        pass
+    return np.ascontiguousarray(np.asarray(x, dtype=np.float64))
+
+
+def _ptr(a: Optional[np.ndarray]):
+    if a is None:
+        return None
+    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_double))
+
+
+def forward(q, k, v, g, beta, cu_seqlens, init_state=None, scale: float = 1.0,
+            gate_is_alpha: bool = False, want_o: bool = True, threads: int = 1):
+    """Packed variable-length KDA forward in fp64.
+
+    Shapes: q, k, g [T, H, dk]; v [T, H, dv]; beta [T, H]; cu_seqlens [N+1];
+    init_state [N, H, dk, dv] or None.  Returns ``(o, final_state)`` as float64
+    numpy arrays (``o`` is None when ``want_o`` is False).
+    """
+    lib = _load()
+    k64, v64, g64, b64 = _f64(k), _f64(v), _f64(g), _f64(beta)
+    q64 = _f64(q) if want_o else None
+    cu = np.ascontiguousarray(np.asarray(_f64(cu_seqlens), dtype=np.int64))
+    T, H, dk = k64.shape
+    dv = v64.shape[2]
+    N = cu.shape[0] - 1
+    s0 = _f64(init_state)
+    if s0 is not None and s0.shape != (N, H, dk, dv):
+        raise ValueError(f"init_state shape {s0.shape} != {(N, H, dk, dv)}")
+    o = np.zeros((T, H, dv), dtype=np.float64) if want_o else None
+    fs = np.zeros((N, H, dk, dv), dtype=np.float64)
+    rc = lib.kda_oracle_forward(_ptr(q64), _ptr(k64), _ptr(v64), _ptr(g64), _ptr(b64), _ptr(s0),
+                                cu.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)), N, H, dk, dv,
+                                float(scale), int(bool(gate_is_alpha)), _ptr(o), _ptr(fs),
+                                int(threads))
+    if rc != 0:
+        raise RuntimeError(f"kda_oracle_forward failed with code {rc}")
+    return o, fs
+
+
+def decode(q, k, v, g, beta, state_pool, slots=None, scale: float = 1.0, threads: int = 1):
+    """One decode step per sequence on a slot-indexed pool.
+
+    q, k, g [N, H, dk]; v [N, H, dv]; beta [N, H]; state_pool [S, H, dk, dv];
+    slots [N] (None: sequence n uses slot n).  Returns ``(o, new_pool)``.
+    """
+    pool = _f64(state_pool).copy()
+    N = np.asarray(_f64(k)).shape[0]
+    sl = np.arange(N) if slots is None else np.asarray(_f64(slots), dtype=np.int64)
+    cu = np.arange(N + 1, dtype=np.int64)
+    o, fs = forward(q, k, v, g, beta, cu, pool[sl], scale=scale, threads=threads)
+    pool[sl] = fs
+    return o, pool
+
+
+def replay(k, v, g, beta, cu_accept, state_pool, slots=None, threads: int = 1):
+    """Apply each sequence's accepted tokens to its committed state in the pool.
+
+    k, g [A, H, dk]; v [A, H, dv]; beta [A, H]; cu_accept [N+1].  Returns the
+    new pool.
+    """
+    pool = _f64(state_pool).copy()
+    cu = np.asarray(_f64(cu_accept), dtype=np.int64)
+    N = cu.shape[0] - 1
+    sl = np.arange(N) if slots is None else np.asarray(_f64(slots), dtype=np.int64)
+    _, fs = forward(None, k, v, g, beta, cu, pool[sl], want_o=False, threads=threads)
+    pool[sl] = fs
+    return pool

@@ -1,0 +1,132 @@
+/*
+ * fp64 CPU oracle for the Kimi Delta Attention (KDA) forward.
+ *
+ * TEST INFRASTRUCTURE ONLY.  The tests, the smoke check and the benchmark's
+ * CPU-baseline leg may call this file; the product path never does, and this
+ * file shares no code, header or table with the CUDA library.
+ *
+ * What it computes.  "Kimi K3 on Fireworks: Fast RL at frontier scale" (KDA
+ * paragraph of the kernels section) describes KDA as linear attention that
+ * updates a compact per-head recurrent state with channel-wise gating; its
+ * speculative-decoding paragraph replays the accepted tokens' state-update
+ * inputs onto a committed state (ReplaySSM).  The pages print no equation, so
+ * the recurrence taken here is the gated delta rule with per-channel decay,
+ * the plainest reading that matches "channel-wise gating" and "compact
+ * recurrent state".  Per (sequence, head), with S in R^{dk x dv}:
+ *
+ *     S <- Diag(alpha_t) S                       alpha_t = exp(g_t) in [0,1]^dk
+ *     S <- S - beta_t k_t (k_t^T S) + beta_t k_t v_t^T
+ *     o_t = S^T (scale * q_t)
+ *
+ * i.e. the decay acts on the dk rows first, the delta step reads the decayed
+ * state, and the output reads the state after the update (inclusive).
+ *
+ * Everything is evaluated token by token, row by row, in double precision,
+ * exactly in that order; no chunking, blocking or reassociation.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* Return codes. */
+#define KDA_ORACLE_OK 0
+#define KDA_ORACLE_BAD_ARGS 1
+#define KDA_ORACLE_NO_MEMORY 2
+
+/* One (sequence, head) chain over tokens [bos, eos).
+ * Layouts (token-major, packed): q,k,g [T,H,dk]; v [T,H,dv]; beta [T,H];
+ * o [T,H,dv]; S [dk,dv] row-major. */
+static void oracle_chain(const double *q, const double *k, const double *v, const double *g,
+                         const double *beta, int64_t bos, int64_t eos, int64_t h, int64_t H,
+                         int64_t dk, int64_t dv, double scale, int gate_is_alpha, double *S,
+                         double *y, double *qs, double *o)
+{
+    for (int64_t t = bos; t < eos; ++t) {
+        const double *qt = q + (t * H + h) * dk;
+        const double *kt = k + (t * H + h) * dk;
+        const double *gt = g + (t * H + h) * dk;
+        const double *vt = v + (t * H + h) * dv;
+        const double bt = beta[t * H + h];
+
+        /* 1. channel-wise decay of the dk rows */
+        for (int64_t i = 0; i < dk; ++i) {
+            const double a = gate_is_alpha ? gt[i] : exp(gt[i]);
+            for (int64_t j = 0; j < dv; ++j) S[i * dv + j] *= a;
+        }
+        /* 2. delta rule: y = S^T k, u = beta (v - y), S += k u^T */
+        for (int64_t j = 0; j < dv; ++j) y[j] = 0.0;
+        for (int64_t i = 0; i < dk; ++i)
+            for (int64_t j = 0; j < dv; ++j) y[j] += kt[i] * S[i * dv + j];
+        for (int64_t j = 0; j < dv; ++j) y[j] = bt * (vt[j] - y[j]);
+        for (int64_t i = 0; i < dk; ++i)
+            for (int64_t j = 0; j < dv; ++j) S[i * dv + j] += kt[i] * y[j];
+        /* 3. output from the updated state with the scaled query */
+        if (o) {
+            double *ot = o + (t * H + h) * dv;
+            for (int64_t i = 0; i < dk; ++i) qs[i] = scale * qt[i];
+            for (int64_t j = 0; j < dv; ++j) ot[j] = 0.0;
+            for (int64_t i = 0; i < dk; ++i)
+                for (int64_t j = 0; j < dv; ++j) ot[j] += qs[i] * S[i * dv + j];
+        }
+    }
+}
+
+/*
+ * Packed variable-length forward.
+ *   cu_seqlens [N+1] (non-decreasing, cu[0] = 0): sequence n is tokens
+ *     [cu[n], cu[n+1]).
+ *   init_state [N,H,dk,dv] or NULL (zeros).  final_state [N,H,dk,dv] or NULL.
+ *   o [T,H,dv] or NULL (state-only replay).
+ *   gate_is_alpha: 0 -> g holds log-gates, alpha = exp(g);
+ *                  1 -> g holds alpha itself (lets tests feed alpha = 0).
+ *   nthreads: OpenMP threads over the N*H independent chains (<= 0: default).
+ */
+int kda_oracle_forward(const double *q, const double *k, const double *v, const double *g,
+                       const double *beta, const double *init_state, const int64_t *cu_seqlens,
+                       int64_t N, int64_t H, int64_t dk, int64_t dv, double scale, int gate_is_alpha,
+                       double *o, double *final_state, int nthreads)
+{
+    if (N < 0 || H <= 0 || dk <= 0 || dv <= 0 || !cu_seqlens || !k || !v || !g || !beta)
+        return KDA_ORACLE_BAD_ARGS;
+    if (o && !q) return KDA_ORACLE_BAD_ARGS;
+    if (N > 0 && cu_seqlens[0] != 0) return KDA_ORACLE_BAD_ARGS;
+    for (int64_t n = 0; n < N; ++n)
+        if (cu_seqlens[n + 1] < cu_seqlens[n]) return KDA_ORACLE_BAD_ARGS;
+
+    const int64_t pairs = N * H;
+    int failed = 0;
+#ifdef _OPENMP
+    if (nthreads <= 0) nthreads = omp_get_max_threads();
+#pragma omp parallel for schedule(dynamic, 1) num_threads(nthreads) reduction(| : failed)
+#endif
+    for (int64_t p = 0; p < pairs; ++p) {
+        const int64_t n = p / H, h = p % H;
+        double *S = (double *)malloc(sizeof(double) * (size_t)(dk * dv + dv + dk));
+        if (!S) { failed |= 1; continue; }
+        double *y = S + dk * dv, *qs = y + dv;
+        if (init_state)
+            memcpy(S, init_state + p * dk * dv, sizeof(double) * (size_t)(dk * dv));
+        else
+            memset(S, 0, sizeof(double) * (size_t)(dk * dv));
+        oracle_chain(q, k, v, g, beta, cu_seqlens[n], cu_seqlens[n + 1], h, H, dk, dv, scale,
+                     gate_is_alpha, S, y, qs, o);
+        if (final_state) memcpy(final_state + p * dk * dv, S, sizeof(double) * (size_t)(dk * dv));
+        free(S);
+    }
+    (void)nthreads;
+    return failed ? KDA_ORACLE_NO_MEMORY : KDA_ORACLE_OK;
+}
+
+/* Threads the OpenMP runtime would use by default (1 without OpenMP). */
+int kda_oracle_max_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}

@@ -1,0 +1,363 @@
+"""Pins for the fp64 oracle: closed forms, invariants, exact rational brute force.
+
+Each test fixes a property of the gated delta rule with per-channel decay (the
+reading of the KDA paragraph of "Kimi K3 on Fireworks: Fast RL at frontier
+scale" that the oracle implements) by something other than the oracle itself:
+a closed form, a special case with a known answer, a hand-derived worked
+example, or exact rational arithmetic in a different (matrix-product) form.
+Shapes use dk != dv wherever possible so that a transposed operand fails.
+"""
+import json
+import math
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+import oracle
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+pytestmark = pytest.mark.filterwarnings("ignore::RuntimeWarning")
+
+
+def _rng(seed):
+    return np.random.default_rng(seed)
+
+
+def _orthonormal_rows(n, d, rng):
+    a = rng.standard_normal((d, d))
+    qm, _ = np.linalg.qr(a)
+    return qm[:n].copy()  # n orthonormal rows of length d
+
+
+def _one_seq(x):
+    """Add the head axis: [T, d] -> [T, 1, d]; [T] -> [T, 1]."""
+    return np.asarray(x, dtype=np.float64)[:, None, ...]
+
+
+def test_worked_example_by_hand():
+    """Hand-stepped 2x2, two-token example (stored with its derivation)."""
+    ex = json.load(open(os.path.join(GOLDEN, "worked_example_2x2.json")))
+    q, k, v = (_one_seq(ex[n]) for n in ("q", "k", "v"))
+    a, b = _one_seq(ex["alpha"]), _one_seq(ex["beta"])
+    s0 = np.asarray(ex["init_state"])[None, None]
+    cu = np.array([0, 2])
+    o, fs = oracle.forward(q, k, v, a, b, cu, s0, scale=ex["scale"], gate_is_alpha=True)
+    np.testing.assert_allclose(o[:, 0], ex["expected_o"], rtol=0, atol=1e-14)
+    np.testing.assert_allclose(fs[0, 0], ex["expected_final_state"], rtol=0, atol=1e-14)
+    # the same through log-gates: alpha = exp(g)
+    o2, fs2 = oracle.forward(q, k, v, np.log(a), b, cu, s0, scale=ex["scale"])
+    np.testing.assert_allclose(o2, o, rtol=0, atol=1e-14)
+    np.testing.assert_allclose(fs2, fs, rtol=0, atol=1e-14)
+
+
+def test_no_decay_no_write_keeps_state():
+    """alpha = 1, beta = 0: S_t = S_0 exactly and o_t = S_0^T (scale q_t)."""
+    rng = _rng(1)
+    T, H, dk, dv = 7, 2, 5, 3
+    q = rng.standard_normal((T, H, dk))
+    k = rng.standard_normal((T, H, dk))
+    v = rng.standard_normal((T, H, dv))
+    g = np.zeros((T, H, dk))
+    b = np.zeros((T, H))
+    s0 = rng.standard_normal((1, H, dk, dv))
+    o, fs = oracle.forward(q, k, v, g, b, np.array([0, T]), s0, scale=0.7)
+    assert np.array_equal(fs, s0)
+    exp_o = np.einsum("hij,thi->thj", s0[0], 0.7 * q)
+    np.testing.assert_allclose(o, exp_o, rtol=1e-13, atol=1e-13)
+
+
+def test_pure_decay_closed_form():
+    """beta = 0: S_t = Diag(prod_{s<=t} alpha_s) S_0 (decay acts on the dk rows)."""
+    rng = _rng(2)
+    T, dk, dv = 6, 5, 3
+    q = rng.standard_normal((T, 1, dk))
+    g = -rng.uniform(0.0, 0.7, size=(T, 1, dk))
+    s0 = rng.standard_normal((1, 1, dk, dv))
+    o, fs = oracle.forward(q, rng.standard_normal((T, 1, dk)), rng.standard_normal((T, 1, dv)), g,
+                           np.zeros((T, 1)), np.array([0, T]), s0)
+    cum = np.cumsum(g[:, 0], axis=0)  # [T, dk]
+    for t in range(T):
+        st = np.exp(cum[t])[:, None] * s0[0, 0]
+        np.testing.assert_allclose(o[t, 0], st.T @ q[t, 0], rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(fs[0, 0], np.exp(cum[-1])[:, None] * s0[0, 0], rtol=1e-12)
+
+
+def test_accumulation_reduces_to_causal_linear_attention():
+    """alpha = 1, S_0 = 0, orthonormal keys: o_t = sum_{s<=t} (q_t . k_s) beta_s v_s."""
+    rng = _rng(3)
+    T, dk, dv = 6, 8, 5
+    k = _orthonormal_rows(T, dk, rng)[:, None, :]
+    q = rng.standard_normal((T, 1, dk))
+    v = rng.standard_normal((T, 1, dv))
+    b = rng.uniform(0.1, 0.9, size=(T, 1))
+    o, _ = oracle.forward(q, k, v, np.zeros((T, 1, dk)), b, np.array([0, T]), None, scale=1.0)
+    for t in range(T):
+        exp = sum((q[t, 0] @ k[s, 0]) * b[s, 0] * v[s, 0] for s in range(t + 1))
+        np.testing.assert_allclose(o[t, 0], exp, rtol=1e-12, atol=1e-13)
+
+
+def test_delta_rule_retrieval_and_overwrite():
+    """beta = 1, alpha = 1, orthonormal keys, any S_0: S_t^T k_s = v_s for written s <= t;
+    writing the same key twice keeps only the second value (inclusive output)."""
+    rng = _rng(4)
+    dk, dv, n = 8, 3, 5
+    keys = _orthonormal_rows(n, dk, rng)
+    vals = rng.standard_normal((n, dv))
+    # write keys 0..n-1, then write key 2 again with a new value
+    new_v2 = rng.standard_normal(dv)
+    kk = np.concatenate([keys, keys[2:3]])
+    vv = np.concatenate([vals, new_v2[None]])
+    T = kk.shape[0]
+    # query at token t is the key written at token t (inclusive output gives back v_t)
+    o, fs = oracle.forward(kk[:, None], kk[:, None], vv[:, None], np.zeros((T, 1, dk)), np.ones((T, 1)),
+                           np.array([0, T]), rng.standard_normal((1, 1, dk, dv)))
+    np.testing.assert_allclose(o[:, 0], vv, rtol=1e-12, atol=1e-12)
+    S = fs[0, 0]
+    for s in range(n):
+        want = new_v2 if s == 2 else vals[s]
+        np.testing.assert_allclose(S.T @ keys[s], want, rtol=1e-12, atol=1e-12)
+
+
+def test_basis_key_single_step():
+    """k = e_m: row m becomes (1 - beta) alpha_m S0[m] + beta v, other rows alpha_i S0[i].
+    Fixes that the delta step reads the decayed state and the sign of the correction."""
+    rng = _rng(5)
+    dk, dv, m = 4, 3, 2
+    s0 = rng.standard_normal((dk, dv))
+    alpha = rng.uniform(0.2, 0.9, size=dk)
+    beta, v = 0.3, rng.standard_normal(dv)
+    k = np.zeros(dk)
+    k[m] = 1.0
+    q = rng.standard_normal(dk)
+    o, fs = oracle.forward(q[None, None], k[None, None], v[None, None], alpha[None, None],
+                           np.array([[beta]]), np.array([0, 1]), s0[None, None], gate_is_alpha=True)
+    want = alpha[:, None] * s0
+    want[m] = (1 - beta) * alpha[m] * s0[m] + beta * v
+    np.testing.assert_allclose(fs[0, 0], want, rtol=1e-14, atol=1e-14)
+    np.testing.assert_allclose(o[0, 0], want.T @ q, rtol=1e-13, atol=1e-13)
+
+
+def test_reset_alpha_zero():
+    """alpha_t0 = 0 (g = -inf) erases the state: outputs from t0 on equal a fresh run, bitwise."""
+    rng = _rng(6)
+    T, H, dk, dv, t0 = 12, 2, 6, 4, 5
+    q = rng.standard_normal((T, H, dk))
+    k = rng.standard_normal((T, H, dk))
+    k /= np.linalg.norm(k, axis=-1, keepdims=True)
+    v = rng.standard_normal((T, H, dv))
+    g = -rng.uniform(0.0, 0.5, size=(T, H, dk))
+    b = rng.uniform(0.0, 1.0, size=(T, H))
+    g[t0] = -np.inf
+    s0 = rng.standard_normal((1, H, dk, dv))
+    o, fs = oracle.forward(q, k, v, g, b, np.array([0, T]), s0)
+    o2, fs2 = oracle.forward(q[t0:], k[t0:], v[t0:], g[t0:], b[t0:], np.array([0, T - t0]), None)
+    assert np.array_equal(o[t0:], o2)
+    assert np.array_equal(fs, fs2)
+    # alpha given directly (alpha_t0 = 0) resets the same way
+    a = np.exp(g)
+    o3, fs3 = oracle.forward(q, k, v, a, b, np.array([0, T]), s0, gate_is_alpha=True)
+    o4, fs4 = oracle.forward(q[t0:], k[t0:], v[t0:], a[t0:], b[t0:], np.array([0, T - t0]), None,
+                             gate_is_alpha=True)
+    assert np.array_equal(o3[t0:], o4) and np.array_equal(fs3, fs4)
+
+
+def _random_case(rng, T, H, dk, dv):
+    q = rng.standard_normal((T, H, dk)) / math.sqrt(dk)
+    k = rng.standard_normal((T, H, dk))
+    k /= np.linalg.norm(k, axis=-1, keepdims=True)
+    v = rng.standard_normal((T, H, dv))
+    g = np.log(1.0 / (1.0 + np.exp(-(rng.standard_normal((T, H, dk)) + 3.0))))
+    b = 1.0 / (1.0 + np.exp(-rng.standard_normal((T, H))))
+    return q, k, v, g, b
+
+
+@pytest.mark.parametrize("t_split", [1, 7, 16, 31])
+def test_split_invariance_bitwise(t_split):
+    """[0,t) then [t,T) with the carried state equals [0,T) bit for bit."""
+    rng = _rng(7)
+    T, H, dk, dv = 32, 3, 6, 5
+    q, k, v, g, b = _random_case(rng, T, H, dk, dv)
+    s0 = rng.standard_normal((1, H, dk, dv)) * 0.1
+    o, fs = oracle.forward(q, k, v, g, b, np.array([0, T]), s0)
+    sl1, sl2 = slice(0, t_split), slice(t_split, T)
+    o1, f1 = oracle.forward(q[sl1], k[sl1], v[sl1], g[sl1], b[sl1], np.array([0, t_split]), s0)
+    o2, f2 = oracle.forward(q[sl2], k[sl2], v[sl2], g[sl2], b[sl2], np.array([0, T - t_split]), f1)
+    assert np.array_equal(np.concatenate([o1, o2]), o)
+    assert np.array_equal(f2, fs)
+
+
+def test_varlen_packing_equals_separate_runs():
+    rng = _rng(8)
+    lens = [5, 0, 9, 1]
+    H, dk, dv = 2, 4, 6
+    T = sum(lens)
+    q, k, v, g, b = _random_case(rng, T, H, dk, dv)
+    s0 = rng.standard_normal((len(lens), H, dk, dv))
+    cu = np.concatenate([[0], np.cumsum(lens)])
+    o, fs = oracle.forward(q, k, v, g, b, cu, s0)
+    for n, L in enumerate(lens):
+        sl = slice(cu[n], cu[n + 1])
+        on, fn = oracle.forward(q[sl], k[sl], v[sl], g[sl], b[sl], np.array([0, L]), s0[n:n + 1])
+        assert np.array_equal(o[sl], on)
+        assert np.array_equal(fs[n], fn[0])
+    # a length-0 sequence returns its initial state unchanged
+    assert np.array_equal(fs[1], s0[1])
+
+
+def test_scale_is_linear_on_the_query():
+    rng = _rng(9)
+    T, H, dk, dv = 9, 2, 5, 3
+    q, k, v, g, b = _random_case(rng, T, H, dk, dv)
+    o1, f1 = oracle.forward(q, k, v, g, b, np.array([0, T]), None, scale=1.0)
+    o2, f2 = oracle.forward(q, k, v, g, b, np.array([0, T]), None, scale=0.125)
+    assert np.array_equal(o2, 0.125 * o1)  # power-of-two scale: exact
+    assert np.array_equal(f1, f2)
+
+
+def test_decode_and_replay_helpers_follow_forward():
+    rng = _rng(10)
+    H, dk, dv, N, slots_n = 2, 4, 3, 3, 5
+    pool = rng.standard_normal((slots_n, H, dk, dv))
+    slots = np.array([4, 0, 2])
+    q, k, v, g, b = _random_case(rng, N, H, dk, dv)
+    o, new_pool = oracle.decode(q, k, v, g, b, pool, slots, scale=0.5)
+    for n in range(N):
+        on, fn = oracle.forward(q[n:n + 1], k[n:n + 1], v[n:n + 1], g[n:n + 1], b[n:n + 1],
+                                np.array([0, 1]), pool[slots[n]][None], scale=0.5)
+        assert np.array_equal(o[n], on[0]) and np.array_equal(new_pool[slots[n]], fn[0])
+    assert np.array_equal(new_pool[[1, 3]], pool[[1, 3]])
+    acc = [2, 0, 3]
+    qa, ka, va, ga, ba = _random_case(rng, sum(acc), H, dk, dv)
+    cu = np.concatenate([[0], np.cumsum(acc)])
+    rp = oracle.replay(ka, va, ga, ba, cu, pool, slots)
+    for n in range(N):
+        sl = slice(cu[n], cu[n + 1])
+        _, fn = oracle.forward(qa[sl], ka[sl], va[sl], ga[sl], ba[sl], np.array([0, acc[n]]),
+                               pool[slots[n]][None])
+        assert np.array_equal(rp[slots[n]], fn[0])
+
+
+# ----------------------------------------------------------------------------------------------
+# Exact rational arithmetic
+# ----------------------------------------------------------------------------------------------
+
+def _frac_matrix(rows, cols, rng, lo=-4, hi=4, den=8):
+    return [[Fraction(int(rng.integers(lo, hi + 1)), den) for _ in range(cols)] for _ in range(rows)]
+
+
+def _mm(a, b):
+    return [[sum((a[i][p] * b[p][j] for p in range(len(b))), Fraction(0)) for j in range(len(b[0]))]
+            for i in range(len(a))]
+
+
+def _madd(a, b, s=1):
+    return [[a[i][j] + s * b[i][j] for j in range(len(a[0]))] for i in range(len(a))]
+
+
+def _transpose(a):
+    return [list(r) for r in zip(*a)]
+
+
+def _eye(n):
+    return [[Fraction(int(i == j)) for j in range(n)] for i in range(n)]
+
+
+def _diag(d):
+    return [[d[i] if i == j else Fraction(0) for j in range(len(d))] for i in range(len(d))]
+
+
+def _bruteforce_matrix_form(q, k, v, alpha, beta, s0, scale):
+    """Recurrence as matrix products: S_t = (I - b k k^T) Diag(alpha) S_{t-1} + b k v^T; o_t = S_t^T q."""
+    dk = len(s0)
+    S = [row[:] for row in s0]
+    outs = []
+    for t in range(len(k)):
+        kc = [[x] for x in k[t]]                       # dk x 1
+        house = _madd(_eye(dk), _mm(kc, _transpose(kc)), -beta[t])
+        S = _madd(_mm(house, _mm(_diag(alpha[t]), S)), _mm(kc, [v[t]]), beta[t])
+        qs = [[scale * x] for x in q[t]]
+        outs.append([r[0] for r in _mm(_transpose(S), qs)])
+    return outs, S
+
+
+@pytest.mark.parametrize("seed,dk,dv,T", [(11, 4, 4, 8), (12, 4, 3, 7), (13, 3, 5, 6)])
+def test_bruteforce_rational_matches_oracle(seed, dk, dv, T):
+    rng = _rng(seed)
+    q = _frac_matrix(T, dk, rng)
+    k = _frac_matrix(T, dk, rng)
+    v = _frac_matrix(T, dv, rng)
+    alpha = [[Fraction(int(rng.integers(1, 9)), 8) for _ in range(dk)] for _ in range(T)]
+    beta = [Fraction(int(rng.integers(0, 9)), 8) for _ in range(T)]
+    s0 = _frac_matrix(dk, dv, rng)
+    scale = Fraction(3, 4)
+    outs, S = _bruteforce_matrix_form(q, k, v, alpha, beta, s0, scale)
+    f = lambda m: np.array([[float(x) for x in r] for r in m])
+    o, fs = oracle.forward(f(q)[:, None], f(k)[:, None], f(v)[:, None], f(alpha)[:, None],
+                           np.array([float(x) for x in beta])[:, None], np.array([0, T]),
+                           f(s0)[None, None], scale=float(scale), gate_is_alpha=True)
+    np.testing.assert_allclose(o[:, 0], f(outs), rtol=1e-13, atol=1e-13)
+    np.testing.assert_allclose(fs[0, 0], f(S), rtol=1e-13, atol=1e-13)
+
+
+def _chunked_wy(q, k, v, alpha, beta, s0, scale, C):
+    """The 64-token chunked form the CUDA kernel evaluates, in exact rationals, for chunk size C.
+
+    Per chunk with state S (prefix products A_r = prod_{j<=r} alpha_j, A_C its last row):
+      Kbar = K*A, Qbar = scale*Q*A, Ktil = K/A, Khat = K*A_C/A,
+      M[r,i] = beta_r Kbar_r.Ktil_i (i<r), P[r,i] = Qbar_r.Ktil_i (i<=r), T = (I+M)^-1,
+      W = T diag(beta) Kbar, Utl = T diag(beta) V, U = Utl - W S,
+      O = Qbar S + P U, S <- Diag(A_C) S + Khat^T U.
+    """
+    dk, dv = len(s0), len(s0[0])
+    S = [r[:] for r in s0]
+    outs = []
+    for c0 in range(0, len(k), C):
+        idx = list(range(c0, min(c0 + C, len(k))))
+        n = len(idx)
+        A, acc = [], [Fraction(1)] * dk
+        for t in idx:
+            acc = [acc[c] * alpha[t][c] for c in range(dk)]
+            A.append(acc)
+        AC = A[-1]
+        Kbar = [[k[t][c] * A[r][c] for c in range(dk)] for r, t in enumerate(idx)]
+        Qbar = [[scale * q[t][c] * A[r][c] for c in range(dk)] for r, t in enumerate(idx)]
+        Ktil = [[k[t][c] / A[r][c] for c in range(dk)] for r, t in enumerate(idx)]
+        Khat = [[k[t][c] * AC[c] / A[r][c] for c in range(dk)] for r, t in enumerate(idx)]
+        dot = lambda a, b: sum((x * y for x, y in zip(a, b)), Fraction(0))
+        M = [[beta[idx[r]] * dot(Kbar[r], Ktil[i]) if i < r else Fraction(0) for i in range(n)]
+             for r in range(n)]
+        P = [[dot(Qbar[r], Ktil[i]) if i <= r else Fraction(0) for i in range(n)] for r in range(n)]
+        # T = (I + M)^-1 by forward substitution (unit lower triangular)
+        Tm = [[Fraction(0)] * n for _ in range(n)]
+        for r in range(n):
+            for m in range(n):
+                Tm[r][m] = Fraction(int(r == m)) - sum((M[r][i] * Tm[i][m] for i in range(r)),
+                                                       Fraction(0))
+        Tb = [[Tm[r][i] * beta[idx[i]] for i in range(n)] for r in range(n)]
+        W = _mm(Tb, Kbar)
+        Utl = _mm(Tb, [v[t] for t in idx])
+        U = _madd(Utl, _mm(W, S), -1)
+        O = _madd(_mm(Qbar, S), _mm(P, U))
+        outs.extend(O)
+        S = _madd(_mm(_diag(AC), S), _mm(_transpose(Khat), U))
+    return outs, S
+
+
+@pytest.mark.parametrize("C", [1, 3, 4, 8])
+def test_chunked_wy_identities_exact(C):
+    """The chunked WY form used on the GPU equals the token recurrence exactly."""
+    rng = _rng(20 + C)
+    T, dk, dv = 10, 4, 3
+    q = _frac_matrix(T, dk, rng)
+    k = _frac_matrix(T, dk, rng)
+    v = _frac_matrix(T, dv, rng)
+    alpha = [[Fraction(int(rng.integers(1, 9)), 8) for _ in range(dk)] for _ in range(T)]
+    beta = [Fraction(int(rng.integers(0, 9)), 8) for _ in range(T)]
+    s0 = _frac_matrix(dk, dv, rng)
+    scale = Fraction(1, 2)
+    o_ref, s_ref = _bruteforce_matrix_form(q, k, v, alpha, beta, s0, scale)
+    o_chk, s_chk = _chunked_wy(q, k, v, alpha, beta, s0, scale, C)
+    assert o_chk == o_ref
+    assert s_chk == s_ref
