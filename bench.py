@@ -1,0 +1,399 @@
+"""Benchmark: KDA chunk_fwd tokens/s on one GB300, with roofline fraction.
+
+One step = one kda_chunk_fwd over the whole packed batch of the chosen workload
+(default ``prefill_4k``: 4 sequences x 4096 tokens, H=32, dk=dv=128, bf16,
+fp32 initial and final states), inputs resident in HBM.  ``value`` counts
+sequence tokens (heads not multiplied in) per second over all ranks.
+
+Multi-GPU: (sequence, head) chains are independent, so each rank runs its own
+copy of the batch (weak scaling, no collective on the data path); the timed
+region is bracketed by barriers and the max over ranks is taken.
+
+``--impl reference`` times the fp64 CPU oracle (the correctness reference, a
+deliberately slow program) on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+METRIC = "KDA chunk_fwd tokens/s at T=4K-128K (1 GB300) and % of roofline"
+UNIT = "tokens/s"
+
+# DRAM traffic of the dominant kernel per launch from an ncu capture (None until
+# captured for the current kernel build).  Source: profiles/.
+DOMINANT_TRAFFIC = None
+
+
+# ------------------------------------------------------------------------------------------------
+# algorithmic work (per step)
+# ------------------------------------------------------------------------------------------------
+
+def algorithmic_bytes(case) -> int:
+    """Bytes a perfect kernel moves: every input once, o once, states in and out once."""
+    T, H, dk, dv = case.T_total, case.H, case.dk, case.dv
+    es = case.q.element_size()
+    b = T * H * (3 * dk + dv) * es          # q, k, g, v
+    b += T * H * es                         # beta
+    b += T * H * dv * es                    # o
+    b += case.N * H * dk * dv * 4           # final state
+    if case.init_state is not None:
+        b += case.N * H * dk * dv * 4       # initial state
+    b += (case.N + 1) * 4                   # cu_seqlens
+    return int(b)
+
+
+def algorithmic_flops(case, C: int = 64) -> int:
+    """6 d^2 + 5 C d flop per token-head for dk = dv = d (triangular halves counted once)."""
+    d = case.dk
+    return int(case.T_total * case.H * (6 * d * d + 5 * C * d))
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            j = json.load(f)
+        return float(j["hbm_gbs"]), float(j["bf16_tflops"]), "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+# ------------------------------------------------------------------------------------------------
+# distributed helpers (host logic; covered by gloo tests)
+# ------------------------------------------------------------------------------------------------
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def aggregate(max_elapsed_ms: float, world: int, tokens_per_rank_step: int, steps: int):
+    """Whole-job throughput: every rank's tokens over the slowest rank's time.
+    Returns (tokens/s, ms per step)."""
+    return world * tokens_per_rank_step * steps / (max_elapsed_ms / 1e3), max_elapsed_ms / steps
+
+
+def max_over_ranks(value: float, device=None) -> float:
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------------------------------------
+# clocks sampled during the timed region
+# ------------------------------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int = 0):
+        self.samples = []
+        self.proc = None
+        sel = []
+        try:
+            bus = torch.cuda.get_device_properties(device_index).pci_bus_id
+            if bus:
+                sel = ["-i", str(bus)]
+        except Exception:
+            sel = []
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", *sel, f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), line.strip()))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self, t0: float, t1: float):
+        rows = [s for ts, s in self.samples if t0 <= ts <= t1]
+        if not rows and self.samples:  # region shorter than the sampling period: nearest samples
+            mid = 0.5 * (t0 + t1)
+            rows = [min(self.samples, key=lambda x: abs(x[0] - mid))[1]]
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            parts = [p.strip() for p in r.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax = float(parts[1])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        sm.sort()
+        return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": smax, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------------------------------------
+# CPU oracle timing (bounded sample)
+# ------------------------------------------------------------------------------------------------
+
+def oracle_sample_rate(case, budget_s: float = 10.0):
+    """Oracle tokens/s on a prefix of sequence 0 (all heads), sized to about ``budget_s``."""
+    import oracle
+    threads = max(1, min(os.cpu_count() or 1, case.H))
+
+    def run(L):
+        sl = slice(0, L)
+        t = time.perf_counter()
+        oracle.forward(case.q[sl], case.k[sl], case.v[sl], case.g[sl], case.beta[sl],
+                       torch.tensor([0, L], dtype=torch.int64),
+                       None if case.init_state is None else case.init_state[:1],
+                       scale=case.scale, threads=threads)
+        return time.perf_counter() - t
+
+    L0 = min(case.lengths[0], 16)
+    t0 = run(L0)
+    L = int(min(case.lengths[0], max(L0, L0 * budget_s / max(t0, 1e-6))))
+    t = run(L) if L > L0 else t0
+    return {"value": L / t, "unit": UNIT, "cores": threads, "kind": "oracle", "seconds": t,
+            "sample": f"first {L} tokens of sequence 0, all {case.H} heads (fp64, {threads} threads),"
+                      f" {t:.1f} s"}
+
+
+# ------------------------------------------------------------------------------------------------
+# arms
+# ------------------------------------------------------------------------------------------------
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return 0
+    case = workloads.named_case(args.workload)
+    # the whole run (warm-up + timed samples) stays within about three minutes
+    budget = min(args.ref_budget, 150.0 / (args.steps + args.warmup))
+    per_step = []
+    for _ in range(args.warmup):
+        oracle_sample_rate(case, budget_s=budget)
+    for _ in range(args.steps):
+        per_step.append(oracle_sample_rate(case, budget_s=budget))
+    vals = [r["value"] for r in per_step]
+    v = sum(vals) / len(vals)
+    cb = dict(per_step[-1])
+    cb["value"] = v
+    cb["sample"] = f"{args.steps} timed samples; last: " + cb["sample"]
+    ms = 1e3 * sum(r["seconds"] for r in per_step) / len(per_step)
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": config_dict(args, case), "cpu_baseline": cb,
+            "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def config_dict(args, case):
+    return {"workload": args.workload, "desc": workloads.NAMED_WORKLOADS[args.workload]["desc"],
+            "global_batch": case.N * max(1, args.gpus), "seq_len": max(case.lengths) if case.lengths else 0,
+            "tokens_per_step_per_gpu": case.T_total, "heads": case.H, "dk": case.dk, "dv": case.dv,
+            "parallelism": f"dp{max(1, args.gpus)} (independent replicas)",
+            "l2": "inputs larger than L2 (no flush needed)" if algorithmic_bytes(case) > 256e6
+                  else "L2 flushed between steps"}
+
+
+def run_gpu(args, world, rank, local):
+    import gated_linear_attention_chunk_gb300 as kda
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    import torch.distributed as dist
+    distributed = world > 1
+    if distributed:
+        dist.init_process_group("nccl", device_id=dev)
+
+    case = workloads.named_case(args.workload)
+    q, k, v, g, b = (x.to(dev) for x in (case.q, case.k, case.v, case.g, case.beta))
+    cu = case.cu_seqlens.to(dev)
+    s0 = None if case.init_state is None else case.init_state.to(dev)
+    N, T, H, dk, dv = case.N, case.T_total, case.H, case.dk, case.dv
+    o = torch.empty(T, H, dv, dtype=q.dtype, device=dev)
+    fs = torch.empty(N, H, dk, dv, dtype=torch.float32, device=dev)
+    ws = kda.new_workspace(kda.KDA_WS_HEADER_BYTES, dev)
+    flush = None
+    if algorithmic_bytes(case) <= 256e6:
+        flush = torch.empty(int(256e6), dtype=torch.uint8, device=dev)
+
+    def step():
+        kda.kda_chunk_fwd(q, k, v, g, b, cu_seqlens=cu, init_state=s0, scale=case.scale, o=o,
+                          final_state=fs, workspace=ws)
+
+    # kernels of ours per kda_chunk_fwd: the chunked tensor-core kernel (when it serves this shape)
+    # plus the token-sequential partial-chunk kernel
+    launches_per_step = 1 + int(kda.kda_chunk_fwd_uses_tensor_cores(dk, dv, q.dtype))
+    clocks = ClockSampler(local)
+    for _ in range(args.warmup):
+        step()
+    st = kda.kda_device_status(ws)
+    if st != kda.KDA_OK:
+        raise RuntimeError(f"device status {kda.kda_status_string(st)}")
+    torch.cuda.synchronize()
+    if distributed:
+        dist.barrier()
+    stream = torch.cuda.current_stream()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    torch.cuda.synchronize()
+    wall0 = time.time()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for i in range(args.steps):
+        if flush is not None:
+            flush.zero_()
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    wall1 = time.time()
+    if distributed:
+        dist.barrier()
+    step_ms = [a.elapsed_time(bb) for a, bb in ev]
+    total_ms = sum(step_ms)
+    clk = clocks.summary(wall0, wall1)
+    clocks.stop()
+    total_ms = max_over_ranks(total_ms, dev)
+    value, ms_per_step = aggregate(total_ms, world, T, args.steps)
+    st = kda.kda_device_status(ws)
+    if st != kda.KDA_OK:
+        raise RuntimeError(f"device status {kda.kda_status_string(st)}")
+
+    # end to end through the public API with host buffers: H2D inputs, call, D2H outputs
+    e2e = None
+    host = {n: x.pin_memory() for n, x in (("q", case.q), ("k", case.k), ("v", case.v), ("g", case.g),
+                                           ("beta", case.beta), ("cu", case.cu_seqlens))}
+    if case.init_state is not None:
+        host["s0"] = case.init_state.pin_memory()
+    host_o = torch.empty(T, H, dv, dtype=q.dtype).pin_memory()
+    host_fs = torch.empty(N, H, dk, dv, dtype=torch.float32).pin_memory()
+    dq, dk_, dvv, dg, db = (torch.empty_like(x) for x in (q, k, v, g, b))
+    dcu = torch.empty_like(cu)
+    ds0 = None if s0 is None else torch.empty_like(s0)
+    h2d = sum(x.numel() * x.element_size() for x in host.values())
+    d2h = host_o.numel() * host_o.element_size() + host_fs.numel() * 4
+    e2e_steps = max(1, min(args.steps, 20))
+
+    def e2e_step():
+        dq.copy_(host["q"], non_blocking=True)
+        dk_.copy_(host["k"], non_blocking=True)
+        dvv.copy_(host["v"], non_blocking=True)
+        dg.copy_(host["g"], non_blocking=True)
+        db.copy_(host["beta"], non_blocking=True)
+        dcu.copy_(host["cu"], non_blocking=True)
+        if ds0 is not None:
+            ds0.copy_(host["s0"], non_blocking=True)
+        kda.kda_chunk_fwd(dq, dk_, dvv, dg, db, cu_seqlens=dcu, init_state=ds0, scale=case.scale, o=o,
+                          final_state=fs, workspace=ws)
+        host_o.copy_(o, non_blocking=True)
+        host_fs.copy_(fs, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    if distributed:
+        dist.barrier()
+    a, bb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    bb.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(a.elapsed_time(bb), dev)
+    e2e = {"value": world * T * e2e_steps / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+           "d2h_bytes_per_step": int(d2h), "steps": e2e_steps}
+
+    hbm_peak, tf_peak, peak_src = measured_peaks()
+    nbytes = algorithmic_bytes(case)
+    flops = algorithmic_flops(case)
+    kern_ms = sorted(step_ms)[len(step_ms) // 2]
+    t_hbm = nbytes / (hbm_peak * 1e9)
+    t_tc = flops / (tf_peak * 1e12)
+    bound = "hbm" if t_hbm >= t_tc else "tensor"
+    if bound == "hbm":
+        achieved = nbytes / (kern_ms / 1e3) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                "frac": achieved / hbm_peak, "traffic": DOMINANT_TRAFFIC}
+    else:
+        achieved = flops / (kern_ms / 1e3) / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": tf_peak, "unit": "TFLOP/s",
+                "frac": achieved / tf_peak, "traffic": DOMINANT_TRAFFIC}
+    roof.update({"peak_source": f"{peak_src} (MEASURED_PEAKS.json)" if peak_src == "measured" else peak_src,
+                 "algorithmic_bytes": nbytes, "algorithmic_flops": flops,
+                 "kernel_ms_median": kern_ms, "roofline_ms": 1e3 * max(t_hbm, t_tc),
+                 "timing": "median per-step CUDA-event time of kda_chunk_fwd (includes the status-word memset"
+                           " and the partial-chunk launch)"})
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = oracle_sample_rate(case, budget_s=args.ref_budget)
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "bf16" if q.dtype == torch.bfloat16 else "f32",
+                "data": "synthetic", "config": config_dict(args, case), "roofline": roof,
+                "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches_per_step * args.steps,
+                "clocks": clk}
+        print(json.dumps(line), flush=True)
+    if distributed:
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["libkda", "reference"], default="libkda")
+    ap.add_argument("--workload", default="prefill_4k", choices=sorted(workloads.NAMED_WORKLOADS))
+    ap.add_argument("--ref-budget", type=float, default=10.0, help="seconds of oracle work per sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    world, rank, local = dist_env()
+    if args.impl == "reference":
+        return run_reference(args, world, rank)
+    return run_gpu(args, world, rank, local)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

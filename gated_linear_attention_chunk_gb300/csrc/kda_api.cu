@@ -1,0 +1,191 @@
+// C-ABI entry points of libkda: argument validation, workspace layout and
+// kernel launches.  Declared and documented in include/kda.h.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/kda.h"
+#include "kda_internal.h"
+
+namespace {
+
+constexpr int kVersion = 10000;  // 1.0.0
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned_to(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+bool dim_ok(int d) { return d == 64 || d == 128; }
+bool dtype_ok(kda_dtype t) { return t == KDA_BF16 || t == KDA_F32; }
+size_t elem_size(kda_dtype t) { return t == KDA_BF16 ? 2 : 4; }
+
+size_t staging_offset() { return KDA_WS_HEADER_BYTES; }
+
+// Clears the status word at the start of the workspace (asynchronously on the stream).
+kda_status clear_status(void *workspace, cudaStream_t s) {
+    if (cudaMemsetAsync(workspace, 0, sizeof(uint32_t), s) != cudaSuccess) return KDA_ERR_CUDA;
+    return KDA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t kda_chunk_fwd_workspace_size(int N, int64_t T_total, int H, int dk, int dv) {
+    if (N < 0 || T_total < 0 || H <= 0 || !dim_ok(dk) || !dim_ok(dv)) return 0;
+    const size_t states = static_cast<size_t>(N) * static_cast<size_t>(H) * dk * dv * sizeof(float);
+    return staging_offset() + states;
+}
+
+kda_status kda_chunk_fwd(const void *q, const void *k, const void *v, const void *g, const void *beta,
+                         kda_dtype dtype, const float *init_state, const int32_t *cu_seqlens, int N,
+                         int64_t T_total, int H, int dk, int dv, float scale, void *o, float *final_state,
+                         void *workspace, size_t ws_bytes, void *stream) {
+    if (!dtype_ok(dtype) || !dim_ok(dk) || !dim_ok(dv)) return KDA_ERR_UNSUPPORTED;
+    if (N < 0 || T_total < 0 || H <= 0) return KDA_ERR_INVALID_ARGUMENT;
+    if (!workspace || !aligned16(workspace)) return KDA_ERR_WORKSPACE;
+    if (ws_bytes < KDA_WS_HEADER_BYTES) return KDA_ERR_WORKSPACE;
+    if (!final_state && ws_bytes < kda_chunk_fwd_workspace_size(N, T_total, H, dk, dv)) return KDA_ERR_WORKSPACE;
+    if (T_total > 0) {
+        if (!q || !k || !v || !g || !beta || !o) return KDA_ERR_INVALID_ARGUMENT;
+        if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(g) || !aligned16(o))
+            return KDA_ERR_INVALID_ARGUMENT;
+        if (!aligned_to(beta, elem_size(dtype))) return KDA_ERR_INVALID_ARGUMENT;
+    }
+    if ((init_state && !aligned16(init_state)) || (final_state && !aligned16(final_state)))
+        return KDA_ERR_INVALID_ARGUMENT;
+    if (!cu_seqlens && N > 0 && (T_total % N) != 0) return KDA_ERR_INVALID_ARGUMENT;
+    if (!cu_seqlens && N == 0 && T_total != 0) return KDA_ERR_INVALID_ARGUMENT;
+    if (cu_seqlens && !aligned_to(cu_seqlens, 4)) return KDA_ERR_INVALID_ARGUMENT;
+    if (!cu_seqlens && N == 0 && T_total == 0) { /* nothing */ }
+
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    kda_status st = clear_status(workspace, s);
+    if (st != KDA_OK) return st;
+    if (N == 0) return KDA_OK;
+
+    uint32_t *status = static_cast<uint32_t *>(workspace);
+    const int64_t fixed_len = cu_seqlens ? 0 : T_total / N;
+    const bool use_tc = kda::chunk_tc_supported(dk, dv, static_cast<int>(dtype));
+    float *chunk_state = final_state
+                             ? final_state
+                             : reinterpret_cast<float *>(static_cast<char *>(workspace) + staging_offset());
+
+    if (use_tc) {
+        kda::ChunkParams cp{};
+        cp.q = q; cp.k = k; cp.v = v; cp.g = g; cp.beta = beta; cp.o = o;
+        cp.N = N; cp.H = H; cp.scale = scale;
+        cp.cu = cu_seqlens; cp.T_total = T_total; cp.seq_len_fixed = fixed_len;
+        cp.init_state = init_state; cp.state_out = chunk_state; cp.status = status;
+        if (kda::launch_chunk_tc(cp, s) != cudaSuccess) return KDA_ERR_CUDA;
+    }
+
+    kda::SeqParams sp{};
+    sp.q = q; sp.k = k; sp.v = v; sp.g = g; sp.beta = beta; sp.o = o;
+    sp.N = N; sp.H = H; sp.scale = scale;
+    sp.mode = kda::SEQ_MODE_PREFILL;
+    sp.cu = cu_seqlens; sp.T_total = T_total; sp.seq_len_fixed = fixed_len;
+    sp.chunk_skip = use_tc ? 1 : 0;
+    sp.state_in = init_state; sp.state_out = final_state; sp.chunk_state = chunk_state;
+    sp.slots = nullptr; sp.num_slots = 0; sp.status = status;
+    if (kda::launch_seq(sp, dk, dv, static_cast<int>(dtype), s) != cudaSuccess) return KDA_ERR_CUDA;
+    return KDA_OK;
+}
+
+kda_status kda_decode_step(const void *q, const void *k, const void *v, const void *g, const void *beta,
+                           kda_dtype dtype, float *state_pool, int64_t num_slots, const int32_t *slots,
+                           int N, int H, int dk, int dv, float scale, void *o, void *workspace,
+                           size_t ws_bytes, void *stream) {
+    if (!dtype_ok(dtype) || !dim_ok(dk) || !dim_ok(dv)) return KDA_ERR_UNSUPPORTED;
+    if (N < 0 || H <= 0 || num_slots < 0) return KDA_ERR_INVALID_ARGUMENT;
+    if (!workspace || !aligned16(workspace) || ws_bytes < KDA_WS_HEADER_BYTES) return KDA_ERR_WORKSPACE;
+    if (N > 0) {
+        if (!q || !k || !v || !g || !beta || !o || !state_pool) return KDA_ERR_INVALID_ARGUMENT;
+        if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(g) || !aligned16(o) ||
+            !aligned16(state_pool))
+            return KDA_ERR_INVALID_ARGUMENT;
+        if (!aligned_to(beta, elem_size(dtype))) return KDA_ERR_INVALID_ARGUMENT;
+        if (slots && !aligned_to(slots, 4)) return KDA_ERR_INVALID_ARGUMENT;
+        if (!slots && N > num_slots) return KDA_ERR_INVALID_ARGUMENT;
+    }
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    kda_status st = clear_status(workspace, s);
+    if (st != KDA_OK || N == 0) return st;
+
+    kda::SeqParams sp{};
+    sp.q = q; sp.k = k; sp.v = v; sp.g = g; sp.beta = beta; sp.o = o;
+    sp.N = N; sp.H = H; sp.scale = scale;
+    sp.mode = kda::SEQ_MODE_DECODE;
+    sp.cu = nullptr; sp.T_total = N; sp.seq_len_fixed = 1; sp.chunk_skip = 0;
+    sp.state_in = state_pool; sp.state_out = state_pool; sp.chunk_state = nullptr;
+    sp.slots = slots; sp.num_slots = num_slots; sp.status = static_cast<uint32_t *>(workspace);
+    if (kda::launch_seq(sp, dk, dv, static_cast<int>(dtype), s) != cudaSuccess) return KDA_ERR_CUDA;
+    return KDA_OK;
+}
+
+kda_status kda_replay(float *state_pool, int64_t num_slots, const int32_t *slots, const void *k,
+                      const void *v, const void *g, const void *beta, kda_dtype dtype,
+                      const int32_t *cu_accept, int N, int64_t A_total, int H, int dk, int dv,
+                      void *workspace, size_t ws_bytes, void *stream) {
+    if (!dtype_ok(dtype) || !dim_ok(dk) || !dim_ok(dv)) return KDA_ERR_UNSUPPORTED;
+    if (N < 0 || A_total < 0 || H <= 0 || num_slots < 0) return KDA_ERR_INVALID_ARGUMENT;
+    if (!workspace || !aligned16(workspace) || ws_bytes < KDA_WS_HEADER_BYTES) return KDA_ERR_WORKSPACE;
+    if (N > 0) {
+        if (!state_pool || !cu_accept) return KDA_ERR_INVALID_ARGUMENT;
+        if (!aligned16(state_pool) || !aligned_to(cu_accept, 4)) return KDA_ERR_INVALID_ARGUMENT;
+        if (slots && !aligned_to(slots, 4)) return KDA_ERR_INVALID_ARGUMENT;
+        if (!slots && N > num_slots) return KDA_ERR_INVALID_ARGUMENT;
+    }
+    if (A_total > 0) {
+        if (!k || !v || !g || !beta) return KDA_ERR_INVALID_ARGUMENT;
+        if (!aligned16(k) || !aligned16(v) || !aligned16(g) || !aligned_to(beta, elem_size(dtype)))
+            return KDA_ERR_INVALID_ARGUMENT;
+    }
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    kda_status st = clear_status(workspace, s);
+    if (st != KDA_OK || N == 0) return st;
+
+    kda::SeqParams sp{};
+    sp.q = nullptr; sp.k = k; sp.v = v; sp.g = g; sp.beta = beta; sp.o = nullptr;
+    sp.N = N; sp.H = H; sp.scale = 1.0f;
+    sp.mode = kda::SEQ_MODE_REPLAY;
+    sp.cu = cu_accept; sp.T_total = A_total; sp.seq_len_fixed = 0; sp.chunk_skip = 0;
+    sp.state_in = state_pool; sp.state_out = state_pool; sp.chunk_state = nullptr;
+    sp.slots = slots; sp.num_slots = num_slots; sp.status = static_cast<uint32_t *>(workspace);
+    if (kda::launch_seq(sp, dk, dv, static_cast<int>(dtype), s) != cudaSuccess) return KDA_ERR_CUDA;
+    return KDA_OK;
+}
+
+kda_status kda_device_status(const void *workspace, void *stream) {
+    if (!workspace) return KDA_ERR_WORKSPACE;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(s) != cudaSuccess) return KDA_ERR_CUDA;
+    uint32_t word = 0;
+    if (cudaMemcpy(&word, workspace, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess) return KDA_ERR_CUDA;
+    if (word & kda::DEV_ERR_SEQLENS) return KDA_ERR_BAD_SEQLENS;
+    if (word & kda::DEV_ERR_SLOT) return KDA_ERR_BAD_SLOT;
+    if (word & kda::DEV_ERR_GATE) return KDA_ERR_GATE_RANGE;
+    if (word & kda::DEV_ERR_TIMEOUT) return KDA_ERR_TIMEOUT;
+    return KDA_OK;
+}
+
+int kda_chunk_fwd_uses_tensor_cores(int dk, int dv, kda_dtype dtype) {
+    if (!dtype_ok(dtype) || !dim_ok(dk) || !dim_ok(dv)) return 0;
+    return kda::chunk_tc_supported(dk, dv, static_cast<int>(dtype)) ? 1 : 0;
+}
+
+const char *kda_status_string(kda_status status) {
+    switch (status) {
+        case KDA_OK: return "KDA_OK";
+        case KDA_ERR_INVALID_ARGUMENT: return "KDA_ERR_INVALID_ARGUMENT";
+        case KDA_ERR_UNSUPPORTED: return "KDA_ERR_UNSUPPORTED";
+        case KDA_ERR_WORKSPACE: return "KDA_ERR_WORKSPACE";
+        case KDA_ERR_CUDA: return "KDA_ERR_CUDA";
+        case KDA_ERR_GATE_RANGE: return "KDA_ERR_GATE_RANGE";
+        case KDA_ERR_TIMEOUT: return "KDA_ERR_TIMEOUT";
+        case KDA_ERR_BAD_SEQLENS: return "KDA_ERR_BAD_SEQLENS";
+        case KDA_ERR_BAD_SLOT: return "KDA_ERR_BAD_SLOT";
+    }
+    return "KDA_ERR_UNKNOWN";
+}
+
+int kda_version(void) { return kVersion; }
+
+}  // extern "C"

@@ -1,0 +1,63 @@
+// Internal declarations shared by the host launcher and the kernel translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace kda {
+
+// Device-side error bits OR-ed into the workspace status word.
+enum DeviceError : uint32_t {
+    DEV_ERR_SEQLENS = 1u,  // cu_seqlens / cu_accept not a valid partition
+    DEV_ERR_SLOT = 2u,     // slot outside [0, num_slots)
+    DEV_ERR_GATE = 4u,     // a chunk's cumulative decay left the supported range
+    DEV_ERR_TIMEOUT = 8u,  // a bounded wait gave up
+};
+
+enum SeqMode : int {
+    SEQ_MODE_PREFILL = 0,  // tokens [cu[n], cu[n+1]) of a packed prefill
+    SEQ_MODE_DECODE = 1,   // token n, state in a slot-indexed pool
+    SEQ_MODE_REPLAY = 2,   // tokens [cu[n], cu[n+1]) onto a pool state, no output
+};
+
+// Arguments of the token-sequential kernel.  One CTA per (sequence, head).
+struct SeqParams {
+    const void *q, *k, *v, *g, *beta;
+    void *o;                    // may be null (replay)
+    int N, H;
+    float scale;
+    int mode;                   // SeqMode
+    const int32_t *cu;          // cu_seqlens / cu_accept (prefill: may be null)
+    int64_t T_total;            // total packed tokens (validation)
+    int64_t seq_len_fixed;      // prefill with cu == null: every sequence has this length
+    int chunk_skip;             // prefill: 1 = the first 64*floor(len/64) tokens were done by the chunked kernel
+    const float *state_in;      // prefill: init_state or null; decode/replay: pool
+    float *state_out;           // prefill: final_state or null; decode/replay: pool
+    const float *chunk_state;   // prefill with chunk_skip: states left by the chunked kernel
+    const int32_t *slots;       // decode/replay: slot map or null
+    int64_t num_slots;
+    uint32_t *status;           // device status word
+};
+
+// dtype: 0 = bf16, 1 = fp32 (kda_dtype).  Returns the launch error.
+cudaError_t launch_seq(const SeqParams &p, int dk, int dv, int dtype, cudaStream_t stream);
+
+// Arguments of the chunked (64-token WY, tcgen05) kernel: bf16, dk = dv = 128.
+struct ChunkParams {
+    const void *q, *k, *v, *g, *beta;
+    void *o;
+    int N, H;
+    float scale;
+    const int32_t *cu;          // may be null: equal lengths seq_len_fixed
+    int64_t T_total;
+    int64_t seq_len_fixed;
+    const float *init_state;    // may be null (zeros)
+    float *state_out;           // final_state or staging (never null)
+    uint32_t *status;
+};
+
+// True when the chunked tensor-core kernel is compiled in and supports the shape.
+bool chunk_tc_supported(int dk, int dv, int dtype);
+cudaError_t launch_chunk_tc(const ChunkParams &p, cudaStream_t stream);
+
+}  // namespace kda

@@ -1,0 +1,270 @@
+// Token-sequential KDA kernel: decode, ReplaySSM replay, and the partial-chunk
+// tail of the packed prefill.
+//
+// Per (sequence, head) the gated delta rule with per-channel decay is stepped
+// one token at a time on an fp32 state held in registers ("Kimi K3 on
+// Fireworks: Fast RL at frontier scale", KDA paragraph: compact recurrent state
+// with channel-wise gating; speculative-decoding paragraph: replay of accepted
+// tokens from a committed checkpoint).  For token t with alpha = exp(g_t):
+//
+//     S' = Diag(alpha) S
+//     y  = S'^T k,  z = S'^T (scale q),  qk = (scale q) . k
+//     u  = beta (v - y)
+//     S  = S' + k u^T
+//     o  = z + qk u            (= S^T (scale q), the output after the update)
+//
+// Computing z and qk from the decayed state lets one reduction pass serve both
+// the delta step and the output, so each token costs one __syncthreads.
+//
+// Layout: 256 threads; a thread owns NS rows x 4 consecutive columns of S
+// (float4), so state loads/stores are 128-bit and a warp covers whole rows.
+// Reductions over dk run in a fixed order (rows in order inside a thread, then
+// the two row-halves of a warp, then warps 0..7 in order), and every
+// floating-point step uses an explicit round-to-nearest intrinsic, so every
+// caller of this routine -- decode, replay and the prefill tail -- produces
+// the same bits for the same state and tokens.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "kda_internal.h"
+
+namespace kda {
+namespace {
+
+constexpr int kSeqThreads = 256;
+constexpr int kSeqWarps = kSeqThreads / 32;
+
+__device__ __forceinline__ float ld_in(const float *p, int64_t i) { return p[i]; }
+__device__ __forceinline__ float ld_in(const __nv_bfloat16 *p, int64_t i) { return __bfloat162float(p[i]); }
+
+__device__ __forceinline__ void st_out4(float *p, float4 v) { *reinterpret_cast<float4 *>(p) = v; }
+__device__ __forceinline__ void st_out4(__nv_bfloat16 *p, float4 v) {
+    __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y);
+    __nv_bfloat162 hi = __floats2bfloat162_rn(v.z, v.w);
+    uint2 packed;
+    packed.x = *reinterpret_cast<uint32_t *>(&lo);
+    packed.y = *reinterpret_cast<uint32_t *>(&hi);
+    *reinterpret_cast<uint2 *>(p) = packed;
+}
+
+__device__ __forceinline__ float4 f4_fma(float a, float4 b, float4 c) {
+    return make_float4(__fmaf_rn(a, b.x, c.x), __fmaf_rn(a, b.y, c.y), __fmaf_rn(a, b.z, c.z),
+                       __fmaf_rn(a, b.w, c.w));
+}
+__device__ __forceinline__ float4 f4_add(float4 a, float4 b) {
+    return make_float4(__fadd_rn(a.x, b.x), __fadd_rn(a.y, b.y), __fadd_rn(a.z, b.z), __fadd_rn(a.w, b.w));
+}
+__device__ __forceinline__ float4 f4_scale(float4 a, float s) {
+    return make_float4(__fmul_rn(a.x, s), __fmul_rn(a.y, s), __fmul_rn(a.z, s), __fmul_rn(a.w, s));
+}
+__device__ __forceinline__ float4 f4_shfl_xor(float4 a, int m) {
+    return make_float4(__shfl_xor_sync(0xffffffffu, a.x, m), __shfl_xor_sync(0xffffffffu, a.y, m),
+                       __shfl_xor_sync(0xffffffffu, a.z, m), __shfl_xor_sync(0xffffffffu, a.w, m));
+}
+
+template <int DK, int DV, typename Tin, bool WRITE_O>
+__global__ void __launch_bounds__(kSeqThreads) kda_seq_kernel(SeqParams p) {
+    constexpr int LPR = DV / 4;           // lanes per state row
+    constexpr int RPW = 32 / LPR;         // rows per warp per step (1 or 2)
+    constexpr int RPS = kSeqWarps * RPW;  // rows per step
+    constexpr int NS = DK / RPS;          // rows per thread
+    static_assert(LPR * RPW == 32 && NS * RPS == DK, "thread layout");
+
+    __shared__ float tok_a[3][DK], tok_k[3][DK], tok_q[3][DK];
+    __shared__ __align__(16) float tok_v[3][DV];
+    __shared__ float tok_b[3];
+    __shared__ float4 red_y[2][kSeqWarps][LPR], red_z[2][kSeqWarps][LPR];
+    __shared__ float red_qk[2][kSeqWarps];
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int cg = lane % LPR, rsub = lane / LPR;
+    const int row0 = warp * RPW + rsub;
+    const int64_t pair = blockIdx.x;
+    const int n = static_cast<int>(pair / p.H), h = static_cast<int>(pair % p.H);
+    const int64_t H = p.H;
+
+    // ---- resolve the token range and the state source/destination
+    int64_t t0, t1;
+    const float *src;
+    float *dst;
+    if (p.mode == SEQ_MODE_DECODE) {
+        t0 = n;
+        t1 = n + 1;
+    } else if (p.cu) {
+        t0 = p.cu[n];
+        t1 = p.cu[n + 1];
+        bool ok = (t0 >= 0) && (t0 <= t1) && (t1 <= p.T_total);
+        if (n == 0 && t0 != 0) ok = false;
+        if (n == p.N - 1 && t1 != p.T_total) ok = false;
+        if (!ok) {
+            if (tid == 0 && h == 0) atomicOr(p.status, DEV_ERR_SEQLENS);
+            return;
+        }
+    } else {
+        t0 = static_cast<int64_t>(n) * p.seq_len_fixed;
+        t1 = t0 + p.seq_len_fixed;
+    }
+    if (p.mode == SEQ_MODE_PREFILL) {
+        const int64_t len = t1 - t0;
+        const int64_t nfull = p.chunk_skip ? len / 64 : 0;
+        if (nfull > 0) {
+            if (len % 64 == 0) return;  // the chunked kernel already left the final state
+            src = p.chunk_state + pair * DK * DV;
+            t0 += 64 * nfull;
+        } else {
+            src = p.state_in ? p.state_in + pair * DK * DV : nullptr;
+        }
+        dst = p.state_out ? p.state_out + pair * DK * DV : nullptr;
+    } else {
+        const int64_t slot = p.slots ? static_cast<int64_t>(p.slots[n]) : static_cast<int64_t>(n);
+        if (slot < 0 || slot >= p.num_slots) {
+            if (tid == 0 && h == 0) atomicOr(p.status, DEV_ERR_SLOT);
+            return;
+        }
+        src = p.state_in + (slot * H + h) * DK * DV;
+        dst = p.state_out + (slot * H + h) * DK * DV;
+    }
+
+    const Tin *Q = static_cast<const Tin *>(p.q);
+    const Tin *K = static_cast<const Tin *>(p.k);
+    const Tin *V = static_cast<const Tin *>(p.v);
+    const Tin *G = static_cast<const Tin *>(p.g);
+    const Tin *B = static_cast<const Tin *>(p.beta);
+
+    // ---- state into registers (128-bit loads; a warp reads whole rows)
+    float4 S[NS];
+#pragma unroll
+    for (int s = 0; s < NS; ++s) {
+        const int row = s * RPS + row0;
+        S[s] = src ? *reinterpret_cast<const float4 *>(src + row * DV + 4 * cg) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+
+    // Token staging: threads [0, DK) hold alpha/k/q of one channel, threads
+    // [128, 128 + DV) one value column, thread 255 beta.
+    auto load_raw = [&](int64_t t, float &rg, float &rk, float &rq, float &rv, float &rb) {
+        if (tid < DK) {
+            const int64_t base = (t * H + h) * DK + tid;
+            rg = ld_in(G, base);
+            rk = ld_in(K, base);
+            if (WRITE_O) rq = ld_in(Q, base);
+        }
+        if (tid >= 128 && tid - 128 < DV) rv = ld_in(V, (t * H + h) * DV + (tid - 128));
+        if (tid == kSeqThreads - 1) rb = ld_in(B, t * H + h);
+    };
+    auto stage = [&](int buf, float rg, float rk, float rq, float rv, float rb) {
+        if (tid < DK) {
+            tok_a[buf][tid] = expf(rg);
+            tok_k[buf][tid] = rk;
+            if (WRITE_O) tok_q[buf][tid] = __fmul_rn(rq, p.scale);
+        }
+        if (tid >= 128 && tid - 128 < DV) tok_v[buf][tid - 128] = rv;
+        if (tid == kSeqThreads - 1) tok_b[buf] = rb;
+    };
+
+    if (t0 < t1) {
+        float rg = 0.f, rk = 0.f, rq = 0.f, rv = 0.f, rb = 0.f;
+        load_raw(t0, rg, rk, rq, rv, rb);
+        stage(0, rg, rk, rq, rv, rb);
+    }
+    __syncthreads();
+
+    int it = 0;
+    for (int64_t t = t0; t < t1; ++t, ++it) {
+        const int b = it % 3, r = it & 1;
+        const bool has_next = (t + 1 < t1);
+        float ng = 0.f, nk = 0.f, nq = 0.f, nv = 0.f, nb = 0.f;
+        if (has_next) load_raw(t + 1, ng, nk, nq, nv, nb);
+
+        // decay, then partial reductions over this thread's rows (rows in order)
+        float4 py = make_float4(0.f, 0.f, 0.f, 0.f), pz = py;
+        float pqk = 0.f;
+#pragma unroll
+        for (int s = 0; s < NS; ++s) {
+            const int row = s * RPS + row0;
+            const float a = tok_a[b][row], kk = tok_k[b][row];
+            S[s] = f4_scale(S[s], a);
+            py = f4_fma(kk, S[s], py);
+            if (WRITE_O) {
+                const float qq = tok_q[b][row];
+                pz = f4_fma(qq, S[s], pz);
+                pqk = __fmaf_rn(qq, kk, pqk);
+            }
+        }
+        if (RPW == 2) {  // combine the two row halves of the warp (a + b == b + a exactly)
+            py = f4_add(py, f4_shfl_xor(py, LPR));
+            if (WRITE_O) {
+                pz = f4_add(pz, f4_shfl_xor(pz, LPR));
+                pqk = __fadd_rn(pqk, __shfl_xor_sync(0xffffffffu, pqk, LPR));
+            }
+        }
+        if (rsub == 0) {
+            red_y[r][warp][cg] = py;
+            if (WRITE_O) red_z[r][warp][cg] = pz;
+        }
+        if (WRITE_O && lane == 0) red_qk[r][warp] = pqk;
+        if (has_next) stage((it + 1) % 3, ng, nk, nq, nv, nb);
+        __syncthreads();
+
+        // every thread reduces the warps' partials for its columns, warps in order
+        float4 y = red_y[r][0][cg];
+#pragma unroll
+        for (int w = 1; w < kSeqWarps; ++w) y = f4_add(y, red_y[r][w][cg]);
+        const float4 vv = *reinterpret_cast<const float4 *>(&tok_v[b][4 * cg]);
+        const float bt = tok_b[b];
+        const float4 u = make_float4(__fmul_rn(bt, __fsub_rn(vv.x, y.x)), __fmul_rn(bt, __fsub_rn(vv.y, y.y)),
+                                     __fmul_rn(bt, __fsub_rn(vv.z, y.z)), __fmul_rn(bt, __fsub_rn(vv.w, y.w)));
+#pragma unroll
+        for (int s = 0; s < NS; ++s) S[s] = f4_fma(tok_k[b][s * RPS + row0], u, S[s]);
+
+        if (WRITE_O && warp == 0 && rsub == 0) {
+            float4 z = red_z[r][0][cg];
+            float qk = red_qk[r][0];
+#pragma unroll
+            for (int w = 1; w < kSeqWarps; ++w) {
+                z = f4_add(z, red_z[r][w][cg]);
+                qk = __fadd_rn(qk, red_qk[r][w]);
+            }
+            const float4 o = f4_fma(qk, u, z);
+            st_out4(static_cast<Tin *>(p.o) + (t * H + h) * DV + 4 * cg, o);
+        }
+    }
+
+    if (dst) {
+#pragma unroll
+        for (int s = 0; s < NS; ++s) {
+            const int row = s * RPS + row0;
+            *reinterpret_cast<float4 *>(dst + row * DV + 4 * cg) = S[s];
+        }
+    }
+}
+
+template <int DK, int DV, typename Tin>
+cudaError_t launch_typed(const SeqParams &p, cudaStream_t stream) {
+    const int64_t blocks = static_cast<int64_t>(p.N) * p.H;
+    if (blocks <= 0) return cudaSuccess;
+    if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    if (p.o)
+        kda_seq_kernel<DK, DV, Tin, true><<<static_cast<unsigned>(blocks), kSeqThreads, 0, stream>>>(p);
+    else
+        kda_seq_kernel<DK, DV, Tin, false><<<static_cast<unsigned>(blocks), kSeqThreads, 0, stream>>>(p);
+    return cudaGetLastError();
+}
+
+template <typename Tin>
+cudaError_t launch_dims(const SeqParams &p, int dk, int dv, cudaStream_t stream) {
+    if (dk == 128 && dv == 128) return launch_typed<128, 128, Tin>(p, stream);
+    if (dk == 64 && dv == 64) return launch_typed<64, 64, Tin>(p, stream);
+    if (dk == 128 && dv == 64) return launch_typed<128, 64, Tin>(p, stream);
+    if (dk == 64 && dv == 128) return launch_typed<64, 128, Tin>(p, stream);
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace
+
+cudaError_t launch_seq(const SeqParams &p, int dk, int dv, int dtype, cudaStream_t stream) {
+    if (dtype == 0) return launch_dims<__nv_bfloat16>(p, dk, dv, stream);
+    return launch_dims<float>(p, dk, dv, stream);
+}
+
+}  // namespace kda

@@ -1,0 +1,239 @@
+"""Python binding of libkda (ctypes).  Argument marshalling only.
+
+Each function takes torch CUDA tensors, checks dtypes/shapes/contiguity,
+allocates outputs the caller did not pass (torch is the device allocator and
+stream provider), and calls the C entry point of the same name in
+``_lib/libkda.so`` on the current CUDA stream.  All arithmetic runs in the CUDA
+kernels; there is no fallback path: if the library is missing, importing the
+binding raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+from typing import Optional, Tuple
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "_lib", "libkda.so")
+HEADER_PATH = os.path.join(os.path.dirname(_PKG), "include", "kda.h")
+
+KDA_OK = 0
+KDA_ERR_INVALID_ARGUMENT = 1
+KDA_ERR_UNSUPPORTED = 2
+KDA_ERR_WORKSPACE = 3
+KDA_ERR_CUDA = 4
+KDA_ERR_GATE_RANGE = 5
+KDA_ERR_TIMEOUT = 6
+KDA_ERR_BAD_SEQLENS = 7
+KDA_ERR_BAD_SLOT = 8
+KDA_BF16 = 0
+KDA_F32 = 1
+KDA_WS_HEADER_BYTES = 256
+
+_vp = ctypes.c_void_p
+_i64 = ctypes.c_int64
+_int = ctypes.c_int
+_SIGS = {
+    "kda_chunk_fwd_workspace_size": (ctypes.c_size_t, [_int, _i64, _int, _int, _int]),
+    "kda_chunk_fwd": (_int, [_vp, _vp, _vp, _vp, _vp, _int, _vp, _vp, _int, _i64, _int, _int, _int,
+                             ctypes.c_float, _vp, _vp, _vp, ctypes.c_size_t, _vp]),
+    "kda_decode_step": (_int, [_vp, _vp, _vp, _vp, _vp, _int, _vp, _i64, _vp, _int, _int, _int, _int,
+                               ctypes.c_float, _vp, _vp, ctypes.c_size_t, _vp]),
+    "kda_replay": (_int, [_vp, _i64, _vp, _vp, _vp, _vp, _vp, _int, _vp, _int, _i64, _int, _int, _int,
+                          _vp, ctypes.c_size_t, _vp]),
+    "kda_device_status": (_int, [_vp, _vp]),
+    "kda_status_string": (ctypes.c_char_p, [_int]),
+    "kda_version": (_int, []),
+    "kda_chunk_fwd_uses_tensor_cores": (_int, [_int, _int, _int]),
+}
+
+_lib = None
+
+
+class KdaError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = int(code)
+        super().__init__(f"{where}: {kda_status_string(code)}")
+
+
+def load_library():
+    """Load ``libkda.so`` (raises ImportError if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise ImportError(f"libkda.so is not built ({LIB_PATH}); run __graft_entry__.build()")
+        lib = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in _SIGS.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+    return _lib
+
+
+def header_functions():
+    """Names of the functions declared in include/kda.h."""
+    text = open(HEADER_PATH).read()
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[a-z_0-9]+\s*\*?\s*(kda_[a-z_0-9]+)\s*\(", text, re.M)))
+
+
+def kda_status_string(code: int) -> str:
+    return load_library().kda_status_string(int(code)).decode()
+
+
+def kda_version() -> int:
+    return int(load_library().kda_version())
+
+
+def _check(code: int, where: str):
+    if code != KDA_OK:
+        raise KdaError(code, where)
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return KDA_BF16
+    if t.dtype == torch.float32:
+        return KDA_F32
+    raise TypeError(f"unsupported dtype {t.dtype} (bf16 or fp32)")
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _need(t: torch.Tensor, name: str, dtype=None, shape=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} has dtype {t.dtype}, expected {dtype}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+
+
+def _stream_handle(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def kda_chunk_fwd_uses_tensor_cores(dk: int, dv: int, dtype) -> bool:
+    """Whether kda_chunk_fwd runs full chunks on the tcgen05 kernel for this shape/dtype."""
+    code = dtype if isinstance(dtype, int) else (KDA_BF16 if dtype == torch.bfloat16 else KDA_F32)
+    return bool(load_library().kda_chunk_fwd_uses_tensor_cores(int(dk), int(dv), code))
+
+
+def kda_chunk_fwd_workspace_size(N: int, T_total: int, H: int, dk: int, dv: int) -> int:
+    return int(load_library().kda_chunk_fwd_workspace_size(N, T_total, H, dk, dv))
+
+
+def new_workspace(nbytes: int, device) -> torch.Tensor:
+    """A workspace buffer (uint8, 256-byte aligned by the caching allocator)."""
+    return torch.empty(max(int(nbytes), KDA_WS_HEADER_BYTES), dtype=torch.uint8, device=device)
+
+
+def kda_chunk_fwd(q, k, v, g, beta, cu_seqlens=None, init_state=None, scale: float = 1.0,
+                  output_final_state: bool = True, o=None, final_state=None, workspace=None,
+                  stream=None) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
+    """Packed varlen KDA prefill.  Returns ``(o, final_state)``.
+
+    q, k, g [T, H, dk]; v [T, H, dv]; beta [T, H] (bf16 or fp32, one dtype);
+    cu_seqlens [N+1] int32 CUDA (None: one sequence of length T);
+    init_state [N, H, dk, dv] fp32 or None.  ``final_state`` may be passed (and
+    may be ``init_state`` itself for an in-place update).
+    """
+    lib = load_library()
+    dt = q.dtype
+    T, H, dk = q.shape
+    dv = v.shape[2]
+    for name, t, shp in (("q", q, (T, H, dk)), ("k", k, (T, H, dk)), ("v", v, (T, H, dv)),
+                         ("g", g, (T, H, dk)), ("beta", beta, (T, H))):
+        _need(t, name, dt, shp)
+    if cu_seqlens is None:
+        N = 1
+    else:
+        _need(cu_seqlens, "cu_seqlens", torch.int32)
+        N = cu_seqlens.numel() - 1
+    if init_state is not None:
+        _need(init_state, "init_state", torch.float32, (N, H, dk, dv))
+    if o is None:
+        o = torch.empty(T, H, dv, dtype=dt, device=q.device)
+    _need(o, "o", dt, (T, H, dv))
+    if final_state is None and output_final_state:
+        final_state = torch.empty(N, H, dk, dv, dtype=torch.float32, device=q.device)
+    if final_state is not None:
+        _need(final_state, "final_state", torch.float32, (N, H, dk, dv))
+    need = (KDA_WS_HEADER_BYTES if final_state is not None
+            else kda_chunk_fwd_workspace_size(N, T, H, dk, dv))
+    if workspace is None:
+        workspace = new_workspace(need, q.device)
+    rc = lib.kda_chunk_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _dtype_code(q), _ptr(init_state),
+                           _ptr(cu_seqlens), N, T, H, dk, dv, float(scale), _ptr(o), _ptr(final_state),
+                           _ptr(workspace), workspace.numel() * workspace.element_size(),
+                           _stream_handle(stream))
+    _check(rc, "kda_chunk_fwd")
+    return o, final_state
+
+
+def kda_decode_step(q, k, v, g, beta, state_pool, slots=None, scale: float = 1.0, o=None, workspace=None,
+                    stream=None) -> torch.Tensor:
+    """One token per sequence; updates ``state_pool`` [S, H, dk, dv] in place.  Returns o [N, H, dv]."""
+    lib = load_library()
+    dt = q.dtype
+    N, H, dk = q.shape
+    dv = v.shape[2]
+    for name, t, shp in (("q", q, (N, H, dk)), ("k", k, (N, H, dk)), ("v", v, (N, H, dv)),
+                         ("g", g, (N, H, dk)), ("beta", beta, (N, H))):
+        _need(t, name, dt, shp)
+    _need(state_pool, "state_pool", torch.float32)
+    if tuple(state_pool.shape[1:]) != (H, dk, dv):
+        raise ValueError(f"state_pool shape {tuple(state_pool.shape)} != [S, {H}, {dk}, {dv}]")
+    if slots is not None:
+        _need(slots, "slots", torch.int32, (N,))
+    if o is None:
+        o = torch.empty(N, H, dv, dtype=dt, device=q.device)
+    _need(o, "o", dt, (N, H, dv))
+    if workspace is None:
+        workspace = new_workspace(KDA_WS_HEADER_BYTES, q.device)
+    rc = lib.kda_decode_step(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _dtype_code(q), _ptr(state_pool),
+                             state_pool.shape[0], _ptr(slots), N, H, dk, dv, float(scale), _ptr(o),
+                             _ptr(workspace), workspace.numel() * workspace.element_size(),
+                             _stream_handle(stream))
+    _check(rc, "kda_decode_step")
+    return o
+
+
+def kda_replay(state_pool, k, v, g, beta, cu_accept, slots=None, workspace=None, stream=None) -> None:
+    """Apply accepted tokens [A, H, .] to the pool states in place (cu_accept [N+1] int32)."""
+    lib = load_library()
+    dt = k.dtype
+    A, H, dk = k.shape
+    dv = v.shape[2]
+    for name, t, shp in (("k", k, (A, H, dk)), ("v", v, (A, H, dv)), ("g", g, (A, H, dk)),
+                         ("beta", beta, (A, H))):
+        _need(t, name, dt, shp)
+    _need(cu_accept, "cu_accept", torch.int32)
+    N = cu_accept.numel() - 1
+    _need(state_pool, "state_pool", torch.float32)
+    if tuple(state_pool.shape[1:]) != (H, dk, dv):
+        raise ValueError(f"state_pool shape {tuple(state_pool.shape)} != [S, {H}, {dk}, {dv}]")
+    if slots is not None:
+        _need(slots, "slots", torch.int32, (N,))
+    if workspace is None:
+        workspace = new_workspace(KDA_WS_HEADER_BYTES, k.device)
+    rc = lib.kda_replay(_ptr(state_pool), state_pool.shape[0], _ptr(slots), _ptr(k), _ptr(v), _ptr(g),
+                        _ptr(beta), _dtype_code(k), _ptr(cu_accept), N, A, H, dk, dv, _ptr(workspace),
+                        workspace.numel() * workspace.element_size(), _stream_handle(stream))
+    _check(rc, "kda_replay")
+
+
+def kda_device_status(workspace, stream=None) -> int:
+    """Synchronize the stream and return the device status code of the last call on ``workspace``."""
+    return int(load_library().kda_device_status(_ptr(workspace), _stream_handle(stream)))

@@ -1,0 +1,171 @@
+/*
+ * libkda -- Kimi Delta Attention (KDA) forward on one GB300 (sm_103a).
+ *
+ * What is computed.  The KDA paragraph of "Kimi K3 on Fireworks: Fast RL at
+ * frontier scale" (kernels section) describes KDA as linear attention that
+ * updates a compact, fixed-size recurrent state per head with channel-wise
+ * gating, trained in chunk-parallel form.  The pages print no equation; this
+ * library implements the gated delta rule with per-channel decay, for each
+ * (sequence, head) with state S in R^{dk x dv}:
+ *
+ *     S <- Diag(exp(g_t)) S                    (decay of the dk rows)
+ *     S <- S - beta_t k_t (k_t^T S) + beta_t k_t v_t^T
+ *     o_t = S^T (scale * q_t)                  (output after the update)
+ *
+ * The same page's speculative-decoding paragraph (ReplaySSM) keeps the
+ * recurrent state consistent after rejected draft tokens by replaying the
+ * accepted tokens' update inputs from a committed checkpoint: kda_replay.
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * - All tensor arguments are DEVICE pointers to caller-owned memory.  The
+ *   library never allocates or frees device memory; its only scratch is the
+ *   caller's workspace.
+ * - Token-major packed layouts, C-contiguous:
+ *     q, k, g  [T, H, dk]     v, o [T, H, dv]     beta [T, H]
+ *   of dtype `kda_dtype` (bf16 or fp32; o uses the same dtype as the inputs).
+ *   States are always fp32, [.., H, dk, dv] with dv contiguous.
+ * - g holds log-gates (alpha = exp(g) in [0, 1]); g = -inf erases the state.
+ * - dk and dv must each be 64 or 128 (KDA_ERR_UNSUPPORTED otherwise).
+ * - Pointers must be 16-byte aligned (beta: element-aligned).
+ * - `stream` is a cudaStream_t (NULL = legacy default stream).  Every call is
+ *   asynchronous on `stream`; none synchronizes except kda_device_status.
+ * - Errors the host can see (NULL pointers, bad sizes, dtype, alignment, small
+ *   workspace) return immediately and launch nothing.  Errors only the device
+ *   can see (bad cu_seqlens / cu_accept, slot out of range, gate range, a
+ *   bounded wait that gave up) are OR-ed into a status word in the workspace;
+ *   read it with kda_device_status.  Each call clears that word first.  A
+ *   work item that detects a device error skips its work and writes nothing.
+ *   No call aborts, prints or traps.
+ * - Results are deterministic: fixed reduction order, no floating-point
+ *   atomics; the same sequence gives the same bits whatever else is batched
+ *   with it.
+ */
+#ifndef KDA_H_
+#define KDA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum kda_status {
+    KDA_OK = 0,
+    KDA_ERR_INVALID_ARGUMENT = 1, /* NULL pointer, negative size, misaligned pointer          */
+    KDA_ERR_UNSUPPORTED = 2,      /* dk/dv not in {64,128}, unknown dtype                     */
+    KDA_ERR_WORKSPACE = 3,        /* workspace NULL or smaller than required                  */
+    KDA_ERR_CUDA = 4,             /* a CUDA runtime call or launch failed                     */
+    KDA_ERR_GATE_RANGE = 5,       /* device: a 64-token chunk decays a channel below 2^-100  */
+    KDA_ERR_TIMEOUT = 6,          /* device: a bounded wait gave up                           */
+    KDA_ERR_BAD_SEQLENS = 7,      /* device: cu_seqlens / cu_accept not a valid partition     */
+    KDA_ERR_BAD_SLOT = 8          /* device: slot index outside [0, num_slots)                */
+} kda_status;
+
+typedef enum kda_dtype {
+    KDA_BF16 = 0, /* q, k, v, g, beta and o are bfloat16 */
+    KDA_F32 = 1   /* q, k, v, g, beta and o are float32  */
+} kda_dtype;
+
+/* Bytes at the start of every workspace: the device status word and padding. */
+#define KDA_WS_HEADER_BYTES 256
+
+/*
+ * Workspace for kda_chunk_fwd, in bytes.
+ *
+ * With final_state != NULL, KDA_WS_HEADER_BYTES suffice.  With final_state ==
+ * NULL the chunked path needs a staging copy of every (sequence, head) state
+ * (N*H*dk*dv*4 bytes after the header) to hand the state from the chunked
+ * kernel to the partial-chunk kernel; this function returns that larger size.
+ * Returns 0 for invalid arguments.
+ */
+size_t kda_chunk_fwd_workspace_size(int N, int64_t T_total, int H, int dk, int dv);
+
+/*
+ * Packed variable-length prefill (the chunk-parallel training/prefill form).
+ *
+ *   q, k, g      [T_total, H, dk]   dtype
+ *   v            [T_total, H, dv]   dtype
+ *   beta         [T_total, H]       dtype
+ *   init_state   [N, H, dk, dv] fp32, or NULL for zeros
+ *   cu_seqlens   [N+1] int32 on the device, cu[0] = 0, non-decreasing,
+ *                cu[N] = T_total; sequence n is tokens [cu[n], cu[n+1]).
+ *                NULL means N sequences of equal length T_total / N.
+ *   scale        multiplies q (pass 1/sqrt(dk) for raw queries)
+ *   o            [T_total, H, dv]   dtype (written for every token)
+ *   final_state  [N, H, dk, dv] fp32, or NULL (not written).  May alias
+ *                init_state (in-place update).
+ *   workspace    >= kda_chunk_fwd_workspace_size() bytes (see above), device.
+ *
+ * Full 64-token chunks run through the chunked WY kernel (bf16, dk=dv=128);
+ * the last len % 64 tokens of each sequence, sequences shorter than 64, and
+ * the other dtype/size combinations run through the token-sequential kernel,
+ * which is the same routine kda_decode_step and kda_replay use: a 1-token
+ * sequence here gives the same bits as kda_decode_step on the same state.
+ * An empty sequence copies init_state to final_state.
+ */
+kda_status kda_chunk_fwd(const void *q, const void *k, const void *v, const void *g, const void *beta,
+                         kda_dtype dtype, const float *init_state, const int32_t *cu_seqlens, int N,
+                         int64_t T_total, int H, int dk, int dv, float scale, void *o, float *final_state,
+                         void *workspace, size_t ws_bytes, void *stream);
+
+/*
+ * One decode token per sequence on a slot-indexed state pool (in place).
+ *
+ *   q, k, g      [N, H, dk]   dtype;  v [N, H, dv];  beta [N, H]
+ *   state_pool   [num_slots, H, dk, dv] fp32, read and written in place
+ *   slots        [N] int32 device, or NULL for slot n = n (needs N <= num_slots).
+ *                Two sequences must not name the same slot.
+ *   o            [N, H, dv]   dtype
+ *   workspace    >= KDA_WS_HEADER_BYTES bytes (status word)
+ */
+kda_status kda_decode_step(const void *q, const void *k, const void *v, const void *g, const void *beta,
+                           kda_dtype dtype, float *state_pool, int64_t num_slots, const int32_t *slots,
+                           int N, int H, int dk, int dv, float scale, void *o, void *workspace,
+                           size_t ws_bytes, void *stream);
+
+/*
+ * ReplaySSM-style rollback: apply each sequence's accepted tokens to its
+ * committed state, in place, without producing outputs.  Equivalent to
+ * kda_chunk_fwd over the accepted tokens with init_state = final_state =
+ * the committed state (bit for bit).
+ *
+ *   state_pool   [num_slots, H, dk, dv] fp32, in place
+ *   slots        [N] int32 device, or NULL for slot n = n
+ *   k, g         [A_total, H, dk] dtype;  v [A_total, H, dv];  beta [A_total, H]
+ *   cu_accept    [N+1] int32 device; sequence n's accepted tokens are
+ *                [cu_accept[n], cu_accept[n+1]) (0 tokens leaves the state)
+ *   workspace    >= KDA_WS_HEADER_BYTES bytes (status word)
+ */
+kda_status kda_replay(float *state_pool, int64_t num_slots, const int32_t *slots, const void *k,
+                      const void *v, const void *g, const void *beta, kda_dtype dtype,
+                      const int32_t *cu_accept, int N, int64_t A_total, int H, int dk, int dv,
+                      void *workspace, size_t ws_bytes, void *stream);
+
+/*
+ * Synchronizes `stream`, then reads the device status word of `workspace`
+ * (errors from the last call that used it).  Returns KDA_OK or the first of
+ * BAD_SEQLENS, BAD_SLOT, GATE_RANGE, TIMEOUT that was raised; KDA_ERR_CUDA if
+ * the synchronization or the copy failed.
+ */
+kda_status kda_device_status(const void *workspace, void *stream);
+
+/*
+ * 1 if kda_chunk_fwd runs its full 64-token chunks on the tensor-core (tcgen05)
+ * kernel for this shape and dtype, 0 if every token goes through the
+ * token-sequential kernel.  Pure query; touches no device.
+ */
+int kda_chunk_fwd_uses_tensor_cores(int dk, int dv, kda_dtype dtype);
+
+/* Static, human-readable name of a status code. */
+const char *kda_status_string(kda_status status);
+
+/* Library version: major*10000 + minor*100 + patch. */
+int kda_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KDA_H_ */

@@ -1,0 +1,81 @@
+"""The C-ABI library: it loads without a GPU, exports every declared symbol, and
+rejects bad arguments on the host (before any CUDA call)."""
+import ctypes
+
+import pytest
+
+from tests._helpers import ensure_built
+
+
+@pytest.fixture(scope="module")
+def lib():
+    ensure_built()
+    from gated_linear_attention_chunk_gb300 import kda
+    return kda.load_library()
+
+
+def test_exports_every_declared_symbol(lib):
+    from gated_linear_attention_chunk_gb300 import kda
+    names = kda.header_functions()
+    assert {"kda_chunk_fwd", "kda_decode_step", "kda_replay", "kda_device_status",
+            "kda_chunk_fwd_workspace_size", "kda_status_string", "kda_version"} <= set(names)
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_status_strings_and_version(lib):
+    from gated_linear_attention_chunk_gb300 import kda
+    assert kda.kda_status_string(0) == "KDA_OK"
+    assert kda.kda_status_string(7) == "KDA_ERR_BAD_SEQLENS"
+    assert kda.kda_status_string(99) == "KDA_ERR_UNKNOWN"
+    assert kda.kda_version() >= 10000
+
+
+def test_workspace_size(lib):
+    from gated_linear_attention_chunk_gb300 import kda
+    assert kda.kda_chunk_fwd_workspace_size(4, 16384, 32, 128, 128) == 256 + 4 * 32 * 128 * 128 * 4
+    assert kda.kda_chunk_fwd_workspace_size(0, 0, 1, 64, 64) == 256
+    assert kda.kda_chunk_fwd_workspace_size(1, 10, 2, 96, 128) == 0
+    assert kda.kda_chunk_fwd_workspace_size(-1, 10, 2, 64, 128) == 0
+
+
+FAKE = 0x10000  # a 16-byte aligned non-null value; never dereferenced (the checks fail first)
+
+
+def _chunk(lib, **kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, g=FAKE, beta=FAKE, dtype=0, init=None, cu=None, N=1, T=64, H=2,
+             dk=128, dv=128, scale=1.0, o=FAKE, fs=FAKE, ws=FAKE, wsb=256, stream=None)
+    a.update(kw)
+    return lib.kda_chunk_fwd(a["q"], a["k"], a["v"], a["g"], a["beta"], a["dtype"], a["init"], a["cu"], a["N"],
+                             a["T"], a["H"], a["dk"], a["dv"], a["scale"], a["o"], a["fs"], a["ws"], a["wsb"],
+                             a["stream"])
+
+
+def test_chunk_fwd_host_errors(lib):
+    assert _chunk(lib, dk=96) == 2                       # UNSUPPORTED
+    assert _chunk(lib, dv=32) == 2
+    assert _chunk(lib, dtype=7) == 2
+    assert _chunk(lib, H=0) == 1                         # INVALID_ARGUMENT
+    assert _chunk(lib, N=-1) == 1
+    assert _chunk(lib, q=None) == 1
+    assert _chunk(lib, o=None) == 1
+    assert _chunk(lib, k=FAKE + 4) == 1                  # misaligned
+    assert _chunk(lib, beta=FAKE + 1) == 1               # bf16 beta must be 2-byte aligned
+    assert _chunk(lib, N=3, T=64) == 1                   # equal lengths need N | T
+    assert _chunk(lib, ws=None) == 3                     # WORKSPACE
+    assert _chunk(lib, wsb=255) == 3
+    assert _chunk(lib, fs=None, wsb=256) == 3            # no final_state: staging space needed
+    assert _chunk(lib, init=FAKE + 8) == 1
+
+
+def test_decode_and_replay_host_errors(lib):
+    d = lib.kda_decode_step
+    assert d(FAKE, FAKE, FAKE, FAKE, FAKE, 0, FAKE, 4, None, 2, 2, 128, 96, 1.0, FAKE, FAKE, 256, None) == 2
+    assert d(FAKE, FAKE, FAKE, FAKE, FAKE, 0, None, 4, None, 2, 2, 128, 128, 1.0, FAKE, FAKE, 256, None) == 1
+    assert d(FAKE, FAKE, FAKE, FAKE, FAKE, 0, FAKE, 1, None, 2, 2, 128, 128, 1.0, FAKE, FAKE, 256, None) == 1
+    assert d(FAKE, FAKE, FAKE, FAKE, FAKE, 0, FAKE, 4, None, 2, 2, 128, 128, 1.0, FAKE, FAKE, 100, None) == 3
+    r = lib.kda_replay
+    assert r(FAKE, 4, None, FAKE, FAKE, FAKE, FAKE, 0, None, 2, 8, 2, 128, 128, FAKE, 256, None) == 1
+    assert r(FAKE, 4, None, FAKE, FAKE, FAKE, FAKE, 1, FAKE, 2, 8, 2, 64, 48, FAKE, 256, None) == 2
+    assert r(FAKE, 1, None, FAKE, FAKE, FAKE, FAKE, 0, FAKE, 2, 8, 2, 128, 128, FAKE, 256, None) == 1
+    assert r(FAKE, 4, None, FAKE, FAKE, FAKE, FAKE, 0, FAKE, 2, 8, 2, 128, 128, None, 256, None) == 3
