@@ -63,7 +63,8 @@ kda_status kda_chunk_fwd(const void *q, const void *k, const void *v, const void
 
     uint32_t *status = static_cast<uint32_t *>(workspace);
     const int64_t fixed_len = cu_seqlens ? 0 : T_total / N;
-    const bool use_tc = kda::chunk_tc_supported(dk, dv, static_cast<int>(dtype));
+    // the tensor-core kernel addresses tokens with 32-bit TMA coordinates
+    const bool use_tc = kda::chunk_tc_supported(dk, dv, static_cast<int>(dtype)) && T_total <= 0x7fffffffLL;
     float *chunk_state = final_state
                              ? final_state
                              : reinterpret_cast<float *>(static_cast<char *>(workspace) + staging_offset());

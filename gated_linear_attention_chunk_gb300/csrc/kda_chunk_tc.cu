@@ -1,14 +1,638 @@
-// Chunked (64-token) KDA forward on tcgen05 tensor cores.  (Placeholder until
-// the kernel lands: reports the shape as unsupported so every prefill runs
-// through the token-sequential kernel.)
+// Chunked (64-token) KDA forward on tcgen05 tensor cores, bf16 inputs, dk = dv = 128.
+//
+// The recurrence is the gated delta rule with per-channel decay ("Kimi K3 on
+// Fireworks: Fast RL at frontier scale", KDA paragraph: chunk-parallel training
+// of linear attention whose compact recurrent state is updated with
+// channel-wise gating; the kernel fuses the chunk-local work and keeps the
+// state on chip so intermediates never touch HBM).  Unrolled over one chunk of
+// C = 64 tokens with state S (dk x dv) at the chunk start, alpha_r = exp(g_r),
+// A_r = prod_{j<=r} alpha_j (prefix products, per channel), A_C = A_63:
+//
+//   Kbar = K * A,  Qbar = scale * Q * A,  Ktil = K / A          (row-wise, per channel)
+//   M[r,i] = beta_r Kbar_r . Ktil_i  (i < r),   P[r,i] = Qbar_r . Ktil_i  (i <= r)
+//   T' = (I + M)^-1 Diag(beta),  W = T' Kbar,  Utl = T' V
+//   U = Utl - W S,   O = Qbar S + P U,   S <- Diag(A_C) (S + Ktil^T U)
+//
+// Every factor stays bounded except Ktil (<= 1/A_C); the kernel therefore
+// requires A_C >= 2^-100 per channel and chunk (checked; KDA_ERR_GATE_RANGE).
+//
+// One CTA per (sequence, head) walks its full chunks in order.  Warp roles:
+//   warp 0      TMA producer: q, k, g, v tiles (SW128) + beta, 2-stage ring
+//   warp 1      chain MMA issuer (and TMEM owner)
+//   warp 2      prep MMA issuer
+//   warps 4-7   chain group: U and state epilogues in TMEM, O to HBM
+//   warps 8-11  prep group: decay factors, M/P, T' = (I+M)^-1 Diag(beta), W
+// The prep group and its MMAs run one chunk ahead of the chain.  The state
+// lives in TMEM transposed (lane = value column j, column = channel c) as an
+// fp32 master plus a bf16 copy that feeds the next chunk's MMAs as the A
+// operand straight from TMEM.
+//
+// Every mbarrier wait is bounded (about one second); a wait that gives up sets
+// the timeout bit in the status word, and all roles drain and exit.
+#include <cuda.h>
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+#include <stdint.h>
 
 #include "kda_internal.h"
+#include "sm100_ptx.cuh"
 
 namespace kda {
+namespace {
 
-bool chunk_tc_supported(int, int, int) { return false; }
+using namespace ptx;
 
-cudaError_t launch_chunk_tc(const ChunkParams &, cudaStream_t) { return cudaErrorNotSupported; }
+constexpr int kC = 64;          // chunk length
+constexpr int kD = 128;         // dk = dv
+constexpr int kThreads = 384;   // 12 warps
+constexpr uint64_t kWaitNs = 1000000000ull;
+
+// dynamic shared memory map (offsets from a 1024-byte aligned base)
+constexpr uint32_t kStage = 65536;                 // per-stage: R (k|q, 32K), G (16K), V (16K)
+constexpr uint32_t OFF_R = 0, OFF_G = 32768, OFF_V = 49152;
+constexpr uint32_t OFF_W = 2 * kStage;             // 2 x 16K   W (MN-major: row = channel)
+constexpr uint32_t OFF_P = OFF_W + 2 * 16384;      // 2 x 8K    P (K-major: row = token)
+constexpr uint32_t OFF_TT = OFF_P + 2 * 8192;      // 8K        T' (K-major)
+constexpr uint32_t OFF_M = OFF_TT + 8192;          // fp32 64 x 65
+constexpr uint32_t OFF_T = OFF_M + 64 * 65 * 4;    // fp32 64 x 65
+constexpr uint32_t kDynSmem = OFF_T + 64 * 65 * 4 + 1024;
+constexpr int kLd = 65;                            // row stride of the fp32 M and T buffers
+
+// TMEM columns (512 allocated)
+constexpr uint32_t TM_S = 0, TM_SB = 128, TM_U = 192, TM_UB = 320, TM_O = 352, TM_PREP = 416;
+
+struct TcParams {
+    CUtensorMap tm_q, tm_k, tm_g, tm_v;
+    const __nv_bfloat16 *beta;
+    __nv_bfloat16 *o;
+    const int32_t *cu;
+    const float *init_state;
+    float *state_out;
+    uint32_t *status;
+    int64_t T_total, seq_len_fixed;
+    int N, H;
+    float scale;
+};
+
+// byte offset of 16-bit element (row, col) in a 128-byte-row tile with the 128B swizzle
+__device__ __forceinline__ uint32_t swz(int row, int col) {
+    return static_cast<uint32_t>(row * 128 + ((((col >> 3) ^ (row & 7)) << 4) | ((col & 7) << 1)));
+}
+__device__ __forceinline__ uint32_t chunk16(int row, int chunk) {
+    return static_cast<uint32_t>(row * 128 + ((chunk ^ (row & 7)) << 4));
+}
+__device__ __forceinline__ float ld_bf16(const uint8_t *base, uint32_t off) {
+    return __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(base + off));
+}
+__device__ __forceinline__ void st_bf16(uint8_t *base, uint32_t off, float v) {
+    *reinterpret_cast<__nv_bfloat16 *>(base + off) = __float2bfloat16_rn(v);
+}
+__device__ __forceinline__ void named_bar(int id, int n) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
+struct Ctl {
+    volatile int *abort;
+    uint32_t *status;
+};
+
+// Bounded wait that also stops early once another role has aborted.
+__device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, const Ctl &ctl) {
+    const uint64_t deadline = globaltimer_ns() + kWaitNs;
+    uint32_t spins = 0;
+    while (!mbar_try_wait(bar, parity)) {
+        if ((++spins & 63u) == 0) {
+            if (*ctl.abort) return false;
+            if (globaltimer_ns() > deadline) {
+                *ctl.abort = 1;
+                atomicOr(ctl.status, DEV_ERR_TIMEOUT);
+                return false;
+            }
+        }
+    }
+    return true;
+}
+
+// Wait taken by all 128 threads of a warpgroup: every thread waits, then the group
+// agrees through a named barrier and its own "first failed wait" index, so either
+// all threads go on or all stop (no thread is left alone at a later named
+// barrier).  `seq` counts this group's waits identically in every thread.
+__device__ __forceinline__ bool group_wait(uint64_t *bar, uint32_t parity, const Ctl &ctl, int *grp_fail, int bar_id,
+                                           int &seq) {
+    const int w = seq++;
+    if (!wait_bar(bar, parity, ctl)) atomicMin(grp_fail, w);
+    named_bar(bar_id, 128);
+    return *reinterpret_cast<volatile int *>(grp_fail) > w;
+}
+
+// Wait taken by lane 0 of a warp, result broadcast to the warp.
+__device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, const Ctl &ctl, int lane) {
+    int ok = 1;
+    if (lane == 0) ok = wait_bar(bar, parity, ctl) ? 1 : 0;
+    return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+
+__global__ void __launch_bounds__(kThreads, 1) kda_chunk_tc_kernel(const __grid_constant__ TcParams p) {
+    extern __shared__ uint8_t dsmem_raw[];
+    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(dsmem_raw) + 1023) & ~uintptr_t(1023));
+    __shared__ float s_beta[2][kC];
+    __shared__ float s_ac[2][kD];
+    __shared__ float s_x[16 * 48];
+    __shared__ uint64_t bar_full[2], bar_free[2], bar_prepdone[2];
+    __shared__ uint64_t bar_elem, bar_mma1, bar_tready, bar_mma2, bar_sready, bar_c1, bar_uready, bar_c3;
+    __shared__ uint64_t bar_drain[2];
+    __shared__ uint32_t s_tmem;
+    __shared__ int s_abort;
+    __shared__ int s_grp_fail[2];  // [0] prep group, [1] chain group
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int64_t pair = blockIdx.x;
+    const int n = static_cast<int>(pair / p.H), h = static_cast<int>(pair % p.H);
+    const int64_t H = p.H;
+
+    int64_t bos, eos;
+    if (p.cu) {
+        bos = p.cu[n];
+        eos = p.cu[n + 1];
+        bool ok = (bos >= 0) && (bos <= eos) && (eos <= p.T_total);
+        if (n == 0 && bos != 0) ok = false;
+        if (n == p.N - 1 && eos != p.T_total) ok = false;
+        if (!ok) {
+            if (tid == 0 && h == 0) atomicOr(p.status, DEV_ERR_SEQLENS);
+            return;
+        }
+    } else {
+        bos = static_cast<int64_t>(n) * p.seq_len_fixed;
+        eos = bos + p.seq_len_fixed;
+    }
+    const int nfull = static_cast<int>((eos - bos) / kC);
+    if (nfull == 0) return;
+
+    if (tid == 0) {
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&bar_full[s], 2);
+            mbar_init(&bar_free[s], 2);
+            mbar_init(&bar_prepdone[s], 1);
+        }
+        mbar_init(&bar_elem, 1);
+        mbar_init(&bar_mma1, 1);
+        mbar_init(&bar_tready, 1);
+        mbar_init(&bar_mma2, 1);
+        mbar_init(&bar_sready, 1);
+        mbar_init(&bar_c1, 1);
+        mbar_init(&bar_uready, 1);
+        mbar_init(&bar_c3, 1);
+        mbar_init(&bar_drain[0], 1);
+        mbar_init(&bar_drain[1], 1);
+        s_abort = 0;
+        s_grp_fail[0] = 0x7fffffff;
+        s_grp_fail[1] = 0x7fffffff;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(&s_tmem, 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = s_tmem;
+    const Ctl ctl{&s_abort, p.status};
+    const uint32_t sm_base = smem_u32(sm);
+
+    if (warp == 0) {
+        // ------------------------------------------------------------------ TMA producer
+        int issued[2] = {-1, -1};
+        for (int c = 0; c < nfull; ++c) {
+            const int s = c & 1;
+            if (c >= 2 && !warp_wait(&bar_free[s], ((c >> 1) - 1) & 1, ctl, lane)) break;
+            const int t0 = static_cast<int>(bos + static_cast<int64_t>(c) * kC);
+            uint8_t *st = sm + s * kStage;
+            if (lane == 0) {
+                mbar_arrive_expect_tx(&bar_full[s], kStage);
+                tma_load_3d(st + OFF_R + 0, &p.tm_k, 0, h, t0, &bar_full[s]);
+                tma_load_3d(st + OFF_R + 16384, &p.tm_k, 64, h, t0, &bar_full[s]);
+                tma_load_3d(st + OFF_R + 8192, &p.tm_q, 0, h, t0, &bar_full[s]);
+                tma_load_3d(st + OFF_R + 24576, &p.tm_q, 64, h, t0, &bar_full[s]);
+                tma_load_3d(st + OFF_G + 0, &p.tm_g, 0, h, t0, &bar_full[s]);
+                tma_load_3d(st + OFF_G + 8192, &p.tm_g, 64, h, t0, &bar_full[s]);
+                tma_load_3d(st + OFF_V + 0, &p.tm_v, 0, h, t0, &bar_full[s]);
+                tma_load_3d(st + OFF_V + 8192, &p.tm_v, 64, h, t0, &bar_full[s]);
+            }
+            issued[s] = c;
+            s_beta[s][lane] = __bfloat162float(p.beta[(static_cast<int64_t>(t0) + lane) * H + h]);
+            s_beta[s][lane + 32] = __bfloat162float(p.beta[(static_cast<int64_t>(t0) + lane + 32) * H + h]);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bar_full[s]);
+        }
+        // make sure no TMA copy is still landing in shared memory when the CTA exits
+        for (int s = 0; s < 2; ++s)
+            if (issued[s] >= 0) {
+                const uint64_t deadline = globaltimer_ns() + kWaitNs;
+                while (!mbar_try_wait(&bar_full[s], (issued[s] >> 1) & 1) && globaltimer_ns() < deadline) {
+                }
+            }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------------ chain MMA issuer
+        if (lane == 0) {
+            const uint32_t idU = idesc_bf16(128, 64, false, true, true);    // U -= S^T W  (W MN-major)
+            const uint32_t idO = idesc_bf16(128, 64, false, false);         // O  = S^T Qbar^T, += U^T P^T
+            const uint32_t idS = idesc_bf16(128, 128, false, true);         // S += U^T Ktil (Ktil MN-major)
+            bool ok = true;
+            for (int c = 0; c < nfull && ok; ++c) {
+                const int s = c & 1;
+                if (!wait_bar(&bar_prepdone[s], (c >> 1) & 1, ctl) || !wait_bar(&bar_sready, c & 1, ctl)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t st = sm_base + s * kStage;
+                const uint32_t w = sm_base + OFF_W + s * 16384;
+                const uint32_t pp = sm_base + OFF_P + s * 8192;
+                for (int ks = 0; ks < 8; ++ks)
+                    mma_bf16_ts(tmem + TM_U + 64 * s, tmem + TM_SB + 8 * ks, sdesc_sw128(w + ks * 2048, 8192, 1024),
+                                idU, 1u);
+                for (int ks = 0; ks < 8; ++ks)
+                    mma_bf16_ts(tmem + TM_O, tmem + TM_SB + 8 * ks,
+                                sdesc_sw128(st + OFF_R + 8192 + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024), idO,
+                                ks > 0 ? 1u : 0u);
+                mma_commit(&bar_c1);
+                if (!wait_bar(&bar_uready, c & 1, ctl)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                for (int ks = 0; ks < 4; ++ks)
+                    mma_bf16_ts(tmem + TM_O, tmem + TM_UB + 8 * ks, sdesc_sw128(pp + ks * 32, 16, 1024), idO, 1u);
+                for (int ks = 0; ks < 4; ++ks)
+                    mma_bf16_ts(tmem + TM_S, tmem + TM_UB + 8 * ks, sdesc_sw128(st + OFF_G + ks * 2048, 8192, 1024),
+                                idS, 1u);
+                mma_commit(&bar_c3);
+                mma_commit(&bar_free[s]);
+            }
+            // drain: every MMA this thread issued completes before the TMEM is freed
+            mma_commit(&bar_drain[0]);
+            const uint64_t deadline = globaltimer_ns() + kWaitNs;
+            while (!mbar_try_wait(&bar_drain[0], 0) && globaltimer_ns() < deadline) {
+            }
+        }
+    } else if (warp == 2) {
+        // ------------------------------------------------------------------ prep MMA issuer
+        if (lane == 0) {
+            const uint32_t id1 = idesc_bf16(128, 64, false, false);  // [Kbar; Qbar] Ktil^T
+            const uint32_t id2 = idesc_bf16(128, 64, true, false);   // Kbar^T T'^T, V^T T'^T (A MN-major)
+            for (int c = 0; c < nfull; ++c) {
+                const int s = c & 1;
+                const uint32_t st = sm_base + s * kStage;
+                if (!wait_bar(&bar_elem, c & 1, ctl)) break;
+                tc_fence_after();
+                for (int ks = 0; ks < 8; ++ks)
+                    mma_bf16_ss(tmem + TM_PREP,
+                                sdesc_sw128(st + OFF_R + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024),
+                                sdesc_sw128(st + OFF_G + (ks >> 2) * 8192 + (ks & 3) * 32, 16, 1024), id1,
+                                ks > 0 ? 1u : 0u);
+                mma_commit(&bar_mma1);
+                if (!wait_bar(&bar_tready, c & 1, ctl)) break;
+                tc_fence_after();
+                const uint32_t tt = sm_base + OFF_TT;
+                for (int ks = 0; ks < 4; ++ks)
+                    mma_bf16_ss(tmem + TM_PREP, sdesc_sw128(st + OFF_R + ks * 2048, 16384, 1024),
+                                sdesc_sw128(tt + ks * 32, 16, 1024), id2, ks > 0 ? 1u : 0u);
+                for (int ks = 0; ks < 4; ++ks)
+                    mma_bf16_ss(tmem + TM_U + 64 * s, sdesc_sw128(st + OFF_V + ks * 2048, 8192, 1024),
+                                sdesc_sw128(tt + ks * 32, 16, 1024), id2, ks > 0 ? 1u : 0u);
+                mma_commit(&bar_mma2);
+            }
+            mma_commit(&bar_drain[1]);
+            const uint64_t deadline = globaltimer_ns() + kWaitNs;
+            while (!mbar_try_wait(&bar_drain[1], 0) && globaltimer_ns() < deadline) {
+            }
+        }
+    } else if (warp >= 4 && warp < 8) {
+        // ------------------------------------------------------------------ chain group
+        const int j = tid - 128;                       // value column == TMEM lane
+        int gseq = 0;
+        const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+        const uint32_t tS = tmem + lane_base + TM_S, tSB = tmem + lane_base + TM_SB;
+        const float *s0 = p.init_state ? p.init_state + pair * kD * kD : nullptr;
+        for (int cc = 0; cc < kD; cc += 32) {
+            uint32_t a[16], b[16], pk[16];
+            for (int e = 0; e < 16; ++e) {
+                a[e] = __float_as_uint(s0 ? s0[(cc + e) * kD + j] : 0.f);
+                b[e] = __float_as_uint(s0 ? s0[(cc + 16 + e) * kD + j] : 0.f);
+            }
+            for (int e = 0; e < 8; ++e) {
+                pk[e] = pack_bf16x2(__uint_as_float(a[2 * e]), __uint_as_float(a[2 * e + 1]));
+                pk[8 + e] = pack_bf16x2(__uint_as_float(b[2 * e]), __uint_as_float(b[2 * e + 1]));
+            }
+            tmem_st16(tS + cc, a);
+            tmem_st16(tS + cc + 16, b);
+            tmem_st16(tSB + cc / 2, pk);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        named_bar(2, 128);
+        if (j == 0) mbar_arrive(&bar_sready);
+
+        for (int c = 0; c < nfull; ++c) {
+            const int s = c & 1;
+            // U (fp32 in TMEM) -> bf16 copy in TMEM, the A operand of P U and Ktil^T U
+            if (!group_wait(&bar_c1, c & 1, ctl, &s_grp_fail[1], 2, gseq)) break;
+            tc_fence_after();
+            {
+                uint32_t u[64], pk[32];
+                const uint32_t tU = tmem + lane_base + TM_U + 64 * s;
+                tmem_ld16(tU + 0, *reinterpret_cast<uint32_t(*)[16]>(&u[0]));
+                tmem_ld16(tU + 16, *reinterpret_cast<uint32_t(*)[16]>(&u[16]));
+                tmem_ld16(tU + 32, *reinterpret_cast<uint32_t(*)[16]>(&u[32]));
+                tmem_ld16(tU + 48, *reinterpret_cast<uint32_t(*)[16]>(&u[48]));
+                tmem_ld_wait();
+#pragma unroll
+                for (int e = 0; e < 32; ++e) pk[e] = pack_bf16x2(__uint_as_float(u[2 * e]), __uint_as_float(u[2 * e + 1]));
+                tmem_st16(tmem + lane_base + TM_UB, *reinterpret_cast<uint32_t(*)[16]>(&pk[0]));
+                tmem_st16(tmem + lane_base + TM_UB + 16, *reinterpret_cast<uint32_t(*)[16]>(&pk[16]));
+                tmem_st_wait();
+            }
+            tc_fence_before();
+            named_bar(2, 128);
+            if (j == 0) mbar_arrive(&bar_uready);
+
+            // state: S <- Diag(A_C)(S + Ktil^T U); bf16 copy; O -> HBM
+            if (!group_wait(&bar_c3, c & 1, ctl, &s_grp_fail[1], 2, gseq)) break;
+            tc_fence_after();
+            const bool last = (c == nfull - 1);
+            float *sout = p.state_out + pair * kD * kD;
+            for (int cc = 0; cc < kD; cc += 32) {
+                uint32_t a[16], b[16], pk[16];
+                tmem_ld16(tS + cc, a);
+                tmem_ld16(tS + cc + 16, b);
+                tmem_ld_wait();
+                for (int e = 0; e < 16; ++e) {
+                    a[e] = __float_as_uint(__uint_as_float(a[e]) * s_ac[s][cc + e]);
+                    b[e] = __float_as_uint(__uint_as_float(b[e]) * s_ac[s][cc + 16 + e]);
+                }
+                for (int e = 0; e < 8; ++e) {
+                    pk[e] = pack_bf16x2(__uint_as_float(a[2 * e]), __uint_as_float(a[2 * e + 1]));
+                    pk[8 + e] = pack_bf16x2(__uint_as_float(b[2 * e]), __uint_as_float(b[2 * e + 1]));
+                }
+                tmem_st16(tS + cc, a);
+                tmem_st16(tS + cc + 16, b);
+                tmem_st16(tSB + cc / 2, pk);
+                if (last) {
+                    for (int e = 0; e < 16; ++e) {
+                        sout[(cc + e) * kD + j] = __uint_as_float(a[e]);
+                        sout[(cc + 16 + e) * kD + j] = __uint_as_float(b[e]);
+                    }
+                }
+            }
+            {
+                const int64_t t0 = bos + static_cast<int64_t>(c) * kC;
+                __nv_bfloat16 *orow = p.o + (t0 * H + h) * kD + j;
+                for (int r0 = 0; r0 < kC; r0 += 16) {
+                    uint32_t ov[16];
+                    tmem_ld16(tmem + lane_base + TM_O + r0, ov);
+                    tmem_ld_wait();
+                    for (int e = 0; e < 16; ++e)
+                        orow[static_cast<int64_t>(r0 + e) * H * kD] = __float2bfloat16_rn(__uint_as_float(ov[e]));
+                }
+            }
+            tmem_st_wait();
+            tc_fence_before();
+            named_bar(2, 128);
+            if (j == 0) {
+                mbar_arrive(&bar_sready);
+                mbar_arrive(&bar_free[s]);
+            }
+        }
+    } else if (warp >= 8) {
+        // ------------------------------------------------------------------ prep group
+        const int pt = tid - 256;         // channel for the elementwise pass / TMEM lane
+        int gseq = 0;
+        const int wq = warp - 8;
+        const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
+        float *Mb = reinterpret_cast<float *>(sm + OFF_M);
+        float *Tb = reinterpret_cast<float *>(sm + OFF_T);
+        const float kMinDecay = 7.888609052210118e-31f;  // 2^-100
+        for (int c = 0; c < nfull; ++c) {
+            const int s = c & 1;
+            uint8_t *st = sm + s * kStage;
+            if (!group_wait(&bar_full[s], (c >> 1) & 1, ctl, &s_grp_fail[0], 1, gseq)) break;
+
+            // (1) decay factors and the scaled operand tiles, one channel per thread
+            {
+                const int ch = pt, kb = ch >> 6, cc = ch & 63;
+                uint8_t *Rk = st + OFF_R + kb * 16384;
+                uint8_t *Rq = Rk + 8192;
+                uint8_t *G = st + OFF_G + kb * 8192;
+                float a = 1.f;
+                const float sc = p.scale;
+#pragma unroll 4
+                for (int r = 0; r < kC; ++r) {
+                    const uint32_t off = swz(r, cc);
+                    const float alpha = __expf(ld_bf16(G, off));
+                    a = a * alpha;
+                    const float kv = ld_bf16(Rk, off);
+                    const float qv = ld_bf16(Rq, off);
+                    const float ainv = __frcp_rn(a);
+                    st_bf16(Rk, off, kv * a);
+                    st_bf16(Rq, off, qv * (sc * a));
+                    st_bf16(G, off, kv * ainv);
+                }
+                if (!(a >= kMinDecay)) atomicOr(p.status, DEV_ERR_GATE);
+                s_ac[s][ch] = a;
+            }
+            fence_proxy_async_smem();
+            named_bar(1, 128);
+            if (pt == 0) mbar_arrive(&bar_elem);
+
+            // (2) M (fp32, rows scaled by beta, strictly lower) and P (bf16, lower incl.)
+            if (!group_wait(&bar_mma1, c & 1, ctl, &s_grp_fail[0], 1, gseq)) break;
+            tc_fence_after();
+            {
+                uint32_t m[64];
+                const uint32_t tP = tmem + lane_base + TM_PREP;
+                tmem_ld16(tP + 0, *reinterpret_cast<uint32_t(*)[16]>(&m[0]));
+                tmem_ld16(tP + 16, *reinterpret_cast<uint32_t(*)[16]>(&m[16]));
+                tmem_ld16(tP + 32, *reinterpret_cast<uint32_t(*)[16]>(&m[32]));
+                tmem_ld16(tP + 48, *reinterpret_cast<uint32_t(*)[16]>(&m[48]));
+                tmem_ld_wait();
+                if (wq < 2) {
+                    const int r = pt;
+                    const float br = s_beta[s][r];
+#pragma unroll
+                    for (int i = 0; i < kC; ++i) Mb[r * kLd + i] = (i < r) ? br * __uint_as_float(m[i]) : 0.f;
+                } else {
+                    const int r = pt - 64;
+                    uint8_t *P = sm + OFF_P + s * 8192;
+#pragma unroll
+                    for (int q8 = 0; q8 < 8; ++q8) {
+                        uint4 v;
+                        uint32_t *vw = reinterpret_cast<uint32_t *>(&v);
+                        for (int e = 0; e < 4; ++e) {
+                            const int i0 = q8 * 8 + 2 * e;
+                            const float x0 = (i0 <= r) ? __uint_as_float(m[i0]) : 0.f;
+                            const float x1 = (i0 + 1 <= r) ? __uint_as_float(m[i0 + 1]) : 0.f;
+                            vw[e] = pack_bf16x2(x0, x1);
+                        }
+                        *reinterpret_cast<uint4 *>(P + chunk16(r, q8)) = v;
+                    }
+                }
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            named_bar(1, 128);
+
+            // (3) T = (I + M)^-1: 16x16 diagonal blocks by forward substitution ...
+            if (pt < 64) {
+                const int b = pt >> 4, m = pt & 15, R0 = 16 * b;
+                float x[16];
+#pragma unroll
+                for (int l = 0; l < 16; ++l) {
+                    float acc = 0.f;
+#pragma unroll
+                    for (int i = 0; i < l; ++i) acc = fmaf(Mb[(R0 + l) * kLd + R0 + i], x[i], acc);
+                    x[l] = (l < m) ? 0.f : ((l == m) ? 1.f : -acc);
+                }
+#pragma unroll
+                for (int l = 0; l < 16; ++l) Tb[(R0 + l) * kLd + R0 + m] = x[l];
+            }
+            named_bar(1, 128);
+            // ... then block rows a = 1..3: T[a, <a] = -D_a (M[a, <a] T[<a, <a])
+            for (int ab = 1; ab < 4; ++ab) {
+                const int wdt = 16 * ab;
+                for (int e = pt; e < 16 * wdt; e += 128) {
+                    const int l = e / wdt, col = e - l * wdt;
+                    float acc = 0.f;
+                    for (int k = col; k < wdt; ++k) acc = fmaf(Mb[(wdt + l) * kLd + k], Tb[k * kLd + col], acc);
+                    s_x[l * 48 + col] = acc;
+                }
+                named_bar(1, 128);
+                for (int e = pt; e < 16 * wdt; e += 128) {
+                    const int l = e / wdt, col = e - l * wdt;
+                    float acc = 0.f;
+                    for (int q = 0; q <= l; ++q) acc = fmaf(Tb[(wdt + l) * kLd + wdt + q], s_x[q * 48 + col], acc);
+                    Tb[(wdt + l) * kLd + col] = -acc;
+                }
+                named_bar(1, 128);
+            }
+            // T' = T Diag(beta) -> bf16, K-major rows r
+            {
+                const int r = pt >> 1, half = pt & 1;
+                uint8_t *TT = sm + OFF_TT;
+                for (int q8 = 0; q8 < 4; ++q8) {
+                    const int c0 = half * 32 + q8 * 8;
+                    uint4 v;
+                    uint32_t *vw = reinterpret_cast<uint32_t *>(&v);
+                    for (int e = 0; e < 4; ++e) {
+                        const int i0 = c0 + 2 * e;
+                        const float x0 = (i0 <= r) ? Tb[r * kLd + i0] * s_beta[s][i0] : 0.f;
+                        const float x1 = (i0 + 1 <= r) ? Tb[r * kLd + i0 + 1] * s_beta[s][i0 + 1] : 0.f;
+                        vw[e] = pack_bf16x2(x0, x1);
+                    }
+                    *reinterpret_cast<uint4 *>(TT + chunk16(r, c0 >> 3)) = v;
+                }
+            }
+            fence_proxy_async_smem();
+            named_bar(1, 128);
+            if (pt == 0) mbar_arrive(&bar_tready);
+
+            // (4) W^T (lane = channel) -> bf16 W tile, MN-major (row = channel, 64 tokens)
+            if (!group_wait(&bar_mma2, c & 1, ctl, &s_grp_fail[0], 1, gseq)) break;
+            tc_fence_after();
+            {
+                uint32_t wv[64];
+                const uint32_t tP = tmem + lane_base + TM_PREP;
+                tmem_ld16(tP + 0, *reinterpret_cast<uint32_t(*)[16]>(&wv[0]));
+                tmem_ld16(tP + 16, *reinterpret_cast<uint32_t(*)[16]>(&wv[16]));
+                tmem_ld16(tP + 32, *reinterpret_cast<uint32_t(*)[16]>(&wv[32]));
+                tmem_ld16(tP + 48, *reinterpret_cast<uint32_t(*)[16]>(&wv[48]));
+                tmem_ld_wait();
+                uint8_t *W = sm + OFF_W + s * 16384;
+                const int ch = pt;
+#pragma unroll
+                for (int q8 = 0; q8 < 8; ++q8) {
+                    uint4 v;
+                    uint32_t *vw = reinterpret_cast<uint32_t *>(&v);
+                    for (int e = 0; e < 4; ++e)
+                        vw[e] = pack_bf16x2(__uint_as_float(wv[q8 * 8 + 2 * e]), __uint_as_float(wv[q8 * 8 + 2 * e + 1]));
+                    *reinterpret_cast<uint4 *>(W + chunk16(ch, q8)) = v;
+                }
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            named_bar(1, 128);
+            if (pt == 0) mbar_arrive(&bar_prepdone[s]);
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 get_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        cudaDriverEntryPointQueryResult q;
+        void *ptr = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    }
+    return fn;
+}
+
+// [T, H, 128] bf16 tensor, 64 x 64 boxes with the 128-byte swizzle.
+bool encode_tile_map(CUtensorMap *map, const void *base, int64_t T, int H) {
+    auto enc = get_encoder();
+    if (!enc) return false;
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(T)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(kD) * 2, static_cast<cuuint64_t>(H) * kD * 2};
+    cuuint32_t box[3] = {64, 1, 64};
+    cuuint32_t es[3] = {1, 1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+bool chunk_tc_supported(int dk, int dv, int dtype) { return dk == 128 && dv == 128 && dtype == 0; }
+
+cudaError_t launch_chunk_tc(const ChunkParams &cp, cudaStream_t stream) {
+    if (!chunk_tc_supported(128, 128, 0)) return cudaErrorNotSupported;
+    const int64_t blocks = static_cast<int64_t>(cp.N) * cp.H;
+    if (blocks <= 0 || cp.T_total <= 0) return cudaSuccess;
+    if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    TcParams p{};
+    if (!encode_tile_map(&p.tm_q, cp.q, cp.T_total, cp.H) || !encode_tile_map(&p.tm_k, cp.k, cp.T_total, cp.H) ||
+        !encode_tile_map(&p.tm_g, cp.g, cp.T_total, cp.H) || !encode_tile_map(&p.tm_v, cp.v, cp.T_total, cp.H))
+        return cudaErrorInvalidValue;
+    p.beta = static_cast<const __nv_bfloat16 *>(cp.beta);
+    p.o = static_cast<__nv_bfloat16 *>(cp.o);
+    p.cu = cp.cu;
+    p.init_state = cp.init_state;
+    p.state_out = cp.state_out;
+    p.status = cp.status;
+    p.T_total = cp.T_total;
+    p.seq_len_fixed = cp.seq_len_fixed;
+    p.N = cp.N;
+    p.H = cp.H;
+    p.scale = cp.scale;
+    static bool attr_set = false;
+    if (!attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(kda_chunk_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(kDynSmem));
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    kda_chunk_tc_kernel<<<static_cast<unsigned>(blocks), kThreads, kDynSmem, stream>>>(p);
+    return cudaGetLastError();
+}
 
 }  // namespace kda
