@@ -54,10 +54,12 @@ constexpr uint32_t OFF_R = 0, OFF_G = 32768, OFF_V = 49152;
 constexpr uint32_t OFF_W = 2 * kStage;             // 2 x 16K   W (MN-major: row = channel)
 constexpr uint32_t OFF_P = OFF_W + 2 * 16384;      // 2 x 8K    P (K-major: row = token)
 constexpr uint32_t OFF_TT = OFF_P + 2 * 8192;      // 8K        T' (K-major)
-constexpr uint32_t OFF_M = OFF_TT + 8192;          // fp32 64 x 65
-constexpr uint32_t OFF_T = OFF_M + 64 * 65 * 4;    // fp32 64 x 65
-constexpr uint32_t kDynSmem = OFF_T + 64 * 65 * 4 + 1024;
-constexpr int kLd = 65;                            // row stride of the fp32 M and T buffers
+constexpr int kLdM = 65;                           // row stride (floats) of the fp32 M buffer
+constexpr int kLdT = 68;                           // row stride of the fp32 T buffer (16-byte rows)
+constexpr int kLdX = 36;                           // row stride of the block-product scratch
+constexpr uint32_t OFF_M = OFF_TT + 8192;          // fp32 64 x kLdM
+constexpr uint32_t OFF_T = OFF_M + 64 * kLdM * 4;  // fp32 64 x kLdT
+constexpr uint32_t kDynSmem = OFF_T + 64 * kLdT * 4 + 1024;
 
 // TMEM columns (512 allocated)
 constexpr uint32_t TM_S = 0, TM_SB = 128, TM_U = 192, TM_UB = 320, TM_O = 352, TM_PREP = 416;
@@ -88,6 +90,21 @@ __device__ __forceinline__ float ld_bf16(const uint8_t *base, uint32_t off) {
 __device__ __forceinline__ void st_bf16(uint8_t *base, uint32_t off, float v) {
     *reinterpret_cast<__nv_bfloat16 *>(base + off) = __float2bfloat16_rn(v);
 }
+__device__ __forceinline__ uint32_t ld32(const uint8_t *base, uint32_t off) {
+    return *reinterpret_cast<const uint32_t *>(base + off);
+}
+__device__ __forceinline__ void st32(uint8_t *base, uint32_t off, uint32_t v) {
+    *reinterpret_cast<uint32_t *>(base + off) = v;
+}
+__device__ __forceinline__ float2 bf2_to_f2(uint32_t w) {
+    return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w));
+}
+__device__ __forceinline__ float4 fma4(float a, float4 b, float4 c) {
+    return make_float4(fmaf(a, b.x, c.x), fmaf(a, b.y, c.y), fmaf(a, b.z, c.z), fmaf(a, b.w, c.w));
+}
+__device__ __forceinline__ float4 ld4(const float *p) { return *reinterpret_cast<const float4 *>(p); }
+__device__ __forceinline__ void st4(float *p, float4 v) { *reinterpret_cast<float4 *>(p) = v; }
+__device__ __forceinline__ float4 neg4(float4 v) { return make_float4(-v.x, -v.y, -v.z, -v.w); }
 __device__ __forceinline__ void named_bar(int id, int n) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
@@ -136,9 +153,10 @@ __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, const 
 __global__ void __launch_bounds__(kThreads, 1) kda_chunk_tc_kernel(const __grid_constant__ TcParams p) {
     extern __shared__ uint8_t dsmem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(dsmem_raw) + 1023) & ~uintptr_t(1023));
-    __shared__ float s_beta[2][kC];
+    __shared__ __align__(16) float s_beta[2][kC];
     __shared__ float s_ac[2][kD];
-    __shared__ float s_x[16 * 48];
+    __shared__ __align__(16) float s_x[32 * kLdX];
+    __shared__ float s_tot[kD];
     __shared__ uint64_t bar_full[2], bar_free[2], bar_prepdone[2];
     __shared__ uint64_t bar_elem, bar_mma1, bar_tready, bar_mma2, bar_sready, bar_c1, bar_uready, bar_c3;
     __shared__ uint64_t bar_drain[2];
@@ -414,33 +432,71 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_tc_kernel(const __grid_
         float *Mb = reinterpret_cast<float *>(sm + OFF_M);
         float *Tb = reinterpret_cast<float *>(sm + OFF_T);
         const float kMinDecay = 7.888609052210118e-31f;  // 2^-100
+        for (int i = pt; i < 64 * kLdT; i += 128) Tb[i] = 0.f;  // blocks above the diagonal stay zero
+        named_bar(1, 128);
         for (int c = 0; c < nfull; ++c) {
             const int s = c & 1;
             uint8_t *st = sm + s * kStage;
             if (!group_wait(&bar_full[s], (c >> 1) & 1, ctl, &s_grp_fail[0], 1, gseq)) break;
 
-            // (1) decay factors and the scaled operand tiles, one channel per thread
+            // (1) decay factors and the scaled operand tiles.  Thread = (token half,
+            // channel pair): alpha = exp(g), prefix products A within the half, the
+            // first half's totals carried into the second, then Kbar, Qbar, Ktil.
             {
-                const int ch = pt, kb = ch >> 6, cc = ch & 63;
+                const int cp = pt & 63, half = pt >> 6;
+                const int kb = cp >> 5, cc = 2 * (cp & 31), ch = kb * 64 + cc;
                 uint8_t *Rk = st + OFF_R + kb * 16384;
                 uint8_t *Rq = Rk + 8192;
                 uint8_t *G = st + OFF_G + kb * 8192;
-                float a = 1.f;
-                const float sc = p.scale;
-#pragma unroll 4
-                for (int r = 0; r < kC; ++r) {
-                    const uint32_t off = swz(r, cc);
-                    const float alpha = __expf(ld_bf16(G, off));
-                    a = a * alpha;
-                    const float kv = ld_bf16(Rk, off);
-                    const float qv = ld_bf16(Rq, off);
-                    const float ainv = __frcp_rn(a);
-                    st_bf16(Rk, off, kv * a);
-                    st_bf16(Rq, off, qv * (sc * a));
-                    st_bf16(G, off, kv * ainv);
+                const int r0 = 32 * half;
+                float A0[32], A1[32];
+                float p0 = 1.f, p1 = 1.f;
+#pragma unroll
+                for (int rr = 0; rr < 32; rr += 8) {
+                    uint32_t gw[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) gw[e] = ld32(G, swz(r0 + rr + e, cc));
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const float2 gf = bf2_to_f2(gw[e]);
+                        p0 *= __expf(gf.x);
+                        p1 *= __expf(gf.y);
+                        A0[rr + e] = p0;
+                        A1[rr + e] = p1;
+                    }
                 }
-                if (!(a >= kMinDecay)) atomicOr(p.status, DEV_ERR_GATE);
-                s_ac[s][ch] = a;
+                if (half == 0) {
+                    s_tot[ch] = p0;
+                    s_tot[ch + 1] = p1;
+                }
+                named_bar(1, 128);
+                const float m0 = half ? s_tot[ch] : 1.f, m1 = half ? s_tot[ch + 1] : 1.f;
+                const float sc = p.scale;
+#pragma unroll
+                for (int rr = 0; rr < 32; rr += 8) {
+                    uint32_t kw[8], qw[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const uint32_t off = swz(r0 + rr + e, cc);
+                        kw[e] = ld32(Rk, off);
+                        qw[e] = ld32(Rq, off);
+                    }
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const uint32_t off = swz(r0 + rr + e, cc);
+                        const float a0 = m0 * A0[rr + e], a1 = m1 * A1[rr + e];
+                        const float2 kf = bf2_to_f2(kw[e]), qf = bf2_to_f2(qw[e]);
+                        st32(Rk, off, pack_bf16x2(kf.x * a0, kf.y * a1));
+                        st32(Rq, off, pack_bf16x2(qf.x * (sc * a0), qf.y * (sc * a1)));
+                        st32(G, off, pack_bf16x2(kf.x * __fdividef(1.f, a0), kf.y * __fdividef(1.f, a1)));
+                    }
+                }
+                if (half == 1) {
+                    const float ac0 = m0 * p0, ac1 = m1 * p1;
+                    if (!(ac0 >= kMinDecay) || !(ac1 >= kMinDecay)) atomicOr(p.status, DEV_ERR_GATE);
+                    s_ac[s][ch] = ac0;
+                    s_ac[s][ch + 1] = ac1;
+                }
             }
             fence_proxy_async_smem();
             named_bar(1, 128);
@@ -461,7 +517,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_tc_kernel(const __grid_
                     const int r = pt;
                     const float br = s_beta[s][r];
 #pragma unroll
-                    for (int i = 0; i < kC; ++i) Mb[r * kLd + i] = (i < r) ? br * __uint_as_float(m[i]) : 0.f;
+                    for (int i = 0; i < kC; ++i) Mb[r * kLdM + i] = (i < r) ? br * __uint_as_float(m[i]) : 0.f;
                 } else {
                     const int r = pt - 64;
                     uint8_t *P = sm + OFF_P + s * 8192;
@@ -483,7 +539,8 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_tc_kernel(const __grid_
             tc_fence_before();
             named_bar(1, 128);
 
-            // (3) T = (I + M)^-1: 16x16 diagonal blocks by forward substitution ...
+            // (3) T = (I + M)^-1, blocked: the four 16x16 diagonal blocks D_b by forward
+            // substitution (thread = block, column) ...
             if (pt < 64) {
                 const int b = pt >> 4, m = pt & 15, R0 = 16 * b;
                 float x[16];
@@ -491,45 +548,71 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_tc_kernel(const __grid_
                 for (int l = 0; l < 16; ++l) {
                     float acc = 0.f;
 #pragma unroll
-                    for (int i = 0; i < l; ++i) acc = fmaf(Mb[(R0 + l) * kLd + R0 + i], x[i], acc);
+                    for (int i = 0; i < l; ++i) acc = fmaf(Mb[(R0 + l) * kLdM + R0 + i], x[i], acc);
                     x[l] = (l < m) ? 0.f : ((l == m) ? 1.f : -acc);
                 }
 #pragma unroll
-                for (int l = 0; l < 16; ++l) Tb[(R0 + l) * kLd + R0 + m] = x[l];
+                for (int l = 0; l < 16; ++l) Tb[(R0 + l) * kLdT + R0 + m] = x[l];
             }
             named_bar(1, 128);
-            // ... then block rows a = 1..3: T[a, <a] = -D_a (M[a, <a] T[<a, <a])
-            for (int ab = 1; ab < 4; ++ab) {
-                const int wdt = 16 * ab;
-                for (int e = pt; e < 16 * wdt; e += 128) {
-                    const int l = e / wdt, col = e - l * wdt;
-                    float acc = 0.f;
-                    for (int k = col; k < wdt; ++k) acc = fmaf(Mb[(wdt + l) * kLd + k], Tb[k * kLd + col], acc);
-                    s_x[l * 48 + col] = acc;
-                }
+            // ... the sub-diagonal blocks T[a][a-1] = -D_a M[a][a-1] D_{a-1} for a = 1, 3 ...
+            {
+                const int pr = pt >> 6, u = pt & 63, l = u >> 2, c0 = (u & 3) * 4;
+                const int Ra = 16 + 32 * pr, Rb = Ra - 16;
+                float *X = s_x + pr * 16 * kLdX;
+                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                for (int k = 0; k < 16; ++k)
+                    acc = fma4(Mb[(Ra + l) * kLdM + Rb + k], ld4(&Tb[(Rb + k) * kLdT + Rb + c0]), acc);
+                st4(&X[l * kLdX + c0], acc);
                 named_bar(1, 128);
-                for (int e = pt; e < 16 * wdt; e += 128) {
-                    const int l = e / wdt, col = e - l * wdt;
-                    float acc = 0.f;
-                    for (int q = 0; q <= l; ++q) acc = fmaf(Tb[(wdt + l) * kLd + wdt + q], s_x[q * 48 + col], acc);
-                    Tb[(wdt + l) * kLd + col] = -acc;
-                }
-                named_bar(1, 128);
+                float4 out = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                for (int q = 0; q < 16; ++q) out = fma4(Tb[(Ra + l) * kLdT + Ra + q], ld4(&X[q * kLdX + c0]), out);
+                st4(&Tb[(Ra + l) * kLdT + Rb + c0], neg4(out));
             }
-            // T' = T Diag(beta) -> bf16, K-major rows r
+            named_bar(1, 128);
+            // ... and the lower-left quadrant T[32:64, 0:32] = -T22 (M[32:64, 0:32] T11),
+            // T11 = T[0:32, 0:32], T22 = T[32:64, 32:64] (their upper-right blocks are zero).
+            {
+                const int l0 = (pt >> 3) * 2, c0 = (pt & 7) * 4;
+                float4 a0 = make_float4(0.f, 0.f, 0.f, 0.f), a1 = a0;
+#pragma unroll
+                for (int k = 0; k < 32; ++k) {
+                    const float4 t = ld4(&Tb[k * kLdT + c0]);
+                    a0 = fma4(Mb[(32 + l0) * kLdM + k], t, a0);
+                    a1 = fma4(Mb[(33 + l0) * kLdM + k], t, a1);
+                }
+                st4(&s_x[l0 * kLdX + c0], a0);
+                st4(&s_x[(l0 + 1) * kLdX + c0], a1);
+                named_bar(1, 128);
+                float4 b0 = make_float4(0.f, 0.f, 0.f, 0.f), b1 = b0;
+#pragma unroll
+                for (int q = 0; q < 32; ++q) {
+                    const float4 xv = ld4(&s_x[q * kLdX + c0]);
+                    b0 = fma4(Tb[(32 + l0) * kLdT + 32 + q], xv, b0);
+                    b1 = fma4(Tb[(33 + l0) * kLdT + 32 + q], xv, b1);
+                }
+                st4(&Tb[(32 + l0) * kLdT + c0], neg4(b0));
+                st4(&Tb[(33 + l0) * kLdT + c0], neg4(b1));
+            }
+            named_bar(1, 128);
+            // T' = T Diag(beta) -> bf16, K-major rows r (entries above the diagonal are zero)
             {
                 const int r = pt >> 1, half = pt & 1;
                 uint8_t *TT = sm + OFF_TT;
+#pragma unroll
                 for (int q8 = 0; q8 < 4; ++q8) {
                     const int c0 = half * 32 + q8 * 8;
+                    const float4 t0 = ld4(&Tb[r * kLdT + c0]), t1 = ld4(&Tb[r * kLdT + c0 + 4]);
+                    const float4 b0 = ld4(&s_beta[s][c0]), b1 = ld4(&s_beta[s][c0 + 4]);
+                    const float tv[8] = {t0.x * b0.x, t0.y * b0.y, t0.z * b0.z, t0.w * b0.w,
+                                         t1.x * b1.x, t1.y * b1.y, t1.z * b1.z, t1.w * b1.w};
                     uint4 v;
                     uint32_t *vw = reinterpret_cast<uint32_t *>(&v);
-                    for (int e = 0; e < 4; ++e) {
-                        const int i0 = c0 + 2 * e;
-                        const float x0 = (i0 <= r) ? Tb[r * kLd + i0] * s_beta[s][i0] : 0.f;
-                        const float x1 = (i0 + 1 <= r) ? Tb[r * kLd + i0 + 1] * s_beta[s][i0 + 1] : 0.f;
-                        vw[e] = pack_bf16x2(x0, x1);
-                    }
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        vw[e] = pack_bf16x2(c0 + 2 * e <= r ? tv[2 * e] : 0.f, c0 + 2 * e + 1 <= r ? tv[2 * e + 1] : 0.f);
                     *reinterpret_cast<uint4 *>(TT + chunk16(r, c0 >> 3)) = v;
                 }
             }
