@@ -20,9 +20,11 @@
 //   warp 0      TMA producer: q, k, g, v tiles (SW128) + beta, 2-stage ring
 //   warp 1      chain MMA issuer (and TMEM owner)
 //   warp 2      prep MMA issuer
-//   warps 4-7   chain group: U and state epilogues in TMEM, O to HBM
-//   warps 8-11  prep group: decay factors, M/P, T' = (I+M)^-1 Diag(beta), W
-// The prep group and its MMAs run one chunk ahead of the chain.  The state
+//   warps 4-7   chain group: W tile from W^T, U and state epilogues in TMEM, O to HBM
+//   warps 8-15  prep group: decay factors, M/P, T' = (I+M)^-1 Diag(beta)
+// The prep group and its MMAs run one chunk ahead of the chain; the chain group
+// turns each chunk's W^T accumulator into the W tile, so the prep group goes on
+// to the next chunk as soon as T' is written.  The state
 // lives in TMEM transposed (lane = value column j, column = channel c) as an
 // fp32 master plus a bf16 copy that feeds the next chunk's MMAs as the A
 // operand straight from TMEM.
@@ -45,7 +47,8 @@ using namespace ptx;
 
 constexpr int kC = 64;          // chunk length
 constexpr int kD = 128;         // dk = dv
-constexpr int kThreads = 384;   // 12 warps
+constexpr int kThreads = 512;   // 16 warps
+constexpr int kPrep = 256;      // prep group: warps 8-15
 constexpr uint64_t kWaitNs = 1000000000ull;
 
 // dynamic shared memory map (offsets from a 1024-byte aligned base)
@@ -131,15 +134,15 @@ __device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, const C
     return true;
 }
 
-// Wait taken by all 128 threads of a warpgroup: every thread waits, then the group
+// Wait taken by all threads of a group: every thread waits, then the group
 // agrees through a named barrier and its own "first failed wait" index, so either
 // all threads go on or all stop (no thread is left alone at a later named
 // barrier).  `seq` counts this group's waits identically in every thread.
 __device__ __forceinline__ bool group_wait(uint64_t *bar, uint32_t parity, const Ctl &ctl, int *grp_fail, int bar_id,
-                                           int &seq) {
+                                           int nthreads, int &seq) {
     const int w = seq++;
     if (!wait_bar(bar, parity, ctl)) atomicMin(grp_fail, w);
-    named_bar(bar_id, 128);
+    named_bar(bar_id, nthreads);
     return *reinterpret_cast<volatile int *>(grp_fail) > w;
 }
 
@@ -156,9 +159,9 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_tc_kernel(const __grid_
     __shared__ __align__(16) float s_beta[2][kC];
     __shared__ float s_ac[2][kD];
     __shared__ __align__(16) float s_x[32 * kLdX];
-    __shared__ float s_tot[kD];
-    __shared__ uint64_t bar_full[2], bar_free[2], bar_prepdone[2];
-    __shared__ uint64_t bar_elem, bar_mma1, bar_tready, bar_mma2, bar_sready, bar_c1, bar_uready, bar_c3;
+    __shared__ float s_tot[4][kD];
+    __shared__ uint64_t bar_full[2], bar_free[2];
+    __shared__ uint64_t bar_elem, bar_mma1, bar_tready, bar_mma2, bar_ready, bar_wfree, bar_c1, bar_uready, bar_c3;
     __shared__ uint64_t bar_drain[2];
     __shared__ uint32_t s_tmem;
     __shared__ int s_abort;
@@ -191,13 +194,13 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_tc_kernel(const __grid_
         for (int s = 0; s < 2; ++s) {
             mbar_init(&bar_full[s], 2);
             mbar_init(&bar_free[s], 2);
-            mbar_init(&bar_prepdone[s], 1);
         }
         mbar_init(&bar_elem, 1);
         mbar_init(&bar_mma1, 1);
         mbar_init(&bar_tready, 1);
         mbar_init(&bar_mma2, 1);
-        mbar_init(&bar_sready, 1);
+        mbar_init(&bar_ready, 1);
+        mbar_init(&bar_wfree, 1);
         mbar_init(&bar_c1, 1);
         mbar_init(&bar_uready, 1);
         mbar_init(&bar_c3, 1);
@@ -257,13 +260,9 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_tc_kernel(const __grid_
             const uint32_t idU = idesc_bf16(128, 64, false, true, true);    // U -= S^T W  (W MN-major)
             const uint32_t idO = idesc_bf16(128, 64, false, false);         // O  = S^T Qbar^T, += U^T P^T
             const uint32_t idS = idesc_bf16(128, 128, false, true);         // S += U^T Ktil (Ktil MN-major)
-            bool ok = true;
-            for (int c = 0; c < nfull && ok; ++c) {
+            for (int c = 0; c < nfull; ++c) {
                 const int s = c & 1;
-                if (!wait_bar(&bar_prepdone[s], (c >> 1) & 1, ctl) || !wait_bar(&bar_sready, c & 1, ctl)) {
-                    ok = false;
-                    break;
-                }
+                if (!wait_bar(&bar_ready, c & 1, ctl)) break;
                 tc_fence_after();
                 const uint32_t st = sm_base + s * kStage;
                 const uint32_t w = sm_base + OFF_W + s * 16384;
@@ -276,10 +275,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_tc_kernel(const __grid_
                                 sdesc_sw128(st + OFF_R + 8192 + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024), idO,
                                 ks > 0 ? 1u : 0u);
                 mma_commit(&bar_c1);
-                if (!wait_bar(&bar_uready, c & 1, ctl)) {
-                    ok = false;
-                    break;
-                }
+                if (!wait_bar(&bar_uready, c & 1, ctl)) break;
                 tc_fence_after();
                 for (int ks = 0; ks < 4; ++ks)
                     mma_bf16_ts(tmem + TM_O, tmem + TM_UB + 8 * ks, sdesc_sw128(pp + ks * 32, 16, 1024), idO, 1u);
@@ -304,6 +300,8 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_tc_kernel(const __grid_
                 const int s = c & 1;
                 const uint32_t st = sm_base + s * kStage;
                 if (!wait_bar(&bar_elem, c & 1, ctl)) break;
+                // W^T of the previous chunk must have left the PREP columns
+                if (c > 0 && !wait_bar(&bar_wfree, (c - 1) & 1, ctl)) break;
                 tc_fence_after();
                 for (int ks = 0; ks < 8; ++ks)
                     mma_bf16_ss(tmem + TM_PREP,
@@ -329,17 +327,19 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_tc_kernel(const __grid_
         }
     } else if (warp >= 4 && warp < 8) {
         // ------------------------------------------------------------------ chain group
-        const int j = tid - 128;                       // value column == TMEM lane
+        const int j = tid - 128;  // TMEM lane: value column j (state, U, O); channel j (W^T)
         int gseq = 0;
         const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
         const uint32_t tS = tmem + lane_base + TM_S, tSB = tmem + lane_base + TM_SB;
         const float *s0 = p.init_state ? p.init_state + pair * kD * kD : nullptr;
         for (int cc = 0; cc < kD; cc += 32) {
             uint32_t a[16], b[16], pk[16];
+#pragma unroll
             for (int e = 0; e < 16; ++e) {
                 a[e] = __float_as_uint(s0 ? s0[(cc + e) * kD + j] : 0.f);
                 b[e] = __float_as_uint(s0 ? s0[(cc + 16 + e) * kD + j] : 0.f);
             }
+#pragma unroll
             for (int e = 0; e < 8; ++e) {
                 pk[e] = pack_bf16x2(__uint_as_float(a[2 * e]), __uint_as_float(a[2 * e + 1]));
                 pk[8 + e] = pack_bf16x2(__uint_as_float(b[2 * e]), __uint_as_float(b[2 * e + 1]));
@@ -349,35 +349,86 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_tc_kernel(const __grid_
             tmem_st16(tSB + cc / 2, pk);
         }
         tmem_st_wait();
-        tc_fence_before();
-        named_bar(2, 128);
-        if (j == 0) mbar_arrive(&bar_sready);
 
+        uint32_t opk[32];          // previous chunk's O row block, bf16 pairs (r, r+1)
+        int64_t o_t0 = -1;
+        auto store_o = [&](int64_t t0) {
+            __nv_bfloat16 *orow = p.o + (t0 * H + h) * kD + j;
+            const int64_t rs = H * kD;
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+                const __nv_bfloat162 v = *reinterpret_cast<const __nv_bfloat162 *>(&opk[e]);
+                orow[(2 * e) * rs] = v.x;
+                orow[(2 * e + 1) * rs] = v.y;
+            }
+        };
+        bool done = true;
         for (int c = 0; c < nfull; ++c) {
             const int s = c & 1;
-            // U (fp32 in TMEM) -> bf16 copy in TMEM, the A operand of P U and Ktil^T U
-            if (!group_wait(&bar_c1, c & 1, ctl, &s_grp_fail[1], 2, gseq)) break;
+            // W^T (lane = channel) -> bf16 W tile, MN-major (row = channel, 64 tokens)
+            if (!group_wait(&bar_mma2, c & 1, ctl, &s_grp_fail[1], 2, 128, gseq)) {
+                done = false;
+                break;
+            }
             tc_fence_after();
             {
-                uint32_t u[64], pk[32];
-                const uint32_t tU = tmem + lane_base + TM_U + 64 * s;
-                tmem_ld16(tU + 0, *reinterpret_cast<uint32_t(*)[16]>(&u[0]));
-                tmem_ld16(tU + 16, *reinterpret_cast<uint32_t(*)[16]>(&u[16]));
-                tmem_ld16(tU + 32, *reinterpret_cast<uint32_t(*)[16]>(&u[32]));
-                tmem_ld16(tU + 48, *reinterpret_cast<uint32_t(*)[16]>(&u[48]));
-                tmem_ld_wait();
+                uint8_t *W = sm + OFF_W + s * 16384;
+                const uint32_t tP = tmem + lane_base + TM_PREP;
 #pragma unroll
-                for (int e = 0; e < 32; ++e) pk[e] = pack_bf16x2(__uint_as_float(u[2 * e]), __uint_as_float(u[2 * e + 1]));
-                tmem_st16(tmem + lane_base + TM_UB, *reinterpret_cast<uint32_t(*)[16]>(&pk[0]));
-                tmem_st16(tmem + lane_base + TM_UB + 16, *reinterpret_cast<uint32_t(*)[16]>(&pk[16]));
+                for (int hf = 0; hf < 2; ++hf) {
+                    uint32_t wv[32];
+                    tmem_ld16(tP + 32 * hf, *reinterpret_cast<uint32_t(*)[16]>(&wv[0]));
+                    tmem_ld16(tP + 32 * hf + 16, *reinterpret_cast<uint32_t(*)[16]>(&wv[16]));
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int q8 = 0; q8 < 4; ++q8) {
+                        uint4 v;
+                        uint32_t *vw = reinterpret_cast<uint32_t *>(&v);
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            vw[e] = pack_bf16x2(__uint_as_float(wv[q8 * 8 + 2 * e]), __uint_as_float(wv[q8 * 8 + 2 * e + 1]));
+                        *reinterpret_cast<uint4 *>(W + chunk16(j, 4 * hf + q8)) = v;
+                    }
+                }
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            named_bar(2, 128);
+            if (j == 0) {
+                mbar_arrive(&bar_ready);   // W(c) written and the state of chunk c-1 final
+                mbar_arrive(&bar_wfree);   // PREP columns may take the next chunk's M/P
+            }
+            if (o_t0 >= 0) store_o(o_t0);  // previous chunk's O while C1 runs
+
+            // U (fp32 in TMEM) -> bf16 copy in TMEM, the A operand of P U and Ktil^T U
+            if (!group_wait(&bar_c1, c & 1, ctl, &s_grp_fail[1], 2, 128, gseq)) {
+                done = false;
+                break;
+            }
+            tc_fence_after();
+            {
+                const uint32_t tU = tmem + lane_base + TM_U + 64 * s;
+#pragma unroll
+                for (int hf = 0; hf < 2; ++hf) {
+                    uint32_t u[32], pk[16];
+                    tmem_ld16(tU + 32 * hf, *reinterpret_cast<uint32_t(*)[16]>(&u[0]));
+                    tmem_ld16(tU + 32 * hf + 16, *reinterpret_cast<uint32_t(*)[16]>(&u[16]));
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) pk[e] = pack_bf16x2(__uint_as_float(u[2 * e]), __uint_as_float(u[2 * e + 1]));
+                    tmem_st16(tmem + lane_base + TM_UB + 16 * hf, pk);
+                }
                 tmem_st_wait();
             }
             tc_fence_before();
             named_bar(2, 128);
             if (j == 0) mbar_arrive(&bar_uready);
 
-            // state: S <- Diag(A_C)(S + Ktil^T U); bf16 copy; O -> HBM
-            if (!group_wait(&bar_c3, c & 1, ctl, &s_grp_fail[1], 2, gseq)) break;
+            // state: S <- Diag(A_C)(S + Ktil^T U) with its bf16 copy; O into registers
+            if (!group_wait(&bar_c3, c & 1, ctl, &s_grp_fail[1], 2, 128, gseq)) {
+                done = false;
+                break;
+            }
             tc_fence_after();
             const bool last = (c == nfull - 1);
             float *sout = p.state_out + pair * kD * kD;
@@ -386,10 +437,12 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_tc_kernel(const __grid_
                 tmem_ld16(tS + cc, a);
                 tmem_ld16(tS + cc + 16, b);
                 tmem_ld_wait();
+#pragma unroll
                 for (int e = 0; e < 16; ++e) {
                     a[e] = __float_as_uint(__uint_as_float(a[e]) * s_ac[s][cc + e]);
                     b[e] = __float_as_uint(__uint_as_float(b[e]) * s_ac[s][cc + 16 + e]);
                 }
+#pragma unroll
                 for (int e = 0; e < 8; ++e) {
                     pk[e] = pack_bf16x2(__uint_as_float(a[2 * e]), __uint_as_float(a[2 * e + 1]));
                     pk[8 + e] = pack_bf16x2(__uint_as_float(b[2 * e]), __uint_as_float(b[2 * e + 1]));
@@ -398,61 +451,58 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_tc_kernel(const __grid_
                 tmem_st16(tS + cc + 16, b);
                 tmem_st16(tSB + cc / 2, pk);
                 if (last) {
+#pragma unroll
                     for (int e = 0; e < 16; ++e) {
                         sout[(cc + e) * kD + j] = __uint_as_float(a[e]);
                         sout[(cc + 16 + e) * kD + j] = __uint_as_float(b[e]);
                     }
                 }
             }
-            {
-                const int64_t t0 = bos + static_cast<int64_t>(c) * kC;
-                __nv_bfloat16 *orow = p.o + (t0 * H + h) * kD + j;
-                for (int r0 = 0; r0 < kC; r0 += 16) {
-                    uint32_t ov[16];
-                    tmem_ld16(tmem + lane_base + TM_O + r0, ov);
-                    tmem_ld_wait();
-                    for (int e = 0; e < 16; ++e)
-                        orow[static_cast<int64_t>(r0 + e) * H * kD] = __float2bfloat16_rn(__uint_as_float(ov[e]));
-                }
+#pragma unroll
+            for (int r0 = 0; r0 < kC; r0 += 32) {
+                uint32_t ov[32];
+                tmem_ld16(tmem + lane_base + TM_O + r0, *reinterpret_cast<uint32_t(*)[16]>(&ov[0]));
+                tmem_ld16(tmem + lane_base + TM_O + r0 + 16, *reinterpret_cast<uint32_t(*)[16]>(&ov[16]));
+                tmem_ld_wait();
+#pragma unroll
+                for (int e = 0; e < 16; ++e)
+                    opk[r0 / 2 + e] = pack_bf16x2(__uint_as_float(ov[2 * e]), __uint_as_float(ov[2 * e + 1]));
             }
+            o_t0 = bos + static_cast<int64_t>(c) * kC;
             tmem_st_wait();
             tc_fence_before();
             named_bar(2, 128);
-            if (j == 0) {
-                mbar_arrive(&bar_sready);
-                mbar_arrive(&bar_free[s]);
-            }
+            if (j == 0) mbar_arrive(&bar_free[s]);
         }
+        if (done && o_t0 >= 0) store_o(o_t0);
     } else if (warp >= 8) {
-        // ------------------------------------------------------------------ prep group
-        const int pt = tid - 256;         // channel for the elementwise pass / TMEM lane
+        // ------------------------------------------------------------------ prep group (8 warps)
+        const int pt = tid - 256;
         int gseq = 0;
-        const int wq = warp - 8;
-        const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
         float *Mb = reinterpret_cast<float *>(sm + OFF_M);
         float *Tb = reinterpret_cast<float *>(sm + OFF_T);
         const float kMinDecay = 7.888609052210118e-31f;  // 2^-100
-        for (int i = pt; i < 64 * kLdT; i += 128) Tb[i] = 0.f;  // blocks above the diagonal stay zero
-        named_bar(1, 128);
+        for (int i = pt; i < 64 * kLdT; i += kPrep) Tb[i] = 0.f;  // blocks above the diagonal stay zero
+        named_bar(1, kPrep);
         for (int c = 0; c < nfull; ++c) {
             const int s = c & 1;
             uint8_t *st = sm + s * kStage;
-            if (!group_wait(&bar_full[s], (c >> 1) & 1, ctl, &s_grp_fail[0], 1, gseq)) break;
+            if (!group_wait(&bar_full[s], (c >> 1) & 1, ctl, &s_grp_fail[0], 1, kPrep, gseq)) break;
 
-            // (1) decay factors and the scaled operand tiles.  Thread = (token half,
-            // channel pair): alpha = exp(g), prefix products A within the half, the
-            // first half's totals carried into the second, then Kbar, Qbar, Ktil.
+            // (1) decay factors and the scaled operand tiles.  Thread = (token quarter,
+            // channel pair): alpha = exp(g), prefix products within the quarter, the
+            // earlier quarters' totals carried in, then Kbar, Qbar, Ktil in place.
             {
-                const int cp = pt & 63, half = pt >> 6;
+                const int cp = pt & 63, qt = pt >> 6;
                 const int kb = cp >> 5, cc = 2 * (cp & 31), ch = kb * 64 + cc;
                 uint8_t *Rk = st + OFF_R + kb * 16384;
                 uint8_t *Rq = Rk + 8192;
                 uint8_t *G = st + OFF_G + kb * 8192;
-                const int r0 = 32 * half;
-                float A0[32], A1[32];
+                const int r0 = 16 * qt;
+                float A0[16], A1[16];
                 float p0 = 1.f, p1 = 1.f;
 #pragma unroll
-                for (int rr = 0; rr < 32; rr += 8) {
+                for (int rr = 0; rr < 16; rr += 8) {
                     uint32_t gw[8];
 #pragma unroll
                     for (int e = 0; e < 8; ++e) gw[e] = ld32(G, swz(r0 + rr + e, cc));
@@ -465,15 +515,17 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_tc_kernel(const __grid_
                         A1[rr + e] = p1;
                     }
                 }
-                if (half == 0) {
-                    s_tot[ch] = p0;
-                    s_tot[ch + 1] = p1;
+                s_tot[qt][ch] = p0;
+                s_tot[qt][ch + 1] = p1;
+                named_bar(1, kPrep);
+                float m0 = 1.f, m1 = 1.f;
+                for (int q = 0; q < qt; ++q) {
+                    m0 *= s_tot[q][ch];
+                    m1 *= s_tot[q][ch + 1];
                 }
-                named_bar(1, 128);
-                const float m0 = half ? s_tot[ch] : 1.f, m1 = half ? s_tot[ch + 1] : 1.f;
                 const float sc = p.scale;
 #pragma unroll
-                for (int rr = 0; rr < 32; rr += 8) {
+                for (int rr = 0; rr < 16; rr += 8) {
                     uint32_t kw[8], qw[8];
 #pragma unroll
                     for (int e = 0; e < 8; ++e) {
@@ -491,7 +543,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_tc_kernel(const __grid_
                         st32(G, off, pack_bf16x2(kf.x * __fdividef(1.f, a0), kf.y * __fdividef(1.f, a1)));
                     }
                 }
-                if (half == 1) {
+                if (qt == 3) {
                     const float ac0 = m0 * p0, ac1 = m1 * p1;
                     if (!(ac0 >= kMinDecay) || !(ac1 >= kMinDecay)) atomicOr(p.status, DEV_ERR_GATE);
                     s_ac[s][ch] = ac0;
@@ -499,111 +551,116 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_tc_kernel(const __grid_
                 }
             }
             fence_proxy_async_smem();
-            named_bar(1, 128);
+            named_bar(1, kPrep);
             if (pt == 0) mbar_arrive(&bar_elem);
 
-            // (2) M (fp32, rows scaled by beta, strictly lower) and P (bf16, lower incl.)
-            if (!group_wait(&bar_mma1, c & 1, ctl, &s_grp_fail[0], 1, gseq)) break;
+            // (2) M (fp32, rows scaled by beta, strictly lower) and P (bf16, lower incl.).
+            // Accumulator lane x: rows 0-63 = Kbar . Ktil, 64-127 = Qbar . Ktil; two warps
+            // per lane quarter split the 64 columns.
+            if (!group_wait(&bar_mma1, c & 1, ctl, &s_grp_fail[0], 1, kPrep, gseq)) break;
             tc_fence_after();
             {
-                uint32_t m[64];
-                const uint32_t tP = tmem + lane_base + TM_PREP;
-                tmem_ld16(tP + 0, *reinterpret_cast<uint32_t(*)[16]>(&m[0]));
+                const int wq = pt >> 5, quarter = wq & 3, ch2 = wq >> 2;
+                const int x = quarter * 32 + lane;
+                uint32_t m[32];
+                const uint32_t tP = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + TM_PREP + 32 * ch2;
+                tmem_ld16(tP, *reinterpret_cast<uint32_t(*)[16]>(&m[0]));
                 tmem_ld16(tP + 16, *reinterpret_cast<uint32_t(*)[16]>(&m[16]));
-                tmem_ld16(tP + 32, *reinterpret_cast<uint32_t(*)[16]>(&m[32]));
-                tmem_ld16(tP + 48, *reinterpret_cast<uint32_t(*)[16]>(&m[48]));
                 tmem_ld_wait();
-                if (wq < 2) {
-                    const int r = pt;
+                if (x < 64) {
+                    const int r = x;
                     const float br = s_beta[s][r];
 #pragma unroll
-                    for (int i = 0; i < kC; ++i) Mb[r * kLdM + i] = (i < r) ? br * __uint_as_float(m[i]) : 0.f;
+                    for (int i = 0; i < 32; ++i) {
+                        const int col = 32 * ch2 + i;
+                        Mb[r * kLdM + col] = (col < r) ? br * __uint_as_float(m[i]) : 0.f;
+                    }
                 } else {
-                    const int r = pt - 64;
+                    const int r = x - 64;
                     uint8_t *P = sm + OFF_P + s * 8192;
 #pragma unroll
-                    for (int q8 = 0; q8 < 8; ++q8) {
+                    for (int q8 = 0; q8 < 4; ++q8) {
                         uint4 v;
                         uint32_t *vw = reinterpret_cast<uint32_t *>(&v);
+#pragma unroll
                         for (int e = 0; e < 4; ++e) {
-                            const int i0 = q8 * 8 + 2 * e;
-                            const float x0 = (i0 <= r) ? __uint_as_float(m[i0]) : 0.f;
-                            const float x1 = (i0 + 1 <= r) ? __uint_as_float(m[i0 + 1]) : 0.f;
+                            const int i0 = 32 * ch2 + q8 * 8 + 2 * e;
+                            const float x0 = (i0 <= r) ? __uint_as_float(m[q8 * 8 + 2 * e]) : 0.f;
+                            const float x1 = (i0 + 1 <= r) ? __uint_as_float(m[q8 * 8 + 2 * e + 1]) : 0.f;
                             vw[e] = pack_bf16x2(x0, x1);
                         }
-                        *reinterpret_cast<uint4 *>(P + chunk16(r, q8)) = v;
+                        *reinterpret_cast<uint4 *>(P + chunk16(r, 4 * ch2 + q8)) = v;
                     }
                 }
             }
             fence_proxy_async_smem();
             tc_fence_before();
-            named_bar(1, 128);
+            named_bar(1, kPrep);
 
             // (3) T = (I + M)^-1, blocked: the four 16x16 diagonal blocks D_b by forward
             // substitution (thread = block, column) ...
             if (pt < 64) {
-                const int b = pt >> 4, m = pt & 15, R0 = 16 * b;
-                float x[16];
+                const int b = pt >> 4, mm = pt & 15, R0 = 16 * b;
+                float xv[16];
 #pragma unroll
                 for (int l = 0; l < 16; ++l) {
                     float acc = 0.f;
 #pragma unroll
-                    for (int i = 0; i < l; ++i) acc = fmaf(Mb[(R0 + l) * kLdM + R0 + i], x[i], acc);
-                    x[l] = (l < m) ? 0.f : ((l == m) ? 1.f : -acc);
+                    for (int i = 0; i < l; ++i) acc = fmaf(Mb[(R0 + l) * kLdM + R0 + i], xv[i], acc);
+                    xv[l] = (l < mm) ? 0.f : ((l == mm) ? 1.f : -acc);
                 }
 #pragma unroll
-                for (int l = 0; l < 16; ++l) Tb[(R0 + l) * kLdT + R0 + m] = x[l];
+                for (int l = 0; l < 16; ++l) Tb[(R0 + l) * kLdT + R0 + mm] = xv[l];
             }
-            named_bar(1, 128);
+            named_bar(1, kPrep);
             // ... the sub-diagonal blocks T[a][a-1] = -D_a M[a][a-1] D_{a-1} for a = 1, 3 ...
             {
-                const int pr = pt >> 6, u = pt & 63, l = u >> 2, c0 = (u & 3) * 4;
+                const int pr = pt >> 7, u = pt & 127, l = u >> 3, c0 = (u & 7) * 2;
                 const int Ra = 16 + 32 * pr, Rb = Ra - 16;
                 float *X = s_x + pr * 16 * kLdX;
-                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+                float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
-                for (int k = 0; k < 16; ++k)
-                    acc = fma4(Mb[(Ra + l) * kLdM + Rb + k], ld4(&Tb[(Rb + k) * kLdT + Rb + c0]), acc);
-                st4(&X[l * kLdX + c0], acc);
-                named_bar(1, 128);
-                float4 out = make_float4(0.f, 0.f, 0.f, 0.f);
+                for (int k = 0; k < 16; ++k) {
+                    const float mv = Mb[(Ra + l) * kLdM + Rb + k];
+                    const float2 t = *reinterpret_cast<const float2 *>(&Tb[(Rb + k) * kLdT + Rb + c0]);
+                    acc.x = fmaf(mv, t.x, acc.x);
+                    acc.y = fmaf(mv, t.y, acc.y);
+                }
+                *reinterpret_cast<float2 *>(&X[l * kLdX + c0]) = acc;
+                named_bar(1, kPrep);
+                float2 out = make_float2(0.f, 0.f);
 #pragma unroll
-                for (int q = 0; q < 16; ++q) out = fma4(Tb[(Ra + l) * kLdT + Ra + q], ld4(&X[q * kLdX + c0]), out);
-                st4(&Tb[(Ra + l) * kLdT + Rb + c0], neg4(out));
+                for (int q = 0; q < 16; ++q) {
+                    const float dv = Tb[(Ra + l) * kLdT + Ra + q];
+                    const float2 xq = *reinterpret_cast<const float2 *>(&X[q * kLdX + c0]);
+                    out.x = fmaf(dv, xq.x, out.x);
+                    out.y = fmaf(dv, xq.y, out.y);
+                }
+                *reinterpret_cast<float2 *>(&Tb[(Ra + l) * kLdT + Rb + c0]) = make_float2(-out.x, -out.y);
             }
-            named_bar(1, 128);
+            named_bar(1, kPrep);
             // ... and the lower-left quadrant T[32:64, 0:32] = -T22 (M[32:64, 0:32] T11),
             // T11 = T[0:32, 0:32], T22 = T[32:64, 32:64] (their upper-right blocks are zero).
             {
-                const int l0 = (pt >> 3) * 2, c0 = (pt & 7) * 4;
-                float4 a0 = make_float4(0.f, 0.f, 0.f, 0.f), a1 = a0;
+                const int l = pt >> 3, c0 = (pt & 7) * 4;
+                float4 a0 = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-                for (int k = 0; k < 32; ++k) {
-                    const float4 t = ld4(&Tb[k * kLdT + c0]);
-                    a0 = fma4(Mb[(32 + l0) * kLdM + k], t, a0);
-                    a1 = fma4(Mb[(33 + l0) * kLdM + k], t, a1);
-                }
-                st4(&s_x[l0 * kLdX + c0], a0);
-                st4(&s_x[(l0 + 1) * kLdX + c0], a1);
-                named_bar(1, 128);
-                float4 b0 = make_float4(0.f, 0.f, 0.f, 0.f), b1 = b0;
+                for (int k = 0; k < 32; ++k) a0 = fma4(Mb[(32 + l) * kLdM + k], ld4(&Tb[k * kLdT + c0]), a0);
+                st4(&s_x[l * kLdX + c0], a0);
+                named_bar(1, kPrep);
+                float4 b0 = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-                for (int q = 0; q < 32; ++q) {
-                    const float4 xv = ld4(&s_x[q * kLdX + c0]);
-                    b0 = fma4(Tb[(32 + l0) * kLdT + 32 + q], xv, b0);
-                    b1 = fma4(Tb[(33 + l0) * kLdT + 32 + q], xv, b1);
-                }
-                st4(&Tb[(32 + l0) * kLdT + c0], neg4(b0));
-                st4(&Tb[(33 + l0) * kLdT + c0], neg4(b1));
+                for (int q = 0; q < 32; ++q) b0 = fma4(Tb[(32 + l) * kLdT + 32 + q], ld4(&s_x[q * kLdX + c0]), b0);
+                st4(&Tb[(32 + l) * kLdT + c0], neg4(b0));
             }
-            named_bar(1, 128);
+            named_bar(1, kPrep);
             // T' = T Diag(beta) -> bf16, K-major rows r (entries above the diagonal are zero)
             {
-                const int r = pt >> 1, half = pt & 1;
+                const int r = pt >> 2;
                 uint8_t *TT = sm + OFF_TT;
 #pragma unroll
-                for (int q8 = 0; q8 < 4; ++q8) {
-                    const int c0 = half * 32 + q8 * 8;
+                for (int hq = 0; hq < 2; ++hq) {
+                    const int c0 = ((pt & 3) * 2 + hq) * 8;
                     const float4 t0 = ld4(&Tb[r * kLdT + c0]), t1 = ld4(&Tb[r * kLdT + c0 + 4]);
                     const float4 b0 = ld4(&s_beta[s][c0]), b1 = ld4(&s_beta[s][c0 + 4]);
                     const float tv[8] = {t0.x * b0.x, t0.y * b0.y, t0.z * b0.z, t0.w * b0.w,
@@ -617,35 +674,8 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_tc_kernel(const __grid_
                 }
             }
             fence_proxy_async_smem();
-            named_bar(1, 128);
+            named_bar(1, kPrep);
             if (pt == 0) mbar_arrive(&bar_tready);
-
-            // (4) W^T (lane = channel) -> bf16 W tile, MN-major (row = channel, 64 tokens)
-            if (!group_wait(&bar_mma2, c & 1, ctl, &s_grp_fail[0], 1, gseq)) break;
-            tc_fence_after();
-            {
-                uint32_t wv[64];
-                const uint32_t tP = tmem + lane_base + TM_PREP;
-                tmem_ld16(tP + 0, *reinterpret_cast<uint32_t(*)[16]>(&wv[0]));
-                tmem_ld16(tP + 16, *reinterpret_cast<uint32_t(*)[16]>(&wv[16]));
-                tmem_ld16(tP + 32, *reinterpret_cast<uint32_t(*)[16]>(&wv[32]));
-                tmem_ld16(tP + 48, *reinterpret_cast<uint32_t(*)[16]>(&wv[48]));
-                tmem_ld_wait();
-                uint8_t *W = sm + OFF_W + s * 16384;
-                const int ch = pt;
-#pragma unroll
-                for (int q8 = 0; q8 < 8; ++q8) {
-                    uint4 v;
-                    uint32_t *vw = reinterpret_cast<uint32_t *>(&v);
-                    for (int e = 0; e < 4; ++e)
-                        vw[e] = pack_bf16x2(__uint_as_float(wv[q8 * 8 + 2 * e]), __uint_as_float(wv[q8 * 8 + 2 * e + 1]));
-                    *reinterpret_cast<uint4 *>(W + chunk16(ch, q8)) = v;
-                }
-            }
-            fence_proxy_async_smem();
-            tc_fence_before();
-            named_bar(1, 128);
-            if (pt == 0) mbar_arrive(&bar_prepdone[s]);
         }
     }
 
