@@ -48,6 +48,8 @@ _SIGS = {
     "kda_status_string": (ctypes.c_char_p, [_int]),
     "kda_version": (_int, []),
     "kda_chunk_fwd_uses_tensor_cores": (_int, [_int, _int, _int]),
+    "kda_chunk_fwd_noalloc": (_int, [_vp, _vp, _vp, _vp, _vp, _int, _vp, _vp, _int, _i64, _int, _int, _int,
+                                     ctypes.c_float, _vp, _vp, ctypes.POINTER(ctypes.c_void_p), _vp]),
 }
 
 _lib = None
@@ -182,6 +184,34 @@ def kda_chunk_fwd(q, k, v, g, beta, cu_seqlens=None, init_state=None, scale: flo
     return o, final_state
 
 
+def kda_chunk_fwd_noalloc(q, k, v, g, beta, o, cu_seqlens=None, init_state=None, final_state=None,
+                          scale: float = 1.0, stream=None) -> int:
+    """kda_chunk_fwd without a workspace: the library's fixed device scratch is used
+    instead, for callers that cannot allocate.  ``o`` (and ``final_state`` when wanted)
+    must be passed in.  Returns the scratch's device address, which
+    ``kda_device_status`` accepts."""
+    lib = load_library()
+    dt = q.dtype
+    T, H, dk = q.shape
+    dv = v.shape[2]
+    for name, t, shp in (("q", q, (T, H, dk)), ("k", k, (T, H, dk)), ("v", v, (T, H, dv)),
+                         ("g", g, (T, H, dk)), ("beta", beta, (T, H)), ("o", o, (T, H, dv))):
+        _need(t, name, dt, shp)
+    N = 1 if cu_seqlens is None else cu_seqlens.numel() - 1
+    if cu_seqlens is not None:
+        _need(cu_seqlens, "cu_seqlens", torch.int32)
+    if init_state is not None:
+        _need(init_state, "init_state", torch.float32, (N, H, dk, dv))
+    if final_state is not None:
+        _need(final_state, "final_state", torch.float32, (N, H, dk, dv))
+    ws = ctypes.c_void_p()
+    rc = lib.kda_chunk_fwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _dtype_code(q),
+                                   _ptr(init_state), _ptr(cu_seqlens), N, T, H, dk, dv, float(scale), _ptr(o),
+                                   _ptr(final_state), ctypes.byref(ws), _stream_handle(stream))
+    _check(rc, "kda_chunk_fwd_noalloc")
+    return int(ws.value)
+
+
 def kda_decode_step(q, k, v, g, beta, state_pool, slots=None, scale: float = 1.0, o=None, workspace=None,
                     stream=None) -> torch.Tensor:
     """One token per sequence; updates ``state_pool`` [S, H, dk, dv] in place.  Returns o [N, H, dv]."""
@@ -235,5 +265,7 @@ def kda_replay(state_pool, k, v, g, beta, cu_accept, slots=None, workspace=None,
 
 
 def kda_device_status(workspace, stream=None) -> int:
-    """Synchronize the stream and return the device status code of the last call on ``workspace``."""
-    return int(load_library().kda_device_status(_ptr(workspace), _stream_handle(stream)))
+    """Synchronize the stream and return the device status code of the last call on ``workspace``
+    (a tensor, or a raw device address such as the one kda_chunk_fwd_noalloc returns)."""
+    ptr = ctypes.c_void_p(workspace) if isinstance(workspace, int) else _ptr(workspace)
+    return int(load_library().kda_device_status(ptr, _stream_handle(stream)))

@@ -151,6 +151,38 @@ kda_status kda_replay(float *state_pool, int64_t num_slots, const int32_t *slots
  */
 kda_status kda_device_status(const void *workspace, void *stream);
 
+/* Size of the library-owned scratch behind kda_chunk_fwd_noalloc: the status
+ * header plus staging room for 128 states of 128 x 128 fp32 (8 MiB). */
+#define KDA_NOALLOC_WORKSPACE_BYTES ((size_t)KDA_WS_HEADER_BYTES + (size_t)8 * 1024 * 1024)
+
+/*
+ * kda_chunk_fwd for callers that cannot allocate device memory.  The pages
+ * have no counterpart to this call: it exists for hosts that plan every device
+ * byte themselves and give plug-in kernels no workspace hook, and for
+ * latency-critical loops where a cudaMalloc (which can synchronize the device)
+ * is not allowed.  It computes exactly what kda_chunk_fwd computes, with the
+ * same arguments minus the workspace, and calls no allocator.
+ *
+ * Scratch: one array of KDA_NOALLOC_WORKSPACE_BYTES in the library's own
+ * device memory; every GPU that loads libkda holds it until the process exits.
+ * - The first call on a device (with that device current) looks up the
+ *   array's device address; make that first call before any stream capture.
+ * - Every call shares the array: calls that could run at the same time on the
+ *   GPU (other streams, other host threads on the same device) race on it and
+ *   must be serialized by the caller.  The status word is cleared by each call.
+ * - With final_state != NULL only the 256-byte header is used and any size is
+ *   accepted.  With final_state == NULL the states are staged in the array, so
+ *   N*H*dk*dv*4 must not exceed 8 MiB; larger requests return
+ *   KDA_ERR_WORKSPACE and launch nothing.
+ *
+ *   status_workspace  optional out: receives the array's device address, which
+ *                     kda_device_status() accepts to read this call's status.
+ */
+kda_status kda_chunk_fwd_noalloc(const void *q, const void *k, const void *v, const void *g, const void *beta,
+                                 kda_dtype dtype, const float *init_state, const int32_t *cu_seqlens, int N,
+                                 int64_t T_total, int H, int dk, int dv, float scale, void *o, float *final_state,
+                                 const void **status_workspace, void *stream);
+
 /*
  * 1 if kda_chunk_fwd runs its full 64-token chunks on the tensor-core (tcgen05)
  * kernel for this shape and dtype, 0 if every token goes through the
