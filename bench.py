@@ -230,6 +230,43 @@ def config_dict(args, case):
                   else "L2 flushed between steps"}
 
 
+def measure_state_kernels(kda, dev, hbm_peak, n_seq=128, H=32, d=128, reps=50):
+    """Achieved HBM bandwidth of kda_decode_step and kda_replay on a pool of n_seq x H
+    128x128 fp32 states (256 MiB, larger than L2): the state read + write per call is the
+    algorithmic traffic; replay applies 4 accepted tokens per sequence."""
+    pool = torch.randn(n_seq, H, d, d, device=dev) * 0.02
+    q, k, v, g, b = (x.to(dev) for x in workloads.make_decode_tokens(4 * n_seq, H, d, d, torch.bfloat16, seed=77))
+    ws = kda.new_workspace(kda.KDA_WS_HEADER_BYTES, dev)
+    o = torch.empty(n_seq, H, d, dtype=torch.bfloat16, device=dev)
+    cu = torch.arange(0, 4 * n_seq + 1, 4, dtype=torch.int32, device=dev)
+    state_bytes = 2 * pool.numel() * 4
+    out = {}
+    for name in ("decode", "replay"):
+        def call():
+            if name == "decode":
+                kda.kda_decode_step(q[:n_seq], k[:n_seq], v[:n_seq], g[:n_seq], b[:n_seq], pool, o=o, workspace=ws)
+            else:
+                kda.kda_replay(pool, k, v, g, b, cu, workspace=ws)
+        for _ in range(3):
+            call()
+        torch.cuda.synchronize()
+        st = torch.cuda.current_stream()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(st)
+        for _ in range(reps):
+            call()
+        e1.record(st)
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / reps
+        tok_bytes = (n_seq if name == "decode" else 4 * n_seq) * H * (4 * d * 2 + 2)
+        gbs = (state_bytes + tok_bytes) / (ms / 1e3) / 1e9
+        out[name] = {"ms_per_call": ms, "achieved_GBs": gbs, "frac_of_hbm": gbs / hbm_peak,
+                     "states": n_seq * H, "tokens_per_seq": 1 if name == "decode" else 4}
+    if kda.kda_device_status(ws) != kda.KDA_OK:
+        raise RuntimeError("decode/replay device status")
+    return out
+
+
 def run_gpu(args, world, rank, local):
     import gated_linear_attention_chunk_gb300 as kda
 
@@ -360,6 +397,8 @@ def run_gpu(args, world, rank, local):
                  "timing": "median per-step CUDA-event time of kda_chunk_fwd (includes the status-word memset"
                            " and the partial-chunk launch)"})
 
+    state_kernels = measure_state_kernels(kda, dev, hbm_peak) if not args.no_state_kernels else None
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = oracle_sample_rate(case, budget_s=args.ref_budget)
@@ -370,7 +409,7 @@ def run_gpu(args, world, rank, local):
                 "vs_baseline": None, "dtype": "bf16" if q.dtype == torch.bfloat16 else "f32",
                 "data": "synthetic", "config": config_dict(args, case), "roofline": roof,
                 "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches_per_step * args.steps,
-                "clocks": clk}
+                "clocks": clk, "state_kernels": state_kernels}
         print(json.dumps(line), flush=True)
     if distributed:
         dist.destroy_process_group()
@@ -380,12 +419,13 @@ def run_gpu(args, world, rank, local):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["libkda", "reference"], default="libkda")
     ap.add_argument("--workload", default="prefill_4k", choices=sorted(workloads.NAMED_WORKLOADS))
     ap.add_argument("--ref-budget", type=float, default=10.0, help="seconds of oracle work per sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-state-kernels", action="store_true", help="skip the decode/replay bandwidth check")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

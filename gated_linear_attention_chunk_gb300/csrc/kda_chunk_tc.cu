@@ -17,17 +17,16 @@
 // requires A_C >= 2^-100 per channel and chunk (checked; KDA_ERR_GATE_RANGE).
 //
 // One CTA per (sequence, head) walks its full chunks in order.  Warp roles:
-//   warp 0      TMA producer: q, k, g, v tiles (SW128) + beta, 2-stage ring
-//   warp 1      chain MMA issuer (and TMEM owner)
-//   warp 2      prep MMA issuer
-//   warps 4-7   chain group: W tile from W^T, U and state epilogues in TMEM, O to HBM
-//   warps 8-15  prep group: decay factors, M/P, T' = (I+M)^-1 Diag(beta)
-// The prep group and its MMAs run one chunk ahead of the chain; the chain group
-// turns each chunk's W^T accumulator into the W tile, so the prep group goes on
-// to the next chunk as soon as T' is written.  The state
-// lives in TMEM transposed (lane = value column j, column = channel c) as an
-// fp32 master plus a bf16 copy that feeds the next chunk's MMAs as the A
-// operand straight from TMEM.
+//   warp 0       TMA producer: q, k, g, v tiles (SW128) + beta, 2-stage ring
+//   warp 1       chain MMA issuer (and TMEM owner)
+//   warp 2       prep MMA issuer (polls both prep products)
+//   warps 4-7    chain group: W tile from W^T, U and state epilogues in TMEM, O to HBM
+//   warps 8-11   decay group: prefix products, Kbar / Qbar / Ktil in place
+//   warps 12-15  solve group: M and P from the accumulator, T' = (I+M)^-1 Diag(beta)
+// The decay group runs up to one chunk ahead of the solve group, which runs one
+// chunk ahead of the chain.  The state lives in TMEM transposed (lane = value
+// column j, column = channel c) as an fp32 master plus a bf16 copy that feeds
+// the next chunk's MMAs as the A operand straight from TMEM.
 //
 // Every mbarrier wait is bounded (about one second); a wait that gives up sets
 // the timeout bit in the status word, and all roles drain and exit.
@@ -48,24 +47,24 @@ using namespace ptx;
 constexpr int kC = 64;          // chunk length
 constexpr int kD = 128;         // dk = dv
 constexpr int kThreads = 512;   // 16 warps
-constexpr int kPrep = 256;      // prep group: warps 8-15
 constexpr uint64_t kWaitNs = 1000000000ull;
 
 // dynamic shared memory map (offsets from a 1024-byte aligned base)
 constexpr uint32_t kStage = 65536;                 // per-stage: R (k|q, 32K), G (16K), V (16K)
 constexpr uint32_t OFF_R = 0, OFF_G = 32768, OFF_V = 49152;
-constexpr uint32_t OFF_W = 2 * kStage;             // 2 x 16K   W (MN-major: row = channel)
-constexpr uint32_t OFF_P = OFF_W + 2 * 16384;      // 2 x 8K    P (K-major: row = token)
+// The W tile of a chunk (MN-major, row = channel) is written over the Kbar half of
+// its R tile once Kbar's last reader (the W / Utl product) has completed.
+constexpr uint32_t OFF_P = 2 * kStage;             // 2 x 8K    P (K-major: row = token)
 constexpr uint32_t OFF_TT = OFF_P + 2 * 8192;      // 8K        T' (K-major)
-constexpr int kLdM = 65;                           // row stride (floats) of the fp32 M buffer
-constexpr int kLdT = 68;                           // row stride of the fp32 T buffer (16-byte rows)
-constexpr int kLdX = 36;                           // row stride of the block-product scratch
+constexpr int kLdM = 68;                           // row stride (floats) of the fp32 M buffer (16-byte rows)
+constexpr int kLdT = 72;                           // row stride of the fp32 T buffer (16-byte rows)
+constexpr int kLdX = 40;                           // row stride of the block-product scratch
 constexpr uint32_t OFF_M = OFF_TT + 8192;          // fp32 64 x kLdM
 constexpr uint32_t OFF_T = OFF_M + 64 * kLdM * 4;  // fp32 64 x kLdT
 constexpr uint32_t kDynSmem = OFF_T + 64 * kLdT * 4 + 1024;
 
 // TMEM columns (512 allocated)
-constexpr uint32_t TM_S = 0, TM_SB = 128, TM_U = 192, TM_UB = 320, TM_O = 352, TM_PREP = 416;
+constexpr uint32_t TM_S = 0, TM_SB = 128, TM_U = 192, TM_W = 256, TM_UB = 320, TM_O = 352, TM_PREP = 416;
 
 struct TcParams {
     CUtensorMap tm_q, tm_k, tm_g, tm_v;
@@ -87,12 +86,6 @@ __device__ __forceinline__ uint32_t swz(int row, int col) {
 __device__ __forceinline__ uint32_t chunk16(int row, int chunk) {
     return static_cast<uint32_t>(row * 128 + ((chunk ^ (row & 7)) << 4));
 }
-__device__ __forceinline__ float ld_bf16(const uint8_t *base, uint32_t off) {
-    return __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(base + off));
-}
-__device__ __forceinline__ void st_bf16(uint8_t *base, uint32_t off, float v) {
-    *reinterpret_cast<__nv_bfloat16 *>(base + off) = __float2bfloat16_rn(v);
-}
 __device__ __forceinline__ uint32_t ld32(const uint8_t *base, uint32_t off) {
     return *reinterpret_cast<const uint32_t *>(base + off);
 }
@@ -108,6 +101,15 @@ __device__ __forceinline__ float4 fma4(float a, float4 b, float4 c) {
 __device__ __forceinline__ float4 ld4(const float *p) { return *reinterpret_cast<const float4 *>(p); }
 __device__ __forceinline__ void st4(float *p, float4 v) { *reinterpret_cast<float4 *>(p) = v; }
 __device__ __forceinline__ float4 neg4(float4 v) { return make_float4(-v.x, -v.y, -v.z, -v.w); }
+// One m16n8k8 tf32 tile product c += a b (fp32 bit patterns as tf32 operands).
+__device__ __forceinline__ void mma_tf32(float (&c)[4], float a0, float a1, float a2, float a3, float b0, float b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(__float_as_uint(a0)), "r"(__float_as_uint(a1)), "r"(__float_as_uint(a2)), "r"(__float_as_uint(a3)),
+          "r"(__float_as_uint(b0)), "r"(__float_as_uint(b1)));
+}
 __device__ __forceinline__ void named_bar(int id, int n) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
@@ -118,17 +120,17 @@ struct Ctl {
 };
 
 // Bounded wait that also stops early once another role has aborted.
+// The waiting thread sleeps inside the barrier probe (up to 20 us at a time), so
+// idle roles do not take issue slots from the working ones.
 __device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, const Ctl &ctl) {
+    if (mbar_try_wait(bar, parity)) return true;
     const uint64_t deadline = globaltimer_ns() + kWaitNs;
-    uint32_t spins = 0;
-    while (!mbar_try_wait(bar, parity)) {
-        if ((++spins & 63u) == 0) {
-            if (*ctl.abort) return false;
-            if (globaltimer_ns() > deadline) {
-                *ctl.abort = 1;
-                atomicOr(ctl.status, DEV_ERR_TIMEOUT);
-                return false;
-            }
+    while (!mbar_try_wait_sleep(bar, parity, 20000u)) {
+        if (*ctl.abort) return false;
+        if (globaltimer_ns() > deadline) {
+            *ctl.abort = 1;
+            atomicOr(ctl.status, DEV_ERR_TIMEOUT);
+            return false;
         }
     }
     return true;
@@ -157,15 +159,16 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_tc_kernel(const __grid_
     extern __shared__ uint8_t dsmem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(dsmem_raw) + 1023) & ~uintptr_t(1023));
     __shared__ __align__(16) float s_beta[2][kC];
-    __shared__ float s_ac[2][kD];
+    __shared__ __align__(16) float s_ac[2][kD];
     __shared__ __align__(16) float s_x[32 * kLdX];
-    __shared__ float s_tot[4][kD];
+    __shared__ float s_tot[kD];
     __shared__ uint64_t bar_full[2], bar_free[2];
-    __shared__ uint64_t bar_elem, bar_mma1, bar_tready, bar_mma2, bar_ready, bar_wfree, bar_c1, bar_uready, bar_c3;
+    __shared__ uint64_t bar_elem, bar_mma1, bar_mfree, bar_tready, bar_mma2, bar_ready, bar_wfree, bar_c1, bar_uready,
+        bar_c3;
     __shared__ uint64_t bar_drain[2];
     __shared__ uint32_t s_tmem;
     __shared__ int s_abort;
-    __shared__ int s_grp_fail[2];  // [0] prep group, [1] chain group
+    __shared__ int s_grp_fail[3];  // [0] decay group, [1] chain group, [2] solve group
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int64_t pair = blockIdx.x;
@@ -197,6 +200,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_tc_kernel(const __grid_
         }
         mbar_init(&bar_elem, 1);
         mbar_init(&bar_mma1, 1);
+        mbar_init(&bar_mfree, 1);
         mbar_init(&bar_tready, 1);
         mbar_init(&bar_mma2, 1);
         mbar_init(&bar_ready, 1);
@@ -209,6 +213,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_tc_kernel(const __grid_
         s_abort = 0;
         s_grp_fail[0] = 0x7fffffff;
         s_grp_fail[1] = 0x7fffffff;
+        s_grp_fail[2] = 0x7fffffff;
         fence_mbar_init();
     }
     if (warp == 1) {
@@ -224,11 +229,14 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_tc_kernel(const __grid_
 
     if (warp == 0) {
         // ------------------------------------------------------------------ TMA producer
-        int issued[2] = {-1, -1};
+        int issued0 = -1, issued1 = -1;
         for (int c = 0; c < nfull; ++c) {
             const int s = c & 1;
-            if (c >= 2 && !warp_wait(&bar_free[s], ((c >> 1) - 1) & 1, ctl, lane)) break;
             const int t0 = static_cast<int>(bos + static_cast<int64_t>(c) * kC);
+            // beta for this chunk: loaded before waiting for the stage, so its latency overlaps the wait
+            const float b_lo = __bfloat162float(p.beta[(static_cast<int64_t>(t0) + lane) * H + h]);
+            const float b_hi = __bfloat162float(p.beta[(static_cast<int64_t>(t0) + lane + 32) * H + h]);
+            if (c >= 2 && !warp_wait(&bar_free[s], ((c >> 1) - 1) & 1, ctl, lane)) break;
             uint8_t *st = sm + s * kStage;
             if (lane == 0) {
                 mbar_arrive_expect_tx(&bar_full[s], kStage);
@@ -240,19 +248,30 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_tc_kernel(const __grid_
                 tma_load_3d(st + OFF_G + 8192, &p.tm_g, 64, h, t0, &bar_full[s]);
                 tma_load_3d(st + OFF_V + 0, &p.tm_v, 0, h, t0, &bar_full[s]);
                 tma_load_3d(st + OFF_V + 8192, &p.tm_v, 64, h, t0, &bar_full[s]);
+                // warm L2 with the chunk that will reuse this stage, so its load is short
+                if (c + 2 < nfull) {
+                    const int t2 = t0 + 2 * kC;
+                    for (int x = 0; x < 128; x += 64) {
+                        tma_prefetch_l2_3d(&p.tm_q, x, h, t2);
+                        tma_prefetch_l2_3d(&p.tm_k, x, h, t2);
+                        tma_prefetch_l2_3d(&p.tm_g, x, h, t2);
+                        tma_prefetch_l2_3d(&p.tm_v, x, h, t2);
+                    }
+                }
             }
-            issued[s] = c;
-            s_beta[s][lane] = __bfloat162float(p.beta[(static_cast<int64_t>(t0) + lane) * H + h]);
-            s_beta[s][lane + 32] = __bfloat162float(p.beta[(static_cast<int64_t>(t0) + lane + 32) * H + h]);
+            if (s == 0) issued0 = c; else issued1 = c;
+            s_beta[s][lane] = b_lo;
+            s_beta[s][lane + 32] = b_hi;
             __syncwarp();
             if (lane == 0) mbar_arrive(&bar_full[s]);
         }
         // make sure no TMA copy is still landing in shared memory when the CTA exits
-        for (int s = 0; s < 2; ++s)
-            if (issued[s] >= 0) {
-                const uint64_t deadline = globaltimer_ns() + kWaitNs;
-                while (!mbar_try_wait(&bar_full[s], (issued[s] >> 1) & 1) && globaltimer_ns() < deadline) {
-                }
+        const uint64_t deadline = globaltimer_ns() + kWaitNs;
+        if (issued0 >= 0)
+            while (!mbar_try_wait(&bar_full[0], (issued0 >> 1) & 1) && globaltimer_ns() < deadline) {
+            }
+        if (issued1 >= 0)
+            while (!mbar_try_wait(&bar_full[1], (issued1 >> 1) & 1) && globaltimer_ns() < deadline) {
             }
     } else if (warp == 1) {
         // ------------------------------------------------------------------ chain MMA issuer
@@ -265,11 +284,10 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_tc_kernel(const __grid_
                 if (!wait_bar(&bar_ready, c & 1, ctl)) break;
                 tc_fence_after();
                 const uint32_t st = sm_base + s * kStage;
-                const uint32_t w = sm_base + OFF_W + s * 16384;
                 const uint32_t pp = sm_base + OFF_P + s * 8192;
                 for (int ks = 0; ks < 8; ++ks)
-                    mma_bf16_ts(tmem + TM_U + 64 * s, tmem + TM_SB + 8 * ks, sdesc_sw128(w + ks * 2048, 8192, 1024),
-                                idU, 1u);
+                    mma_bf16_ts(tmem + TM_U, tmem + TM_SB + 8 * ks,
+                                sdesc_sw128(st + OFF_R + (ks >> 2) * 16384 + (ks & 3) * 2048, 8192, 1024), idU, 1u);
                 for (int ks = 0; ks < 8; ++ks)
                     mma_bf16_ts(tmem + TM_O, tmem + TM_SB + 8 * ks,
                                 sdesc_sw128(st + OFF_R + 8192 + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024), idO,
@@ -293,36 +311,62 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_tc_kernel(const __grid_
         }
     } else if (warp == 2) {
         // ------------------------------------------------------------------ prep MMA issuer
+        // Polls both prep MMAs so that the next chunk's [Kbar; Qbar] Ktil^T product can go
+        // as soon as its tiles are ready, while this chunk's W / Utl product waits for T'.
         if (lane == 0) {
             const uint32_t id1 = idesc_bf16(128, 64, false, false);  // [Kbar; Qbar] Ktil^T
             const uint32_t id2 = idesc_bf16(128, 64, true, false);   // Kbar^T T'^T, V^T T'^T (A MN-major)
-            for (int c = 0; c < nfull; ++c) {
-                const int s = c & 1;
-                const uint32_t st = sm_base + s * kStage;
-                if (!wait_bar(&bar_elem, c & 1, ctl)) break;
-                // W^T of the previous chunk must have left the PREP columns
-                if (c > 0 && !wait_bar(&bar_wfree, (c - 1) & 1, ctl)) break;
-                tc_fence_after();
-                for (int ks = 0; ks < 8; ++ks)
-                    mma_bf16_ss(tmem + TM_PREP,
-                                sdesc_sw128(st + OFF_R + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024),
-                                sdesc_sw128(st + OFF_G + (ks >> 2) * 8192 + (ks & 3) * 32, 16, 1024), id1,
-                                ks > 0 ? 1u : 0u);
-                mma_commit(&bar_mma1);
-                if (!wait_bar(&bar_tready, c & 1, ctl)) break;
-                tc_fence_after();
-                const uint32_t tt = sm_base + OFF_TT;
-                for (int ks = 0; ks < 4; ++ks)
-                    mma_bf16_ss(tmem + TM_PREP, sdesc_sw128(st + OFF_R + ks * 2048, 16384, 1024),
-                                sdesc_sw128(tt + ks * 32, 16, 1024), id2, ks > 0 ? 1u : 0u);
-                for (int ks = 0; ks < 4; ++ks)
-                    mma_bf16_ss(tmem + TM_U + 64 * s, sdesc_sw128(st + OFF_V + ks * 2048, 8192, 1024),
-                                sdesc_sw128(tt + ks * 32, 16, 1024), id2, ks > 0 ? 1u : 0u);
-                mma_commit(&bar_mma2);
+            const uint32_t tt = sm_base + OFF_TT;
+            int c1 = 0, c2 = 0;
+            uint64_t deadline = globaltimer_ns() + kWaitNs;
+            uint32_t spins = 0;
+            while (c2 < nfull) {
+                bool progress = false;
+                if (c1 < nfull && c1 <= c2 + 1 && mbar_test_wait(&bar_elem, c1 & 1) &&
+                    (c1 == 0 || mbar_test_wait(&bar_mfree, (c1 - 1) & 1))) {
+                    tc_fence_after();
+                    const uint32_t st = sm_base + (c1 & 1) * kStage;
+                    for (int ks = 0; ks < 8; ++ks)
+                        mma_bf16_ss(tmem + TM_PREP,
+                                    sdesc_sw128(st + OFF_R + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024),
+                                    sdesc_sw128(st + OFF_G + (ks >> 2) * 8192 + (ks & 3) * 32, 16, 1024), id1,
+                                    ks > 0 ? 1u : 0u);
+                    mma_commit(&bar_mma1);
+                    ++c1;
+                    progress = true;
+                }
+                if (c2 < c1 && mbar_test_wait(&bar_tready, c2 & 1) &&
+                    (c2 == 0 || (mbar_test_wait(&bar_wfree, (c2 - 1) & 1) && mbar_test_wait(&bar_uready, (c2 - 1) & 1)))) {
+                    tc_fence_after();
+                    const uint32_t st = sm_base + (c2 & 1) * kStage;
+                    for (int ks = 0; ks < 4; ++ks)
+                        mma_bf16_ss(tmem + TM_W, sdesc_sw128(st + OFF_R + ks * 2048, 16384, 1024),
+                                    sdesc_sw128(tt + ks * 32, 16, 1024), id2, ks > 0 ? 1u : 0u);
+                    for (int ks = 0; ks < 4; ++ks)
+                        mma_bf16_ss(tmem + TM_U, sdesc_sw128(st + OFF_V + ks * 2048, 8192, 1024),
+                                    sdesc_sw128(tt + ks * 32, 16, 1024), id2, ks > 0 ? 1u : 0u);
+                    mma_commit(&bar_mma2);
+                    ++c2;
+                    progress = true;
+                }
+                if (progress) {
+                    deadline = globaltimer_ns() + kWaitNs;
+                    spins = 0;
+                    continue;
+                }
+                __nanosleep(32);  // back off without stealing issue slots from the math warps
+                if ((++spins & 63u) == 0) {
+                    if (*ctl.abort) break;
+                    if (globaltimer_ns() > deadline) {
+                        *ctl.abort = 1;
+                        atomicOr(ctl.status, DEV_ERR_TIMEOUT);
+                        break;
+                    }
+                }
             }
             mma_commit(&bar_drain[1]);
-            const uint64_t deadline = globaltimer_ns() + kWaitNs;
-            while (!mbar_try_wait(&bar_drain[1], 0) && globaltimer_ns() < deadline) {
+            const uint64_t dl = globaltimer_ns() + kWaitNs;
+            while (!mbar_try_wait(&bar_drain[1], 0) && globaltimer_ns() < dl) {
             }
         }
     } else if (warp >= 4 && warp < 8) {
@@ -372,8 +416,8 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_tc_kernel(const __grid_
             }
             tc_fence_after();
             {
-                uint8_t *W = sm + OFF_W + s * 16384;
-                const uint32_t tP = tmem + lane_base + TM_PREP;
+                uint8_t *W = sm + s * kStage + OFF_R + (j >> 6) * 16384;  // over Kbar
+                const uint32_t tP = tmem + lane_base + TM_W;
 #pragma unroll
                 for (int hf = 0; hf < 2; ++hf) {
                     uint32_t wv[32];
@@ -387,7 +431,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_tc_kernel(const __grid_
 #pragma unroll
                         for (int e = 0; e < 4; ++e)
                             vw[e] = pack_bf16x2(__uint_as_float(wv[q8 * 8 + 2 * e]), __uint_as_float(wv[q8 * 8 + 2 * e + 1]));
-                        *reinterpret_cast<uint4 *>(W + chunk16(j, 4 * hf + q8)) = v;
+                        *reinterpret_cast<uint4 *>(W + chunk16(j & 63, 4 * hf + q8)) = v;
                     }
                 }
             }
@@ -396,7 +440,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_tc_kernel(const __grid_
             named_bar(2, 128);
             if (j == 0) {
                 mbar_arrive(&bar_ready);   // W(c) written and the state of chunk c-1 final
-                mbar_arrive(&bar_wfree);   // PREP columns may take the next chunk's M/P
+                mbar_arrive(&bar_wfree);   // W^T columns may take the next chunk's product
             }
             if (o_t0 >= 0) store_o(o_t0);  // previous chunk's O while C1 runs
 
@@ -407,7 +451,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_tc_kernel(const __grid_
             }
             tc_fence_after();
             {
-                const uint32_t tU = tmem + lane_base + TM_U + 64 * s;
+                const uint32_t tU = tmem + lane_base + TM_U;
 #pragma unroll
                 for (int hf = 0; hf < 2; ++hf) {
                     uint32_t u[32], pk[16];
@@ -438,9 +482,16 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_tc_kernel(const __grid_
                 tmem_ld16(tS + cc + 16, b);
                 tmem_ld_wait();
 #pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    a[e] = __float_as_uint(__uint_as_float(a[e]) * s_ac[s][cc + e]);
-                    b[e] = __float_as_uint(__uint_as_float(b[e]) * s_ac[s][cc + 16 + e]);
+                for (int e = 0; e < 16; e += 4) {
+                    const float4 fa = ld4(&s_ac[s][cc + e]), fb = ld4(&s_ac[s][cc + 16 + e]);
+                    a[e] = __float_as_uint(__uint_as_float(a[e]) * fa.x);
+                    a[e + 1] = __float_as_uint(__uint_as_float(a[e + 1]) * fa.y);
+                    a[e + 2] = __float_as_uint(__uint_as_float(a[e + 2]) * fa.z);
+                    a[e + 3] = __float_as_uint(__uint_as_float(a[e + 3]) * fa.w);
+                    b[e] = __float_as_uint(__uint_as_float(b[e]) * fb.x);
+                    b[e + 1] = __float_as_uint(__uint_as_float(b[e + 1]) * fb.y);
+                    b[e + 2] = __float_as_uint(__uint_as_float(b[e + 2]) * fb.z);
+                    b[e + 3] = __float_as_uint(__uint_as_float(b[e + 3]) * fb.w);
                 }
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
@@ -475,34 +526,30 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_tc_kernel(const __grid_
             if (j == 0) mbar_arrive(&bar_free[s]);
         }
         if (done && o_t0 >= 0) store_o(o_t0);
-    } else if (warp >= 8) {
-        // ------------------------------------------------------------------ prep group (8 warps)
+    } else if (warp >= 8 && warp < 12) {
+        // ------------------------------------------------------------------ decay group (warps 8-11)
+        // Decay factors and the scaled operand tiles, one chunk ahead of the solve group.
+        // Thread = (token half, channel pair): alpha = exp(g), prefix products within
+        // the half, the first half's totals carried into the second, then Kbar, Qbar,
+        // Ktil written over k, q, g in place.
         const int pt = tid - 256;
         int gseq = 0;
-        float *Mb = reinterpret_cast<float *>(sm + OFF_M);
-        float *Tb = reinterpret_cast<float *>(sm + OFF_T);
         const float kMinDecay = 7.888609052210118e-31f;  // 2^-100
-        for (int i = pt; i < 64 * kLdT; i += kPrep) Tb[i] = 0.f;  // blocks above the diagonal stay zero
-        named_bar(1, kPrep);
         for (int c = 0; c < nfull; ++c) {
             const int s = c & 1;
             uint8_t *st = sm + s * kStage;
-            if (!group_wait(&bar_full[s], (c >> 1) & 1, ctl, &s_grp_fail[0], 1, kPrep, gseq)) break;
-
-            // (1) decay factors and the scaled operand tiles.  Thread = (token quarter,
-            // channel pair): alpha = exp(g), prefix products within the quarter, the
-            // earlier quarters' totals carried in, then Kbar, Qbar, Ktil in place.
+            if (!group_wait(&bar_full[s], (c >> 1) & 1, ctl, &s_grp_fail[0], 1, 128, gseq)) break;
             {
-                const int cp = pt & 63, qt = pt >> 6;
+                const int cp = pt & 63, half = pt >> 6;
                 const int kb = cp >> 5, cc = 2 * (cp & 31), ch = kb * 64 + cc;
                 uint8_t *Rk = st + OFF_R + kb * 16384;
                 uint8_t *Rq = Rk + 8192;
                 uint8_t *G = st + OFF_G + kb * 8192;
-                const int r0 = 16 * qt;
-                float A0[16], A1[16];
+                const int r0 = 32 * half;
+                float A0[32], A1[32];
                 float p0 = 1.f, p1 = 1.f;
 #pragma unroll
-                for (int rr = 0; rr < 16; rr += 8) {
+                for (int rr = 0; rr < 32; rr += 8) {
                     uint32_t gw[8];
 #pragma unroll
                     for (int e = 0; e < 8; ++e) gw[e] = ld32(G, swz(r0 + rr + e, cc));
@@ -515,17 +562,15 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_tc_kernel(const __grid_
                         A1[rr + e] = p1;
                     }
                 }
-                s_tot[qt][ch] = p0;
-                s_tot[qt][ch + 1] = p1;
-                named_bar(1, kPrep);
-                float m0 = 1.f, m1 = 1.f;
-                for (int q = 0; q < qt; ++q) {
-                    m0 *= s_tot[q][ch];
-                    m1 *= s_tot[q][ch + 1];
+                if (half == 0) {
+                    s_tot[ch] = p0;
+                    s_tot[ch + 1] = p1;
                 }
+                named_bar(1, 128);
+                const float m0 = half ? s_tot[ch] : 1.f, m1 = half ? s_tot[ch + 1] : 1.f;
                 const float sc = p.scale;
 #pragma unroll
-                for (int rr = 0; rr < 16; rr += 8) {
+                for (int rr = 0; rr < 32; rr += 8) {
                     uint32_t kw[8], qw[8];
 #pragma unroll
                     for (int e = 0; e < 8; ++e) {
@@ -543,7 +588,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_tc_kernel(const __grid_
                         st32(G, off, pack_bf16x2(kf.x * __fdividef(1.f, a0), kf.y * __fdividef(1.f, a1)));
                     }
                 }
-                if (qt == 3) {
+                if (half == 1) {
                     const float ac0 = m0 * p0, ac1 = m1 * p1;
                     if (!(ac0 >= kMinDecay) || !(ac1 >= kMinDecay)) atomicOr(p.status, DEV_ERR_GATE);
                     s_ac[s][ch] = ac0;
@@ -551,116 +596,189 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_tc_kernel(const __grid_
                 }
             }
             fence_proxy_async_smem();
-            named_bar(1, kPrep);
-            if (pt == 0) mbar_arrive(&bar_elem);
-
+            named_bar(1, 128);
+            if (pt == 0) {
+                // at most one chunk ahead of the MMA that consumes these tiles
+                if (c > 0) wait_bar(&bar_mma1, (c - 1) & 1, ctl);
+                mbar_arrive(&bar_elem);
+            }
+        }
+    } else if (warp >= 12) {
+        // ------------------------------------------------------------------ solve group (warps 12-15)
+        const int pt = tid - 384;
+        const int wq = warp & 3;
+        int gseq = 0;
+        float *Mb = reinterpret_cast<float *>(sm + OFF_M);
+        float *Tb = reinterpret_cast<float *>(sm + OFF_T);
+        for (int i = pt; i < 64 * kLdT; i += 128) Tb[i] = 0.f;  // blocks above the diagonal stay zero
+        named_bar(3, 128);
+        for (int c = 0; c < nfull; ++c) {
+            const int s = c & 1;
             // (2) M (fp32, rows scaled by beta, strictly lower) and P (bf16, lower incl.).
-            // Accumulator lane x: rows 0-63 = Kbar . Ktil, 64-127 = Qbar . Ktil; two warps
-            // per lane quarter split the 64 columns.
-            if (!group_wait(&bar_mma1, c & 1, ctl, &s_grp_fail[0], 1, kPrep, gseq)) break;
+            // Accumulator lane x: rows 0-63 = Kbar . Ktil, 64-127 = Qbar . Ktil.
+            if (!group_wait(&bar_mma1, c & 1, ctl, &s_grp_fail[2], 3, 128, gseq)) break;
             tc_fence_after();
             {
-                const int wq = pt >> 5, quarter = wq & 3, ch2 = wq >> 2;
-                const int x = quarter * 32 + lane;
-                uint32_t m[32];
-                const uint32_t tP = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + TM_PREP + 32 * ch2;
-                tmem_ld16(tP, *reinterpret_cast<uint32_t(*)[16]>(&m[0]));
+                const int x = wq * 32 + lane;
+                uint32_t m[64];
+                const uint32_t tP = tmem + (static_cast<uint32_t>(wq * 32) << 16) + TM_PREP;
+                tmem_ld16(tP + 0, *reinterpret_cast<uint32_t(*)[16]>(&m[0]));
                 tmem_ld16(tP + 16, *reinterpret_cast<uint32_t(*)[16]>(&m[16]));
+                tmem_ld16(tP + 32, *reinterpret_cast<uint32_t(*)[16]>(&m[32]));
+                tmem_ld16(tP + 48, *reinterpret_cast<uint32_t(*)[16]>(&m[48]));
                 tmem_ld_wait();
                 if (x < 64) {
                     const int r = x;
                     const float br = s_beta[s][r];
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        const int col = 32 * ch2 + i;
-                        Mb[r * kLdM + col] = (col < r) ? br * __uint_as_float(m[i]) : 0.f;
-                    }
+                    for (int i = 0; i < kC; i += 4)
+                        st4(&Mb[r * kLdM + i], make_float4(i < r ? br * __uint_as_float(m[i]) : 0.f,
+                                                           i + 1 < r ? br * __uint_as_float(m[i + 1]) : 0.f,
+                                                           i + 2 < r ? br * __uint_as_float(m[i + 2]) : 0.f,
+                                                           i + 3 < r ? br * __uint_as_float(m[i + 3]) : 0.f));
                 } else {
                     const int r = x - 64;
                     uint8_t *P = sm + OFF_P + s * 8192;
 #pragma unroll
-                    for (int q8 = 0; q8 < 4; ++q8) {
+                    for (int q8 = 0; q8 < 8; ++q8) {
                         uint4 v;
                         uint32_t *vw = reinterpret_cast<uint32_t *>(&v);
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
-                            const int i0 = 32 * ch2 + q8 * 8 + 2 * e;
-                            const float x0 = (i0 <= r) ? __uint_as_float(m[q8 * 8 + 2 * e]) : 0.f;
-                            const float x1 = (i0 + 1 <= r) ? __uint_as_float(m[q8 * 8 + 2 * e + 1]) : 0.f;
+                            const int i0 = q8 * 8 + 2 * e;
+                            const float x0 = (i0 <= r) ? __uint_as_float(m[i0]) : 0.f;
+                            const float x1 = (i0 + 1 <= r) ? __uint_as_float(m[i0 + 1]) : 0.f;
                             vw[e] = pack_bf16x2(x0, x1);
                         }
-                        *reinterpret_cast<uint4 *>(P + chunk16(r, 4 * ch2 + q8)) = v;
+                        *reinterpret_cast<uint4 *>(P + chunk16(r, q8)) = v;
                     }
                 }
             }
             fence_proxy_async_smem();
             tc_fence_before();
-            named_bar(1, kPrep);
+            named_bar(3, 128);
+            if (pt == 0) mbar_arrive(&bar_mfree);  // PREP columns may take the next chunk's product
 
             // (3) T = (I + M)^-1, blocked: the four 16x16 diagonal blocks D_b by forward
-            // substitution (thread = block, column) ...
+            // substitution, column-oriented (thread = block, column; each solved entry is
+            // pushed into every later row at once; M read four columns at a time) ...
             if (pt < 64) {
                 const int b = pt >> 4, mm = pt & 15, R0 = 16 * b;
-                float xv[16];
+                float acc[16], xv[16];
 #pragma unroll
-                for (int l = 0; l < 16; ++l) {
-                    float acc = 0.f;
+                for (int l = 0; l < 16; ++l) acc[l] = 0.f;
 #pragma unroll
-                    for (int i = 0; i < l; ++i) acc = fmaf(Mb[(R0 + l) * kLdM + R0 + i], xv[i], acc);
-                    xv[l] = (l < mm) ? 0.f : ((l == mm) ? 1.f : -acc);
+                for (int i0 = 0; i0 < 16; i0 += 4) {
+                    float4 mq[16];
+#pragma unroll
+                    for (int l = i0 + 1; l < 16; ++l) mq[l] = ld4(&Mb[(R0 + l) * kLdM + R0 + i0]);
+#pragma unroll
+                    for (int ii = 0; ii < 4; ++ii) {
+                        const int i = i0 + ii;
+                        xv[i] = (i < mm) ? 0.f : ((i == mm) ? 1.f : -acc[i]);
+#pragma unroll
+                        for (int l = i + 1; l < 16; ++l) {
+                            const float mv = ii == 0 ? mq[l].x : ii == 1 ? mq[l].y : ii == 2 ? mq[l].z : mq[l].w;
+                            acc[l] = fmaf(mv, xv[i], acc[l]);
+                        }
+                    }
                 }
 #pragma unroll
                 for (int l = 0; l < 16; ++l) Tb[(R0 + l) * kLdT + R0 + mm] = xv[l];
             }
-            named_bar(1, kPrep);
-            // ... the sub-diagonal blocks T[a][a-1] = -D_a M[a][a-1] D_{a-1} for a = 1, 3 ...
+            named_bar(3, 128);
+            // ... then the off-diagonal blocks as tf32 tensor-core tiles (m16n8k8; each warp
+            // owns output tiles): fragment row gq = lane / 4, column tq = lane % 4.
+            const int gq = lane >> 2, tq = lane & 3;
             {
-                const int pr = pt >> 7, u = pt & 127, l = u >> 3, c0 = (u & 7) * 2;
-                const int Ra = 16 + 32 * pr, Rb = Ra - 16;
+                // sub-diagonal blocks T[a][a-1] = -D_a (M[a][a-1] D_{a-1}), a = 1 (warps 0,1), 3 (warps 2,3)
+                const int pr = wq >> 1, nt = wq & 1;
+                const int Ra = 16 + 32 * pr, Rb = Ra - 16, n0 = 8 * nt;
                 float *X = s_x + pr * 16 * kLdX;
-                float2 acc = make_float2(0.f, 0.f);
+                float c[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                for (int k = 0; k < 16; ++k) {
-                    const float mv = Mb[(Ra + l) * kLdM + Rb + k];
-                    const float2 t = *reinterpret_cast<const float2 *>(&Tb[(Rb + k) * kLdT + Rb + c0]);
-                    acc.x = fmaf(mv, t.x, acc.x);
-                    acc.y = fmaf(mv, t.y, acc.y);
+                for (int ks = 0; ks < 2; ++ks) {
+                    const int k0 = 8 * ks;
+                    mma_tf32(c, Mb[(Ra + gq) * kLdM + Rb + k0 + tq], Mb[(Ra + gq + 8) * kLdM + Rb + k0 + tq],
+                             Mb[(Ra + gq) * kLdM + Rb + k0 + tq + 4], Mb[(Ra + gq + 8) * kLdM + Rb + k0 + tq + 4],
+                             Tb[(Rb + k0 + tq) * kLdT + Rb + n0 + gq], Tb[(Rb + k0 + tq + 4) * kLdT + Rb + n0 + gq]);
                 }
-                *reinterpret_cast<float2 *>(&X[l * kLdX + c0]) = acc;
-                named_bar(1, kPrep);
-                float2 out = make_float2(0.f, 0.f);
+                X[gq * kLdX + n0 + 2 * tq] = c[0];
+                X[gq * kLdX + n0 + 2 * tq + 1] = c[1];
+                X[(gq + 8) * kLdX + n0 + 2 * tq] = c[2];
+                X[(gq + 8) * kLdX + n0 + 2 * tq + 1] = c[3];
+                named_bar(3, 128);
+                float d[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                for (int q = 0; q < 16; ++q) {
-                    const float dv = Tb[(Ra + l) * kLdT + Ra + q];
-                    const float2 xq = *reinterpret_cast<const float2 *>(&X[q * kLdX + c0]);
-                    out.x = fmaf(dv, xq.x, out.x);
-                    out.y = fmaf(dv, xq.y, out.y);
+                for (int ks = 0; ks < 2; ++ks) {
+                    const int k0 = 8 * ks;
+                    mma_tf32(d, Tb[(Ra + gq) * kLdT + Ra + k0 + tq], Tb[(Ra + gq + 8) * kLdT + Ra + k0 + tq],
+                             Tb[(Ra + gq) * kLdT + Ra + k0 + tq + 4], Tb[(Ra + gq + 8) * kLdT + Ra + k0 + tq + 4],
+                             X[(k0 + tq) * kLdX + n0 + gq], X[(k0 + tq + 4) * kLdX + n0 + gq]);
                 }
-                *reinterpret_cast<float2 *>(&Tb[(Ra + l) * kLdT + Rb + c0]) = make_float2(-out.x, -out.y);
+                Tb[(Ra + gq) * kLdT + Rb + n0 + 2 * tq] = -d[0];
+                Tb[(Ra + gq) * kLdT + Rb + n0 + 2 * tq + 1] = -d[1];
+                Tb[(Ra + gq + 8) * kLdT + Rb + n0 + 2 * tq] = -d[2];
+                Tb[(Ra + gq + 8) * kLdT + Rb + n0 + 2 * tq + 1] = -d[3];
             }
-            named_bar(1, kPrep);
-            // ... and the lower-left quadrant T[32:64, 0:32] = -T22 (M[32:64, 0:32] T11),
-            // T11 = T[0:32, 0:32], T22 = T[32:64, 32:64] (their upper-right blocks are zero).
+            named_bar(3, 128);
             {
-                const int l = pt >> 3, c0 = (pt & 7) * 4;
-                float4 a0 = make_float4(0.f, 0.f, 0.f, 0.f);
+                // lower-left quadrant T[32:64, 0:32] = -T22 (M[32:64, 0:32] T11); T11 = T[0:32, 0:32],
+                // T22 = T[32:64, 32:64] (their upper-right blocks are zero).  Warp: 16 rows x 16 cols.
+                const int mt = wq >> 1, nh = wq & 1;
+                const int r0 = 16 * mt;
+                float c[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
-                for (int k = 0; k < 32; ++k) a0 = fma4(Mb[(32 + l) * kLdM + k], ld4(&Tb[k * kLdT + c0]), a0);
-                st4(&s_x[l * kLdX + c0], a0);
-                named_bar(1, kPrep);
-                float4 b0 = make_float4(0.f, 0.f, 0.f, 0.f);
+                for (int ks = 0; ks < 4; ++ks) {
+                    const int k0 = 8 * ks;
+                    const float a0 = Mb[(32 + r0 + gq) * kLdM + k0 + tq], a1 = Mb[(40 + r0 + gq) * kLdM + k0 + tq];
+                    const float a2 = Mb[(32 + r0 + gq) * kLdM + k0 + tq + 4], a3 = Mb[(40 + r0 + gq) * kLdM + k0 + tq + 4];
 #pragma unroll
-                for (int q = 0; q < 32; ++q) b0 = fma4(Tb[(32 + l) * kLdT + 32 + q], ld4(&s_x[q * kLdX + c0]), b0);
-                st4(&Tb[(32 + l) * kLdT + c0], neg4(b0));
+                    for (int nt = 0; nt < 2; ++nt) {
+                        const int n0 = 16 * nh + 8 * nt;
+                        mma_tf32(c[nt], a0, a1, a2, a3, Tb[(k0 + tq) * kLdT + n0 + gq], Tb[(k0 + tq + 4) * kLdT + n0 + gq]);
+                    }
+                }
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt) {
+                    const int n0 = 16 * nh + 8 * nt;
+                    s_x[(r0 + gq) * kLdX + n0 + 2 * tq] = c[nt][0];
+                    s_x[(r0 + gq) * kLdX + n0 + 2 * tq + 1] = c[nt][1];
+                    s_x[(r0 + gq + 8) * kLdX + n0 + 2 * tq] = c[nt][2];
+                    s_x[(r0 + gq + 8) * kLdX + n0 + 2 * tq + 1] = c[nt][3];
+                }
+                named_bar(3, 128);
+                float d[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks) {
+                    const int k0 = 8 * ks;
+                    const float a0 = Tb[(32 + r0 + gq) * kLdT + 32 + k0 + tq], a1 = Tb[(40 + r0 + gq) * kLdT + 32 + k0 + tq];
+                    const float a2 = Tb[(32 + r0 + gq) * kLdT + 36 + k0 + tq], a3 = Tb[(40 + r0 + gq) * kLdT + 36 + k0 + tq];
+#pragma unroll
+                    for (int nt = 0; nt < 2; ++nt) {
+                        const int n0 = 16 * nh + 8 * nt;
+                        mma_tf32(d[nt], a0, a1, a2, a3, s_x[(k0 + tq) * kLdX + n0 + gq], s_x[(k0 + tq + 4) * kLdX + n0 + gq]);
+                    }
+                }
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt) {
+                    const int n0 = 16 * nh + 8 * nt;
+                    Tb[(32 + r0 + gq) * kLdT + n0 + 2 * tq] = -d[nt][0];
+                    Tb[(32 + r0 + gq) * kLdT + n0 + 2 * tq + 1] = -d[nt][1];
+                    Tb[(40 + r0 + gq) * kLdT + n0 + 2 * tq] = -d[nt][2];
+                    Tb[(40 + r0 + gq) * kLdT + n0 + 2 * tq + 1] = -d[nt][3];
+                }
             }
-            named_bar(1, kPrep);
+            // T' of the previous chunk must have been consumed before it is overwritten
+            if (c > 0 && !group_wait(&bar_mma2, (c - 1) & 1, ctl, &s_grp_fail[2], 3, 128, gseq)) break;
+            if (c == 0) named_bar(3, 128);
             // T' = T Diag(beta) -> bf16, K-major rows r (entries above the diagonal are zero)
             {
-                const int r = pt >> 2;
+                const int r = pt >> 1, half = pt & 1;
                 uint8_t *TT = sm + OFF_TT;
 #pragma unroll
-                for (int hq = 0; hq < 2; ++hq) {
-                    const int c0 = ((pt & 3) * 2 + hq) * 8;
+                for (int q8 = 0; q8 < 4; ++q8) {
+                    const int c0 = half * 32 + q8 * 8;
                     const float4 t0 = ld4(&Tb[r * kLdT + c0]), t1 = ld4(&Tb[r * kLdT + c0 + 4]);
                     const float4 b0 = ld4(&s_beta[s][c0]), b1 = ld4(&s_beta[s][c0 + 4]);
                     const float tv[8] = {t0.x * b0.x, t0.y * b0.y, t0.z * b0.z, t0.w * b0.w,
@@ -674,7 +792,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_tc_kernel(const __grid_
                 }
             }
             fence_proxy_async_smem();
-            named_bar(1, kPrep);
+            named_bar(3, 128);
             if (pt == 0) mbar_arrive(&bar_tready);
         }
     }
