@@ -55,11 +55,11 @@ constexpr uint32_t OFF_R = 0, OFF_G = 32768, OFF_V = 49152;
 // The W tile of a chunk (MN-major, row = channel) is written over the Kbar half of
 // its R tile once Kbar's last reader (the W / Utl product) has completed.
 constexpr uint32_t OFF_P = 2 * kStage;             // 2 x 8K    P (K-major: row = token)
-constexpr uint32_t OFF_TT = OFF_P + 2 * 8192;      // 8K        T' (K-major)
+constexpr uint32_t OFF_TT = OFF_P + 2 * 8192;      // 2 x 8K    T' (K-major), by chunk parity
 constexpr int kLdM = 68;                           // row stride (floats) of the fp32 M buffer (16-byte rows)
 constexpr int kLdT = 72;                           // row stride of the fp32 T buffer (16-byte rows)
 constexpr int kLdX = 40;                           // row stride of the block-product scratch
-constexpr uint32_t OFF_M = OFF_TT + 8192;          // fp32 64 x kLdM
+constexpr uint32_t OFF_M = OFF_TT + 2 * 8192;      // fp32 64 x kLdM
 constexpr uint32_t OFF_T = OFF_M + 64 * kLdM * 4;  // fp32 64 x kLdT
 constexpr uint32_t kDynSmem = OFF_T + 64 * kLdT * 4 + 1024;
 
@@ -86,21 +86,16 @@ __device__ __forceinline__ uint32_t swz(int row, int col) {
 __device__ __forceinline__ uint32_t chunk16(int row, int chunk) {
     return static_cast<uint32_t>(row * 128 + ((chunk ^ (row & 7)) << 4));
 }
-__device__ __forceinline__ uint32_t ld32(const uint8_t *base, uint32_t off) {
-    return *reinterpret_cast<const uint32_t *>(base + off);
-}
-__device__ __forceinline__ void st32(uint8_t *base, uint32_t off, uint32_t v) {
-    *reinterpret_cast<uint32_t *>(base + off) = v;
-}
 __device__ __forceinline__ float2 bf2_to_f2(uint32_t w) {
     return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w));
 }
-__device__ __forceinline__ float4 fma4(float a, float4 b, float4 c) {
-    return make_float4(fmaf(a, b.x, c.x), fmaf(a, b.y, c.y), fmaf(a, b.z, c.z), fmaf(a, b.w, c.w));
-}
 __device__ __forceinline__ float4 ld4(const float *p) { return *reinterpret_cast<const float4 *>(p); }
 __device__ __forceinline__ void st4(float *p, float4 v) { *reinterpret_cast<float4 *>(p) = v; }
-__device__ __forceinline__ float4 neg4(float4 v) { return make_float4(-v.x, -v.y, -v.z, -v.w); }
+__device__ __forceinline__ float rcp_approx(float x) {
+    float r;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+    return r;
+}
 // One m16n8k8 tf32 tile product c += a b (fp32 bit patterns as tf32 operands).
 __device__ __forceinline__ void mma_tf32(float (&c)[4], float a0, float a1, float a2, float a3, float b0, float b1) {
     asm volatile(
@@ -159,9 +154,9 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_tc_kernel(const __grid_
     extern __shared__ uint8_t dsmem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(dsmem_raw) + 1023) & ~uintptr_t(1023));
     __shared__ __align__(16) float s_beta[2][kC];
-    __shared__ __align__(16) float s_ac[2][kD];
+    __shared__ __align__(16) float s_ac[3][kD];  // per-chunk A_C, ring of three
     __shared__ __align__(16) float s_x[32 * kLdX];
-    __shared__ float s_tot[kD];
+    __shared__ __align__(16) float s_tot[4][kD];
     __shared__ uint64_t bar_full[2], bar_free[2];
     __shared__ uint64_t bar_elem, bar_mma1, bar_mfree, bar_tready, bar_mma2, bar_ready, bar_wfree, bar_c1, bar_uready,
         bar_c3;
@@ -196,7 +191,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_tc_kernel(const __grid_
     if (tid == 0) {
         for (int s = 0; s < 2; ++s) {
             mbar_init(&bar_full[s], 2);
-            mbar_init(&bar_free[s], 2);
+            mbar_init(&bar_free[s], 1);
         }
         mbar_init(&bar_elem, 1);
         mbar_init(&bar_mma1, 1);
@@ -284,22 +279,28 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_tc_kernel(const __grid_
                 if (!wait_bar(&bar_ready, c & 1, ctl)) break;
                 tc_fence_after();
                 const uint32_t st = sm_base + s * kStage;
-                const uint32_t pp = sm_base + OFF_P + s * 8192;
+                // descriptors built once per chunk; k-steps add constant start offsets
+                const uint64_t dW = sdesc_sw128(st + OFF_R, 8192, 1024);          // W over Kbar, MN-major
+                const uint64_t dQ = sdesc_sw128(st + OFF_R + 8192, 16, 1024);     // Qbar, K-major
+                const uint64_t dP = sdesc_sw128(sm_base + OFF_P + s * 8192, 16, 1024);
+                const uint64_t dG = sdesc_sw128(st + OFF_G, 8192, 1024);          // Ktil, MN-major
+#pragma unroll
                 for (int ks = 0; ks < 8; ++ks)
-                    mma_bf16_ts(tmem + TM_U, tmem + TM_SB + 8 * ks,
-                                sdesc_sw128(st + OFF_R + (ks >> 2) * 16384 + (ks & 3) * 2048, 8192, 1024), idU, 1u);
+                    mma_bf16_ts(tmem + TM_U, tmem + TM_SB + 8 * ks, dW + (((ks >> 2) * 16384 + (ks & 3) * 2048) >> 4),
+                                idU, 1u);
+#pragma unroll
                 for (int ks = 0; ks < 8; ++ks)
-                    mma_bf16_ts(tmem + TM_O, tmem + TM_SB + 8 * ks,
-                                sdesc_sw128(st + OFF_R + 8192 + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024), idO,
-                                ks > 0 ? 1u : 0u);
+                    mma_bf16_ts(tmem + TM_O, tmem + TM_SB + 8 * ks, dQ + (((ks >> 2) * 16384 + (ks & 3) * 32) >> 4),
+                                idO, ks > 0 ? 1u : 0u);
                 mma_commit(&bar_c1);
                 if (!wait_bar(&bar_uready, c & 1, ctl)) break;
                 tc_fence_after();
+#pragma unroll
                 for (int ks = 0; ks < 4; ++ks)
-                    mma_bf16_ts(tmem + TM_O, tmem + TM_UB + 8 * ks, sdesc_sw128(pp + ks * 32, 16, 1024), idO, 1u);
+                    mma_bf16_ts(tmem + TM_O, tmem + TM_UB + 8 * ks, dP + ((ks * 32) >> 4), idO, 1u);
+#pragma unroll
                 for (int ks = 0; ks < 4; ++ks)
-                    mma_bf16_ts(tmem + TM_S, tmem + TM_UB + 8 * ks, sdesc_sw128(st + OFF_G + ks * 2048, 8192, 1024),
-                                idS, 1u);
+                    mma_bf16_ts(tmem + TM_S, tmem + TM_UB + 8 * ks, dG + ((ks * 2048) >> 4), idS, 1u);
                 mma_commit(&bar_c3);
                 mma_commit(&bar_free[s]);
             }
@@ -316,7 +317,6 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_tc_kernel(const __grid_
         if (lane == 0) {
             const uint32_t id1 = idesc_bf16(128, 64, false, false);  // [Kbar; Qbar] Ktil^T
             const uint32_t id2 = idesc_bf16(128, 64, true, false);   // Kbar^T T'^T, V^T T'^T (A MN-major)
-            const uint32_t tt = sm_base + OFF_TT;
             int c1 = 0, c2 = 0;
             uint64_t deadline = globaltimer_ns() + kWaitNs;
             uint32_t spins = 0;
@@ -326,11 +326,12 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_tc_kernel(const __grid_
                     (c1 == 0 || mbar_test_wait(&bar_mfree, (c1 - 1) & 1))) {
                     tc_fence_after();
                     const uint32_t st = sm_base + (c1 & 1) * kStage;
+                    const uint64_t dA = sdesc_sw128(st + OFF_R, 16, 1024);   // [Kbar; Qbar], K-major
+                    const uint64_t dB = sdesc_sw128(st + OFF_G, 16, 1024);   // Ktil, K-major
+#pragma unroll
                     for (int ks = 0; ks < 8; ++ks)
-                        mma_bf16_ss(tmem + TM_PREP,
-                                    sdesc_sw128(st + OFF_R + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024),
-                                    sdesc_sw128(st + OFF_G + (ks >> 2) * 8192 + (ks & 3) * 32, 16, 1024), id1,
-                                    ks > 0 ? 1u : 0u);
+                        mma_bf16_ss(tmem + TM_PREP, dA + (((ks >> 2) * 16384 + (ks & 3) * 32) >> 4),
+                                    dB + (((ks >> 2) * 8192 + (ks & 3) * 32) >> 4), id1, ks > 0 ? 1u : 0u);
                     mma_commit(&bar_mma1);
                     ++c1;
                     progress = true;
@@ -339,12 +340,15 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_tc_kernel(const __grid_
                     (c2 == 0 || (mbar_test_wait(&bar_wfree, (c2 - 1) & 1) && mbar_test_wait(&bar_uready, (c2 - 1) & 1)))) {
                     tc_fence_after();
                     const uint32_t st = sm_base + (c2 & 1) * kStage;
+                    const uint64_t dK = sdesc_sw128(st + OFF_R, 16384, 1024);  // Kbar^T, MN-major
+                    const uint64_t dV = sdesc_sw128(st + OFF_V, 8192, 1024);   // V^T, MN-major
+                    const uint64_t dT = sdesc_sw128(sm_base + OFF_TT + (c2 & 1) * 8192, 16, 1024);  // T', K-major
+#pragma unroll
                     for (int ks = 0; ks < 4; ++ks)
-                        mma_bf16_ss(tmem + TM_W, sdesc_sw128(st + OFF_R + ks * 2048, 16384, 1024),
-                                    sdesc_sw128(tt + ks * 32, 16, 1024), id2, ks > 0 ? 1u : 0u);
+                        mma_bf16_ss(tmem + TM_W, dK + ((ks * 2048) >> 4), dT + ((ks * 32) >> 4), id2, ks > 0 ? 1u : 0u);
+#pragma unroll
                     for (int ks = 0; ks < 4; ++ks)
-                        mma_bf16_ss(tmem + TM_U, sdesc_sw128(st + OFF_V + ks * 2048, 8192, 1024),
-                                    sdesc_sw128(tt + ks * 32, 16, 1024), id2, ks > 0 ? 1u : 0u);
+                        mma_bf16_ss(tmem + TM_U, dV + ((ks * 2048) >> 4), dT + ((ks * 32) >> 4), id2, ks > 0 ? 1u : 0u);
                     mma_commit(&bar_mma2);
                     ++c2;
                     progress = true;
@@ -483,7 +487,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_tc_kernel(const __grid_
                 tmem_ld_wait();
 #pragma unroll
                 for (int e = 0; e < 16; e += 4) {
-                    const float4 fa = ld4(&s_ac[s][cc + e]), fb = ld4(&s_ac[s][cc + 16 + e]);
+                    const float4 fa = ld4(&s_ac[c % 3][cc + e]), fb = ld4(&s_ac[c % 3][cc + 16 + e]);
                     a[e] = __float_as_uint(__uint_as_float(a[e]) * fa.x);
                     a[e + 1] = __float_as_uint(__uint_as_float(a[e + 1]) * fa.y);
                     a[e + 2] = __float_as_uint(__uint_as_float(a[e + 2]) * fa.z);
@@ -523,15 +527,14 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_tc_kernel(const __grid_
             tmem_st_wait();
             tc_fence_before();
             named_bar(2, 128);
-            if (j == 0) mbar_arrive(&bar_free[s]);
         }
         if (done && o_t0 >= 0) store_o(o_t0);
     } else if (warp >= 8 && warp < 12) {
         // ------------------------------------------------------------------ decay group (warps 8-11)
         // Decay factors and the scaled operand tiles, one chunk ahead of the solve group.
-        // Thread = (token half, channel pair): alpha = exp(g), prefix products within
-        // the half, the first half's totals carried into the second, then Kbar, Qbar,
-        // Ktil written over k, q, g in place.
+        // Thread = (16-token segment, 4 channels): alpha = exp(g), prefix products within
+        // the segment, the earlier segments' totals carried in, then Kbar, Qbar, Ktil
+        // written over k, q, g in place.
         const int pt = tid - 256;
         int gseq = 0;
         const float kMinDecay = 7.888609052210118e-31f;  // 2^-100
@@ -540,59 +543,72 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_tc_kernel(const __grid_
             uint8_t *st = sm + s * kStage;
             if (!group_wait(&bar_full[s], (c >> 1) & 1, ctl, &s_grp_fail[0], 1, 128, gseq)) break;
             {
-                const int cp = pt & 63, half = pt >> 6;
-                const int kb = cp >> 5, cc = 2 * (cp & 31), ch = kb * 64 + cc;
+                // thread = (token segment of 16, channel quad): 64-bit shared accesses
+                const int cq = pt & 31, seg = pt >> 5;
+                const int kb = cq >> 4, cc = 4 * (cq & 15), ch = kb * 64 + cc;
                 uint8_t *Rk = st + OFF_R + kb * 16384;
                 uint8_t *Rq = Rk + 8192;
                 uint8_t *G = st + OFF_G + kb * 8192;
-                const int r0 = 32 * half;
-                float A0[32], A1[32];
-                float p0 = 1.f, p1 = 1.f;
+                const int r0 = 16 * seg;
+                float A[16][4];
+                float p0 = 1.f, p1 = 1.f, p2 = 1.f, p3 = 1.f;
 #pragma unroll
-                for (int rr = 0; rr < 32; rr += 8) {
-                    uint32_t gw[8];
+                for (int rr = 0; rr < 16; rr += 4) {
+                    uint2 gw[4];
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) gw[e] = ld32(G, swz(r0 + rr + e, cc));
+                    for (int e = 0; e < 4; ++e) gw[e] = *reinterpret_cast<const uint2 *>(G + swz(r0 + rr + e, cc));
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        const float2 gf = bf2_to_f2(gw[e]);
-                        p0 *= __expf(gf.x);
-                        p1 *= __expf(gf.y);
-                        A0[rr + e] = p0;
-                        A1[rr + e] = p1;
+                    for (int e = 0; e < 4; ++e) {
+                        const float2 lo = bf2_to_f2(gw[e].x), hi = bf2_to_f2(gw[e].y);
+                        p0 *= __expf(lo.x);
+                        p1 *= __expf(lo.y);
+                        p2 *= __expf(hi.x);
+                        p3 *= __expf(hi.y);
+                        A[rr + e][0] = p0;
+                        A[rr + e][1] = p1;
+                        A[rr + e][2] = p2;
+                        A[rr + e][3] = p3;
                     }
                 }
-                if (half == 0) {
-                    s_tot[ch] = p0;
-                    s_tot[ch + 1] = p1;
-                }
+                st4(&s_tot[seg][ch], make_float4(p0, p1, p2, p3));
                 named_bar(1, 128);
-                const float m0 = half ? s_tot[ch] : 1.f, m1 = half ? s_tot[ch + 1] : 1.f;
+                float4 m = make_float4(1.f, 1.f, 1.f, 1.f);
+                for (int q = 0; q < seg; ++q) {
+                    const float4 t = ld4(&s_tot[q][ch]);
+                    m = make_float4(m.x * t.x, m.y * t.y, m.z * t.z, m.w * t.w);
+                }
                 const float sc = p.scale;
 #pragma unroll
-                for (int rr = 0; rr < 32; rr += 8) {
-                    uint32_t kw[8], qw[8];
+                for (int rr = 0; rr < 16; rr += 4) {
+                    uint2 kw[4], qw[4];
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) {
+                    for (int e = 0; e < 4; ++e) {
                         const uint32_t off = swz(r0 + rr + e, cc);
-                        kw[e] = ld32(Rk, off);
-                        qw[e] = ld32(Rq, off);
+                        kw[e] = *reinterpret_cast<const uint2 *>(Rk + off);
+                        qw[e] = *reinterpret_cast<const uint2 *>(Rq + off);
                     }
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) {
+                    for (int e = 0; e < 4; ++e) {
                         const uint32_t off = swz(r0 + rr + e, cc);
-                        const float a0 = m0 * A0[rr + e], a1 = m1 * A1[rr + e];
-                        const float2 kf = bf2_to_f2(kw[e]), qf = bf2_to_f2(qw[e]);
-                        st32(Rk, off, pack_bf16x2(kf.x * a0, kf.y * a1));
-                        st32(Rq, off, pack_bf16x2(qf.x * (sc * a0), qf.y * (sc * a1)));
-                        st32(G, off, pack_bf16x2(kf.x * __fdividef(1.f, a0), kf.y * __fdividef(1.f, a1)));
+                        const float a0 = m.x * A[rr + e][0], a1 = m.y * A[rr + e][1];
+                        const float a2 = m.z * A[rr + e][2], a3 = m.w * A[rr + e][3];
+                        const float2 k01 = bf2_to_f2(kw[e].x), k23 = bf2_to_f2(kw[e].y);
+                        const float2 q01 = bf2_to_f2(qw[e].x), q23 = bf2_to_f2(qw[e].y);
+                        *reinterpret_cast<uint2 *>(Rk + off) =
+                            make_uint2(pack_bf16x2(k01.x * a0, k01.y * a1), pack_bf16x2(k23.x * a2, k23.y * a3));
+                        *reinterpret_cast<uint2 *>(Rq + off) =
+                            make_uint2(pack_bf16x2(q01.x * (sc * a0), q01.y * (sc * a1)),
+                                       pack_bf16x2(q23.x * (sc * a2), q23.y * (sc * a3)));
+                        *reinterpret_cast<uint2 *>(G + off) =
+                            make_uint2(pack_bf16x2(k01.x * rcp_approx(a0), k01.y * rcp_approx(a1)),
+                                       pack_bf16x2(k23.x * rcp_approx(a2), k23.y * rcp_approx(a3)));
                     }
                 }
-                if (half == 1) {
-                    const float ac0 = m0 * p0, ac1 = m1 * p1;
-                    if (!(ac0 >= kMinDecay) || !(ac1 >= kMinDecay)) atomicOr(p.status, DEV_ERR_GATE);
-                    s_ac[s][ch] = ac0;
-                    s_ac[s][ch + 1] = ac1;
+                if (seg == 3) {
+                    const float4 ac = make_float4(m.x * p0, m.y * p1, m.z * p2, m.w * p3);
+                    if (!(ac.x >= kMinDecay) || !(ac.y >= kMinDecay) || !(ac.z >= kMinDecay) || !(ac.w >= kMinDecay))
+                        atomicOr(p.status, DEV_ERR_GATE);
+                    st4(&s_ac[c % 3][ch], ac);
                 }
             }
             fence_proxy_async_smem();
@@ -611,9 +627,12 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_tc_kernel(const __grid_
         float *Mb = reinterpret_cast<float *>(sm + OFF_M);
         float *Tb = reinterpret_cast<float *>(sm + OFF_T);
         for (int i = pt; i < 64 * kLdT; i += 128) Tb[i] = 0.f;  // blocks above the diagonal stay zero
+        for (int i = pt; i < 2 * 8192 / 16; i += 128)           // likewise in both T' tiles
+            reinterpret_cast<uint4 *>(sm + OFF_TT)[i] = make_uint4(0u, 0u, 0u, 0u);
         named_bar(3, 128);
         for (int c = 0; c < nfull; ++c) {
             const int s = c & 1;
+            uint8_t *TT = sm + OFF_TT + (c & 1) * 8192;  // this chunk's T' = T Diag(beta), bf16
             // (2) M (fp32, rows scaled by beta, strictly lower) and P (bf16, lower incl.).
             // Accumulator lane x: rows 0-63 = Kbar . Ktil, 64-127 = Qbar . Ktil.
             if (!group_wait(&bar_mma1, c & 1, ctl, &s_grp_fail[2], 3, 128, gseq)) break;
@@ -683,8 +702,12 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_tc_kernel(const __grid_
                         }
                     }
                 }
+                const float bm = s_beta[s][R0 + mm];
 #pragma unroll
-                for (int l = 0; l < 16; ++l) Tb[(R0 + l) * kLdT + R0 + mm] = xv[l];
+                for (int l = 0; l < 16; ++l) {
+                    Tb[(R0 + l) * kLdT + R0 + mm] = xv[l];
+                    *reinterpret_cast<__nv_bfloat16 *>(TT + swz(R0 + l, R0 + mm)) = __float2bfloat16_rn(xv[l] * bm);
+                }
             }
             named_bar(3, 128);
             // ... then the off-diagonal blocks as tf32 tensor-core tiles (m16n8k8; each warp
@@ -716,10 +739,14 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_tc_kernel(const __grid_
                              Tb[(Ra + gq) * kLdT + Ra + k0 + tq + 4], Tb[(Ra + gq + 8) * kLdT + Ra + k0 + tq + 4],
                              X[(k0 + tq) * kLdX + n0 + gq], X[(k0 + tq + 4) * kLdX + n0 + gq]);
                 }
-                Tb[(Ra + gq) * kLdT + Rb + n0 + 2 * tq] = -d[0];
-                Tb[(Ra + gq) * kLdT + Rb + n0 + 2 * tq + 1] = -d[1];
-                Tb[(Ra + gq + 8) * kLdT + Rb + n0 + 2 * tq] = -d[2];
-                Tb[(Ra + gq + 8) * kLdT + Rb + n0 + 2 * tq + 1] = -d[3];
+                const int cl = Rb + n0 + 2 * tq;
+                Tb[(Ra + gq) * kLdT + cl] = -d[0];
+                Tb[(Ra + gq) * kLdT + cl + 1] = -d[1];
+                Tb[(Ra + gq + 8) * kLdT + cl] = -d[2];
+                Tb[(Ra + gq + 8) * kLdT + cl + 1] = -d[3];
+                const float b0 = s_beta[s][cl], b1 = s_beta[s][cl + 1];
+                *reinterpret_cast<uint32_t *>(TT + swz(Ra + gq, cl)) = pack_bf16x2(-d[0] * b0, -d[1] * b1);
+                *reinterpret_cast<uint32_t *>(TT + swz(Ra + gq + 8, cl)) = pack_bf16x2(-d[2] * b0, -d[3] * b1);
             }
             named_bar(3, 128);
             {
@@ -762,35 +789,16 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_tc_kernel(const __grid_
                 }
 #pragma unroll
                 for (int nt = 0; nt < 2; ++nt) {
-                    const int n0 = 16 * nh + 8 * nt;
-                    Tb[(32 + r0 + gq) * kLdT + n0 + 2 * tq] = -d[nt][0];
-                    Tb[(32 + r0 + gq) * kLdT + n0 + 2 * tq + 1] = -d[nt][1];
-                    Tb[(40 + r0 + gq) * kLdT + n0 + 2 * tq] = -d[nt][2];
-                    Tb[(40 + r0 + gq) * kLdT + n0 + 2 * tq + 1] = -d[nt][3];
+                    const int cl = 16 * nh + 8 * nt + 2 * tq;
+                    const float b0 = s_beta[s][cl], b1 = s_beta[s][cl + 1];
+                    *reinterpret_cast<uint32_t *>(TT + swz(32 + r0 + gq, cl)) =
+                        pack_bf16x2(-d[nt][0] * b0, -d[nt][1] * b1);
+                    *reinterpret_cast<uint32_t *>(TT + swz(40 + r0 + gq, cl)) =
+                        pack_bf16x2(-d[nt][2] * b0, -d[nt][3] * b1);
                 }
             }
-            // T' of the previous chunk must have been consumed before it is overwritten
-            if (c > 0 && !group_wait(&bar_mma2, (c - 1) & 1, ctl, &s_grp_fail[2], 3, 128, gseq)) break;
-            if (c == 0) named_bar(3, 128);
-            // T' = T Diag(beta) -> bf16, K-major rows r (entries above the diagonal are zero)
-            {
-                const int r = pt >> 1, half = pt & 1;
-                uint8_t *TT = sm + OFF_TT;
-#pragma unroll
-                for (int q8 = 0; q8 < 4; ++q8) {
-                    const int c0 = half * 32 + q8 * 8;
-                    const float4 t0 = ld4(&Tb[r * kLdT + c0]), t1 = ld4(&Tb[r * kLdT + c0 + 4]);
-                    const float4 b0 = ld4(&s_beta[s][c0]), b1 = ld4(&s_beta[s][c0 + 4]);
-                    const float tv[8] = {t0.x * b0.x, t0.y * b0.y, t0.z * b0.z, t0.w * b0.w,
-                                         t1.x * b1.x, t1.y * b1.y, t1.z * b1.z, t1.w * b1.w};
-                    uint4 v;
-                    uint32_t *vw = reinterpret_cast<uint32_t *>(&v);
-#pragma unroll
-                    for (int e = 0; e < 4; ++e)
-                        vw[e] = pack_bf16x2(c0 + 2 * e <= r ? tv[2 * e] : 0.f, c0 + 2 * e + 1 <= r ? tv[2 * e + 1] : 0.f);
-                    *reinterpret_cast<uint4 *>(TT + chunk16(r, c0 >> 3)) = v;
-                }
-            }
+            // (T' was written block by block above; the tile of chunk c-2, its previous
+            // content, was consumed before MMA1 of this chunk was issued.)
             fence_proxy_async_smem();
             named_bar(3, 128);
             if (pt == 0) mbar_arrive(&bar_tready);
