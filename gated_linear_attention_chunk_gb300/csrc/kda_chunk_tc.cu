@@ -322,7 +322,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_tc_kernel(const __grid_
             uint32_t spins = 0;
             while (c2 < nfull) {
                 bool progress = false;
-                if (c1 < nfull && c1 <= c2 + 1 && mbar_test_wait(&bar_elem, c1 & 1) &&
+                if (c1 < nfull && mbar_test_wait(&bar_elem, c1 & 1) &&
                     (c1 == 0 || mbar_test_wait(&bar_mfree, (c1 - 1) & 1))) {
                     tc_fence_after();
                     const uint32_t st = sm_base + (c1 & 1) * kStage;
@@ -797,8 +797,11 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_tc_kernel(const __grid_
                         pack_bf16x2(-d[nt][2] * b0, -d[nt][3] * b1);
                 }
             }
-            // (T' was written block by block above; the tile of chunk c-2, its previous
-            // content, was consumed before MMA1 of this chunk was issued.)
+            // T' was written block by block above (its tile's previous content, chunk c-2,
+            // was consumed before the previous chunk announced its T').  Announce this
+            // chunk's T' only once the previous chunk's W / Utl product has completed: that
+            // product consumed the previous announcement, so the barrier phases cannot alias.
+            if (c > 0 && !group_wait(&bar_mma2, (c - 1) & 1, ctl, &s_grp_fail[2], 3, 128, gseq)) break;
             fence_proxy_async_smem();
             named_bar(3, 128);
             if (pt == 0) mbar_arrive(&bar_tready);
