@@ -34,9 +34,10 @@ import workloads  # noqa: E402
 METRIC = "KDA chunk_fwd tokens/s at T=4K-128K (1 GB300) and % of roofline"
 UNIT = "tokens/s"
 
-# DRAM traffic of the dominant kernel per launch from an ncu capture (None until
-# captured for the current kernel build).  Source: profiles/.
-DOMINANT_TRAFFIC = None
+# DRAM bytes (read + write) of one kda_chunk_tc_kernel launch on prefill_4k, from the
+# ncu capture summarised in profiles/kda_chunk_tc_prefill_4k.md (546.7 MB read +
+# 117.8 MB written).  Reset to None whenever that kernel changes until it is re-captured.
+DOMINANT_TRAFFIC = {"prefill_4k": 664497664}
 
 
 # ------------------------------------------------------------------------------------------------
@@ -386,11 +387,11 @@ def run_gpu(args, world, rank, local):
     if bound == "hbm":
         achieved = nbytes / (kern_ms / 1e3) / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
-                "frac": achieved / hbm_peak, "traffic": DOMINANT_TRAFFIC}
+                "frac": achieved / hbm_peak, "traffic": (DOMINANT_TRAFFIC or {}).get(args.workload)}
     else:
         achieved = flops / (kern_ms / 1e3) / 1e12
         roof = {"bound": "tensor", "achieved": achieved, "peak": tf_peak, "unit": "TFLOP/s",
-                "frac": achieved / tf_peak, "traffic": DOMINANT_TRAFFIC}
+                "frac": achieved / tf_peak, "traffic": (DOMINANT_TRAFFIC or {}).get(args.workload)}
     roof.update({"peak_source": f"{peak_src} (MEASURED_PEAKS.json)" if peak_src == "measured" else peak_src,
                  "algorithmic_bytes": nbytes, "algorithmic_flops": flops,
                  "kernel_ms_median": kern_ms, "roofline_ms": 1e3 * max(t_hbm, t_tc),

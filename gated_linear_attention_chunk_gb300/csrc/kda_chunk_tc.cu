@@ -288,19 +288,19 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_tc_kernel(const __grid_
                 for (int ks = 0; ks < 8; ++ks)
                     mma_bf16_ts(tmem + TM_U, tmem + TM_SB + 8 * ks, dW + (((ks >> 2) * 16384 + (ks & 3) * 2048) >> 4),
                                 idU, 1u);
+                mma_commit(&bar_c1);  // U is on the critical path: release its epilogue first
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks)
                     mma_bf16_ts(tmem + TM_O, tmem + TM_SB + 8 * ks, dQ + (((ks >> 2) * 16384 + (ks & 3) * 32) >> 4),
                                 idO, ks > 0 ? 1u : 0u);
-                mma_commit(&bar_c1);
                 if (!wait_bar(&bar_uready, c & 1, ctl)) break;
                 tc_fence_after();
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks)
-                    mma_bf16_ts(tmem + TM_O, tmem + TM_UB + 8 * ks, dP + ((ks * 32) >> 4), idO, 1u);
+                    mma_bf16_ts(tmem + TM_S, tmem + TM_UB + 8 * ks, dG + ((ks * 2048) >> 4), idS, 1u);
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks)
-                    mma_bf16_ts(tmem + TM_S, tmem + TM_UB + 8 * ks, dG + ((ks * 2048) >> 4), idS, 1u);
+                    mma_bf16_ts(tmem + TM_O, tmem + TM_UB + 8 * ks, dP + ((ks * 32) >> 4), idO, 1u);
                 mma_commit(&bar_c3);
                 mma_commit(&bar_free[s]);
             }
