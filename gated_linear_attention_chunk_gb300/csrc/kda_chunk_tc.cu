@@ -86,9 +86,6 @@ __device__ __forceinline__ uint32_t swz(int row, int col) {
 __device__ __forceinline__ uint32_t chunk16(int row, int chunk) {
     return static_cast<uint32_t>(row * 128 + ((chunk ^ (row & 7)) << 4));
 }
-__device__ __forceinline__ float2 bf2_to_f2(uint32_t w) {
-    return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w));
-}
 __device__ __forceinline__ float4 ld4(const float *p) { return *reinterpret_cast<const float4 *>(p); }
 __device__ __forceinline__ void st4(float *p, float4 v) { *reinterpret_cast<float4 *>(p) = v; }
 __device__ __forceinline__ float rcp_approx(float x) {
@@ -104,6 +101,43 @@ __device__ __forceinline__ void mma_tf32(float (&c)[4], float a0, float a1, floa
         : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
         : "r"(__float_as_uint(a0)), "r"(__float_as_uint(a1)), "r"(__float_as_uint(a2)), "r"(__float_as_uint(a3)),
           "r"(__float_as_uint(b0)), "r"(__float_as_uint(b1)));
+}
+
+// Packed fp32 pairs: two floats in one 64-bit register pair, multiplied with one
+// f32x2 instruction (the decay and state-scaling loops are issue-bound).
+__device__ __forceinline__ uint64_t f2(float x, float y) {
+    uint64_t d;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "f"(x), "f"(y));
+    return d;
+}
+__device__ __forceinline__ float2 uf2(uint64_t v) {
+    float2 r;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
+    return r;
+}
+__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+// bf16x2 word -> fp32 pair (exact)
+__device__ __forceinline__ uint64_t bf2x(uint32_t w) { return f2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u)); }
+// fp32 pair -> bf16x2 word (round to nearest even)
+__device__ __forceinline__ uint32_t pk2(uint64_t v) {
+    const float2 f = uf2(v);
+    return pack_bf16x2(f.x, f.y);
+}
+// (x, y) *= (fx, fy) on fp32 bit patterns, one packed multiply
+__device__ __forceinline__ void scale2(uint32_t &x, uint32_t &y, float fx, float fy) {
+    const float2 t = uf2(mul2(f2(__uint_as_float(x), __uint_as_float(y)), f2(fx, fy)));
+    x = __float_as_uint(t.x);
+    y = __float_as_uint(t.y);
+}
+// 2^x (exp(g) is evaluated as 2^(g log2 e))
+__device__ __forceinline__ float ex2_approx(float x) {
+    float r;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+    return r;
 }
 __device__ __forceinline__ void named_bar(int id, int n) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
@@ -488,14 +522,10 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_tc_kernel(const __grid_
 #pragma unroll
                 for (int e = 0; e < 16; e += 4) {
                     const float4 fa = ld4(&s_ac[c % 3][cc + e]), fb = ld4(&s_ac[c % 3][cc + 16 + e]);
-                    a[e] = __float_as_uint(__uint_as_float(a[e]) * fa.x);
-                    a[e + 1] = __float_as_uint(__uint_as_float(a[e + 1]) * fa.y);
-                    a[e + 2] = __float_as_uint(__uint_as_float(a[e + 2]) * fa.z);
-                    a[e + 3] = __float_as_uint(__uint_as_float(a[e + 3]) * fa.w);
-                    b[e] = __float_as_uint(__uint_as_float(b[e]) * fb.x);
-                    b[e + 1] = __float_as_uint(__uint_as_float(b[e + 1]) * fb.y);
-                    b[e + 2] = __float_as_uint(__uint_as_float(b[e + 2]) * fb.z);
-                    b[e + 3] = __float_as_uint(__uint_as_float(b[e + 3]) * fb.w);
+                    scale2(a[e], a[e + 1], fa.x, fa.y);
+                    scale2(a[e + 2], a[e + 3], fa.z, fa.w);
+                    scale2(b[e], b[e + 1], fb.x, fb.y);
+                    scale2(b[e + 2], b[e + 3], fb.z, fb.w);
                 }
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
@@ -550,8 +580,9 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_tc_kernel(const __grid_
                 uint8_t *Rq = Rk + 8192;
                 uint8_t *G = st + OFF_G + kb * 8192;
                 const int r0 = 16 * seg;
-                float A[16][4];
-                float p0 = 1.f, p1 = 1.f, p2 = 1.f, p3 = 1.f;
+                uint64_t A01[16], A23[16];
+                uint64_t P01 = f2(1.f, 1.f), P23 = f2(1.f, 1.f);
+                const uint64_t L2E = f2(1.4426950408889634f, 1.4426950408889634f);
 #pragma unroll
                 for (int rr = 0; rr < 16; rr += 4) {
                     uint2 gw[4];
@@ -559,17 +590,15 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_tc_kernel(const __grid_
                     for (int e = 0; e < 4; ++e) gw[e] = *reinterpret_cast<const uint2 *>(G + swz(r0 + rr + e, cc));
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
-                        const float2 lo = bf2_to_f2(gw[e].x), hi = bf2_to_f2(gw[e].y);
-                        p0 *= __expf(lo.x);
-                        p1 *= __expf(lo.y);
-                        p2 *= __expf(hi.x);
-                        p3 *= __expf(hi.y);
-                        A[rr + e][0] = p0;
-                        A[rr + e][1] = p1;
-                        A[rr + e][2] = p2;
-                        A[rr + e][3] = p3;
+                        const float2 l01 = uf2(mul2(bf2x(gw[e].x), L2E)), l23 = uf2(mul2(bf2x(gw[e].y), L2E));
+                        P01 = mul2(P01, f2(ex2_approx(l01.x), ex2_approx(l01.y)));
+                        P23 = mul2(P23, f2(ex2_approx(l23.x), ex2_approx(l23.y)));
+                        A01[rr + e] = P01;
+                        A23[rr + e] = P23;
                     }
                 }
+                const float2 pp01 = uf2(P01), pp23 = uf2(P23);
+                const float p0 = pp01.x, p1 = pp01.y, p2 = pp23.x, p3 = pp23.y;
                 st4(&s_tot[seg][ch], make_float4(p0, p1, p2, p3));
                 named_bar(1, 128);
                 float4 m = make_float4(1.f, 1.f, 1.f, 1.f);
@@ -578,30 +607,30 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_tc_kernel(const __grid_
                     m = make_float4(m.x * t.x, m.y * t.y, m.z * t.z, m.w * t.w);
                 }
                 const float sc = p.scale;
+                const uint64_t m01 = f2(m.x, m.y), m23 = f2(m.z, m.w);
+                const uint64_t ms01 = f2(m.x * sc, m.y * sc), ms23 = f2(m.z * sc, m.w * sc);
 #pragma unroll
-                for (int rr = 0; rr < 16; rr += 4) {
-                    uint2 kw[4], qw[4];
+                for (int rr = 0; rr < 16; rr += 2) {
+                    uint2 kw[2], qw[2];
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
+                    for (int e = 0; e < 2; ++e) {
                         const uint32_t off = swz(r0 + rr + e, cc);
                         kw[e] = *reinterpret_cast<const uint2 *>(Rk + off);
                         qw[e] = *reinterpret_cast<const uint2 *>(Rq + off);
                     }
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
+                    for (int e = 0; e < 2; ++e) {
                         const uint32_t off = swz(r0 + rr + e, cc);
-                        const float a0 = m.x * A[rr + e][0], a1 = m.y * A[rr + e][1];
-                        const float a2 = m.z * A[rr + e][2], a3 = m.w * A[rr + e][3];
-                        const float2 k01 = bf2_to_f2(kw[e].x), k23 = bf2_to_f2(kw[e].y);
-                        const float2 q01 = bf2_to_f2(qw[e].x), q23 = bf2_to_f2(qw[e].y);
-                        *reinterpret_cast<uint2 *>(Rk + off) =
-                            make_uint2(pack_bf16x2(k01.x * a0, k01.y * a1), pack_bf16x2(k23.x * a2, k23.y * a3));
+                        const uint64_t a01 = mul2(m01, A01[rr + e]), a23 = mul2(m23, A23[rr + e]);
+                        const uint64_t aq01 = mul2(ms01, A01[rr + e]), aq23 = mul2(ms23, A23[rr + e]);
+                        const uint64_t k01 = bf2x(kw[e].x), k23 = bf2x(kw[e].y);
+                        const float2 fa01 = uf2(a01), fa23 = uf2(a23);
+                        const uint64_t r01 = f2(rcp_approx(fa01.x), rcp_approx(fa01.y));
+                        const uint64_t r23 = f2(rcp_approx(fa23.x), rcp_approx(fa23.y));
+                        *reinterpret_cast<uint2 *>(Rk + off) = make_uint2(pk2(mul2(k01, a01)), pk2(mul2(k23, a23)));
                         *reinterpret_cast<uint2 *>(Rq + off) =
-                            make_uint2(pack_bf16x2(q01.x * (sc * a0), q01.y * (sc * a1)),
-                                       pack_bf16x2(q23.x * (sc * a2), q23.y * (sc * a3)));
-                        *reinterpret_cast<uint2 *>(G + off) =
-                            make_uint2(pack_bf16x2(k01.x * rcp_approx(a0), k01.y * rcp_approx(a1)),
-                                       pack_bf16x2(k23.x * rcp_approx(a2), k23.y * rcp_approx(a3)));
+                            make_uint2(pk2(mul2(bf2x(qw[e].x), aq01)), pk2(mul2(bf2x(qw[e].y), aq23)));
+                        *reinterpret_cast<uint2 *>(G + off) = make_uint2(pk2(mul2(k01, r01)), pk2(mul2(k23, r23)));
                     }
                 }
                 if (seg == 3) {
@@ -679,10 +708,11 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_tc_kernel(const __grid_
             if (pt == 0) mbar_arrive(&bar_mfree);  // PREP columns may take the next chunk's product
 
             // (3) T = (I + M)^-1, blocked: the four 16x16 diagonal blocks D_b by forward
-            // substitution, column-oriented (thread = block, column; each solved entry is
-            // pushed into every later row at once; M read four columns at a time) ...
-            if (pt < 64) {
-                const int b = pt >> 4, mm = pt & 15, R0 = 16 * b;
+            // substitution, column-oriented (warp = block, lane = column, so the four blocks run
+            // on all four schedulers; each solved entry is pushed into every later row at once;
+            // M read four columns at a time) ...
+            if (lane < 16) {
+                const int b = wq, mm = lane, R0 = 16 * b;
                 float acc[16], xv[16];
 #pragma unroll
                 for (int l = 0; l < 16; ++l) acc[l] = 0.f;
