@@ -656,8 +656,10 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_tc_kernel(const __grid_
         float *Mb = reinterpret_cast<float *>(sm + OFF_M);
         float *Tb = reinterpret_cast<float *>(sm + OFF_T);
         for (int i = pt; i < 64 * kLdT; i += 128) Tb[i] = 0.f;  // blocks above the diagonal stay zero
-        for (int i = pt; i < 2 * 8192 / 16; i += 128)           // likewise in both T' tiles
+        for (int i = pt; i < 2 * 8192 / 16; i += 128) {         // likewise in both T' tiles; both P tiles
             reinterpret_cast<uint4 *>(sm + OFF_TT)[i] = make_uint4(0u, 0u, 0u, 0u);
+            reinterpret_cast<uint4 *>(sm + OFF_P)[i] = make_uint4(0u, 0u, 0u, 0u);
+        }
         named_bar(3, 128);
         for (int c = 0; c < nfull; ++c) {
             const int s = c & 1;
@@ -667,38 +669,59 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_tc_kernel(const __grid_
             if (!group_wait(&bar_mma1, c & 1, ctl, &s_grp_fail[2], 3, 128, gseq)) break;
             tc_fence_after();
             {
+                // Warps 0 / 2 of the group hold rows 0-31 of M / P, which need only columns 0-31
+                // (M is read strictly below the diagonal; P's columns 32-63 there stay zero).
                 const int x = wq * 32 + lane;
+                const bool low = (wq & 1) == 0;
                 uint32_t m[64];
                 const uint32_t tP = tmem + (static_cast<uint32_t>(wq * 32) << 16) + TM_PREP;
                 tmem_ld16(tP + 0, *reinterpret_cast<uint32_t(*)[16]>(&m[0]));
                 tmem_ld16(tP + 16, *reinterpret_cast<uint32_t(*)[16]>(&m[16]));
-                tmem_ld16(tP + 32, *reinterpret_cast<uint32_t(*)[16]>(&m[32]));
-                tmem_ld16(tP + 48, *reinterpret_cast<uint32_t(*)[16]>(&m[48]));
+                if (!low) {
+                    tmem_ld16(tP + 32, *reinterpret_cast<uint32_t(*)[16]>(&m[32]));
+                    tmem_ld16(tP + 48, *reinterpret_cast<uint32_t(*)[16]>(&m[48]));
+                }
                 tmem_ld_wait();
                 if (x < 64) {
+                    // M = beta_r (Kbar Ktil^T)[r, :]; entries on and above the diagonal are never read
                     const int r = x;
-                    const float br = s_beta[s][r];
+                    const uint64_t b2 = f2(s_beta[s][r], s_beta[s][r]);
+                    float *row = &Mb[r * kLdM];
+                    auto put4 = [&](int i) {
+                        const float2 u = uf2(mul2(f2(__uint_as_float(m[i]), __uint_as_float(m[i + 1])), b2));
+                        const float2 w = uf2(mul2(f2(__uint_as_float(m[i + 2]), __uint_as_float(m[i + 3])), b2));
+                        st4(row + i, make_float4(u.x, u.y, w.x, w.y));
+                    };
 #pragma unroll
-                    for (int i = 0; i < kC; i += 4)
-                        st4(&Mb[r * kLdM + i], make_float4(i < r ? br * __uint_as_float(m[i]) : 0.f,
-                                                           i + 1 < r ? br * __uint_as_float(m[i + 1]) : 0.f,
-                                                           i + 2 < r ? br * __uint_as_float(m[i + 2]) : 0.f,
-                                                           i + 3 < r ? br * __uint_as_float(m[i + 3]) : 0.f));
+                    for (int i = 0; i < 32; i += 4) put4(i);
+                    if (!low) {
+#pragma unroll
+                        for (int i = 32; i < 64; i += 4) put4(i);
+                    }
                 } else {
+                    // P = (Qbar Ktil^T)[r, :] for i <= r, bf16
                     const int r = x - 64;
                     uint8_t *P = sm + OFF_P + s * 8192;
-#pragma unroll
-                    for (int q8 = 0; q8 < 8; ++q8) {
+                    auto put8 = [&](int q8, bool masked) {
                         uint4 v;
                         uint32_t *vw = reinterpret_cast<uint32_t *>(&v);
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
                             const int i0 = q8 * 8 + 2 * e;
-                            const float x0 = (i0 <= r) ? __uint_as_float(m[i0]) : 0.f;
-                            const float x1 = (i0 + 1 <= r) ? __uint_as_float(m[i0 + 1]) : 0.f;
+                            const float x0 = (!masked || i0 <= r) ? __uint_as_float(m[i0]) : 0.f;
+                            const float x1 = (!masked || i0 + 1 <= r) ? __uint_as_float(m[i0 + 1]) : 0.f;
                             vw[e] = pack_bf16x2(x0, x1);
                         }
                         *reinterpret_cast<uint4 *>(P + chunk16(r, q8)) = v;
+                    };
+                    if (low) {
+#pragma unroll
+                        for (int q8 = 0; q8 < 4; ++q8) put8(q8, true);
+                    } else {
+#pragma unroll
+                        for (int q8 = 0; q8 < 4; ++q8) put8(q8, false);
+#pragma unroll
+                        for (int q8 = 4; q8 < 8; ++q8) put8(q8, true);
                     }
                 }
             }
