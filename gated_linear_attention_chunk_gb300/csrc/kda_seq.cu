@@ -16,13 +16,16 @@
 // Computing z and qk from the decayed state lets one reduction pass serve both
 // the delta step and the output, so each token costs one __syncthreads.
 //
-// Layout: 256 threads; a thread owns NS rows x 4 consecutive columns of S
-// (float4), so state loads/stores are 128-bit and a warp covers whole rows.
+// Layout: the dv columns of S follow independent recurrences (y, u and the update
+// of column j involve column j only), so a CTA owns one block of 32 columns of
+// one (sequence, head): 128 threads, a thread holding dk/16 rows x 4 consecutive
+// columns (float4, 128-bit loads/stores).  Four column blocks per state give the
+// SM many small CTAs, whose state loads overlap the other CTAs' token steps.
 // Reductions over dk run in a fixed order (rows in order inside a thread, then
-// the two row-halves of a warp, then warps 0..7 in order), and every
-// floating-point step uses an explicit round-to-nearest intrinsic, so every
-// caller of this routine -- decode, replay and the prefill tail -- produces
-// the same bits for the same state and tokens.
+// the four row groups of a warp as (0+1)+(2+3), then warps 0..3 in order), and
+// every floating-point step uses an explicit round-to-nearest intrinsic, so every
+// caller of this routine -- decode, replay and the prefill tail -- produces the
+// same bits for the same state and tokens.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -32,8 +35,9 @@
 namespace kda {
 namespace {
 
-constexpr int kSeqThreads = 256;
+constexpr int kSeqThreads = 128;
 constexpr int kSeqWarps = kSeqThreads / 32;
+constexpr int kColBlock = 32;  // state columns per CTA
 
 __device__ __forceinline__ float ld_in(const float *p, int64_t i) { return p[i]; }
 __device__ __forceinline__ float ld_in(const __nv_bfloat16 *p, int64_t i) { return __bfloat162float(p[i]); }
@@ -48,15 +52,49 @@ __device__ __forceinline__ void st_out4(__nv_bfloat16 *p, float4 v) {
     *reinterpret_cast<uint2 *>(p) = packed;
 }
 
+// float4 arithmetic as two packed f32x2 instructions each (per-lane IEEE round to
+// nearest, so the bits equal four scalar __fmaf_rn / __fadd_rn / __fmul_rn)
+__device__ __forceinline__ uint64_t f2u(float x, float y) {
+    uint64_t d;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "f"(x), "f"(y));
+    return d;
+}
+__device__ __forceinline__ float2 u2f(uint64_t v) {
+    float2 r;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
+    return r;
+}
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(f2u(a.x, a.y)), "l"(f2u(b.x, b.y)), "l"(f2u(c.x, c.y)));
+    return u2f(d);
+}
+__device__ __forceinline__ float2 add2(float2 a, float2 b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(f2u(a.x, a.y)), "l"(f2u(b.x, b.y)));
+    return u2f(d);
+}
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(f2u(a.x, a.y)), "l"(f2u(b.x, b.y)));
+    return u2f(d);
+}
 __device__ __forceinline__ float4 f4_fma(float a, float4 b, float4 c) {
-    return make_float4(__fmaf_rn(a, b.x, c.x), __fmaf_rn(a, b.y, c.y), __fmaf_rn(a, b.z, c.z),
-                       __fmaf_rn(a, b.w, c.w));
+    const float2 aa = make_float2(a, a);
+    const float2 lo = fma2(aa, make_float2(b.x, b.y), make_float2(c.x, c.y));
+    const float2 hi = fma2(aa, make_float2(b.z, b.w), make_float2(c.z, c.w));
+    return make_float4(lo.x, lo.y, hi.x, hi.y);
 }
 __device__ __forceinline__ float4 f4_add(float4 a, float4 b) {
-    return make_float4(__fadd_rn(a.x, b.x), __fadd_rn(a.y, b.y), __fadd_rn(a.z, b.z), __fadd_rn(a.w, b.w));
+    const float2 lo = add2(make_float2(a.x, a.y), make_float2(b.x, b.y));
+    const float2 hi = add2(make_float2(a.z, a.w), make_float2(b.z, b.w));
+    return make_float4(lo.x, lo.y, hi.x, hi.y);
 }
 __device__ __forceinline__ float4 f4_scale(float4 a, float s) {
-    return make_float4(__fmul_rn(a.x, s), __fmul_rn(a.y, s), __fmul_rn(a.z, s), __fmul_rn(a.w, s));
+    const float2 ss = make_float2(s, s);
+    const float2 lo = mul2(make_float2(a.x, a.y), ss);
+    const float2 hi = mul2(make_float2(a.z, a.w), ss);
+    return make_float4(lo.x, lo.y, hi.x, hi.y);
 }
 __device__ __forceinline__ float4 f4_shfl_xor(float4 a, int m) {
     return make_float4(__shfl_xor_sync(0xffffffffu, a.x, m), __shfl_xor_sync(0xffffffffu, a.y, m),
@@ -64,15 +102,17 @@ __device__ __forceinline__ float4 f4_shfl_xor(float4 a, int m) {
 }
 
 template <int DK, int DV, typename Tin, bool WRITE_O>
-__global__ void __launch_bounds__(kSeqThreads) kda_seq_kernel(SeqParams p) {
-    constexpr int LPR = DV / 4;           // lanes per state row
-    constexpr int RPW = 32 / LPR;         // rows per warp per step (1 or 2)
-    constexpr int RPS = kSeqWarps * RPW;  // rows per step
+__global__ void __launch_bounds__(kSeqThreads, 6) kda_seq_kernel(SeqParams p) {
+    constexpr int CB = kColBlock;         // columns of this CTA
+    constexpr int NCB = DV / CB;          // column blocks per state
+    constexpr int LPR = CB / 4;           // lanes per state row (8)
+    constexpr int RPW = 32 / LPR;         // rows per warp per step (4)
+    constexpr int RPS = kSeqWarps * RPW;  // rows per step (16)
     constexpr int NS = DK / RPS;          // rows per thread
-    static_assert(LPR * RPW == 32 && NS * RPS == DK, "thread layout");
+    static_assert(LPR * RPW == 32 && RPW == 4 && NS * RPS == DK && NCB * CB == DV, "thread layout");
 
     __shared__ float tok_a[3][DK], tok_k[3][DK], tok_q[3][DK];
-    __shared__ __align__(16) float tok_v[3][DV];
+    __shared__ __align__(16) float tok_v[3][CB];
     __shared__ float tok_b[3];
     __shared__ float4 red_y[2][kSeqWarps][LPR], red_z[2][kSeqWarps][LPR];
     __shared__ float red_qk[2][kSeqWarps];
@@ -80,7 +120,8 @@ __global__ void __launch_bounds__(kSeqThreads) kda_seq_kernel(SeqParams p) {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int cg = lane % LPR, rsub = lane / LPR;
     const int row0 = warp * RPW + rsub;
-    const int64_t pair = blockIdx.x;
+    const int64_t pair = blockIdx.x / NCB;
+    const int cb = static_cast<int>(blockIdx.x % NCB), col0 = cb * CB;
     const int n = static_cast<int>(pair / p.H), h = static_cast<int>(pair % p.H);
     const int64_t H = p.H;
 
@@ -98,7 +139,7 @@ __global__ void __launch_bounds__(kSeqThreads) kda_seq_kernel(SeqParams p) {
         if (n == 0 && t0 != 0) ok = false;
         if (n == p.N - 1 && t1 != p.T_total) ok = false;
         if (!ok) {
-            if (tid == 0 && h == 0) atomicOr(p.status, DEV_ERR_SEQLENS);
+            if (tid == 0 && h == 0 && cb == 0) atomicOr(p.status, DEV_ERR_SEQLENS);
             return;
         }
     } else {
@@ -119,7 +160,7 @@ __global__ void __launch_bounds__(kSeqThreads) kda_seq_kernel(SeqParams p) {
     } else {
         const int64_t slot = p.slots ? static_cast<int64_t>(p.slots[n]) : static_cast<int64_t>(n);
         if (slot < 0 || slot >= p.num_slots) {
-            if (tid == 0 && h == 0) atomicOr(p.status, DEV_ERR_SLOT);
+            if (tid == 0 && h == 0 && cb == 0) atomicOr(p.status, DEV_ERR_SLOT);
             return;
         }
         src = p.state_in + (slot * H + h) * DK * DV;
@@ -137,11 +178,11 @@ __global__ void __launch_bounds__(kSeqThreads) kda_seq_kernel(SeqParams p) {
 #pragma unroll
     for (int s = 0; s < NS; ++s) {
         const int row = s * RPS + row0;
-        S[s] = src ? *reinterpret_cast<const float4 *>(src + row * DV + 4 * cg) : make_float4(0.f, 0.f, 0.f, 0.f);
+        S[s] = src ? *reinterpret_cast<const float4 *>(src + row * DV + col0 + 4 * cg) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
 
     // Token staging: threads [0, DK) hold alpha/k/q of one channel, threads
-    // [128, 128 + DV) one value column, thread 255 beta.
+    // [0, CB) also one value column of this block, the last thread beta.
     auto load_raw = [&](int64_t t, float &rg, float &rk, float &rq, float &rv, float &rb) {
         if (tid < DK) {
             const int64_t base = (t * H + h) * DK + tid;
@@ -149,7 +190,7 @@ __global__ void __launch_bounds__(kSeqThreads) kda_seq_kernel(SeqParams p) {
             rk = ld_in(K, base);
             if (WRITE_O) rq = ld_in(Q, base);
         }
-        if (tid >= 128 && tid - 128 < DV) rv = ld_in(V, (t * H + h) * DV + (tid - 128));
+        if (tid < CB) rv = ld_in(V, (t * H + h) * DV + col0 + tid);
         if (tid == kSeqThreads - 1) rb = ld_in(B, t * H + h);
     };
     auto stage = [&](int buf, float rg, float rk, float rq, float rv, float rb) {
@@ -158,7 +199,7 @@ __global__ void __launch_bounds__(kSeqThreads) kda_seq_kernel(SeqParams p) {
             tok_k[buf][tid] = rk;
             if (WRITE_O) tok_q[buf][tid] = __fmul_rn(rq, p.scale);
         }
-        if (tid >= 128 && tid - 128 < DV) tok_v[buf][tid - 128] = rv;
+        if (tid < CB) tok_v[buf][tid] = rv;
         if (tid == kSeqThreads - 1) tok_b[buf] = rb;
     };
 
@@ -191,12 +232,15 @@ __global__ void __launch_bounds__(kSeqThreads) kda_seq_kernel(SeqParams p) {
                 pqk = __fmaf_rn(qq, kk, pqk);
             }
         }
-        if (RPW == 2) {  // combine the two row halves of the warp (a + b == b + a exactly)
-            py = f4_add(py, f4_shfl_xor(py, LPR));
-            if (WRITE_O) {
-                pz = f4_add(pz, f4_shfl_xor(pz, LPR));
-                pqk = __fadd_rn(pqk, __shfl_xor_sync(0xffffffffu, pqk, LPR));
-            }
+        // combine the warp's four row groups as (0 + 1) + (2 + 3); a + b == b + a exactly,
+        // so every lane of a column ends with the same bits
+        py = f4_add(py, f4_shfl_xor(py, LPR));
+        py = f4_add(py, f4_shfl_xor(py, 2 * LPR));
+        if (WRITE_O) {
+            pz = f4_add(pz, f4_shfl_xor(pz, LPR));
+            pz = f4_add(pz, f4_shfl_xor(pz, 2 * LPR));
+            pqk = __fadd_rn(pqk, __shfl_xor_sync(0xffffffffu, pqk, LPR));
+            pqk = __fadd_rn(pqk, __shfl_xor_sync(0xffffffffu, pqk, 2 * LPR));
         }
         if (rsub == 0) {
             red_y[r][warp][cg] = py;
@@ -226,7 +270,7 @@ __global__ void __launch_bounds__(kSeqThreads) kda_seq_kernel(SeqParams p) {
                 qk = __fadd_rn(qk, red_qk[r][w]);
             }
             const float4 o = f4_fma(qk, u, z);
-            st_out4(static_cast<Tin *>(p.o) + (t * H + h) * DV + 4 * cg, o);
+            st_out4(static_cast<Tin *>(p.o) + (t * H + h) * DV + col0 + 4 * cg, o);
         }
     }
 
@@ -234,14 +278,14 @@ __global__ void __launch_bounds__(kSeqThreads) kda_seq_kernel(SeqParams p) {
 #pragma unroll
         for (int s = 0; s < NS; ++s) {
             const int row = s * RPS + row0;
-            *reinterpret_cast<float4 *>(dst + row * DV + 4 * cg) = S[s];
+            *reinterpret_cast<float4 *>(dst + row * DV + col0 + 4 * cg) = S[s];
         }
     }
 }
 
 template <int DK, int DV, typename Tin>
 cudaError_t launch_typed(const SeqParams &p, cudaStream_t stream) {
-    const int64_t blocks = static_cast<int64_t>(p.N) * p.H;
+    const int64_t blocks = static_cast<int64_t>(p.N) * p.H * (DV / kColBlock);
     if (blocks <= 0) return cudaSuccess;
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     if (p.o)
