@@ -228,7 +228,8 @@ def config_dict(args, case):
             "tokens_per_step_per_gpu": case.T_total, "heads": case.H, "dk": case.dk, "dv": case.dv,
             "parallelism": f"dp{max(1, args.gpus)} (independent replicas)",
             "l2": "inputs larger than L2 (no flush needed)" if algorithmic_bytes(case) > 256e6
-                  else "L2 flushed between steps"}
+                  else "L2 flushed between steps",
+            "workspace": "minimum (no T-segment split)" if getattr(args, "plain_workspace", False) else "full"}
 
 
 def measure_state_kernels(kda, dev, hbm_peak, n_seq=128, H=32, d=128, reps=50):
@@ -285,7 +286,12 @@ def run_gpu(args, world, rank, local):
     N, T, H, dk, dv = case.N, case.T_total, case.H, case.dk, case.dv
     o = torch.empty(T, H, dv, dtype=q.dtype, device=dev)
     fs = torch.empty(N, H, dk, dv, dtype=torch.float32, device=dev)
-    ws = kda.new_workspace(kda.KDA_WS_HEADER_BYTES, dev)
+    # The full workspace enables every path of the call (the T-segment split for batches with
+    # few chains and long sequences); --plain-workspace gives only the minimum (unsplit).
+    plain_bytes = kda.KDA_WS_HEADER_BYTES
+    full_bytes = kda.kda_chunk_fwd_workspace_size(N, T, H, dk, dv)
+    split = (not args.plain_workspace) and full_bytes > plain_bytes + N * H * dk * dv * 4
+    ws = kda.new_workspace(plain_bytes if args.plain_workspace else full_bytes, dev)
     flush = None
     if algorithmic_bytes(case) <= 256e6:
         flush = torch.empty(int(256e6), dtype=torch.uint8, device=dev)
@@ -296,7 +302,8 @@ def run_gpu(args, world, rank, local):
 
     # kernels of ours per kda_chunk_fwd: the chunked tensor-core kernel (when it serves this shape)
     # plus the token-sequential partial-chunk kernel
-    launches_per_step = 1 + int(kda.kda_chunk_fwd_uses_tensor_cores(dk, dv, q.dtype))
+    # (with the T-segment split, also the two merge kernels)
+    launches_per_step = 1 + int(kda.kda_chunk_fwd_uses_tensor_cores(dk, dv, q.dtype)) + (2 if split else 0)
     clocks = ClockSampler(local)
     for _ in range(args.warmup):
         step()
@@ -427,6 +434,8 @@ def main(argv=None):
     ap.add_argument("--ref-budget", type=float, default=10.0, help="seconds of oracle work per sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-state-kernels", action="store_true", help="skip the decode/replay bandwidth check")
+    ap.add_argument("--plain-workspace", action="store_true",
+                    help="minimum workspace: kda_chunk_fwd runs without the T-segment split")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -18,6 +18,25 @@ size_t elem_size(kda_dtype t) { return t == KDA_BF16 ? 2 : 4; }
 
 size_t staging_offset() { return KDA_WS_HEADER_BYTES; }
 
+size_t state_bytes(int N, int H, int dk, int dv) {
+    return static_cast<size_t>(N) * static_cast<size_t>(H) * dk * dv * sizeof(float);
+}
+
+// T-segment split (see kda_chunk_fwd_workspace_size in kda.h): used for batches of at
+// most kSplitMaxPairs (sequence, head) chains, which would leave most SMs idle.
+constexpr int64_t kSplitMaxPairs = 48;
+constexpr int64_t kSplitMinTokens = 4096;
+
+bool split_shape(int N, int64_t T_total, int H, int dk, int dv) {
+    return dk == 128 && dv == 128 && N > 0 && static_cast<int64_t>(N) * H <= kSplitMaxPairs &&
+           T_total >= kSplitMinTokens;
+}
+
+// Workspace of a split call: header | staging states | phi | psi | o_phi (bf16 [T, H, dv]).
+size_t split_workspace(int N, int64_t T_total, int H, int dk, int dv) {
+    return staging_offset() + 3 * state_bytes(N, H, dk, dv) + static_cast<size_t>(T_total) * H * dv * 2;
+}
+
 // Clears the status word at the start of the workspace (asynchronously on the stream).
 kda_status clear_status(void *workspace, cudaStream_t s) {
     if (cudaMemsetAsync(workspace, 0, sizeof(uint32_t), s) != cudaSuccess) return KDA_ERR_CUDA;
@@ -30,8 +49,8 @@ extern "C" {
 
 size_t kda_chunk_fwd_workspace_size(int N, int64_t T_total, int H, int dk, int dv) {
     if (N < 0 || T_total < 0 || H <= 0 || !dim_ok(dk) || !dim_ok(dv)) return 0;
-    const size_t states = static_cast<size_t>(N) * static_cast<size_t>(H) * dk * dv * sizeof(float);
-    return staging_offset() + states;
+    if (split_shape(N, T_total, H, dk, dv)) return split_workspace(N, T_total, H, dk, dv);
+    return staging_offset() + state_bytes(N, H, dk, dv);
 }
 
 kda_status kda_chunk_fwd(const void *q, const void *k, const void *v, const void *g, const void *beta,
@@ -42,7 +61,7 @@ kda_status kda_chunk_fwd(const void *q, const void *k, const void *v, const void
     if (N < 0 || T_total < 0 || H <= 0) return KDA_ERR_INVALID_ARGUMENT;
     if (!workspace || !aligned16(workspace)) return KDA_ERR_WORKSPACE;
     if (ws_bytes < KDA_WS_HEADER_BYTES) return KDA_ERR_WORKSPACE;
-    if (!final_state && ws_bytes < kda_chunk_fwd_workspace_size(N, T_total, H, dk, dv)) return KDA_ERR_WORKSPACE;
+    if (!final_state && ws_bytes < staging_offset() + state_bytes(N, H, dk, dv)) return KDA_ERR_WORKSPACE;
     if (T_total > 0) {
         if (!q || !k || !v || !g || !beta || !o) return KDA_ERR_INVALID_ARGUMENT;
         if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(g) || !aligned16(o))
@@ -70,12 +89,26 @@ kda_status kda_chunk_fwd(const void *q, const void *k, const void *v, const void
                              : reinterpret_cast<float *>(static_cast<char *>(workspace) + staging_offset());
 
     if (use_tc) {
+        const bool split = split_shape(N, T_total, H, dk, dv) && ws_bytes >= split_workspace(N, T_total, H, dk, dv);
         kda::ChunkParams cp{};
         cp.q = q; cp.k = k; cp.v = v; cp.g = g; cp.beta = beta; cp.o = o;
         cp.N = N; cp.H = H; cp.scale = scale;
         cp.cu = cu_seqlens; cp.T_total = T_total; cp.seq_len_fixed = fixed_len;
         cp.init_state = init_state; cp.state_out = chunk_state; cp.status = status;
+        if (split) {
+            char *base = static_cast<char *>(workspace) + staging_offset() + state_bytes(N, H, dk, dv);
+            cp.split = 1;
+            cp.phi = reinterpret_cast<float *>(base);
+            cp.psi = reinterpret_cast<float *>(base + state_bytes(N, H, dk, dv));
+            cp.o_phi = base + 2 * state_bytes(N, H, dk, dv);
+        }
         if (kda::launch_chunk_tc(cp, s) != cudaSuccess) return KDA_ERR_CUDA;
+        if (split) {
+            kda::MergeParams mp{};
+            mp.o = o; mp.o_phi = cp.o_phi; mp.state = chunk_state; mp.phi = cp.phi; mp.psi = cp.psi;
+            mp.cu = cu_seqlens; mp.T_total = T_total; mp.seq_len_fixed = fixed_len; mp.N = N; mp.H = H;
+            if (kda::launch_merge(mp, s) != cudaSuccess) return KDA_ERR_CUDA;
+        }
     }
 
     kda::SeqParams sp{};

@@ -74,6 +74,10 @@ struct TcParams {
     const float *init_state;
     float *state_out;
     uint32_t *status;
+    // T-segment split (split != 0): the grid holds three roles per (sequence, head)
+    float *phi, *psi;             // per pair: segment-1 transition and zero-start state
+    __nv_bfloat16 *o_phi;         // [T, H, 128]: segment-1 outputs of the transition run
+    int split;
     int64_t T_total, seq_len_fixed;
     int N, H;
     float scale;
@@ -200,7 +204,14 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_tc_kernel(const __grid_
     __shared__ int s_grp_fail[3];  // [0] decay group, [1] chain group, [2] solve group
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int64_t pair = blockIdx.x;
+    // Without a split, CTA = (sequence, head).  With the T-segment split the full chunks
+    // of a sequence are cut in two at a chunk boundary and the grid holds three roles
+    // per (sequence, head): 0 = segment 0 from the initial state (normal outputs, state
+    // at the cut); 1 = segment 1 from a zero state (its outputs, state Psi); 2 = segment
+    // 1 from the identity with v = 0 (outputs Phi_t^T (scale q_t), transition Phi).
+    const int64_t npairs = static_cast<int64_t>(p.N) * p.H;
+    const int role = p.split ? static_cast<int>(blockIdx.x / npairs) : 0;
+    const int64_t pair = p.split ? static_cast<int64_t>(blockIdx.x) % npairs : static_cast<int64_t>(blockIdx.x);
     const int n = static_cast<int>(pair / p.H), h = static_cast<int>(pair % p.H);
     const int64_t H = p.H;
 
@@ -219,7 +230,16 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_tc_kernel(const __grid_
         bos = static_cast<int64_t>(n) * p.seq_len_fixed;
         eos = bos + p.seq_len_fixed;
     }
-    const int nfull = static_cast<int>((eos - bos) / kC);
+    int nfull = static_cast<int>((eos - bos) / kC);  // full chunks of this CTA's segment
+    if (p.split) {
+        const int n0 = (nfull + 1) / 2;
+        if (role == 0) {
+            nfull = n0;
+        } else {
+            bos += static_cast<int64_t>(kC) * n0;
+            nfull -= n0;
+        }
+    }
     if (nfull == 0) return;
 
     if (tid == 0) {
@@ -249,6 +269,13 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_tc_kernel(const __grid_
         tmem_alloc(&s_tmem, 512);
         tmem_relinquish();
     }
+    if (role == 2) {  // the transition run has v = 0: both stages' V tiles stay zero
+        for (int i = tid; i < 2 * 16384 / 16; i += kThreads) {
+            const int st = i / (16384 / 16), w = i % (16384 / 16);
+            reinterpret_cast<uint4 *>(sm + st * kStage + OFF_V)[w] = make_uint4(0u, 0u, 0u, 0u);
+        }
+        fence_proxy_async_smem();
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -258,6 +285,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_tc_kernel(const __grid_
 
     if (warp == 0) {
         // ------------------------------------------------------------------ TMA producer
+        const bool v_zero = (role == 2);
         int issued0 = -1, issued1 = -1;
         for (int c = 0; c < nfull; ++c) {
             const int s = c & 1;
@@ -268,15 +296,17 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_tc_kernel(const __grid_
             if (c >= 2 && !warp_wait(&bar_free[s], ((c >> 1) - 1) & 1, ctl, lane)) break;
             uint8_t *st = sm + s * kStage;
             if (lane == 0) {
-                mbar_arrive_expect_tx(&bar_full[s], kStage);
+                mbar_arrive_expect_tx(&bar_full[s], v_zero ? kStage - 16384 : kStage);
                 tma_load_3d(st + OFF_R + 0, &p.tm_k, 0, h, t0, &bar_full[s]);
                 tma_load_3d(st + OFF_R + 16384, &p.tm_k, 64, h, t0, &bar_full[s]);
                 tma_load_3d(st + OFF_R + 8192, &p.tm_q, 0, h, t0, &bar_full[s]);
                 tma_load_3d(st + OFF_R + 24576, &p.tm_q, 64, h, t0, &bar_full[s]);
                 tma_load_3d(st + OFF_G + 0, &p.tm_g, 0, h, t0, &bar_full[s]);
                 tma_load_3d(st + OFF_G + 8192, &p.tm_g, 64, h, t0, &bar_full[s]);
-                tma_load_3d(st + OFF_V + 0, &p.tm_v, 0, h, t0, &bar_full[s]);
-                tma_load_3d(st + OFF_V + 8192, &p.tm_v, 64, h, t0, &bar_full[s]);
+                if (!v_zero) {
+                    tma_load_3d(st + OFF_V + 0, &p.tm_v, 0, h, t0, &bar_full[s]);
+                    tma_load_3d(st + OFF_V + 8192, &p.tm_v, 64, h, t0, &bar_full[s]);
+                }
                 // warm L2 with the chunk that will reuse this stage, so its load is short
                 if (c + 2 < nfull) {
                     const int t2 = t0 + 2 * kC;
@@ -284,7 +314,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_tc_kernel(const __grid_
                         tma_prefetch_l2_3d(&p.tm_q, x, h, t2);
                         tma_prefetch_l2_3d(&p.tm_k, x, h, t2);
                         tma_prefetch_l2_3d(&p.tm_g, x, h, t2);
-                        tma_prefetch_l2_3d(&p.tm_v, x, h, t2);
+                        if (!v_zero) tma_prefetch_l2_3d(&p.tm_v, x, h, t2);
                     }
                 }
             }
@@ -413,7 +443,8 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_tc_kernel(const __grid_
         int gseq = 0;
         const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
         const uint32_t tS = tmem + lane_base + TM_S, tSB = tmem + lane_base + TM_SB;
-        const float *s0 = p.init_state ? p.init_state + pair * kD * kD : nullptr;
+        const float *s0 = (role == 0 && p.init_state) ? p.init_state + pair * kD * kD : nullptr;
+        __nv_bfloat16 *const obase = (role == 2) ? p.o_phi : p.o;
         for (int cc = 0; cc < kD; cc += 32) {
             uint32_t a[16], b[16], pk[16];
 #pragma unroll
@@ -430,12 +461,32 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_tc_kernel(const __grid_
             tmem_st16(tS + cc + 16, b);
             tmem_st16(tSB + cc / 2, pk);
         }
+        if (role == 2) {
+            // the transition run starts from the identity: lane j's 1 sits in column j, inside
+            // the 32 columns [32 (warp % 4), +32) of its warp
+            const int wb = (warp & 3) * 32;
+            uint32_t a[16], b[16], pk[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+                a[e] = __float_as_uint(wb + e == j ? 1.f : 0.f);
+                b[e] = __float_as_uint(wb + 16 + e == j ? 1.f : 0.f);
+            }
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                pk[e] = pack_bf16x2(__uint_as_float(a[2 * e]), __uint_as_float(a[2 * e + 1]));
+                pk[8 + e] = pack_bf16x2(__uint_as_float(b[2 * e]), __uint_as_float(b[2 * e + 1]));
+            }
+            tmem_st_wait();
+            tmem_st16(tS + wb, a);
+            tmem_st16(tS + wb + 16, b);
+            tmem_st16(tSB + wb / 2, pk);
+        }
         tmem_st_wait();
 
         uint32_t opk[32];          // previous chunk's O row block, bf16 pairs (r, r+1)
         int64_t o_t0 = -1;
         auto store_o = [&](int64_t t0) {
-            __nv_bfloat16 *orow = p.o + (t0 * H + h) * kD + j;
+            __nv_bfloat16 *orow = obase + (t0 * H + h) * kD + j;
             const int64_t rs = H * kD;
 #pragma unroll
             for (int e = 0; e < 32; ++e) {
@@ -513,7 +564,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_tc_kernel(const __grid_
             }
             tc_fence_after();
             const bool last = (c == nfull - 1);
-            float *sout = p.state_out + pair * kD * kD;
+            float *sout = (role == 0 ? p.state_out : role == 1 ? p.psi : p.phi) + pair * kD * kD;
             for (int cc = 0; cc < kD; cc += 32) {
                 uint32_t a[16], b[16], pk[16];
                 tmem_ld16(tS + cc, a);
@@ -901,7 +952,7 @@ bool chunk_tc_supported(int dk, int dv, int dtype) { return dk == 128 && dv == 1
 
 cudaError_t launch_chunk_tc(const ChunkParams &cp, cudaStream_t stream) {
     if (!chunk_tc_supported(128, 128, 0)) return cudaErrorNotSupported;
-    const int64_t blocks = static_cast<int64_t>(cp.N) * cp.H;
+    const int64_t blocks = static_cast<int64_t>(cp.N) * cp.H * (cp.split ? 3 : 1);
     if (blocks <= 0 || cp.T_total <= 0) return cudaSuccess;
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     TcParams p{};
@@ -919,6 +970,10 @@ cudaError_t launch_chunk_tc(const ChunkParams &cp, cudaStream_t stream) {
     p.N = cp.N;
     p.H = cp.H;
     p.scale = cp.scale;
+    p.split = cp.split;
+    p.phi = cp.phi;
+    p.psi = cp.psi;
+    p.o_phi = static_cast<__nv_bfloat16 *>(cp.o_phi);
     static bool attr_set = false;
     if (!attr_set) {
         cudaError_t e = cudaFuncSetAttribute(kda_chunk_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,

@@ -39,6 +39,19 @@ struct SeqParams {
     uint32_t *status;           // device status word
 };
 
+// T-segment merge after a split chunked launch (kda_merge.cu): o on segment-1 tokens
+// += S1^T o_phi, then state <- phi state + psi.  o, o_phi: [T, H, 128] bf16.
+struct MergeParams {
+    void *o;
+    const void *o_phi;
+    float *state;               // S1 on entry, final full-chunk state on exit
+    const float *phi, *psi;
+    const int32_t *cu;
+    int64_t T_total, seq_len_fixed;
+    int N, H;
+};
+cudaError_t launch_merge(const MergeParams &p, cudaStream_t stream);
+
 // dtype: 0 = bf16, 1 = fp32 (kda_dtype).  Returns the launch error.
 cudaError_t launch_seq(const SeqParams &p, int dk, int dv, int dtype, cudaStream_t stream);
 
@@ -54,6 +67,12 @@ struct ChunkParams {
     const float *init_state;    // may be null (zeros)
     float *state_out;           // final_state or staging (never null)
     uint32_t *status;
+    // T-segment split (see tseg_plan): 0 = off.  With it, state_out receives the state at
+    // the cut, phi / psi the segment-1 transition and zero-start state, o_phi [T, H, 128]
+    // bf16 the transition run's outputs.
+    int split;
+    float *phi, *psi;
+    void *o_phi;
 };
 
 // True when the chunked tensor-core kernel is compiled in and supports the shape.

@@ -57,8 +57,10 @@ extern "C" kda_status kda_chunk_fwd_noalloc(const void *q, const void *k, const 
     if (!(dtype == KDA_BF16 || dtype == KDA_F32) || !(dk == 64 || dk == 128) || !(dv == 64 || dv == 128))
         return KDA_ERR_UNSUPPORTED;
     if (N < 0 || T_total < 0 || H <= 0) return KDA_ERR_INVALID_ARGUMENT;
-    const size_t need =
-        final_state ? static_cast<size_t>(KDA_WS_HEADER_BYTES) : kda_chunk_fwd_workspace_size(N, T_total, H, dk, dv);
+    // the minimum workspace (the status header, plus the staging states without final_state);
+    // kda_chunk_fwd uses the split path only if the scratch also holds its buffers
+    const size_t states = static_cast<size_t>(N) * static_cast<size_t>(H) * dk * dv * sizeof(float);
+    const size_t need = KDA_WS_HEADER_BYTES + (final_state ? 0 : states);
     if (need > kStaticWorkspaceBytes) return KDA_ERR_WORKSPACE;
     void *ws = nullptr;
     const kda_status st = static_workspace(&ws);

@@ -172,8 +172,7 @@ def kda_chunk_fwd(q, k, v, g, beta, cu_seqlens=None, init_state=None, scale: flo
         final_state = torch.empty(N, H, dk, dv, dtype=torch.float32, device=q.device)
     if final_state is not None:
         _need(final_state, "final_state", torch.float32, (N, H, dk, dv))
-    need = (KDA_WS_HEADER_BYTES if final_state is not None
-            else kda_chunk_fwd_workspace_size(N, T, H, dk, dv))
+    need = kda_chunk_fwd_workspace_size(N, T, H, dk, dv)  # the size that enables every path
     if workspace is None:
         workspace = new_workspace(need, q.device)
     rc = lib.kda_chunk_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _dtype_code(q), _ptr(init_state),

@@ -72,13 +72,25 @@ typedef enum kda_dtype {
 #define KDA_WS_HEADER_BYTES 256
 
 /*
- * Workspace for kda_chunk_fwd, in bytes.
+ * Workspace for kda_chunk_fwd, in bytes: the size with which every path of the
+ * call is available.  Returns 0 for invalid arguments.
  *
- * With final_state != NULL, KDA_WS_HEADER_BYTES suffice.  With final_state ==
- * NULL the chunked path needs a staging copy of every (sequence, head) state
- * (N*H*dk*dv*4 bytes after the header) to hand the state from the chunked
- * kernel to the partial-chunk kernel; this function returns that larger size.
- * Returns 0 for invalid arguments.
+ * The minimum is smaller.  With final_state != NULL, KDA_WS_HEADER_BYTES
+ * suffice; with final_state == NULL the chunked path needs a staging copy of
+ * every (sequence, head) state (N*H*dk*dv*4 bytes after the header) to hand the
+ * state from the chunked kernel to the partial-chunk kernel.
+ *
+ * T-segment split: when dk = dv = 128, N*H <= 48 and T_total >= 4096, a batch
+ * has too few (sequence, head) chains to occupy the GPU, and kda_chunk_fwd cuts
+ * the full chunks of every sequence in two at a chunk boundary and runs the
+ * halves concurrently: segment 1 from a zero state and, with v = 0, from the
+ * identity (its transition), then merges the results exactly (the recurrence is
+ * affine in the state) -- the context-parallel hand-over of a long sequence's
+ * state described in "Kimi K3 on Fireworks: Fast RL at frontier scale", done
+ * within one GPU.  It needs 3*N*H*dk*dv*4 + T_total*H*dv*2 bytes after the
+ * header, which this function then includes; with a smaller (but sufficient)
+ * workspace the call runs unsplit.  Results agree within floating-point
+ * rounding either way.
  */
 size_t kda_chunk_fwd_workspace_size(int N, int64_t T_total, int H, int dk, int dv);
 

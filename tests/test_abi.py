@@ -34,6 +34,12 @@ def test_status_strings_and_version(lib):
 def test_workspace_size(lib):
     from gated_linear_attention_chunk_gb300 import kda
     assert kda.kda_chunk_fwd_workspace_size(4, 16384, 32, 128, 128) == 256 + 4 * 32 * 128 * 128 * 4
+    # few chains and long sequences: room for the T-segment split (three state sets + bf16 outputs)
+    assert kda.kda_chunk_fwd_workspace_size(1, 131072, 32, 128, 128) == 256 + 3 * 32 * 65536 + 131072 * 32 * 256
+    assert kda.kda_chunk_fwd_workspace_size(6, 4096, 8, 128, 128) == 256 + 3 * 48 * 65536 + 4096 * 8 * 256
+    assert kda.kda_chunk_fwd_workspace_size(7, 4096, 7, 128, 128) == 256 + 49 * 65536   # 49 chains: no split
+    assert kda.kda_chunk_fwd_workspace_size(1, 4095, 2, 128, 128) == 256 + 2 * 65536    # too short: no split
+    assert kda.kda_chunk_fwd_workspace_size(1, 8192, 2, 64, 64) == 256 + 2 * 16384      # d = 64: no split
     assert kda.kda_chunk_fwd_workspace_size(0, 0, 1, 64, 64) == 256
     assert kda.kda_chunk_fwd_workspace_size(1, 10, 2, 96, 128) == 0
     assert kda.kda_chunk_fwd_workspace_size(-1, 10, 2, 64, 128) == 0
