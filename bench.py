@@ -36,8 +36,8 @@ UNIT = "tokens/s"
 
 # DRAM bytes (read + write) of one kda_chunk_tc_kernel launch on prefill_4k, from the
 # ncu capture summarised in profiles/kda_chunk_tc_prefill_4k.md (546.7 MB read +
-# 118.0 MB written).  Reset to None whenever that kernel changes until it is re-captured.
-DOMINANT_TRAFFIC = {"prefill_4k": 664735488}
+# 117.2 MB written).  Reset to None whenever that kernel changes until it is re-captured.
+DOMINANT_TRAFFIC = {"prefill_4k": 663934208}
 
 
 # ------------------------------------------------------------------------------------------------

@@ -107,6 +107,7 @@ kda_status kda_chunk_fwd(const void *q, const void *k, const void *v, const void
             kda::MergeParams mp{};
             mp.o = o; mp.o_phi = cp.o_phi; mp.state = chunk_state; mp.phi = cp.phi; mp.psi = cp.psi;
             mp.cu = cu_seqlens; mp.T_total = T_total; mp.seq_len_fixed = fixed_len; mp.N = N; mp.H = H;
+            mp.status = status;
             if (kda::launch_merge(mp, s) != cudaSuccess) return KDA_ERR_CUDA;
         }
     }

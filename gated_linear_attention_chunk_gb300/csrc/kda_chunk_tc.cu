@@ -21,8 +21,9 @@
 //   warp 1       chain MMA issuer (and TMEM owner)
 //   warp 2       prep MMA issuer (polls both prep products)
 //   warps 4-7    chain group: W tile from W^T, U and state epilogues in TMEM, O to HBM
-//   warps 8-11   decay group: prefix products, Kbar / Qbar / Ktil in place
-//   warps 12-15  solve group: M and P from the accumulator, T' = (I+M)^-1 Diag(beta)
+//   warps 8-15   decay group: prefix products, Kbar / Qbar / Ktil in place
+//   warps 16-19  solve group: M and P from the accumulator, T' = (I+M)^-1 Diag(beta)
+// Registers are split per warpgroup with setmaxnreg (the control warps need few).
 // The decay group runs up to one chunk ahead of the solve group, which runs one
 // chunk ahead of the chain.  The state lives in TMEM transposed (lane = value
 // column j, column = channel c) as an fp32 master plus a bf16 copy that feeds
@@ -46,7 +47,7 @@ using namespace ptx;
 
 constexpr int kC = 64;          // chunk length
 constexpr int kD = 128;         // dk = dv
-constexpr int kThreads = 512;   // 16 warps
+constexpr int kThreads = 640;   // 20 warps
 constexpr uint64_t kWaitNs = 1000000000ull;
 
 // dynamic shared memory map (offsets from a 1024-byte aligned base)
@@ -143,6 +144,9 @@ __device__ __forceinline__ float ex2_approx(float x) {
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
     return r;
 }
+// Per-warpgroup register budgets (all four warps of a warpgroup execute the same one).
+__device__ __forceinline__ void regs_dec_48() { asm volatile("setmaxnreg.dec.sync.aligned.u32 48;" ::: "memory"); }
+__device__ __forceinline__ void regs_inc_120() { asm volatile("setmaxnreg.inc.sync.aligned.u32 120;" ::: "memory"); }
 __device__ __forceinline__ void named_bar(int id, int n) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
@@ -194,7 +198,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_tc_kernel(const __grid_
     __shared__ __align__(16) float s_beta[2][kC];
     __shared__ __align__(16) float s_ac[3][kD];  // per-chunk A_C, ring of three
     __shared__ __align__(16) float s_x[32 * kLdX];
-    __shared__ __align__(16) float s_tot[4][kD];
+    __shared__ __align__(16) float s_tot[8][kD];
     __shared__ uint64_t bar_full[2], bar_free[2];
     __shared__ uint64_t bar_elem, bar_mma1, bar_mfree, bar_tready, bar_mma2, bar_ready, bar_wfree, bar_c1, bar_uready,
         bar_c3;
@@ -283,161 +287,169 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_tc_kernel(const __grid_
     const Ctl ctl{&s_abort, p.status};
     const uint32_t sm_base = smem_u32(sm);
 
-    if (warp == 0) {
-        // ------------------------------------------------------------------ TMA producer
-        const bool v_zero = (role == 2);
-        int issued0 = -1, issued1 = -1;
-        for (int c = 0; c < nfull; ++c) {
-            const int s = c & 1;
-            const int t0 = static_cast<int>(bos + static_cast<int64_t>(c) * kC);
-            // beta for this chunk: loaded before waiting for the stage, so its latency overlaps the wait
-            const float b_lo = __bfloat162float(p.beta[(static_cast<int64_t>(t0) + lane) * H + h]);
-            const float b_hi = __bfloat162float(p.beta[(static_cast<int64_t>(t0) + lane + 32) * H + h]);
-            if (c >= 2 && !warp_wait(&bar_free[s], ((c >> 1) - 1) & 1, ctl, lane)) break;
-            uint8_t *st = sm + s * kStage;
-            if (lane == 0) {
-                mbar_arrive_expect_tx(&bar_full[s], v_zero ? kStage - 16384 : kStage);
-                tma_load_3d(st + OFF_R + 0, &p.tm_k, 0, h, t0, &bar_full[s]);
-                tma_load_3d(st + OFF_R + 16384, &p.tm_k, 64, h, t0, &bar_full[s]);
-                tma_load_3d(st + OFF_R + 8192, &p.tm_q, 0, h, t0, &bar_full[s]);
-                tma_load_3d(st + OFF_R + 24576, &p.tm_q, 64, h, t0, &bar_full[s]);
-                tma_load_3d(st + OFF_G + 0, &p.tm_g, 0, h, t0, &bar_full[s]);
-                tma_load_3d(st + OFF_G + 8192, &p.tm_g, 64, h, t0, &bar_full[s]);
-                if (!v_zero) {
-                    tma_load_3d(st + OFF_V + 0, &p.tm_v, 0, h, t0, &bar_full[s]);
-                    tma_load_3d(st + OFF_V + 8192, &p.tm_v, 64, h, t0, &bar_full[s]);
-                }
-                // warm L2 with the chunk that will reuse this stage, so its load is short
-                if (c + 2 < nfull) {
-                    const int t2 = t0 + 2 * kC;
-                    for (int x = 0; x < 128; x += 64) {
-                        tma_prefetch_l2_3d(&p.tm_q, x, h, t2);
-                        tma_prefetch_l2_3d(&p.tm_k, x, h, t2);
-                        tma_prefetch_l2_3d(&p.tm_g, x, h, t2);
-                        if (!v_zero) tma_prefetch_l2_3d(&p.tm_v, x, h, t2);
-                    }
-                }
-            }
-            if (s == 0) issued0 = c; else issued1 = c;
-            s_beta[s][lane] = b_lo;
-            s_beta[s][lane + 32] = b_hi;
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bar_full[s]);
-        }
-        // make sure no TMA copy is still landing in shared memory when the CTA exits
-        const uint64_t deadline = globaltimer_ns() + kWaitNs;
-        if (issued0 >= 0)
-            while (!mbar_try_wait(&bar_full[0], (issued0 >> 1) & 1) && globaltimer_ns() < deadline) {
-            }
-        if (issued1 >= 0)
-            while (!mbar_try_wait(&bar_full[1], (issued1 >> 1) & 1) && globaltimer_ns() < deadline) {
-            }
-    } else if (warp == 1) {
-        // ------------------------------------------------------------------ chain MMA issuer
-        if (lane == 0) {
-            const uint32_t idU = idesc_bf16(128, 64, false, true, true);    // U -= S^T W  (W MN-major)
-            const uint32_t idO = idesc_bf16(128, 64, false, false);         // O  = S^T Qbar^T, += U^T P^T
-            const uint32_t idS = idesc_bf16(128, 128, false, true);         // S += U^T Ktil (Ktil MN-major)
+    // Register split per warpgroup (setmaxnreg; each warpgroup's four warps take the same
+    // share): launched with 96 per thread, 61440 for 640 threads (checked on the host);
+    // control warps 48, chain and solve groups 120, the two decay warpgroups 96:
+    // (48 + 120 + 96 + 96 + 120) x 128 = 61440.
+    if (warp < 4) {
+        regs_dec_48();
+        if (warp == 0) {
+            // ------------------------------------------------------------------ TMA producer
+            const bool v_zero = (role == 2);
+            int issued0 = -1, issued1 = -1;
             for (int c = 0; c < nfull; ++c) {
                 const int s = c & 1;
-                if (!wait_bar(&bar_ready, c & 1, ctl)) break;
-                tc_fence_after();
-                const uint32_t st = sm_base + s * kStage;
-                // descriptors built once per chunk; k-steps add constant start offsets
-                const uint64_t dW = sdesc_sw128(st + OFF_R, 8192, 1024);          // W over Kbar, MN-major
-                const uint64_t dQ = sdesc_sw128(st + OFF_R + 8192, 16, 1024);     // Qbar, K-major
-                const uint64_t dP = sdesc_sw128(sm_base + OFF_P + s * 8192, 16, 1024);
-                const uint64_t dG = sdesc_sw128(st + OFF_G, 8192, 1024);          // Ktil, MN-major
-#pragma unroll
-                for (int ks = 0; ks < 8; ++ks)
-                    mma_bf16_ts(tmem + TM_U, tmem + TM_SB + 8 * ks, dW + (((ks >> 2) * 16384 + (ks & 3) * 2048) >> 4),
-                                idU, 1u);
-                mma_commit(&bar_c1);  // U is on the critical path: release its epilogue first
-#pragma unroll
-                for (int ks = 0; ks < 8; ++ks)
-                    mma_bf16_ts(tmem + TM_O, tmem + TM_SB + 8 * ks, dQ + (((ks >> 2) * 16384 + (ks & 3) * 32) >> 4),
-                                idO, ks > 0 ? 1u : 0u);
-                if (!wait_bar(&bar_uready, c & 1, ctl)) break;
-                tc_fence_after();
-#pragma unroll
-                for (int ks = 0; ks < 4; ++ks)
-                    mma_bf16_ts(tmem + TM_S, tmem + TM_UB + 8 * ks, dG + ((ks * 2048) >> 4), idS, 1u);
-#pragma unroll
-                for (int ks = 0; ks < 4; ++ks)
-                    mma_bf16_ts(tmem + TM_O, tmem + TM_UB + 8 * ks, dP + ((ks * 32) >> 4), idO, 1u);
-                mma_commit(&bar_c3);
-                mma_commit(&bar_free[s]);
-            }
-            // drain: every MMA this thread issued completes before the TMEM is freed
-            mma_commit(&bar_drain[0]);
-            const uint64_t deadline = globaltimer_ns() + kWaitNs;
-            while (!mbar_try_wait(&bar_drain[0], 0) && globaltimer_ns() < deadline) {
-            }
-        }
-    } else if (warp == 2) {
-        // ------------------------------------------------------------------ prep MMA issuer
-        // Polls both prep MMAs so that the next chunk's [Kbar; Qbar] Ktil^T product can go
-        // as soon as its tiles are ready, while this chunk's W / Utl product waits for T'.
-        if (lane == 0) {
-            const uint32_t id1 = idesc_bf16(128, 64, false, false);  // [Kbar; Qbar] Ktil^T
-            const uint32_t id2 = idesc_bf16(128, 64, true, false);   // Kbar^T T'^T, V^T T'^T (A MN-major)
-            int c1 = 0, c2 = 0;
-            uint64_t deadline = globaltimer_ns() + kWaitNs;
-            uint32_t spins = 0;
-            while (c2 < nfull) {
-                bool progress = false;
-                if (c1 < nfull && mbar_test_wait(&bar_elem, c1 & 1) &&
-                    (c1 == 0 || mbar_test_wait(&bar_mfree, (c1 - 1) & 1))) {
-                    tc_fence_after();
-                    const uint32_t st = sm_base + (c1 & 1) * kStage;
-                    const uint64_t dA = sdesc_sw128(st + OFF_R, 16, 1024);   // [Kbar; Qbar], K-major
-                    const uint64_t dB = sdesc_sw128(st + OFF_G, 16, 1024);   // Ktil, K-major
-#pragma unroll
-                    for (int ks = 0; ks < 8; ++ks)
-                        mma_bf16_ss(tmem + TM_PREP, dA + (((ks >> 2) * 16384 + (ks & 3) * 32) >> 4),
-                                    dB + (((ks >> 2) * 8192 + (ks & 3) * 32) >> 4), id1, ks > 0 ? 1u : 0u);
-                    mma_commit(&bar_mma1);
-                    ++c1;
-                    progress = true;
-                }
-                if (c2 < c1 && mbar_test_wait(&bar_tready, c2 & 1) &&
-                    (c2 == 0 || (mbar_test_wait(&bar_wfree, (c2 - 1) & 1) && mbar_test_wait(&bar_uready, (c2 - 1) & 1)))) {
-                    tc_fence_after();
-                    const uint32_t st = sm_base + (c2 & 1) * kStage;
-                    const uint64_t dK = sdesc_sw128(st + OFF_R, 16384, 1024);  // Kbar^T, MN-major
-                    const uint64_t dV = sdesc_sw128(st + OFF_V, 8192, 1024);   // V^T, MN-major
-                    const uint64_t dT = sdesc_sw128(sm_base + OFF_TT + (c2 & 1) * 8192, 16, 1024);  // T', K-major
-#pragma unroll
-                    for (int ks = 0; ks < 4; ++ks)
-                        mma_bf16_ss(tmem + TM_W, dK + ((ks * 2048) >> 4), dT + ((ks * 32) >> 4), id2, ks > 0 ? 1u : 0u);
-#pragma unroll
-                    for (int ks = 0; ks < 4; ++ks)
-                        mma_bf16_ss(tmem + TM_U, dV + ((ks * 2048) >> 4), dT + ((ks * 32) >> 4), id2, ks > 0 ? 1u : 0u);
-                    mma_commit(&bar_mma2);
-                    ++c2;
-                    progress = true;
-                }
-                if (progress) {
-                    deadline = globaltimer_ns() + kWaitNs;
-                    spins = 0;
-                    continue;
-                }
-                __nanosleep(32);  // back off without stealing issue slots from the math warps
-                if ((++spins & 63u) == 0) {
-                    if (*ctl.abort) break;
-                    if (globaltimer_ns() > deadline) {
-                        *ctl.abort = 1;
-                        atomicOr(ctl.status, DEV_ERR_TIMEOUT);
-                        break;
+                const int t0 = static_cast<int>(bos + static_cast<int64_t>(c) * kC);
+                // beta for this chunk: loaded before waiting for the stage, so its latency overlaps the wait
+                const float b_lo = __bfloat162float(p.beta[(static_cast<int64_t>(t0) + lane) * H + h]);
+                const float b_hi = __bfloat162float(p.beta[(static_cast<int64_t>(t0) + lane + 32) * H + h]);
+                if (c >= 2 && !warp_wait(&bar_free[s], ((c >> 1) - 1) & 1, ctl, lane)) break;
+                uint8_t *st = sm + s * kStage;
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(&bar_full[s], v_zero ? kStage - 16384 : kStage);
+                    tma_load_3d(st + OFF_R + 0, &p.tm_k, 0, h, t0, &bar_full[s]);
+                    tma_load_3d(st + OFF_R + 16384, &p.tm_k, 64, h, t0, &bar_full[s]);
+                    tma_load_3d(st + OFF_R + 8192, &p.tm_q, 0, h, t0, &bar_full[s]);
+                    tma_load_3d(st + OFF_R + 24576, &p.tm_q, 64, h, t0, &bar_full[s]);
+                    tma_load_3d(st + OFF_G + 0, &p.tm_g, 0, h, t0, &bar_full[s]);
+                    tma_load_3d(st + OFF_G + 8192, &p.tm_g, 64, h, t0, &bar_full[s]);
+                    if (!v_zero) {
+                        tma_load_3d(st + OFF_V + 0, &p.tm_v, 0, h, t0, &bar_full[s]);
+                        tma_load_3d(st + OFF_V + 8192, &p.tm_v, 64, h, t0, &bar_full[s]);
+                    }
+                    // warm L2 with the chunk that will reuse this stage, so its load is short
+                    if (c + 2 < nfull) {
+                        const int t2 = t0 + 2 * kC;
+                        for (int x = 0; x < 128; x += 64) {
+                            tma_prefetch_l2_3d(&p.tm_q, x, h, t2);
+                            tma_prefetch_l2_3d(&p.tm_k, x, h, t2);
+                            tma_prefetch_l2_3d(&p.tm_g, x, h, t2);
+                            if (!v_zero) tma_prefetch_l2_3d(&p.tm_v, x, h, t2);
+                        }
                     }
                 }
+                if (s == 0) issued0 = c; else issued1 = c;
+                s_beta[s][lane] = b_lo;
+                s_beta[s][lane + 32] = b_hi;
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bar_full[s]);
             }
-            mma_commit(&bar_drain[1]);
-            const uint64_t dl = globaltimer_ns() + kWaitNs;
-            while (!mbar_try_wait(&bar_drain[1], 0) && globaltimer_ns() < dl) {
+            // make sure no TMA copy is still landing in shared memory when the CTA exits
+            const uint64_t deadline = globaltimer_ns() + kWaitNs;
+            if (issued0 >= 0)
+                while (!mbar_try_wait(&bar_full[0], (issued0 >> 1) & 1) && globaltimer_ns() < deadline) {
+                }
+            if (issued1 >= 0)
+                while (!mbar_try_wait(&bar_full[1], (issued1 >> 1) & 1) && globaltimer_ns() < deadline) {
+                }
+        } else if (warp == 1) {
+            // ------------------------------------------------------------------ chain MMA issuer
+            if (lane == 0) {
+                const uint32_t idU = idesc_bf16(128, 64, false, true, true);    // U -= S^T W  (W MN-major)
+                const uint32_t idO = idesc_bf16(128, 64, false, false);         // O  = S^T Qbar^T, += U^T P^T
+                const uint32_t idS = idesc_bf16(128, 128, false, true);         // S += U^T Ktil (Ktil MN-major)
+                for (int c = 0; c < nfull; ++c) {
+                    const int s = c & 1;
+                    if (!wait_bar(&bar_ready, c & 1, ctl)) break;
+                    tc_fence_after();
+                    const uint32_t st = sm_base + s * kStage;
+                    // descriptors built once per chunk; k-steps add constant start offsets
+                    const uint64_t dW = sdesc_sw128(st + OFF_R, 8192, 1024);          // W over Kbar, MN-major
+                    const uint64_t dQ = sdesc_sw128(st + OFF_R + 8192, 16, 1024);     // Qbar, K-major
+                    const uint64_t dP = sdesc_sw128(sm_base + OFF_P + s * 8192, 16, 1024);
+                    const uint64_t dG = sdesc_sw128(st + OFF_G, 8192, 1024);          // Ktil, MN-major
+#pragma unroll
+                    for (int ks = 0; ks < 8; ++ks)
+                        mma_bf16_ts(tmem + TM_U, tmem + TM_SB + 8 * ks, dW + (((ks >> 2) * 16384 + (ks & 3) * 2048) >> 4),
+                                    idU, 1u);
+                    mma_commit(&bar_c1);  // U is on the critical path: release its epilogue first
+#pragma unroll
+                    for (int ks = 0; ks < 8; ++ks)
+                        mma_bf16_ts(tmem + TM_O, tmem + TM_SB + 8 * ks, dQ + (((ks >> 2) * 16384 + (ks & 3) * 32) >> 4),
+                                    idO, ks > 0 ? 1u : 0u);
+                    if (!wait_bar(&bar_uready, c & 1, ctl)) break;
+                    tc_fence_after();
+#pragma unroll
+                    for (int ks = 0; ks < 4; ++ks)
+                        mma_bf16_ts(tmem + TM_S, tmem + TM_UB + 8 * ks, dG + ((ks * 2048) >> 4), idS, 1u);
+#pragma unroll
+                    for (int ks = 0; ks < 4; ++ks)
+                        mma_bf16_ts(tmem + TM_O, tmem + TM_UB + 8 * ks, dP + ((ks * 32) >> 4), idO, 1u);
+                    mma_commit(&bar_c3);
+                    mma_commit(&bar_free[s]);
+                }
+                // drain: every MMA this thread issued completes before the TMEM is freed
+                mma_commit(&bar_drain[0]);
+                const uint64_t deadline = globaltimer_ns() + kWaitNs;
+                while (!mbar_try_wait(&bar_drain[0], 0) && globaltimer_ns() < deadline) {
+                }
+            }
+        } else if (warp == 2) {
+            // ------------------------------------------------------------------ prep MMA issuer
+            // Polls both prep MMAs so that the next chunk's [Kbar; Qbar] Ktil^T product can go
+            // as soon as its tiles are ready, while this chunk's W / Utl product waits for T'.
+            if (lane == 0) {
+                const uint32_t id1 = idesc_bf16(128, 64, false, false);  // [Kbar; Qbar] Ktil^T
+                const uint32_t id2 = idesc_bf16(128, 64, true, false);   // Kbar^T T'^T, V^T T'^T (A MN-major)
+                int c1 = 0, c2 = 0;
+                uint64_t deadline = globaltimer_ns() + kWaitNs;
+                uint32_t spins = 0;
+                while (c2 < nfull) {
+                    bool progress = false;
+                    if (c1 < nfull && mbar_test_wait(&bar_elem, c1 & 1) &&
+                        (c1 == 0 || mbar_test_wait(&bar_mfree, (c1 - 1) & 1))) {
+                        tc_fence_after();
+                        const uint32_t st = sm_base + (c1 & 1) * kStage;
+                        const uint64_t dA = sdesc_sw128(st + OFF_R, 16, 1024);   // [Kbar; Qbar], K-major
+                        const uint64_t dB = sdesc_sw128(st + OFF_G, 16, 1024);   // Ktil, K-major
+#pragma unroll
+                        for (int ks = 0; ks < 8; ++ks)
+                            mma_bf16_ss(tmem + TM_PREP, dA + (((ks >> 2) * 16384 + (ks & 3) * 32) >> 4),
+                                        dB + (((ks >> 2) * 8192 + (ks & 3) * 32) >> 4), id1, ks > 0 ? 1u : 0u);
+                        mma_commit(&bar_mma1);
+                        ++c1;
+                        progress = true;
+                    }
+                    if (c2 < c1 && mbar_test_wait(&bar_tready, c2 & 1) &&
+                        (c2 == 0 || (mbar_test_wait(&bar_wfree, (c2 - 1) & 1) && mbar_test_wait(&bar_uready, (c2 - 1) & 1)))) {
+                        tc_fence_after();
+                        const uint32_t st = sm_base + (c2 & 1) * kStage;
+                        const uint64_t dK = sdesc_sw128(st + OFF_R, 16384, 1024);  // Kbar^T, MN-major
+                        const uint64_t dV = sdesc_sw128(st + OFF_V, 8192, 1024);   // V^T, MN-major
+                        const uint64_t dT = sdesc_sw128(sm_base + OFF_TT + (c2 & 1) * 8192, 16, 1024);  // T', K-major
+#pragma unroll
+                        for (int ks = 0; ks < 4; ++ks)
+                            mma_bf16_ss(tmem + TM_W, dK + ((ks * 2048) >> 4), dT + ((ks * 32) >> 4), id2, ks > 0 ? 1u : 0u);
+#pragma unroll
+                        for (int ks = 0; ks < 4; ++ks)
+                            mma_bf16_ss(tmem + TM_U, dV + ((ks * 2048) >> 4), dT + ((ks * 32) >> 4), id2, ks > 0 ? 1u : 0u);
+                        mma_commit(&bar_mma2);
+                        ++c2;
+                        progress = true;
+                    }
+                    if (progress) {
+                        deadline = globaltimer_ns() + kWaitNs;
+                        spins = 0;
+                        continue;
+                    }
+                    __nanosleep(32);  // back off without stealing issue slots from the math warps
+                    if ((++spins & 63u) == 0) {
+                        if (*ctl.abort) break;
+                        if (globaltimer_ns() > deadline) {
+                            *ctl.abort = 1;
+                            atomicOr(ctl.status, DEV_ERR_TIMEOUT);
+                            break;
+                        }
+                    }
+                }
+                mma_commit(&bar_drain[1]);
+                const uint64_t dl = globaltimer_ns() + kWaitNs;
+                while (!mbar_try_wait(&bar_drain[1], 0) && globaltimer_ns() < dl) {
+                }
             }
         }
-    } else if (warp >= 4 && warp < 8) {
+    } else if (warp < 8) {
+        regs_inc_120();
         // ------------------------------------------------------------------ chain group
         const int j = tid - 128;  // TMEM lane: value column j (state, U, O); channel j (W^T)
         int gseq = 0;
@@ -610,10 +622,10 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_tc_kernel(const __grid_
             named_bar(2, 128);
         }
         if (done && o_t0 >= 0) store_o(o_t0);
-    } else if (warp >= 8 && warp < 12) {
-        // ------------------------------------------------------------------ decay group (warps 8-11)
+    } else if (warp >= 8 && warp < 16) {
+        // ------------------------------------------------------------------ decay group (warps 8-15)
         // Decay factors and the scaled operand tiles, one chunk ahead of the solve group.
-        // Thread = (16-token segment, 4 channels): alpha = exp(g), prefix products within
+        // Thread = (8-token segment, 4 channels): alpha = exp(g), prefix products within
         // the segment, the earlier segments' totals carried in, then Kbar, Qbar, Ktil
         // written over k, q, g in place.
         const int pt = tid - 256;
@@ -622,20 +634,20 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_tc_kernel(const __grid_
         for (int c = 0; c < nfull; ++c) {
             const int s = c & 1;
             uint8_t *st = sm + s * kStage;
-            if (!group_wait(&bar_full[s], (c >> 1) & 1, ctl, &s_grp_fail[0], 1, 128, gseq)) break;
+            if (!group_wait(&bar_full[s], (c >> 1) & 1, ctl, &s_grp_fail[0], 1, 256, gseq)) break;
             {
-                // thread = (token segment of 16, channel quad): 64-bit shared accesses
+                // thread = (token segment of 8, channel quad): 64-bit shared accesses
                 const int cq = pt & 31, seg = pt >> 5;
                 const int kb = cq >> 4, cc = 4 * (cq & 15), ch = kb * 64 + cc;
                 uint8_t *Rk = st + OFF_R + kb * 16384;
                 uint8_t *Rq = Rk + 8192;
                 uint8_t *G = st + OFF_G + kb * 8192;
-                const int r0 = 16 * seg;
-                uint64_t A01[16], A23[16];
+                const int r0 = 8 * seg;
+                uint64_t A01[8], A23[8];
                 uint64_t P01 = f2(1.f, 1.f), P23 = f2(1.f, 1.f);
                 const uint64_t L2E = f2(1.4426950408889634f, 1.4426950408889634f);
 #pragma unroll
-                for (int rr = 0; rr < 16; rr += 4) {
+                for (int rr = 0; rr < 8; rr += 4) {
                     uint2 gw[4];
 #pragma unroll
                     for (int e = 0; e < 4; ++e) gw[e] = *reinterpret_cast<const uint2 *>(G + swz(r0 + rr + e, cc));
@@ -651,7 +663,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_tc_kernel(const __grid_
                 const float2 pp01 = uf2(P01), pp23 = uf2(P23);
                 const float p0 = pp01.x, p1 = pp01.y, p2 = pp23.x, p3 = pp23.y;
                 st4(&s_tot[seg][ch], make_float4(p0, p1, p2, p3));
-                named_bar(1, 128);
+                named_bar(1, 256);
                 float4 m = make_float4(1.f, 1.f, 1.f, 1.f);
                 for (int q = 0; q < seg; ++q) {
                     const float4 t = ld4(&s_tot[q][ch]);
@@ -661,7 +673,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_tc_kernel(const __grid_
                 const uint64_t m01 = f2(m.x, m.y), m23 = f2(m.z, m.w);
                 const uint64_t ms01 = f2(m.x * sc, m.y * sc), ms23 = f2(m.z * sc, m.w * sc);
 #pragma unroll
-                for (int rr = 0; rr < 16; rr += 2) {
+                for (int rr = 0; rr < 8; rr += 2) {
                     uint2 kw[2], qw[2];
 #pragma unroll
                     for (int e = 0; e < 2; ++e) {
@@ -684,7 +696,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_tc_kernel(const __grid_
                         *reinterpret_cast<uint2 *>(G + off) = make_uint2(pk2(mul2(k01, r01)), pk2(mul2(k23, r23)));
                     }
                 }
-                if (seg == 3) {
+                if (seg == 7) {
                     const float4 ac = make_float4(m.x * p0, m.y * p1, m.z * p2, m.w * p3);
                     if (!(ac.x >= kMinDecay) || !(ac.y >= kMinDecay) || !(ac.z >= kMinDecay) || !(ac.w >= kMinDecay))
                         atomicOr(p.status, DEV_ERR_GATE);
@@ -692,16 +704,17 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_tc_kernel(const __grid_
                 }
             }
             fence_proxy_async_smem();
-            named_bar(1, 128);
+            named_bar(1, 256);
             if (pt == 0) {
                 // at most one chunk ahead of the MMA that consumes these tiles
                 if (c > 0) wait_bar(&bar_mma1, (c - 1) & 1, ctl);
                 mbar_arrive(&bar_elem);
             }
         }
-    } else if (warp >= 12) {
-        // ------------------------------------------------------------------ solve group (warps 12-15)
-        const int pt = tid - 384;
+    } else if (warp >= 16) {
+        regs_inc_120();
+        // ------------------------------------------------------------------ solve group (warps 16-19)
+        const int pt = tid - 512;
         const int wq = warp & 3;
         int gseq = 0;
         float *Mb = reinterpret_cast<float *>(sm + OFF_M);
@@ -976,6 +989,9 @@ cudaError_t launch_chunk_tc(const ChunkParams &cp, cudaStream_t stream) {
     p.o_phi = static_cast<__nv_bfloat16 *>(cp.o_phi);
     static bool attr_set = false;
     if (!attr_set) {
+        cudaFuncAttributes fa{};
+        if (cudaFuncGetAttributes(&fa, kda_chunk_tc_kernel) != cudaSuccess || fa.numRegs != 96)
+            return cudaErrorInvalidConfiguration;  // the register split assumes 96 per thread at launch
         cudaError_t e = cudaFuncSetAttribute(kda_chunk_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              static_cast<int>(kDynSmem));
         if (e != cudaSuccess) return e;

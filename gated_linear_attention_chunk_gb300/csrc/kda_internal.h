@@ -49,6 +49,7 @@ struct MergeParams {
     const int32_t *cu;
     int64_t T_total, seq_len_fixed;
     int N, H;
+    uint32_t *status;           // device status word (wait timeouts)
 };
 cudaError_t launch_merge(const MergeParams &p, cudaStream_t stream);
 
