@@ -264,8 +264,33 @@ def measure_state_kernels(kda, dev, hbm_peak, n_seq=128, H=32, d=128, reps=50):
         gbs = (state_bytes + tok_bytes) / (ms / 1e3) / 1e9
         out[name] = {"ms_per_call": ms, "achieved_GBs": gbs, "frac_of_hbm": gbs / hbm_peak,
                      "states": n_seq * H, "tokens_per_seq": 1 if name == "decode" else 4}
+    # state-pool operations on the same pool: fork half the slots onto the other half
+    # (read + write of 64 states x H heads), offload them to pinned host memory (write)
+    half = n_seq // 2
+    src = torch.arange(0, half, dtype=torch.int32, device=dev)
+    dst = torch.arange(half, 2 * half, dtype=torch.int32, device=dev)
+    host = torch.empty(half, H, d, d, dtype=torch.float32).pin_memory()
+    slot_bytes = H * d * d * 4
+    for name, call, nbytes in (("fork", lambda: kda.kda_state_fork(pool, src, dst, workspace=ws), 2 * half * slot_bytes),
+                               ("offload", lambda: kda.kda_state_offload(pool, src, host, workspace=ws),
+                                half * slot_bytes)):
+        for _ in range(3):
+            call()
+        torch.cuda.synchronize()
+        st = torch.cuda.current_stream()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(st)
+        for _ in range(reps):
+            call()
+        e1.record(st)
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / reps
+        gbs = nbytes / (ms / 1e3) / 1e9
+        out[name] = {"ms_per_call": ms, "achieved_GBs": gbs, "states": half * H,
+                     "frac_of_hbm": gbs / hbm_peak if name == "fork" else None,
+                     "bytes": "HBM read + write" if name == "fork" else "bytes written to pinned host memory"}
     if kda.kda_device_status(ws) != kda.KDA_OK:
-        raise RuntimeError("decode/replay device status")
+        raise RuntimeError("decode/replay/pool device status")
     return out
 
 

@@ -1,4 +1,4 @@
-"""libkda: Kimi Delta Attention forward (prefill, decode, replay) on GB300.
+"""libkda: Kimi Delta Attention forward (prefill, decode, replay, state-pool ops) on GB300.
 
 The compute path is the CUDA library ``_lib/libkda.so`` (C ABI, declared in
 ``include/kda.h``); this package is its ctypes binding.  Importing the package
@@ -9,13 +9,14 @@ from .kda import (KDA_BF16, KDA_ERR_BAD_SEQLENS, KDA_ERR_BAD_SLOT, KDA_ERR_CUDA,
                   KDA_ERR_INVALID_ARGUMENT, KDA_ERR_TIMEOUT, KDA_ERR_UNSUPPORTED, KDA_ERR_WORKSPACE, KDA_F32,
                   KDA_OK, KDA_WS_HEADER_BYTES, KdaError, kda_chunk_fwd, kda_chunk_fwd_noalloc, kda_chunk_fwd_uses_tensor_cores,
                   kda_chunk_fwd_workspace_size,
-                  kda_decode_step, kda_device_status, kda_replay, kda_status_string, kda_version,
-                  load_library, new_workspace)
+                  kda_decode_step, kda_device_status, kda_replay, kda_state_fork, kda_state_offload,
+                  kda_state_restore, kda_status_string, kda_version, load_library, new_workspace)
 
 load_library()
 
 __all__ = [
-    "kda_chunk_fwd", "kda_chunk_fwd_noalloc", "kda_chunk_fwd_workspace_size", "kda_chunk_fwd_uses_tensor_cores", "kda_decode_step", "kda_replay", "kda_device_status",
+    "kda_chunk_fwd", "kda_chunk_fwd_noalloc", "kda_chunk_fwd_workspace_size", "kda_chunk_fwd_uses_tensor_cores",
+    "kda_decode_step", "kda_replay", "kda_state_fork", "kda_state_offload", "kda_state_restore", "kda_device_status",
     "kda_status_string", "kda_version", "new_workspace", "KdaError", "KDA_OK", "KDA_BF16", "KDA_F32",
     "KDA_WS_HEADER_BYTES", "KDA_ERR_INVALID_ARGUMENT", "KDA_ERR_UNSUPPORTED", "KDA_ERR_WORKSPACE",
     "KDA_ERR_CUDA", "KDA_ERR_GATE_RANGE", "KDA_ERR_TIMEOUT", "KDA_ERR_BAD_SEQLENS", "KDA_ERR_BAD_SLOT",

@@ -50,6 +50,9 @@ _SIGS = {
     "kda_chunk_fwd_uses_tensor_cores": (_int, [_int, _int, _int]),
     "kda_chunk_fwd_noalloc": (_int, [_vp, _vp, _vp, _vp, _vp, _int, _vp, _vp, _int, _i64, _int, _int, _int,
                                      ctypes.c_float, _vp, _vp, ctypes.POINTER(ctypes.c_void_p), _vp]),
+    "kda_state_fork": (_int, [_vp, _i64, _vp, _vp, _int, _int, _int, _int, _vp, ctypes.c_size_t, _vp]),
+    "kda_state_offload": (_int, [_vp, _i64, _vp, _int, _int, _int, _int, _vp, _vp, ctypes.c_size_t, _vp]),
+    "kda_state_restore": (_int, [_vp, _i64, _vp, _int, _int, _int, _int, _vp, _vp, ctypes.c_size_t, _vp]),
 }
 
 _lib = None
@@ -261,6 +264,65 @@ def kda_replay(state_pool, k, v, g, beta, cu_accept, slots=None, workspace=None,
                         _ptr(beta), _dtype_code(k), _ptr(cu_accept), N, A, H, dk, dv, _ptr(workspace),
                         workspace.numel() * workspace.element_size(), _stream_handle(stream))
     _check(rc, "kda_replay")
+
+
+def _pool_shape(state_pool):
+    _need(state_pool, "state_pool", torch.float32)
+    if state_pool.dim() != 4:
+        raise ValueError(f"state_pool must be [S, H, dk, dv], got {tuple(state_pool.shape)}")
+    S, H, dk, dv = state_pool.shape
+    return S, H, dk, dv
+
+
+def kda_state_fork(state_pool, src_slots, dst_slots, workspace=None, stream=None) -> None:
+    """state_pool[dst_slots[i]] = state_pool[src_slots[i]] (int32 CUDA slot arrays), bit for bit."""
+    lib = load_library()
+    S, H, dk, dv = _pool_shape(state_pool)
+    n = src_slots.numel()
+    _need(src_slots, "src_slots", torch.int32, (n,))
+    _need(dst_slots, "dst_slots", torch.int32, (n,))
+    if workspace is None:
+        workspace = new_workspace(KDA_WS_HEADER_BYTES, state_pool.device)
+    rc = lib.kda_state_fork(_ptr(state_pool), S, _ptr(src_slots), _ptr(dst_slots), n, H, dk, dv, _ptr(workspace),
+                            workspace.numel() * workspace.element_size(), _stream_handle(stream))
+    _check(rc, "kda_state_fork")
+
+
+def kda_state_offload(state_pool, slots, host_states, workspace=None, stream=None) -> None:
+    """host_states[i] = state_pool[slots[i]]; host_states is a pinned CPU fp32 tensor [n, H, dk, dv]
+    (slots None: slot i).  Asynchronous: synchronize the stream before reading host_states."""
+    lib = load_library()
+    S, H, dk, dv = _pool_shape(state_pool)
+    if host_states.device.type != "cpu" or not host_states.is_pinned() or not host_states.is_contiguous():
+        raise ValueError("host_states must be a contiguous pinned CPU tensor")
+    n = host_states.shape[0]
+    if tuple(host_states.shape) != (n, H, dk, dv) or host_states.dtype != torch.float32:
+        raise ValueError(f"host_states must be float32 [n, {H}, {dk}, {dv}]")
+    if slots is not None:
+        _need(slots, "slots", torch.int32, (n,))
+    if workspace is None:
+        workspace = new_workspace(KDA_WS_HEADER_BYTES, state_pool.device)
+    rc = lib.kda_state_offload(_ptr(state_pool), S, _ptr(slots), n, H, dk, dv, host_states.data_ptr(),
+                               _ptr(workspace), workspace.numel() * workspace.element_size(), _stream_handle(stream))
+    _check(rc, "kda_state_offload")
+
+
+def kda_state_restore(state_pool, slots, host_states, workspace=None, stream=None) -> None:
+    """state_pool[slots[i]] = host_states[i]; host_states a pinned CPU fp32 tensor [n, H, dk, dv]."""
+    lib = load_library()
+    S, H, dk, dv = _pool_shape(state_pool)
+    if host_states.device.type != "cpu" or not host_states.is_pinned() or not host_states.is_contiguous():
+        raise ValueError("host_states must be a contiguous pinned CPU tensor")
+    n = host_states.shape[0]
+    if tuple(host_states.shape) != (n, H, dk, dv) or host_states.dtype != torch.float32:
+        raise ValueError(f"host_states must be float32 [n, {H}, {dk}, {dv}]")
+    if slots is not None:
+        _need(slots, "slots", torch.int32, (n,))
+    if workspace is None:
+        workspace = new_workspace(KDA_WS_HEADER_BYTES, state_pool.device)
+    rc = lib.kda_state_restore(_ptr(state_pool), S, _ptr(slots), n, H, dk, dv, host_states.data_ptr(),
+                               _ptr(workspace), workspace.numel() * workspace.element_size(), _stream_handle(stream))
+    _check(rc, "kda_state_restore")
 
 
 def kda_device_status(workspace, stream=None) -> int:

@@ -156,6 +156,43 @@ kda_status kda_replay(float *state_pool, int64_t num_slots, const int32_t *slots
                       void *workspace, size_t ws_bytes, void *stream);
 
 /*
+ * State-pool operations for rollout caching.  In RL rollouts many trajectories
+ * branch from a shared prompt, and each branch continues from its own copy of
+ * the prompt's recurrent state; the states of inactive trajectories are kept
+ * in host memory and brought back when the trajectory resumes ("Kimi K3 on
+ * Fireworks: Fast RL at frontier scale": the rollout paragraph on MLA / KDA
+ * histories that stay consistent as trajectories branch from shared prompts,
+ * and the serverless-training paragraph on moving reusable KV and KDA states to
+ * host memory and loading inactive snapshots asynchronously).
+ *
+ * A slot's state is the whole [H, dk, dv] fp32 block of the pool,
+ * state_pool[slot] (H*dk*dv*4 bytes).  Slot arrays are int32 DEVICE arrays of
+ * length n.  A slot outside [0, num_slots) sets KDA_ERR_BAD_SLOT in the status
+ * word and that item copies nothing.  Copies are exact (bit for bit).
+ * workspace: >= KDA_WS_HEADER_BYTES bytes (status word).
+ */
+
+/* Fork: state_pool[dst_slots[i]] = state_pool[src_slots[i]] for i < n.  No
+ * destination may appear twice or be the source of another item (the items
+ * run concurrently); src == dst copies a state onto itself. */
+kda_status kda_state_fork(float *state_pool, int64_t num_slots, const int32_t *src_slots, const int32_t *dst_slots,
+                          int n, int H, int dk, int dv, void *workspace, size_t ws_bytes, void *stream);
+
+/* Offload: host_states[i] = state_pool[slots[i]] (slots NULL: slot i), for i < n.
+ * host_states: [n, H, dk, dv] fp32 in page-locked host memory that the device
+ * can address (cudaHostAlloc / cudaHostRegister with mapping; with unified
+ * addressing every page-locked allocation is), 16-byte aligned; otherwise
+ * KDA_ERR_INVALID_ARGUMENT.  The kernel writes the host memory directly;
+ * synchronize `stream` before reading it on the host. */
+kda_status kda_state_offload(const float *state_pool, int64_t num_slots, const int32_t *slots, int n, int H, int dk,
+                             int dv, float *host_states, void *workspace, size_t ws_bytes, void *stream);
+
+/* Restore: state_pool[slots[i]] = host_states[i] (slots NULL: slot i), for i < n;
+ * host_states as for kda_state_offload.  No slot may appear twice. */
+kda_status kda_state_restore(float *state_pool, int64_t num_slots, const int32_t *slots, int n, int H, int dk,
+                             int dv, const float *host_states, void *workspace, size_t ws_bytes, void *stream);
+
+/*
  * Synchronizes `stream`, then reads the device status word of `workspace`
  * (errors from the last call that used it).  Returns KDA_OK or the first of
  * BAD_SEQLENS, BAD_SLOT, GATE_RANGE, TIMEOUT that was raised; KDA_ERR_CUDA if

@@ -85,3 +85,17 @@ def test_decode_and_replay_host_errors(lib):
     assert r(FAKE, 4, None, FAKE, FAKE, FAKE, FAKE, 1, FAKE, 2, 8, 2, 64, 48, FAKE, 256, None) == 2
     assert r(FAKE, 1, None, FAKE, FAKE, FAKE, FAKE, 0, FAKE, 2, 8, 2, 128, 128, FAKE, 256, None) == 1
     assert r(FAKE, 4, None, FAKE, FAKE, FAKE, FAKE, 0, FAKE, 2, 8, 2, 128, 128, None, 256, None) == 3
+
+
+def test_state_pool_host_errors(lib):
+    """Host-detectable errors of the state-pool calls return before any CUDA work."""
+    import ctypes
+    ws = ctypes.c_void_p(4096)          # never dereferenced on these paths
+    fake = ctypes.c_void_p(1 << 20)     # aligned stand-in for a device pointer
+    assert lib.kda_state_fork(fake, 8, fake, fake, 1, 2, 96, 128, ws, 256, None) == 2   # UNSUPPORTED dk
+    assert lib.kda_state_fork(fake, 8, fake, fake, -1, 2, 128, 128, ws, 256, None) == 1  # negative n
+    assert lib.kda_state_fork(fake, 8, None, fake, 1, 2, 128, 128, ws, 256, None) == 1   # NULL slots
+    assert lib.kda_state_fork(fake, 8, fake, fake, 1, 2, 128, 128, None, 256, None) == 3  # no workspace
+    assert lib.kda_state_offload(fake, 8, None, 1, 2, 128, 128, None, ws, 256, None) == 1  # NULL host
+    assert lib.kda_state_restore(fake, 8, None, 1, 0, 128, 128, fake, ws, 256, None) == 1  # H = 0
+    assert lib.kda_state_offload(fake, 8, None, 1, 2, 128, 128, fake, ws, 16, None) == 3   # small workspace
