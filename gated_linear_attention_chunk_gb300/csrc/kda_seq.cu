@@ -203,6 +203,19 @@ __global__ void __launch_bounds__(kSeqThreads, 6) kda_seq_kernel(SeqParams p) {
         if (tid == kSeqThreads - 1) tok_b[buf] = rb;
     };
 
+    // Warm L2 with the next three tokens' rows (fire and forget): in a multi-token call
+    // (replay, prefill tail) each token's load would otherwise be a full memory round
+    // trip between two dependent token steps.
+    for (int64_t t = t0 + 1; t < t1 && t < t0 + 4; ++t) {
+        if (tid < DK) {
+            const int64_t base = (t * H + h) * DK + tid;
+            asm volatile("prefetch.L2 [%0];" ::"l"(G + base));
+            asm volatile("prefetch.L2 [%0];" ::"l"(K + base));
+            if (WRITE_O) asm volatile("prefetch.L2 [%0];" ::"l"(Q + base));
+        }
+        if (tid < CB) asm volatile("prefetch.L2 [%0];" ::"l"(V + (t * H + h) * DV + col0 + tid));
+        if (tid == kSeqThreads - 1) asm volatile("prefetch.L2 [%0];" ::"l"(B + t * H + h));
+    }
     if (t0 < t1) {
         float rg = 0.f, rk = 0.f, rq = 0.f, rv = 0.f, rb = 0.f;
         load_raw(t0, rg, rk, rq, rv, rb);
