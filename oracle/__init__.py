@@ -59,6 +59,9 @@ def _load():
                                                ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
                                                ctypes.c_int64, ctypes.c_double, ctypes.c_int, dp, dp,
                                                ctypes.c_int]
+            lib.kda_oracle_prep.restype = ctypes.c_int
+            lib.kda_oracle_prep.argtypes = [dp, dp, dp, dp, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                                            ctypes.c_double, ctypes.c_int]
             lib.kda_oracle_max_threads.restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -86,14 +89,37 @@ def _ptr(a: Optional[np.ndarray]):
     return a.ctypes.data_as(ctypes.POINTER(ctypes.c_double))
 
 
+PREP_L2NORM_Q, PREP_L2NORM_K, PREP_SIGMOID_GATE, PREP_SIGMOID_BETA = 1, 2, 4, 8
+
+
+def prep(q, k, g, beta, flags: int, eps: float = 1e-6):
+    """fp64 copies of the inputs with the preprocessing of ``flags`` applied
+    (kda_oracle_prep: L2 normalisation of q / k rows, alpha = sigmoid(x_g),
+    beta = sigmoid(x_beta)).  q may be None when flags has no PREP_L2NORM_Q."""
+    lib = _load()
+    k64, g64, b64 = _f64(k).copy(), _f64(g).copy(), _f64(beta).copy()
+    q64 = None if q is None else _f64(q).copy()
+    T, H, dk = k64.shape
+    rc = lib.kda_oracle_prep(_ptr(q64), _ptr(k64), _ptr(g64), _ptr(b64), T, H, dk, float(eps), int(flags))
+    if rc != 0:
+        raise RuntimeError(f"kda_oracle_prep failed with code {rc}")
+    return q64, k64, g64, b64
+
+
 def forward(q, k, v, g, beta, cu_seqlens, init_state=None, scale: float = 1.0,
-            gate_is_alpha: bool = False, want_o: bool = True, threads: int = 1):
+            gate_is_alpha: bool = False, want_o: bool = True, threads: int = 1, prep_flags: int = 0,
+            prep_eps: float = 1e-6):
     """Packed variable-length KDA forward in fp64.
 
     Shapes: q, k, g [T, H, dk]; v [T, H, dv]; beta [T, H]; cu_seqlens [N+1];
     init_state [N, H, dk, dv] or None.  Returns ``(o, final_state)`` as float64
-    numpy arrays (``o`` is None when ``want_o`` is False).
+    numpy arrays (``o`` is None when ``want_o`` is False).  ``prep_flags`` applies
+    the input preprocessing first (see ``prep``); with PREP_SIGMOID_GATE, g holds
+    the raw gate x and alpha = sigmoid(x).
     """
+    if prep_flags:
+        q, k, g, beta = prep(q if want_o else None, k, g, beta, prep_flags, prep_eps)
+        gate_is_alpha = bool(prep_flags & PREP_SIGMOID_GATE) or gate_is_alpha
     lib = _load()
     k64, v64, g64, b64 = _f64(k), _f64(v), _f64(g), _f64(beta)
     q64 = _f64(q) if want_o else None
@@ -115,7 +141,8 @@ def forward(q, k, v, g, beta, cu_seqlens, init_state=None, scale: float = 1.0,
     return o, fs
 
 
-def decode(q, k, v, g, beta, state_pool, slots=None, scale: float = 1.0, threads: int = 1):
+def decode(q, k, v, g, beta, state_pool, slots=None, scale: float = 1.0, threads: int = 1, prep_flags: int = 0,
+           prep_eps: float = 1e-6):
     """One decode step per sequence on a slot-indexed pool.
 
     q, k, g [N, H, dk]; v [N, H, dv]; beta [N, H]; state_pool [S, H, dk, dv];
@@ -125,12 +152,14 @@ def decode(q, k, v, g, beta, state_pool, slots=None, scale: float = 1.0, threads
     N = np.asarray(_f64(k)).shape[0]
     sl = np.arange(N) if slots is None else np.asarray(_f64(slots), dtype=np.int64)
     cu = np.arange(N + 1, dtype=np.int64)
-    o, fs = forward(q, k, v, g, beta, cu, pool[sl], scale=scale, threads=threads)
+    o, fs = forward(q, k, v, g, beta, cu, pool[sl], scale=scale, threads=threads, prep_flags=prep_flags,
+                    prep_eps=prep_eps)
     pool[sl] = fs
     return o, pool
 
 
-def replay(k, v, g, beta, cu_accept, state_pool, slots=None, threads: int = 1):
+def replay(k, v, g, beta, cu_accept, state_pool, slots=None, threads: int = 1, prep_flags: int = 0,
+           prep_eps: float = 1e-6):
     """Apply each sequence's accepted tokens to its committed state in the pool.
 
     k, g [A, H, dk]; v [A, H, dv]; beta [A, H]; cu_accept [N+1].  Returns the
@@ -140,6 +169,7 @@ def replay(k, v, g, beta, cu_accept, state_pool, slots=None, threads: int = 1):
     cu = np.asarray(_f64(cu_accept), dtype=np.int64)
     N = cu.shape[0] - 1
     sl = np.arange(N) if slots is None else np.asarray(_f64(slots), dtype=np.int64)
-    _, fs = forward(None, k, v, g, beta, cu, pool[sl], want_o=False, threads=threads)
+    _, fs = forward(None, k, v, g, beta, cu, pool[sl], want_o=False, threads=threads,
+                    prep_flags=prep_flags & ~PREP_L2NORM_Q, prep_eps=prep_eps)
     pool[sl] = fs
     return pool

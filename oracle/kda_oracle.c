@@ -121,6 +121,42 @@ int kda_oracle_forward(const double *q, const double *k, const double *v, const 
     return failed ? KDA_ORACLE_NO_MEMORY : KDA_ORACLE_OK;
 }
 
+/*
+ * Input preprocessing, in place, for callers that pass raw projections (the
+ * optional fused preprocessing of the library).  The pages do not define KDA's
+ * input maps; the reading taken is the common one for delta-rule attention:
+ *   flags & 1:  q_t <- q_t / sqrt(sum_i q_{t,i}^2 + eps)   per (token, head), over dk
+ *   flags & 2:  k_t <- k_t / sqrt(sum_i k_{t,i}^2 + eps)
+ *   flags & 4:  g   <- sigmoid(g) elementwise: the log-gate is logsigmoid(x), so the
+ *               decay alpha = exp(logsigmoid(x)) = sigmoid(x) is stored directly
+ *               (call kda_oracle_forward with gate_is_alpha = 1)
+ *   flags & 8:  beta <- sigmoid(beta)
+ * q may be NULL when flags has no bit 1.
+ */
+static double sigmoid(double x) { return 1.0 / (1.0 + exp(-x)); }
+
+int kda_oracle_prep(double *q, double *k, double *g, double *beta, int64_t T, int64_t H, int64_t dk,
+                    double eps, int flags)
+{
+    if (T < 0 || H <= 0 || dk <= 0 || eps < 0.0) return KDA_ORACLE_BAD_ARGS;
+    if (((flags & 1) && !q) || ((flags & 2) && !k) || ((flags & 4) && !g) || ((flags & 8) && !beta))
+        return KDA_ORACLE_BAD_ARGS;
+    for (int64_t r = 0; r < T * H; ++r) {
+        for (int which = 0; which < 2; ++which) {
+            if (!(flags & (1 << which))) continue;
+            double *x = (which == 0 ? q : k) + r * dk;
+            double ss = 0.0;
+            for (int64_t i = 0; i < dk; ++i) ss += x[i] * x[i];
+            const double inv = 1.0 / sqrt(ss + eps);
+            for (int64_t i = 0; i < dk; ++i) x[i] *= inv;
+        }
+        if (flags & 4)
+            for (int64_t i = 0; i < dk; ++i) g[r * dk + i] = sigmoid(g[r * dk + i]);
+        if (flags & 8) beta[r] = sigmoid(beta[r]);
+    }
+    return KDA_ORACLE_OK;
+}
+
 /* Threads the OpenMP runtime would use by default (1 without OpenMP). */
 int kda_oracle_max_threads(void)
 {

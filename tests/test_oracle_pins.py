@@ -361,3 +361,65 @@ def test_chunked_wy_identities_exact(C):
     o_chk, s_chk = _chunked_wy(q, k, v, alpha, beta, s0, scale, C)
     assert o_chk == o_ref
     assert s_chk == s_ref
+
+
+# ---------------------------------------------------------------------------------------------
+# Optional input preprocessing (fused in the library behind flags): L2-normalised q / k rows,
+# alpha = sigmoid(x_g) (the log-gate logsigmoid(x)), beta = sigmoid(x_beta).
+# ---------------------------------------------------------------------------------------------
+PREP_ALL = oracle.PREP_L2NORM_Q | oracle.PREP_L2NORM_K | oracle.PREP_SIGMOID_GATE | oracle.PREP_SIGMOID_BETA
+
+
+def test_prep_closed_forms():
+    x = np.array([[[3.0, 4.0, 0.0, 0.0], [0.0, 0.0, 5.0, 12.0]]])
+    g = np.array([[[0.0, 40.0, -40.0, np.log(3.0)]] * 2]).reshape(1, 2, 4)
+    b = np.array([[0.0, np.log(3.0)]])
+    q2, k2, g2, b2 = oracle.prep(x, x, g, b, PREP_ALL, eps=0.0)
+    np.testing.assert_allclose(q2[0, 0], [0.6, 0.8, 0.0, 0.0], rtol=0, atol=1e-15)
+    np.testing.assert_allclose(k2[0, 1], [0.0, 0.0, 5 / 13, 12 / 13], rtol=0, atol=1e-15)
+    # sigmoid(0) = 1/2, sigmoid(log 3) = 3/4, sigmoid(40) ~ 1, sigmoid(-40) ~ e^-40
+    np.testing.assert_allclose(g2[0, 0], [0.5, 1.0, np.exp(-40.0), 0.75], rtol=1e-12, atol=0)
+    np.testing.assert_allclose(b2[0], [0.5, 0.75], rtol=1e-15, atol=0)
+    # only the flagged inputs change
+    q3, k3, g3, b3 = oracle.prep(x, x, g, b, oracle.PREP_L2NORM_K, eps=0.0)
+    assert np.array_equal(q3, x) and np.array_equal(g3, g) and np.array_equal(b3, b)
+
+
+def test_prep_invariants():
+    rng = np.random.default_rng(11)
+    x = rng.standard_normal((5, 3, 16))
+    g = rng.standard_normal((5, 3, 16)) * 4
+    b = rng.standard_normal((5, 3))
+    q1, k1, g1, b1 = oracle.prep(x, x, g, b, PREP_ALL, eps=0.0)
+    q2, _, g2, b2 = oracle.prep(7.5 * x, x, -g, -b, PREP_ALL, eps=0.0)
+    np.testing.assert_allclose(q2, q1, rtol=1e-14, atol=1e-15)          # scale invariance
+    np.testing.assert_allclose(np.linalg.norm(k1, axis=-1), 1.0, rtol=1e-14)  # unit rows
+    np.testing.assert_allclose(g1 + g2, 1.0, rtol=0, atol=1e-15)       # sigmoid(x) + sigmoid(-x) = 1
+    np.testing.assert_allclose(b1 + b2, 1.0, rtol=0, atol=1e-15)
+    # with eps > 0 the norm shrinks below one, more for short rows
+    _, k_eps, _, _ = oracle.prep(x, x, g, b, oracle.PREP_L2NORM_K, eps=1.0)
+    assert np.all(np.linalg.norm(k_eps, axis=-1) < 1.0)
+
+
+def test_prep_forward_reduces_to_plain_forward():
+    """Gate limits and fixed points of the preprocessing give the plain recurrence."""
+    rng = _rng(21)
+    T, H, dk, dv = 13, 2, 8, 6
+    cu = np.array([0, 9, 13])
+    q, k = rng.standard_normal((T, H, dk)), rng.standard_normal((T, H, dk))
+    v, beta = rng.standard_normal((T, H, dv)), rng.standard_normal((T, H))
+    k = k / np.linalg.norm(k, axis=-1, keepdims=True)            # unit rows: L2 flag is a no-op (eps = 0)
+    q = q / np.linalg.norm(q, axis=-1, keepdims=True)
+    s0 = rng.standard_normal((2, H, dk, dv)) * 0.1
+    xg_inf = np.full(k.shape, np.inf)                              # sigmoid(+inf) = 1: no decay
+    o_a, s_a = oracle.forward(q, k, v, xg_inf, np.zeros_like(beta), cu, s0,
+                              prep_flags=PREP_ALL, prep_eps=0.0)
+    o_b, s_b = oracle.forward(q, k, v, np.zeros(k.shape), np.full(beta.shape, 0.5), cu, s0)
+    np.testing.assert_allclose(o_a, o_b, rtol=1e-13, atol=1e-13)
+    np.testing.assert_allclose(s_a, s_b, rtol=1e-13, atol=1e-13)
+    # sigmoid(-inf) = 0 erases the state: equals a fresh start with no decay afterwards
+    xg = np.full(k.shape, np.inf)
+    xg[0] = -np.inf
+    o_c, _ = oracle.forward(q, k, v, xg, beta, cu, s0, prep_flags=oracle.PREP_SIGMOID_GATE)
+    o_d, _ = oracle.forward(q, k, v, np.zeros(k.shape), beta, cu, np.zeros_like(s0))
+    np.testing.assert_allclose(o_c[:9], o_d[:9], rtol=1e-13, atol=1e-13)
