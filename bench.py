@@ -9,6 +9,10 @@ Multi-GPU: (sequence, head) chains are independent, so each rank runs its own
 copy of the batch (weak scaling, no collective on the data path); the timed
 region is bracketed by barriers and the max over ranks is taken.
 
+``--prep`` runs the same workload on raw inputs (un-normalised q / k, raw gate and
+beta logits) through kda_chunk_fwd_prep with every preprocessing flag, so the
+normalisation, sigmoid gate and sigmoid beta are fused into the kernels.
+
 ``--impl reference`` times the fp64 CPU oracle (the correctness reference, a
 deliberately slow program) on a bounded sample of the same workload.
 """
@@ -38,6 +42,9 @@ UNIT = "tokens/s"
 # ncu capture summarised in profiles/kda_chunk_tc_prefill_4k.md (546.7 MB read +
 # 117.2 MB written).  Reset to None whenever that kernel changes until it is re-captured.
 DOMINANT_TRAFFIC = {"prefill_4k": 663934208}
+
+# every preprocessing flag (KDA_PREP_L2NORM_Q | _L2NORM_K | _SIGMOID_GATE | _SIGMOID_BETA)
+PREP_ALL, PREP_EPS = 15, 1e-6
 
 
 # ------------------------------------------------------------------------------------------------
@@ -169,7 +176,7 @@ class ClockSampler:
 # CPU oracle timing (bounded sample)
 # ------------------------------------------------------------------------------------------------
 
-def oracle_sample_rate(case, budget_s: float = 10.0):
+def oracle_sample_rate(case, budget_s: float = 10.0, prep: int = 0):
     """Oracle tokens/s on a prefix of sequence 0 (all heads), sized to about ``budget_s``."""
     import oracle
     threads = max(1, min(os.cpu_count() or 1, case.H))
@@ -180,7 +187,7 @@ def oracle_sample_rate(case, budget_s: float = 10.0):
         oracle.forward(case.q[sl], case.k[sl], case.v[sl], case.g[sl], case.beta[sl],
                        torch.tensor([0, L], dtype=torch.int64),
                        None if case.init_state is None else case.init_state[:1],
-                       scale=case.scale, threads=threads)
+                       scale=case.scale, threads=threads, prep_flags=prep, prep_eps=PREP_EPS)
         return time.perf_counter() - t
 
     L0 = min(case.lengths[0], 16)
@@ -199,14 +206,15 @@ def oracle_sample_rate(case, budget_s: float = 10.0):
 def run_reference(args, world, rank):
     if rank != 0:
         return 0
-    case = workloads.named_case(args.workload)
+    case = workloads.named_case(args.workload, raw=args.prep)
+    prep = PREP_ALL if args.prep else 0
     # the whole run (warm-up + timed samples) stays within about three minutes
     budget = min(args.ref_budget, 150.0 / (args.steps + args.warmup))
     per_step = []
     for _ in range(args.warmup):
-        oracle_sample_rate(case, budget_s=budget)
+        oracle_sample_rate(case, budget_s=budget, prep=prep)
     for _ in range(args.steps):
-        per_step.append(oracle_sample_rate(case, budget_s=budget))
+        per_step.append(oracle_sample_rate(case, budget_s=budget, prep=prep))
     vals = [r["value"] for r in per_step]
     v = sum(vals) / len(vals)
     cb = dict(per_step[-1])
@@ -229,7 +237,9 @@ def config_dict(args, case):
             "parallelism": f"dp{max(1, args.gpus)} (independent replicas)",
             "l2": "inputs larger than L2 (no flush needed)" if algorithmic_bytes(case) > 256e6
                   else "L2 flushed between steps",
-            "workspace": "minimum (no T-segment split)" if getattr(args, "plain_workspace", False) else "full"}
+            "workspace": "minimum (no T-segment split)" if getattr(args, "plain_workspace", False) else "full",
+            "inputs": ("raw: L2 norm of q / k rows (eps 1e-6), sigmoid gate, sigmoid beta fused"
+                       " (kda_chunk_fwd_prep)") if getattr(args, "prep", False) else "preprocessed"}
 
 
 def measure_state_kernels(kda, dev, hbm_peak, n_seq=128, H=32, d=128, reps=50):
@@ -304,7 +314,8 @@ def run_gpu(args, world, rank, local):
     if distributed:
         dist.init_process_group("nccl", device_id=dev)
 
-    case = workloads.named_case(args.workload)
+    case = workloads.named_case(args.workload, raw=args.prep)
+    prep = PREP_ALL if args.prep else 0
     q, k, v, g, b = (x.to(dev) for x in (case.q, case.k, case.v, case.g, case.beta))
     cu = case.cu_seqlens.to(dev)
     s0 = None if case.init_state is None else case.init_state.to(dev)
@@ -321,9 +332,16 @@ def run_gpu(args, world, rank, local):
     if algorithmic_bytes(case) <= 256e6:
         flush = torch.empty(int(256e6), dtype=torch.uint8, device=dev)
 
+    def call(q, k, v, g, b, cu, s0):
+        if prep:
+            kda.kda_chunk_fwd_prep(q, k, v, g, b, prep, PREP_EPS, cu_seqlens=cu, init_state=s0, scale=case.scale,
+                                   o=o, final_state=fs, workspace=ws)
+        else:
+            kda.kda_chunk_fwd(q, k, v, g, b, cu_seqlens=cu, init_state=s0, scale=case.scale, o=o,
+                              final_state=fs, workspace=ws)
+
     def step():
-        kda.kda_chunk_fwd(q, k, v, g, b, cu_seqlens=cu, init_state=s0, scale=case.scale, o=o,
-                          final_state=fs, workspace=ws)
+        call(q, k, v, g, b, cu, s0)
 
     # kernels of ours per kda_chunk_fwd: the chunked tensor-core kernel (when it serves this shape)
     # plus the token-sequential partial-chunk kernel
@@ -390,8 +408,7 @@ def run_gpu(args, world, rank, local):
         dcu.copy_(host["cu"], non_blocking=True)
         if ds0 is not None:
             ds0.copy_(host["s0"], non_blocking=True)
-        kda.kda_chunk_fwd(dq, dk_, dvv, dg, db, cu_seqlens=dcu, init_state=ds0, scale=case.scale, o=o,
-                          final_state=fs, workspace=ws)
+        call(dq, dk_, dvv, dg, db, dcu, ds0)
         host_o.copy_(o, non_blocking=True)
         host_fs.copy_(fs, non_blocking=True)
 
@@ -416,14 +433,15 @@ def run_gpu(args, world, rank, local):
     t_hbm = nbytes / (hbm_peak * 1e9)
     t_tc = flops / (tf_peak * 1e12)
     bound = "hbm" if t_hbm >= t_tc else "tensor"
+    traffic = None if prep else (DOMINANT_TRAFFIC or {}).get(args.workload)  # captured on preprocessed inputs
     if bound == "hbm":
         achieved = nbytes / (kern_ms / 1e3) / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
-                "frac": achieved / hbm_peak, "traffic": (DOMINANT_TRAFFIC or {}).get(args.workload)}
+                "frac": achieved / hbm_peak, "traffic": traffic}
     else:
         achieved = flops / (kern_ms / 1e3) / 1e12
         roof = {"bound": "tensor", "achieved": achieved, "peak": tf_peak, "unit": "TFLOP/s",
-                "frac": achieved / tf_peak, "traffic": (DOMINANT_TRAFFIC or {}).get(args.workload)}
+                "frac": achieved / tf_peak, "traffic": traffic}
     roof.update({"peak_source": f"{peak_src} (MEASURED_PEAKS.json)" if peak_src == "measured" else peak_src,
                  "algorithmic_bytes": nbytes, "algorithmic_flops": flops,
                  "kernel_ms_median": kern_ms, "roofline_ms": 1e3 * max(t_hbm, t_tc),
@@ -434,7 +452,7 @@ def run_gpu(args, world, rank, local):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = oracle_sample_rate(case, budget_s=args.ref_budget)
+        cpu = oracle_sample_rate(case, budget_s=args.ref_budget, prep=prep)
 
     if rank == 0:
         line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -461,6 +479,8 @@ def main(argv=None):
     ap.add_argument("--no-state-kernels", action="store_true", help="skip the decode/replay bandwidth check")
     ap.add_argument("--plain-workspace", action="store_true",
                     help="minimum workspace: kda_chunk_fwd runs without the T-segment split")
+    ap.add_argument("--prep", action="store_true",
+                    help="raw inputs through kda_chunk_fwd_prep with every preprocessing flag")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -16,6 +16,12 @@ bool dim_ok(int d) { return d == 64 || d == 128; }
 bool dtype_ok(kda_dtype t) { return t == KDA_BF16 || t == KDA_F32; }
 size_t elem_size(kda_dtype t) { return t == KDA_BF16 ? 2 : 4; }
 
+// Known preprocessing flags only, and a finite non-negative epsilon.
+bool prep_ok(uint32_t prep, float eps) {
+    const uint32_t known = KDA_PREP_L2NORM_Q | KDA_PREP_L2NORM_K | KDA_PREP_SIGMOID_GATE | KDA_PREP_SIGMOID_BETA;
+    return (prep & ~known) == 0 && eps >= 0.f && eps < 3.0e38f;
+}
+
 size_t staging_offset() { return KDA_WS_HEADER_BYTES; }
 
 size_t state_bytes(int N, int H, int dk, int dv) {
@@ -53,11 +59,12 @@ size_t kda_chunk_fwd_workspace_size(int N, int64_t T_total, int H, int dk, int d
     return staging_offset() + state_bytes(N, H, dk, dv);
 }
 
-kda_status kda_chunk_fwd(const void *q, const void *k, const void *v, const void *g, const void *beta,
-                         kda_dtype dtype, const float *init_state, const int32_t *cu_seqlens, int N,
-                         int64_t T_total, int H, int dk, int dv, float scale, void *o, float *final_state,
-                         void *workspace, size_t ws_bytes, void *stream) {
+kda_status kda_chunk_fwd_prep(const void *q, const void *k, const void *v, const void *g, const void *beta,
+                              kda_dtype dtype, const float *init_state, const int32_t *cu_seqlens, int N,
+                              int64_t T_total, int H, int dk, int dv, float scale, uint32_t prep, float l2_eps,
+                              void *o, float *final_state, void *workspace, size_t ws_bytes, void *stream) {
     if (!dtype_ok(dtype) || !dim_ok(dk) || !dim_ok(dv)) return KDA_ERR_UNSUPPORTED;
+    if (!prep_ok(prep, l2_eps)) return KDA_ERR_INVALID_ARGUMENT;
     if (N < 0 || T_total < 0 || H <= 0) return KDA_ERR_INVALID_ARGUMENT;
     if (!workspace || !aligned16(workspace)) return KDA_ERR_WORKSPACE;
     if (ws_bytes < KDA_WS_HEADER_BYTES) return KDA_ERR_WORKSPACE;
@@ -95,6 +102,7 @@ kda_status kda_chunk_fwd(const void *q, const void *k, const void *v, const void
         cp.N = N; cp.H = H; cp.scale = scale;
         cp.cu = cu_seqlens; cp.T_total = T_total; cp.seq_len_fixed = fixed_len;
         cp.init_state = init_state; cp.state_out = chunk_state; cp.status = status;
+        cp.prep = static_cast<int>(prep); cp.prep_eps = l2_eps;
         if (split) {
             char *base = static_cast<char *>(workspace) + staging_offset() + state_bytes(N, H, dk, dv);
             cp.split = 1;
@@ -120,15 +128,25 @@ kda_status kda_chunk_fwd(const void *q, const void *k, const void *v, const void
     sp.chunk_skip = use_tc ? 1 : 0;
     sp.state_in = init_state; sp.state_out = final_state; sp.chunk_state = chunk_state;
     sp.slots = nullptr; sp.num_slots = 0; sp.status = status;
+    sp.prep = static_cast<int>(prep); sp.prep_eps = l2_eps;
     if (kda::launch_seq(sp, dk, dv, static_cast<int>(dtype), s) != cudaSuccess) return KDA_ERR_CUDA;
     return KDA_OK;
 }
 
-kda_status kda_decode_step(const void *q, const void *k, const void *v, const void *g, const void *beta,
-                           kda_dtype dtype, float *state_pool, int64_t num_slots, const int32_t *slots,
-                           int N, int H, int dk, int dv, float scale, void *o, void *workspace,
-                           size_t ws_bytes, void *stream) {
+kda_status kda_chunk_fwd(const void *q, const void *k, const void *v, const void *g, const void *beta,
+                         kda_dtype dtype, const float *init_state, const int32_t *cu_seqlens, int N,
+                         int64_t T_total, int H, int dk, int dv, float scale, void *o, float *final_state,
+                         void *workspace, size_t ws_bytes, void *stream) {
+    return kda_chunk_fwd_prep(q, k, v, g, beta, dtype, init_state, cu_seqlens, N, T_total, H, dk, dv, scale, 0u,
+                              0.f, o, final_state, workspace, ws_bytes, stream);
+}
+
+kda_status kda_decode_step_prep(const void *q, const void *k, const void *v, const void *g, const void *beta,
+                                kda_dtype dtype, float *state_pool, int64_t num_slots, const int32_t *slots,
+                                int N, int H, int dk, int dv, float scale, uint32_t prep, float l2_eps, void *o,
+                                void *workspace, size_t ws_bytes, void *stream) {
     if (!dtype_ok(dtype) || !dim_ok(dk) || !dim_ok(dv)) return KDA_ERR_UNSUPPORTED;
+    if (!prep_ok(prep, l2_eps)) return KDA_ERR_INVALID_ARGUMENT;
     if (N < 0 || H <= 0 || num_slots < 0) return KDA_ERR_INVALID_ARGUMENT;
     if (!workspace || !aligned16(workspace) || ws_bytes < KDA_WS_HEADER_BYTES) return KDA_ERR_WORKSPACE;
     if (N > 0) {
@@ -151,15 +169,25 @@ kda_status kda_decode_step(const void *q, const void *k, const void *v, const vo
     sp.cu = nullptr; sp.T_total = N; sp.seq_len_fixed = 1; sp.chunk_skip = 0;
     sp.state_in = state_pool; sp.state_out = state_pool; sp.chunk_state = nullptr;
     sp.slots = slots; sp.num_slots = num_slots; sp.status = static_cast<uint32_t *>(workspace);
+    sp.prep = static_cast<int>(prep); sp.prep_eps = l2_eps;
     if (kda::launch_seq(sp, dk, dv, static_cast<int>(dtype), s) != cudaSuccess) return KDA_ERR_CUDA;
     return KDA_OK;
 }
 
-kda_status kda_replay(float *state_pool, int64_t num_slots, const int32_t *slots, const void *k,
-                      const void *v, const void *g, const void *beta, kda_dtype dtype,
-                      const int32_t *cu_accept, int N, int64_t A_total, int H, int dk, int dv,
-                      void *workspace, size_t ws_bytes, void *stream) {
+kda_status kda_decode_step(const void *q, const void *k, const void *v, const void *g, const void *beta,
+                           kda_dtype dtype, float *state_pool, int64_t num_slots, const int32_t *slots,
+                           int N, int H, int dk, int dv, float scale, void *o, void *workspace,
+                           size_t ws_bytes, void *stream) {
+    return kda_decode_step_prep(q, k, v, g, beta, dtype, state_pool, num_slots, slots, N, H, dk, dv, scale, 0u, 0.f,
+                                o, workspace, ws_bytes, stream);
+}
+
+kda_status kda_replay_prep(float *state_pool, int64_t num_slots, const int32_t *slots, const void *k,
+                           const void *v, const void *g, const void *beta, kda_dtype dtype,
+                           const int32_t *cu_accept, int N, int64_t A_total, int H, int dk, int dv, uint32_t prep,
+                           float l2_eps, void *workspace, size_t ws_bytes, void *stream) {
     if (!dtype_ok(dtype) || !dim_ok(dk) || !dim_ok(dv)) return KDA_ERR_UNSUPPORTED;
+    if (!prep_ok(prep, l2_eps)) return KDA_ERR_INVALID_ARGUMENT;
     if (N < 0 || A_total < 0 || H <= 0 || num_slots < 0) return KDA_ERR_INVALID_ARGUMENT;
     if (!workspace || !aligned16(workspace) || ws_bytes < KDA_WS_HEADER_BYTES) return KDA_ERR_WORKSPACE;
     if (N > 0) {
@@ -184,8 +212,17 @@ kda_status kda_replay(float *state_pool, int64_t num_slots, const int32_t *slots
     sp.cu = cu_accept; sp.T_total = A_total; sp.seq_len_fixed = 0; sp.chunk_skip = 0;
     sp.state_in = state_pool; sp.state_out = state_pool; sp.chunk_state = nullptr;
     sp.slots = slots; sp.num_slots = num_slots; sp.status = static_cast<uint32_t *>(workspace);
+    sp.prep = static_cast<int>(prep & ~static_cast<uint32_t>(KDA_PREP_L2NORM_Q)); sp.prep_eps = l2_eps;  // no q in replay
     if (kda::launch_seq(sp, dk, dv, static_cast<int>(dtype), s) != cudaSuccess) return KDA_ERR_CUDA;
     return KDA_OK;
+}
+
+kda_status kda_replay(float *state_pool, int64_t num_slots, const int32_t *slots, const void *k,
+                      const void *v, const void *g, const void *beta, kda_dtype dtype,
+                      const int32_t *cu_accept, int N, int64_t A_total, int H, int dk, int dv,
+                      void *workspace, size_t ws_bytes, void *stream) {
+    return kda_replay_prep(state_pool, num_slots, slots, k, v, g, beta, dtype, cu_accept, N, A_total, H, dk, dv, 0u,
+                           0.f, workspace, ws_bytes, stream);
 }
 
 kda_status kda_device_status(const void *workspace, void *stream) {

@@ -37,6 +37,8 @@
 #include <cudaTypedefs.h>
 #include <stdint.h>
 
+#include <type_traits>
+
 #include "kda_internal.h"
 #include "sm100_ptx.cuh"
 
@@ -79,6 +81,8 @@ struct TcParams {
     float *phi, *psi;             // per pair: segment-1 transition and zero-start state
     __nv_bfloat16 *o_phi;         // [T, H, 128]: segment-1 outputs of the transition run
     int split;
+    int prep;                     // input preprocessing flags (PREP_*)
+    float prep_eps;               // epsilon of the L2 normalisation
     int64_t T_total, seq_len_fixed;
     int N, H;
     float scale;
@@ -107,6 +111,21 @@ __device__ __forceinline__ void mma_tf32(float (&c)[4], float a0, float a1, floa
         : "r"(__float_as_uint(a0)), "r"(__float_as_uint(a1)), "r"(__float_as_uint(a2)), "r"(__float_as_uint(a3)),
           "r"(__float_as_uint(b0)), "r"(__float_as_uint(b1)));
 }
+// Four 8x8 bf16 tiles from shared memory (lanes 8i .. 8i+7 give the row addresses of tile i).
+__device__ __forceinline__ void ldmatrix_x4(uint32_t (&r)[4], uint32_t addr) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr)
+                 : "memory");
+}
+// One m16n8k16 bf16 tile product c += a b, fp32 accumulation.
+__device__ __forceinline__ void mma_bf16_16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
 
 // Packed fp32 pairs: two floats in one 64-bit register pair, multiplied with one
 // f32x2 instruction (the decay and state-scaling loops are issue-bound).
@@ -123,6 +142,11 @@ __device__ __forceinline__ float2 uf2(uint64_t v) {
 __device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
     uint64_t d;
     asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
     return d;
 }
 // bf16x2 word -> fp32 pair (exact)
@@ -192,6 +216,9 @@ __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, const 
     return __shfl_sync(0xffffffffu, ok, 0) != 0;
 }
 
+// kPrep: the instance that applies the input preprocessing of p.prep (the other
+// instance carries none of its code).
+template <bool kPrep>
 __global__ void __launch_bounds__(kThreads, 1) kda_chunk_tc_kernel(const __grid_constant__ TcParams p) {
     extern __shared__ uint8_t dsmem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(dsmem_raw) + 1023) & ~uintptr_t(1023));
@@ -199,7 +226,8 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_tc_kernel(const __grid_
     __shared__ __align__(16) float s_ac[3][kD];  // per-chunk A_C, ring of three
     __shared__ __align__(16) float s_x[32 * kLdX];
     __shared__ __align__(16) float s_tot[8][kD];
-    __shared__ uint64_t bar_full[2], bar_free[2];
+    __shared__ float s_rn[2][2][kC];  // per stage: inverse L2 norms of the k and q rows (preprocessing)
+    __shared__ uint64_t bar_full[2], bar_free[2], bar_norm[2];
     __shared__ uint64_t bar_elem, bar_mma1, bar_mfree, bar_tready, bar_mma2, bar_ready, bar_wfree, bar_c1, bar_uready,
         bar_c3;
     __shared__ uint64_t bar_drain[2];
@@ -250,6 +278,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_tc_kernel(const __grid_
         for (int s = 0; s < 2; ++s) {
             mbar_init(&bar_full[s], 2);
             mbar_init(&bar_free[s], 1);
+            mbar_init(&bar_norm[s], 32);
         }
         mbar_init(&bar_elem, 1);
         mbar_init(&bar_mma1, 1);
@@ -301,8 +330,14 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_tc_kernel(const __grid_
                 const int s = c & 1;
                 const int t0 = static_cast<int>(bos + static_cast<int64_t>(c) * kC);
                 // beta for this chunk: loaded before waiting for the stage, so its latency overlaps the wait
-                const float b_lo = __bfloat162float(p.beta[(static_cast<int64_t>(t0) + lane) * H + h]);
-                const float b_hi = __bfloat162float(p.beta[(static_cast<int64_t>(t0) + lane + 32) * H + h]);
+                float b_lo = __bfloat162float(p.beta[(static_cast<int64_t>(t0) + lane) * H + h]);
+                float b_hi = __bfloat162float(p.beta[(static_cast<int64_t>(t0) + lane + 32) * H + h]);
+                if constexpr (kPrep) {
+                    if (p.prep & PREP_SIGMOID_BETA) {  // beta = sigmoid(x_beta)
+                        b_lo = 1.f / (1.f + __expf(-b_lo));
+                        b_hi = 1.f / (1.f + __expf(-b_hi));
+                    }
+                }
                 if (c >= 2 && !warp_wait(&bar_free[s], ((c >> 1) - 1) & 1, ctl, lane)) break;
                 uint8_t *st = sm + s * kStage;
                 if (lane == 0) {
@@ -445,6 +480,58 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_tc_kernel(const __grid_
                 mma_commit(&bar_drain[1]);
                 const uint64_t dl = globaltimer_ns() + kWaitNs;
                 while (!mbar_try_wait(&bar_drain[1], 0) && globaltimer_ns() < dl) {
+                }
+            }
+        } else if (warp == 3) {
+            // ------------------------------------------------------------------ row norms (preprocessing)
+            // Squared L2 norms of the chunk's 64 k rows and 64 q rows, taken as the diagonal of
+            // K K^T (and Q Q^T) with m16n8k16 tensor-core tiles: one 16-row block x one 16-column
+            // slice loaded by ldmatrix is both the A operand and, for each half of the block, the
+            // B operand.  The inverse norms go to s_rn before the decay group's second pass,
+            // which overwrites k and q.
+            if constexpr (kPrep) {
+                if (p.prep & (PREP_L2NORM_K | PREP_L2NORM_Q)) {
+                    const int g8 = lane >> 2, t4 = lane & 3;
+                    const bool diag_lane = t4 == (g8 >> 1);
+                    for (int c = 0; c < nfull; ++c) {
+                        const int s = c & 1;
+                        if (!warp_wait(&bar_full[s], (c >> 1) & 1, ctl, lane)) break;
+                        const uint32_t st = sm_base + s * kStage;
+#pragma unroll
+                        for (int tq = 0; tq < 2; ++tq) {  // 0 = k rows, 1 = q rows
+                            const bool on = (p.prep & (tq == 0 ? PREP_L2NORM_K : PREP_L2NORM_Q)) != 0;
+#pragma unroll
+                            for (int bp = 0; bp < 64; bp += 32) {  // two 16-row blocks at a time
+                                float c0[2][4] = {}, c1[2][4] = {};
+#pragma unroll
+                                for (int kb = 0; kb < 2; ++kb) {
+                                    const uint32_t base = st + OFF_R + kb * 16384 + tq * 8192;
+#pragma unroll
+                                    for (int ks = 0; ks < 4; ++ks) {
+#pragma unroll
+                                        for (int b = 0; b < 2; ++b) {
+                                            const int row = bp + 16 * b + (lane & 7) + ((lane >> 3) & 1) * 8;
+                                            uint32_t a[4];
+                                            ldmatrix_x4(a, base + chunk16(row, 2 * ks + (lane >> 4)));
+                                            mma_bf16_16816(c0[b], a, a[0], a[2]);  // block x its rows 0-7
+                                            mma_bf16_16816(c1[b], a, a[1], a[3]);  // block x its rows 8-15
+                                        }
+                                    }
+                                }
+                                if (diag_lane) {
+#pragma unroll
+                                    for (int b = 0; b < 2; ++b) {
+                                        const float lo = (g8 & 1) ? c0[b][1] : c0[b][0];  // row g8 of the block
+                                        const float hi = (g8 & 1) ? c1[b][3] : c1[b][2];  // row g8 + 8
+                                        const int r = bp + 16 * b + g8;
+                                        s_rn[s][tq][r] = on ? rsqrtf(lo + p.prep_eps) : 1.f;
+                                        s_rn[s][tq][r + 8] = on ? rsqrtf(hi + p.prep_eps) : 1.f;
+                                    }
+                                }
+                            }
+                        }
+                        mbar_arrive(&bar_norm[s]);  // every lane (count 32): its reads and writes are done
+                    }
                 }
             }
         }
@@ -645,26 +732,54 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_tc_kernel(const __grid_
                 const int r0 = 8 * seg;
                 uint64_t A01[8], A23[8];
                 uint64_t P01 = f2(1.f, 1.f), P23 = f2(1.f, 1.f);
-                const uint64_t L2E = f2(1.4426950408889634f, 1.4426950408889634f);
+                // Pass 1: running products along the segment.  alpha = exp(g) = 2^(g log2 e),
+                // A_r = alpha_1 ... alpha_r.  With the sigmoid gate (preprocessing) alpha =
+                // 1 / (1 + 2^(-x log2 e)) and the running product is that of the denominators,
+                // D_r = 1 / A_r, so no reciprocal is taken per element here.
+                auto pass1 = [&](auto sig) {
+                    constexpr bool kSig = decltype(sig)::value;
+                    const float l2e = kSig ? -1.4426950408889634f : 1.4426950408889634f;
+                    const uint64_t L2E = f2(l2e, l2e);
 #pragma unroll
-                for (int rr = 0; rr < 8; rr += 4) {
-                    uint2 gw[4];
+                    for (int rr = 0; rr < 8; rr += 4) {
+                        uint2 gw[4];
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) gw[e] = *reinterpret_cast<const uint2 *>(G + swz(r0 + rr + e, cc));
+                        for (int e = 0; e < 4; ++e) gw[e] = *reinterpret_cast<const uint2 *>(G + swz(r0 + rr + e, cc));
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const float2 l01 = uf2(mul2(bf2x(gw[e].x), L2E)), l23 = uf2(mul2(bf2x(gw[e].y), L2E));
-                        P01 = mul2(P01, f2(ex2_approx(l01.x), ex2_approx(l01.y)));
-                        P23 = mul2(P23, f2(ex2_approx(l23.x), ex2_approx(l23.y)));
-                        A01[rr + e] = P01;
-                        A23[rr + e] = P23;
+                        for (int e = 0; e < 4; ++e) {
+                            const float2 l01 = uf2(mul2(bf2x(gw[e].x), L2E)), l23 = uf2(mul2(bf2x(gw[e].y), L2E));
+                            const uint64_t e01 = f2(ex2_approx(l01.x), ex2_approx(l01.y));
+                            const uint64_t e23 = f2(ex2_approx(l23.x), ex2_approx(l23.y));
+                            if constexpr (kSig) {
+                                P01 = fma2(P01, e01, P01);  // D *= 1 + e
+                                P23 = fma2(P23, e23, P23);
+                            } else {
+                                P01 = mul2(P01, e01);
+                                P23 = mul2(P23, e23);
+                            }
+                            A01[rr + e] = P01;
+                            A23[rr + e] = P23;
+                        }
                     }
+                };
+                bool sig_gate = false, norms = false;
+                if constexpr (kPrep) {
+                    sig_gate = (p.prep & PREP_SIGMOID_GATE) != 0;
+                    norms = (p.prep & (PREP_L2NORM_K | PREP_L2NORM_Q)) != 0;
                 }
+                if (sig_gate)
+                    pass1(std::true_type{});
+                else
+                    pass1(std::false_type{});
                 const float2 pp01 = uf2(P01), pp23 = uf2(P23);
                 const float p0 = pp01.x, p1 = pp01.y, p2 = pp23.x, p3 = pp23.y;
                 st4(&s_tot[seg][ch], make_float4(p0, p1, p2, p3));
-                named_bar(1, 256);
-                float4 m = make_float4(1.f, 1.f, 1.f, 1.f);
+                if (norms) {  // the row norms come from the norm warp (it reads k and q before pass 2 rewrites them)
+                    if (!group_wait(&bar_norm[s], (c >> 1) & 1, ctl, &s_grp_fail[0], 1, 256, gseq)) break;
+                } else {
+                    named_bar(1, 256);
+                }
+                float4 m = make_float4(1.f, 1.f, 1.f, 1.f);  // product of the earlier segments' totals
                 for (int q = 0; q < seg; ++q) {
                     const float4 t = ld4(&s_tot[q][ch]);
                     m = make_float4(m.x * t.x, m.y * t.y, m.z * t.z, m.w * t.w);
@@ -672,32 +787,78 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_tc_kernel(const __grid_
                 const float sc = p.scale;
                 const uint64_t m01 = f2(m.x, m.y), m23 = f2(m.z, m.w);
                 const uint64_t ms01 = f2(m.x * sc, m.y * sc), ms23 = f2(m.z * sc, m.w * sc);
+                const uint64_t SC2 = f2(sc, sc);
+                // Pass 2: Kbar = k A, Qbar = scale q A, Ktil = k / A over k, q, g in place; with
+                // L2-normalised rows (preprocessing) k and q are first scaled by their rows'
+                // inverse norms
+                auto pass2 = [&](auto norm, auto sig) {
+                    constexpr bool kNorm = decltype(norm)::value;
+                    constexpr bool kSig = decltype(sig)::value;
 #pragma unroll
-                for (int rr = 0; rr < 8; rr += 2) {
-                    uint2 kw[2], qw[2];
+                    for (int rr = 0; rr < 8; rr += 2) {
+                        uint2 kw[2], qw[2];
 #pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const uint32_t off = swz(r0 + rr + e, cc);
-                        kw[e] = *reinterpret_cast<const uint2 *>(Rk + off);
-                        qw[e] = *reinterpret_cast<const uint2 *>(Rq + off);
+                        for (int e = 0; e < 2; ++e) {
+                            const uint32_t off = swz(r0 + rr + e, cc);
+                            kw[e] = *reinterpret_cast<const uint2 *>(Rk + off);
+                            qw[e] = *reinterpret_cast<const uint2 *>(Rq + off);
+                        }
+#pragma unroll
+                        for (int e = 0; e < 2; ++e) {
+                            const uint32_t off = swz(r0 + rr + e, cc);
+                            uint64_t a01, a23, aq01, aq23, r01, r23;
+                            if constexpr (kSig) {  // the products are D = 1 / A
+                                r01 = mul2(m01, A01[rr + e]);
+                                r23 = mul2(m23, A23[rr + e]);
+                                const float2 fr01 = uf2(r01), fr23 = uf2(r23);
+                                a01 = f2(rcp_approx(fr01.x), rcp_approx(fr01.y));
+                                a23 = f2(rcp_approx(fr23.x), rcp_approx(fr23.y));
+                                aq01 = mul2(a01, SC2);
+                                aq23 = mul2(a23, SC2);
+                            } else {
+                                a01 = mul2(m01, A01[rr + e]);
+                                a23 = mul2(m23, A23[rr + e]);
+                                aq01 = mul2(ms01, A01[rr + e]);
+                                aq23 = mul2(ms23, A23[rr + e]);
+                                const float2 fa01 = uf2(a01), fa23 = uf2(a23);
+                                r01 = f2(rcp_approx(fa01.x), rcp_approx(fa01.y));
+                                r23 = f2(rcp_approx(fa23.x), rcp_approx(fa23.y));
+                            }
+                            uint64_t k01 = bf2x(kw[e].x), k23 = bf2x(kw[e].y);
+                            uint64_t q01 = bf2x(qw[e].x), q23 = bf2x(qw[e].y);
+                            if constexpr (kNorm) {
+                                const float rk = s_rn[s][0][r0 + rr + e], rq = s_rn[s][1][r0 + rr + e];
+                                const uint64_t RK = f2(rk, rk), RQ = f2(rq, rq);
+                                k01 = mul2(k01, RK);
+                                k23 = mul2(k23, RK);
+                                q01 = mul2(q01, RQ);
+                                q23 = mul2(q23, RQ);
+                            }
+                            *reinterpret_cast<uint2 *>(Rk + off) = make_uint2(pk2(mul2(k01, a01)), pk2(mul2(k23, a23)));
+                            *reinterpret_cast<uint2 *>(Rq + off) = make_uint2(pk2(mul2(q01, aq01)), pk2(mul2(q23, aq23)));
+                            *reinterpret_cast<uint2 *>(G + off) = make_uint2(pk2(mul2(k01, r01)), pk2(mul2(k23, r23)));
+                        }
                     }
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const uint32_t off = swz(r0 + rr + e, cc);
-                        const uint64_t a01 = mul2(m01, A01[rr + e]), a23 = mul2(m23, A23[rr + e]);
-                        const uint64_t aq01 = mul2(ms01, A01[rr + e]), aq23 = mul2(ms23, A23[rr + e]);
-                        const uint64_t k01 = bf2x(kw[e].x), k23 = bf2x(kw[e].y);
-                        const float2 fa01 = uf2(a01), fa23 = uf2(a23);
-                        const uint64_t r01 = f2(rcp_approx(fa01.x), rcp_approx(fa01.y));
-                        const uint64_t r23 = f2(rcp_approx(fa23.x), rcp_approx(fa23.y));
-                        *reinterpret_cast<uint2 *>(Rk + off) = make_uint2(pk2(mul2(k01, a01)), pk2(mul2(k23, a23)));
-                        *reinterpret_cast<uint2 *>(Rq + off) =
-                            make_uint2(pk2(mul2(bf2x(qw[e].x), aq01)), pk2(mul2(bf2x(qw[e].y), aq23)));
-                        *reinterpret_cast<uint2 *>(G + off) = make_uint2(pk2(mul2(k01, r01)), pk2(mul2(k23, r23)));
+                };
+                float4 ac;  // A_C of the chunk (segment 7 holds the last products)
+                if constexpr (kPrep) {
+                    if (norms) {
+                        if (sig_gate) pass2(std::true_type{}, std::true_type{});
+                        else pass2(std::true_type{}, std::false_type{});
+                    } else {
+                        if (sig_gate) pass2(std::false_type{}, std::true_type{});
+                        else pass2(std::false_type{}, std::false_type{});
                     }
+                    if (sig_gate)
+                        ac = make_float4(rcp_approx(m.x * p0), rcp_approx(m.y * p1), rcp_approx(m.z * p2),
+                                         rcp_approx(m.w * p3));
+                    else
+                        ac = make_float4(m.x * p0, m.y * p1, m.z * p2, m.w * p3);
+                } else {
+                    pass2(std::false_type{}, std::false_type{});
+                    ac = make_float4(m.x * p0, m.y * p1, m.z * p2, m.w * p3);
                 }
                 if (seg == 7) {
-                    const float4 ac = make_float4(m.x * p0, m.y * p1, m.z * p2, m.w * p3);
                     if (!(ac.x >= kMinDecay) || !(ac.y >= kMinDecay) || !(ac.z >= kMinDecay) || !(ac.w >= kMinDecay))
                         atomicOr(p.status, DEV_ERR_GATE);
                     st4(&s_ac[c % 3][ch], ac);
@@ -984,20 +1145,27 @@ cudaError_t launch_chunk_tc(const ChunkParams &cp, cudaStream_t stream) {
     p.H = cp.H;
     p.scale = cp.scale;
     p.split = cp.split;
+    p.prep = cp.prep;
+    p.prep_eps = cp.prep_eps;
     p.phi = cp.phi;
     p.psi = cp.psi;
     p.o_phi = static_cast<__nv_bfloat16 *>(cp.o_phi);
     static bool attr_set = false;
     if (!attr_set) {
-        cudaFuncAttributes fa{};
-        if (cudaFuncGetAttributes(&fa, kda_chunk_tc_kernel) != cudaSuccess || fa.numRegs != 96)
-            return cudaErrorInvalidConfiguration;  // the register split assumes 96 per thread at launch
-        cudaError_t e = cudaFuncSetAttribute(kda_chunk_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(kDynSmem));
-        if (e != cudaSuccess) return e;
+        for (auto fn : {kda_chunk_tc_kernel<false>, kda_chunk_tc_kernel<true>}) {
+            cudaFuncAttributes fa{};
+            if (cudaFuncGetAttributes(&fa, fn) != cudaSuccess || fa.numRegs != 96)
+                return cudaErrorInvalidConfiguration;  // the register split assumes 96 per thread at launch
+            cudaError_t e =
+                cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kDynSmem));
+            if (e != cudaSuccess) return e;
+        }
         attr_set = true;
     }
-    kda_chunk_tc_kernel<<<static_cast<unsigned>(blocks), kThreads, kDynSmem, stream>>>(p);
+    if (p.prep)
+        kda_chunk_tc_kernel<true><<<static_cast<unsigned>(blocks), kThreads, kDynSmem, stream>>>(p);
+    else
+        kda_chunk_tc_kernel<false><<<static_cast<unsigned>(blocks), kThreads, kDynSmem, stream>>>(p);
     return cudaGetLastError();
 }
 

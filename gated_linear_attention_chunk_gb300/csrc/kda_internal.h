@@ -21,6 +21,9 @@ enum SeqMode : int {
 };
 
 // Arguments of the token-sequential kernel.  One CTA per (sequence, head).
+// Input preprocessing flags (the same values as KDA_PREP_* in kda.h).
+constexpr int PREP_L2NORM_Q = 1, PREP_L2NORM_K = 2, PREP_SIGMOID_GATE = 4, PREP_SIGMOID_BETA = 8;
+
 struct SeqParams {
     const void *q, *k, *v, *g, *beta;
     void *o;                    // may be null (replay)
@@ -37,6 +40,8 @@ struct SeqParams {
     const int32_t *slots;       // decode/replay: slot map or null
     int64_t num_slots;
     uint32_t *status;           // device status word
+    int prep;                   // input preprocessing flags (PREP_*), 0 = inputs used as given
+    float prep_eps;             // epsilon of the L2 normalisation
 };
 
 // T-segment merge after a split chunked launch (kda_merge.cu): o on segment-1 tokens
@@ -74,6 +79,8 @@ struct ChunkParams {
     int split;
     float *phi, *psi;
     void *o_phi;
+    int prep;                   // input preprocessing flags (PREP_*)
+    float prep_eps;
 };
 
 // True when the chunked tensor-core kernel is compiled in and supports the shape.

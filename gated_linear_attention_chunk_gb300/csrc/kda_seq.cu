@@ -101,7 +101,9 @@ __device__ __forceinline__ float4 f4_shfl_xor(float4 a, int m) {
                        __shfl_xor_sync(0xffffffffu, a.z, m), __shfl_xor_sync(0xffffffffu, a.w, m));
 }
 
-template <int DK, int DV, typename Tin, bool WRITE_O>
+// PREP: the instance that applies the input preprocessing of p.prep (the other one
+// carries none of its code).
+template <int DK, int DV, typename Tin, bool WRITE_O, bool PREP>
 __global__ void __launch_bounds__(kSeqThreads, 6) kda_seq_kernel(SeqParams p) {
     constexpr int CB = kColBlock;         // columns of this CTA
     constexpr int NCB = DV / CB;          // column blocks per state
@@ -116,6 +118,7 @@ __global__ void __launch_bounds__(kSeqThreads, 6) kda_seq_kernel(SeqParams p) {
     __shared__ float tok_b[3];
     __shared__ float4 red_y[2][kSeqWarps][LPR], red_z[2][kSeqWarps][LPR];
     __shared__ float red_qk[2][kSeqWarps];
+    __shared__ float red_nk[3][kSeqWarps], red_nq[3][kSeqWarps];  // per-warp sums of k^2, q^2 of a staged token
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int cg = lane % LPR, rsub = lane / LPR;
@@ -193,14 +196,42 @@ __global__ void __launch_bounds__(kSeqThreads, 6) kda_seq_kernel(SeqParams p) {
         if (tid < CB) rv = ld_in(V, (t * H + h) * DV + col0 + tid);
         if (tid == kSeqThreads - 1) rb = ld_in(B, t * H + h);
     };
+    // Optional preprocessing (p.prep): alpha = sigmoid(x_g) instead of exp(g), beta =
+    // sigmoid(x_beta), and k / q rows divided by sqrt(sum of squares + eps); the row sums
+    // are reduced here per warp (a xor butterfly gives every lane the same bits) and the
+    // inverse norms are applied where k and q are read.
     auto stage = [&](int buf, float rg, float rk, float rq, float rv, float rb) {
         if (tid < DK) {
-            tok_a[buf][tid] = expf(rg);
+            tok_a[buf][tid] = (PREP && (p.prep & PREP_SIGMOID_GATE)) ? __fdiv_rn(1.f, __fadd_rn(1.f, expf(-rg)))
+                                                                       : expf(rg);
             tok_k[buf][tid] = rk;
             if (WRITE_O) tok_q[buf][tid] = __fmul_rn(rq, p.scale);
         }
         if (tid < CB) tok_v[buf][tid] = rv;
-        if (tid == kSeqThreads - 1) tok_b[buf] = rb;
+        if (tid == kSeqThreads - 1)
+            tok_b[buf] = (PREP && (p.prep & PREP_SIGMOID_BETA)) ? __fdiv_rn(1.f, __fadd_rn(1.f, expf(-rb))) : rb;
+        if constexpr (PREP) {
+            if (p.prep & (PREP_L2NORM_K | PREP_L2NORM_Q)) {
+                float sk = __fmul_rn(rk, rk), sq = __fmul_rn(rq, rq);  // 0 beyond dk
+#pragma unroll
+                for (int m = 16; m >= 1; m >>= 1) {
+                    sk = __fadd_rn(sk, __shfl_xor_sync(0xffffffffu, sk, m));
+                    sq = __fadd_rn(sq, __shfl_xor_sync(0xffffffffu, sq, m));
+                }
+                if (lane == 0) {
+                    red_nk[buf][warp] = sk;
+                    red_nq[buf][warp] = sq;
+                }
+            }
+        }
+    };
+    // inverse L2 norm of a staged row from the warps' partial sums (warps in order), or 1
+    auto inv_norm = [&](const float (&part)[kSeqWarps], int flag) {
+        if (!PREP || !(p.prep & flag)) return 1.f;
+        float t = part[0];
+#pragma unroll
+        for (int w = 1; w < kSeqWarps; ++w) t = __fadd_rn(t, part[w]);
+        return __frsqrt_rn(__fadd_rn(t, p.prep_eps));
     };
 
     // Warm L2 with the next three tokens' rows (fire and forget): in a multi-token call
@@ -231,16 +262,18 @@ __global__ void __launch_bounds__(kSeqThreads, 6) kda_seq_kernel(SeqParams p) {
         if (has_next) load_raw(t + 1, ng, nk, nq, nv, nb);
 
         // decay, then partial reductions over this thread's rows (rows in order)
+        const float kn = inv_norm(red_nk[b], PREP_L2NORM_K);
+        const float qn = WRITE_O ? inv_norm(red_nq[b], PREP_L2NORM_Q) : 1.f;
         float4 py = make_float4(0.f, 0.f, 0.f, 0.f), pz = py;
         float pqk = 0.f;
 #pragma unroll
         for (int s = 0; s < NS; ++s) {
             const int row = s * RPS + row0;
-            const float a = tok_a[b][row], kk = tok_k[b][row];
+            const float a = tok_a[b][row], kk = PREP ? __fmul_rn(tok_k[b][row], kn) : tok_k[b][row];
             S[s] = f4_scale(S[s], a);
             py = f4_fma(kk, S[s], py);
             if (WRITE_O) {
-                const float qq = tok_q[b][row];
+                const float qq = PREP ? __fmul_rn(tok_q[b][row], qn) : tok_q[b][row];
                 pz = f4_fma(qq, S[s], pz);
                 pqk = __fmaf_rn(qq, kk, pqk);
             }
@@ -272,7 +305,10 @@ __global__ void __launch_bounds__(kSeqThreads, 6) kda_seq_kernel(SeqParams p) {
         const float4 u = make_float4(__fmul_rn(bt, __fsub_rn(vv.x, y.x)), __fmul_rn(bt, __fsub_rn(vv.y, y.y)),
                                      __fmul_rn(bt, __fsub_rn(vv.z, y.z)), __fmul_rn(bt, __fsub_rn(vv.w, y.w)));
 #pragma unroll
-        for (int s = 0; s < NS; ++s) S[s] = f4_fma(tok_k[b][s * RPS + row0], u, S[s]);
+        for (int s = 0; s < NS; ++s) {
+            const float kk = tok_k[b][s * RPS + row0];
+            S[s] = f4_fma(PREP ? __fmul_rn(kk, kn) : kk, u, S[s]);
+        }
 
         if (WRITE_O && warp == 0 && rsub == 0) {
             float4 z = red_z[r][0][cg];
@@ -301,10 +337,18 @@ cudaError_t launch_typed(const SeqParams &p, cudaStream_t stream) {
     const int64_t blocks = static_cast<int64_t>(p.N) * p.H * (DV / kColBlock);
     if (blocks <= 0) return cudaSuccess;
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    if (p.o)
-        kda_seq_kernel<DK, DV, Tin, true><<<static_cast<unsigned>(blocks), kSeqThreads, 0, stream>>>(p);
-    else
-        kda_seq_kernel<DK, DV, Tin, false><<<static_cast<unsigned>(blocks), kSeqThreads, 0, stream>>>(p);
+    const dim3 grid(static_cast<unsigned>(blocks));
+    if (p.o) {
+        if (p.prep)
+            kda_seq_kernel<DK, DV, Tin, true, true><<<grid, kSeqThreads, 0, stream>>>(p);
+        else
+            kda_seq_kernel<DK, DV, Tin, true, false><<<grid, kSeqThreads, 0, stream>>>(p);
+    } else {
+        if (p.prep)
+            kda_seq_kernel<DK, DV, Tin, false, true><<<grid, kSeqThreads, 0, stream>>>(p);
+        else
+            kda_seq_kernel<DK, DV, Tin, false, false><<<grid, kSeqThreads, 0, stream>>>(p);
+    }
     return cudaGetLastError();
 }
 

@@ -32,6 +32,10 @@ KDA_ERR_BAD_SLOT = 8
 KDA_BF16 = 0
 KDA_F32 = 1
 KDA_WS_HEADER_BYTES = 256
+KDA_PREP_L2NORM_Q = 1
+KDA_PREP_L2NORM_K = 2
+KDA_PREP_SIGMOID_GATE = 4
+KDA_PREP_SIGMOID_BETA = 8
 
 _vp = ctypes.c_void_p
 _i64 = ctypes.c_int64
@@ -44,6 +48,14 @@ _SIGS = {
                                ctypes.c_float, _vp, _vp, ctypes.c_size_t, _vp]),
     "kda_replay": (_int, [_vp, _i64, _vp, _vp, _vp, _vp, _vp, _int, _vp, _int, _i64, _int, _int, _int,
                           _vp, ctypes.c_size_t, _vp]),
+    "kda_chunk_fwd_prep": (_int, [_vp, _vp, _vp, _vp, _vp, _int, _vp, _vp, _int, _i64, _int, _int, _int,
+                                  ctypes.c_float, ctypes.c_uint32, ctypes.c_float, _vp, _vp, _vp, ctypes.c_size_t,
+                                  _vp]),
+    "kda_decode_step_prep": (_int, [_vp, _vp, _vp, _vp, _vp, _int, _vp, _i64, _vp, _int, _int, _int, _int,
+                                    ctypes.c_float, ctypes.c_uint32, ctypes.c_float, _vp, _vp, ctypes.c_size_t,
+                                    _vp]),
+    "kda_replay_prep": (_int, [_vp, _i64, _vp, _vp, _vp, _vp, _vp, _int, _vp, _int, _i64, _int, _int, _int,
+                               ctypes.c_uint32, ctypes.c_float, _vp, ctypes.c_size_t, _vp]),
     "kda_device_status": (_int, [_vp, _vp]),
     "kda_status_string": (ctypes.c_char_p, [_int]),
     "kda_version": (_int, []),
@@ -154,6 +166,22 @@ def kda_chunk_fwd(q, k, v, g, beta, cu_seqlens=None, init_state=None, scale: flo
     init_state [N, H, dk, dv] fp32 or None.  ``final_state`` may be passed (and
     may be ``init_state`` itself for an in-place update).
     """
+    return _chunk_fwd(q, k, v, g, beta, cu_seqlens, init_state, scale, output_final_state, o, final_state,
+                      workspace, stream, None, 0.0)
+
+
+def kda_chunk_fwd_prep(q, k, v, g, beta, prep: int, l2_eps: float = 1e-6, cu_seqlens=None, init_state=None,
+                       scale: float = 1.0, output_final_state: bool = True, o=None, final_state=None,
+                       workspace=None, stream=None) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
+    """kda_chunk_fwd on raw inputs: ``prep`` is a set of KDA_PREP_* flags (L2-normalised
+    q / k rows with ``l2_eps``, g as raw gates with alpha = sigmoid(g), beta <- sigmoid(beta)),
+    applied inside the kernels."""
+    return _chunk_fwd(q, k, v, g, beta, cu_seqlens, init_state, scale, output_final_state, o, final_state,
+                      workspace, stream, int(prep), float(l2_eps))
+
+
+def _chunk_fwd(q, k, v, g, beta, cu_seqlens, init_state, scale, output_final_state, o, final_state, workspace,
+               stream, prep, l2_eps):
     lib = load_library()
     dt = q.dtype
     T, H, dk = q.shape
@@ -178,11 +206,14 @@ def kda_chunk_fwd(q, k, v, g, beta, cu_seqlens=None, init_state=None, scale: flo
     need = kda_chunk_fwd_workspace_size(N, T, H, dk, dv)  # the size that enables every path
     if workspace is None:
         workspace = new_workspace(need, q.device)
-    rc = lib.kda_chunk_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _dtype_code(q), _ptr(init_state),
-                           _ptr(cu_seqlens), N, T, H, dk, dv, float(scale), _ptr(o), _ptr(final_state),
-                           _ptr(workspace), workspace.numel() * workspace.element_size(),
-                           _stream_handle(stream))
-    _check(rc, "kda_chunk_fwd")
+    common = (_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _dtype_code(q), _ptr(init_state),
+              _ptr(cu_seqlens), N, T, H, dk, dv, float(scale))
+    tail = (_ptr(o), _ptr(final_state), _ptr(workspace), workspace.numel() * workspace.element_size(),
+            _stream_handle(stream))
+    if prep is None:
+        _check(lib.kda_chunk_fwd(*common, *tail), "kda_chunk_fwd")
+    else:
+        _check(lib.kda_chunk_fwd_prep(*common, prep, l2_eps, *tail), "kda_chunk_fwd_prep")
     return o, final_state
 
 
@@ -217,6 +248,17 @@ def kda_chunk_fwd_noalloc(q, k, v, g, beta, o, cu_seqlens=None, init_state=None,
 def kda_decode_step(q, k, v, g, beta, state_pool, slots=None, scale: float = 1.0, o=None, workspace=None,
                     stream=None) -> torch.Tensor:
     """One token per sequence; updates ``state_pool`` [S, H, dk, dv] in place.  Returns o [N, H, dv]."""
+    return _decode_step(q, k, v, g, beta, state_pool, slots, scale, o, workspace, stream, None, 0.0)
+
+
+def kda_decode_step_prep(q, k, v, g, beta, state_pool, prep: int, l2_eps: float = 1e-6, slots=None,
+                         scale: float = 1.0, o=None, workspace=None, stream=None) -> torch.Tensor:
+    """kda_decode_step on raw inputs (KDA_PREP_* flags, see kda_chunk_fwd_prep)."""
+    return _decode_step(q, k, v, g, beta, state_pool, slots, scale, o, workspace, stream, int(prep),
+                        float(l2_eps))
+
+
+def _decode_step(q, k, v, g, beta, state_pool, slots, scale, o, workspace, stream, prep, l2_eps):
     lib = load_library()
     dt = q.dtype
     N, H, dk = q.shape
@@ -234,16 +276,28 @@ def kda_decode_step(q, k, v, g, beta, state_pool, slots=None, scale: float = 1.0
     _need(o, "o", dt, (N, H, dv))
     if workspace is None:
         workspace = new_workspace(KDA_WS_HEADER_BYTES, q.device)
-    rc = lib.kda_decode_step(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _dtype_code(q), _ptr(state_pool),
-                             state_pool.shape[0], _ptr(slots), N, H, dk, dv, float(scale), _ptr(o),
-                             _ptr(workspace), workspace.numel() * workspace.element_size(),
-                             _stream_handle(stream))
-    _check(rc, "kda_decode_step")
+    common = (_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _dtype_code(q), _ptr(state_pool),
+              state_pool.shape[0], _ptr(slots), N, H, dk, dv, float(scale))
+    tail = (_ptr(o), _ptr(workspace), workspace.numel() * workspace.element_size(), _stream_handle(stream))
+    if prep is None:
+        _check(lib.kda_decode_step(*common, *tail), "kda_decode_step")
+    else:
+        _check(lib.kda_decode_step_prep(*common, prep, l2_eps, *tail), "kda_decode_step_prep")
     return o
 
 
 def kda_replay(state_pool, k, v, g, beta, cu_accept, slots=None, workspace=None, stream=None) -> None:
     """Apply accepted tokens [A, H, .] to the pool states in place (cu_accept [N+1] int32)."""
+    _replay(state_pool, k, v, g, beta, cu_accept, slots, workspace, stream, None, 0.0)
+
+
+def kda_replay_prep(state_pool, k, v, g, beta, cu_accept, prep: int, l2_eps: float = 1e-6, slots=None,
+                    workspace=None, stream=None) -> None:
+    """kda_replay on raw inputs (KDA_PREP_* flags; KDA_PREP_L2NORM_Q has no effect)."""
+    _replay(state_pool, k, v, g, beta, cu_accept, slots, workspace, stream, int(prep), float(l2_eps))
+
+
+def _replay(state_pool, k, v, g, beta, cu_accept, slots, workspace, stream, prep, l2_eps):
     lib = load_library()
     dt = k.dtype
     A, H, dk = k.shape
@@ -260,10 +314,13 @@ def kda_replay(state_pool, k, v, g, beta, cu_accept, slots=None, workspace=None,
         _need(slots, "slots", torch.int32, (N,))
     if workspace is None:
         workspace = new_workspace(KDA_WS_HEADER_BYTES, k.device)
-    rc = lib.kda_replay(_ptr(state_pool), state_pool.shape[0], _ptr(slots), _ptr(k), _ptr(v), _ptr(g),
-                        _ptr(beta), _dtype_code(k), _ptr(cu_accept), N, A, H, dk, dv, _ptr(workspace),
-                        workspace.numel() * workspace.element_size(), _stream_handle(stream))
-    _check(rc, "kda_replay")
+    common = (_ptr(state_pool), state_pool.shape[0], _ptr(slots), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+              _dtype_code(k), _ptr(cu_accept), N, A, H, dk, dv)
+    tail = (_ptr(workspace), workspace.numel() * workspace.element_size(), _stream_handle(stream))
+    if prep is None:
+        _check(lib.kda_replay(*common, *tail), "kda_replay")
+    else:
+        _check(lib.kda_replay_prep(*common, prep, l2_eps, *tail), "kda_replay_prep")
 
 
 def _pool_shape(state_pool):

@@ -123,6 +123,31 @@ kda_status kda_chunk_fwd(const void *q, const void *k, const void *v, const void
                          void *workspace, size_t ws_bytes, void *stream);
 
 /*
+ * Optional input preprocessing, fused into the kernels (the kda_*_prep calls):
+ * callers that hold raw projections pass them as they are and skip a separate
+ * normalisation pass over q, k, g and beta.  The pages do not define KDA's
+ * input maps; the common ones for delta-rule attention are provided, each
+ * behind its own flag:
+ *   KDA_PREP_L2NORM_Q     q_t <- q_t / sqrt(sum_i q_{t,i}^2 + l2_eps)   per (token, head)
+ *   KDA_PREP_L2NORM_K     k_t <- k_t / sqrt(sum_i k_{t,i}^2 + l2_eps)
+ *   KDA_PREP_SIGMOID_GATE g holds raw gates x: the log-gate is logsigmoid(x), so the
+ *                         decay is alpha = sigmoid(x) (never exactly 0 for finite x)
+ *   KDA_PREP_SIGMOID_BETA beta <- sigmoid(beta)
+ * scale still multiplies q after the normalisation.  Unknown flags or a
+ * negative / non-finite l2_eps return KDA_ERR_INVALID_ARGUMENT.  With prep = 0
+ * the _prep calls are exactly the plain ones.
+ */
+#define KDA_PREP_L2NORM_Q 1u
+#define KDA_PREP_L2NORM_K 2u
+#define KDA_PREP_SIGMOID_GATE 4u
+#define KDA_PREP_SIGMOID_BETA 8u
+
+kda_status kda_chunk_fwd_prep(const void *q, const void *k, const void *v, const void *g, const void *beta,
+                              kda_dtype dtype, const float *init_state, const int32_t *cu_seqlens, int N,
+                              int64_t T_total, int H, int dk, int dv, float scale, uint32_t prep, float l2_eps,
+                              void *o, float *final_state, void *workspace, size_t ws_bytes, void *stream);
+
+/*
  * One decode token per sequence on a slot-indexed state pool (in place).
  *
  *   q, k, g      [N, H, dk]   dtype;  v [N, H, dv];  beta [N, H]
@@ -136,6 +161,12 @@ kda_status kda_decode_step(const void *q, const void *k, const void *v, const vo
                            kda_dtype dtype, float *state_pool, int64_t num_slots, const int32_t *slots,
                            int N, int H, int dk, int dv, float scale, void *o, void *workspace,
                            size_t ws_bytes, void *stream);
+
+/* kda_decode_step with input preprocessing (see kda_chunk_fwd_prep). */
+kda_status kda_decode_step_prep(const void *q, const void *k, const void *v, const void *g, const void *beta,
+                                kda_dtype dtype, float *state_pool, int64_t num_slots, const int32_t *slots,
+                                int N, int H, int dk, int dv, float scale, uint32_t prep, float l2_eps, void *o,
+                                void *workspace, size_t ws_bytes, void *stream);
 
 /*
  * ReplaySSM-style rollback: apply each sequence's accepted tokens to its
@@ -191,6 +222,14 @@ kda_status kda_state_offload(const float *state_pool, int64_t num_slots, const i
  * host_states as for kda_state_offload.  No slot may appear twice. */
 kda_status kda_state_restore(float *state_pool, int64_t num_slots, const int32_t *slots, int n, int H, int dk,
                              int dv, const float *host_states, void *workspace, size_t ws_bytes, void *stream);
+
+/* kda_replay with input preprocessing (see kda_chunk_fwd_prep; KDA_PREP_L2NORM_Q has
+ * no effect, replay reads no q).  Bit for bit the final state of
+ * kda_chunk_fwd_prep over the accepted tokens with the same flags. */
+kda_status kda_replay_prep(float *state_pool, int64_t num_slots, const int32_t *slots, const void *k,
+                           const void *v, const void *g, const void *beta, kda_dtype dtype,
+                           const int32_t *cu_accept, int N, int64_t A_total, int H, int dk, int dv, uint32_t prep,
+                           float l2_eps, void *workspace, size_t ws_bytes, void *stream);
 
 /*
  * Synchronizes `stream`, then reads the device status word of `workspace`

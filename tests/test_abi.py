@@ -18,7 +18,9 @@ def test_exports_every_declared_symbol(lib):
     from gated_linear_attention_chunk_gb300 import kda
     names = kda.header_functions()
     assert {"kda_chunk_fwd", "kda_decode_step", "kda_replay", "kda_device_status",
-            "kda_chunk_fwd_workspace_size", "kda_status_string", "kda_version"} <= set(names)
+            "kda_chunk_fwd_workspace_size", "kda_status_string", "kda_version", "kda_chunk_fwd_prep",
+            "kda_decode_step_prep", "kda_replay_prep", "kda_state_fork", "kda_state_offload",
+            "kda_state_restore", "kda_chunk_fwd_noalloc"} <= set(names)
     for n in names:
         assert hasattr(lib, n), n
 
@@ -99,3 +101,28 @@ def test_state_pool_host_errors(lib):
     assert lib.kda_state_offload(fake, 8, None, 1, 2, 128, 128, None, ws, 256, None) == 1  # NULL host
     assert lib.kda_state_restore(fake, 8, None, 1, 0, 128, 128, fake, ws, 256, None) == 1  # H = 0
     assert lib.kda_state_offload(fake, 8, None, 1, 2, 128, 128, fake, ws, 16, None) == 3   # small workspace
+
+
+def test_prep_flag_host_errors(lib):
+    """Unknown preprocessing flags and a bad epsilon are rejected on the host; the
+    plain calls are the _prep calls with no flags (same checks, same codes)."""
+    c = lib.kda_chunk_fwd_prep
+    args = lambda prep, eps, **kw: (FAKE, FAKE, FAKE, FAKE, FAKE, kw.get("dtype", 0), None, None, 1, 64, 2,
+                                    kw.get("dk", 128), 128, 1.0, prep, eps, FAKE, FAKE, FAKE, kw.get("wsb", 256),
+                                    None)
+    assert c(*args(16, 1e-6)) == 1                      # unknown flag
+    assert c(*args(0x80000000, 1e-6)) == 1
+    assert c(*args(2, -1e-6)) == 1                       # negative eps
+    assert c(*args(2, float("nan"))) == 1
+    assert c(*args(2, float("inf"))) == 1
+    assert c(*args(2, 1e-6, dk=96)) == 2                 # shape checks come first
+    assert c(*args(15, 1e-6, wsb=255)) == 3              # valid flags: falls through to the workspace check
+    d = lib.kda_decode_step_prep
+    assert d(FAKE, FAKE, FAKE, FAKE, FAKE, 0, FAKE, 4, None, 2, 2, 128, 128, 1.0, 32, 1e-6, FAKE, FAKE, 256,
+             None) == 1
+    assert d(FAKE, FAKE, FAKE, FAKE, FAKE, 0, FAKE, 4, None, 2, 2, 128, 128, 1.0, 15, 1e-6, FAKE, FAKE, 100,
+             None) == 3
+    r = lib.kda_replay_prep
+    assert r(FAKE, 4, None, FAKE, FAKE, FAKE, FAKE, 0, FAKE, 2, 8, 2, 128, 128, 64, 1e-6, FAKE, 256, None) == 1
+    assert r(FAKE, 4, None, FAKE, FAKE, FAKE, FAKE, 0, FAKE, 2, 8, 2, 128, 128, 15, -2.0, FAKE, 256, None) == 1
+    assert r(FAKE, 4, None, FAKE, FAKE, FAKE, FAKE, 0, FAKE, 2, 8, 2, 128, 128, 15, 1e-6, None, 256, None) == 3

@@ -16,6 +16,11 @@ library standardises on):
 * beta = sigmoid(N(0, 1)), one scalar per (token, head).
 * initial states ~ N(0, 0.02^2) in fp32 (or absent = zeros).
 * draw order: lengths, q, k, v, x_g, x_beta, initial state.
+* raw cases (``raw=True``, for the fused preprocessing): the same draws, but q
+  and k are left un-normalised and unscaled, g holds x_g and beta holds x_beta
+  (the library's preprocessing flags turn them into L2-normalised rows,
+  alpha = sigmoid(x_g) and beta = sigmoid(x_beta)); the caller passes
+  scale = 1/sqrt(dk).
 
 All draws use a CPU ``torch.Generator`` seeded with the case seed.
 """
@@ -86,12 +91,14 @@ def varlen_lengths(n_seq: int, median: int, sigma: float, lo: int, hi: int, gen:
 
 
 def _draw_tokens(T: int, H: int, dk: int, dv: int, dtype: torch.dtype, gen: torch.Generator,
-                 g_mu: float, q_scale: bool = True):
+                 g_mu: float, q_scale: bool = True, raw: bool = False):
     q = torch.randn(T, H, dk, generator=gen, dtype=torch.float32)
     k = torch.randn(T, H, dk, generator=gen, dtype=torch.float32)
     v = torch.randn(T, H, dv, generator=gen, dtype=torch.float32)
     xg = torch.randn(T, H, dk, generator=gen, dtype=torch.float32) + g_mu
     xb = torch.randn(T, H, generator=gen, dtype=torch.float32)
+    if raw:
+        return (q.to(dtype), k.to(dtype), v.to(dtype), xg.to(dtype), xb.to(dtype))
     k = k / k.norm(dim=-1, keepdim=True).clamp_min(1e-12)
     if q_scale:
         q = q * (1.0 / math.sqrt(dk))
@@ -102,15 +109,16 @@ def _draw_tokens(T: int, H: int, dk: int, dv: int, dtype: torch.dtype, gen: torc
 
 def make_case(lengths: List[int], H: int, dk: int, dv: int, dtype: torch.dtype = torch.bfloat16,
               seed: int = 0, init: bool = True, g_mu: float = 3.0, init_std: float = 0.02,
-              q_scale: bool = True, scale: float = 1.0) -> KdaCase:
+              q_scale: bool = True, scale: float = 1.0, raw: bool = False) -> KdaCase:
     """Packed varlen case with the given per-sequence lengths.
 
     ``q_scale`` folds 1/sqrt(dk) into q (then ``scale`` is normally 1.0);
     ``q_scale=False`` leaves q raw so the caller passes ``scale=1/sqrt(dk)``.
+    ``raw`` returns the un-preprocessed draws (see the module docstring).
     """
     gen = _gen(seed)
     T = int(sum(lengths))
-    q, k, v, g, beta = _draw_tokens(T, H, dk, dv, dtype, gen, g_mu, q_scale)
+    q, k, v, g, beta = _draw_tokens(T, H, dk, dv, dtype, gen, g_mu, q_scale, raw)
     cu = torch.zeros(len(lengths) + 1, dtype=torch.int32)
     if lengths:
         cu[1:] = torch.cumsum(torch.tensor(lengths, dtype=torch.int64), 0).to(torch.int32)
@@ -143,8 +151,9 @@ def _torch_dtype(name: str) -> torch.dtype:
     return {"bf16": torch.bfloat16, "f32": torch.float32}[name]
 
 
-def named_case(name: str, lengths_override: Optional[List[int]] = None) -> KdaCase:
-    """Build one of ``NAMED_WORKLOADS`` (the prefill part for ``spec_rollout``)."""
+def named_case(name: str, lengths_override: Optional[List[int]] = None, raw: bool = False) -> KdaCase:
+    """Build one of ``NAMED_WORKLOADS`` (the prefill part for ``spec_rollout``); ``raw``
+    gives the same draws before preprocessing, with scale = 1/sqrt(dk)."""
     w = NAMED_WORKLOADS[name]
     seed = w["seed"]
     if lengths_override is not None:
@@ -154,13 +163,14 @@ def named_case(name: str, lengths_override: Optional[List[int]] = None) -> KdaCa
     else:
         lengths = list(w["lengths"])
     return make_case(lengths, w["H"], w["dk"], w["dv"], _torch_dtype(w["dtype"]), seed=seed,
-                     init=w["init"], g_mu=w["g_mu"])
+                     init=w["init"], g_mu=w["g_mu"], q_scale=not raw, scale=w["dk"] ** -0.5 if raw else 1.0,
+                     raw=raw)
 
 
 def make_decode_tokens(n_tok: int, H: int, dk: int, dv: int, dtype: torch.dtype, seed: int,
-                       g_mu: float = 3.0):
+                       g_mu: float = 3.0, raw: bool = False):
     """Per-token inputs (q, k, v, g, beta) for ``n_tok`` decode/verify tokens."""
-    return _draw_tokens(n_tok, H, dk, dv, dtype, _gen(seed), g_mu, True)
+    return _draw_tokens(n_tok, H, dk, dv, dtype, _gen(seed), g_mu, True, raw)
 
 
 def make_accept_lengths(n_steps: int, n_seq: int, max_accept: int, seed: int) -> torch.Tensor:
