@@ -226,8 +226,8 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_tc_kernel(const __grid_
     __shared__ __align__(16) float s_ac[3][kD];  // per-chunk A_C, ring of three
     __shared__ __align__(16) float s_x[32 * kLdX];
     __shared__ __align__(16) float s_tot[8][kD];
-    __shared__ float s_rn[2][2][kC];  // per stage: inverse L2 norms of the k and q rows (preprocessing)
-    __shared__ uint64_t bar_full[2], bar_free[2], bar_norm[2];
+    __shared__ float s_rn[2][kC];  // inverse L2 norms of this chunk's k and q rows (preprocessing)
+    __shared__ uint64_t bar_full[2], bar_free[2];
     __shared__ uint64_t bar_elem, bar_mma1, bar_mfree, bar_tready, bar_mma2, bar_ready, bar_wfree, bar_c1, bar_uready,
         bar_c3;
     __shared__ uint64_t bar_drain[2];
@@ -278,7 +278,6 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_tc_kernel(const __grid_
         for (int s = 0; s < 2; ++s) {
             mbar_init(&bar_full[s], 2);
             mbar_init(&bar_free[s], 1);
-            mbar_init(&bar_norm[s], 32);
         }
         mbar_init(&bar_elem, 1);
         mbar_init(&bar_mma1, 1);
@@ -480,58 +479,6 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_tc_kernel(const __grid_
                 mma_commit(&bar_drain[1]);
                 const uint64_t dl = globaltimer_ns() + kWaitNs;
                 while (!mbar_try_wait(&bar_drain[1], 0) && globaltimer_ns() < dl) {
-                }
-            }
-        } else if (warp == 3) {
-            // ------------------------------------------------------------------ row norms (preprocessing)
-            // Squared L2 norms of the chunk's 64 k rows and 64 q rows, taken as the diagonal of
-            // K K^T (and Q Q^T) with m16n8k16 tensor-core tiles: one 16-row block x one 16-column
-            // slice loaded by ldmatrix is both the A operand and, for each half of the block, the
-            // B operand.  The inverse norms go to s_rn before the decay group's second pass,
-            // which overwrites k and q.
-            if constexpr (kPrep) {
-                if (p.prep & (PREP_L2NORM_K | PREP_L2NORM_Q)) {
-                    const int g8 = lane >> 2, t4 = lane & 3;
-                    const bool diag_lane = t4 == (g8 >> 1);
-                    for (int c = 0; c < nfull; ++c) {
-                        const int s = c & 1;
-                        if (!warp_wait(&bar_full[s], (c >> 1) & 1, ctl, lane)) break;
-                        const uint32_t st = sm_base + s * kStage;
-#pragma unroll
-                        for (int tq = 0; tq < 2; ++tq) {  // 0 = k rows, 1 = q rows
-                            const bool on = (p.prep & (tq == 0 ? PREP_L2NORM_K : PREP_L2NORM_Q)) != 0;
-#pragma unroll
-                            for (int bp = 0; bp < 64; bp += 32) {  // two 16-row blocks at a time
-                                float c0[2][4] = {}, c1[2][4] = {};
-#pragma unroll
-                                for (int kb = 0; kb < 2; ++kb) {
-                                    const uint32_t base = st + OFF_R + kb * 16384 + tq * 8192;
-#pragma unroll
-                                    for (int ks = 0; ks < 4; ++ks) {
-#pragma unroll
-                                        for (int b = 0; b < 2; ++b) {
-                                            const int row = bp + 16 * b + (lane & 7) + ((lane >> 3) & 1) * 8;
-                                            uint32_t a[4];
-                                            ldmatrix_x4(a, base + chunk16(row, 2 * ks + (lane >> 4)));
-                                            mma_bf16_16816(c0[b], a, a[0], a[2]);  // block x its rows 0-7
-                                            mma_bf16_16816(c1[b], a, a[1], a[3]);  // block x its rows 8-15
-                                        }
-                                    }
-                                }
-                                if (diag_lane) {
-#pragma unroll
-                                    for (int b = 0; b < 2; ++b) {
-                                        const float lo = (g8 & 1) ? c0[b][1] : c0[b][0];  // row g8 of the block
-                                        const float hi = (g8 & 1) ? c1[b][3] : c1[b][2];  // row g8 + 8
-                                        const int r = bp + 16 * b + g8;
-                                        s_rn[s][tq][r] = on ? rsqrtf(lo + p.prep_eps) : 1.f;
-                                        s_rn[s][tq][r + 8] = on ? rsqrtf(hi + p.prep_eps) : 1.f;
-                                    }
-                                }
-                            }
-                        }
-                        mbar_arrive(&bar_norm[s]);  // every lane (count 32): its reads and writes are done
-                    }
                 }
             }
         }
@@ -767,18 +714,44 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_tc_kernel(const __grid_
                     sig_gate = (p.prep & PREP_SIGMOID_GATE) != 0;
                     norms = (p.prep & (PREP_L2NORM_K | PREP_L2NORM_Q)) != 0;
                 }
+                // Row norms (preprocessing): each of the eight warps takes one 16-row block of k
+                // (warps 0-3) or q (warps 4-7) and forms the diagonal of its Gram block with
+                // m16n8k16 tensor-core tiles: a 16 x 16 slice loaded by ldmatrix is the A operand
+                // and, for each 8-row half, the B operand.  Issued before the first pass so that
+                // their latency overlaps it.
+                float nc0[4] = {0.f, 0.f, 0.f, 0.f}, nc1[4] = {0.f, 0.f, 0.f, 0.f};
+                const int ntq = seg >> 2, nblk = seg & 3;
+                if constexpr (kPrep) {
+                    if (norms) {
+                        const uint32_t nbase = sm_base + s * kStage + OFF_R + ntq * 8192;
+                        const int nrow = 16 * nblk + (cq & 7) + ((cq >> 3) & 1) * 8;
+#pragma unroll
+                        for (int nk = 0; nk < 8; ++nk) {
+                            uint32_t fa[4];
+                            ldmatrix_x4(fa, nbase + (nk >> 2) * 16384 + chunk16(nrow, 2 * (nk & 3) + (cq >> 4)));
+                            mma_bf16_16816(nc0, fa, fa[0], fa[2]);  // block x its rows 0-7
+                            mma_bf16_16816(nc1, fa, fa[1], fa[3]);  // block x its rows 8-15
+                        }
+                    }
+                }
                 if (sig_gate)
                     pass1(std::true_type{});
                 else
                     pass1(std::false_type{});
+                if constexpr (kPrep) {
+                    // lane (g, g / 2) of the m16n8 accumulator layout holds rows g and g + 8 of the diagonal
+                    const int g8 = cq >> 2;
+                    if (norms && (cq & 3) == (g8 >> 1)) {
+                        const bool on = (p.prep & (ntq == 0 ? PREP_L2NORM_K : PREP_L2NORM_Q)) != 0;
+                        const float lo = (g8 & 1) ? nc0[1] : nc0[0], hi = (g8 & 1) ? nc1[3] : nc1[2];
+                        s_rn[ntq][16 * nblk + g8] = on ? rsqrtf(lo + p.prep_eps) : 1.f;
+                        s_rn[ntq][16 * nblk + g8 + 8] = on ? rsqrtf(hi + p.prep_eps) : 1.f;
+                    }
+                }
                 const float2 pp01 = uf2(P01), pp23 = uf2(P23);
                 const float p0 = pp01.x, p1 = pp01.y, p2 = pp23.x, p3 = pp23.y;
                 st4(&s_tot[seg][ch], make_float4(p0, p1, p2, p3));
-                if (norms) {  // the row norms come from the norm warp (it reads k and q before pass 2 rewrites them)
-                    if (!group_wait(&bar_norm[s], (c >> 1) & 1, ctl, &s_grp_fail[0], 1, 256, gseq)) break;
-                } else {
-                    named_bar(1, 256);
-                }
+                named_bar(1, 256);
                 float4 m = make_float4(1.f, 1.f, 1.f, 1.f);  // product of the earlier segments' totals
                 for (int q = 0; q < seg; ++q) {
                     const float4 t = ld4(&s_tot[q][ch]);
@@ -787,10 +760,9 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_tc_kernel(const __grid_
                 const float sc = p.scale;
                 const uint64_t m01 = f2(m.x, m.y), m23 = f2(m.z, m.w);
                 const uint64_t ms01 = f2(m.x * sc, m.y * sc), ms23 = f2(m.z * sc, m.w * sc);
-                const uint64_t SC2 = f2(sc, sc);
-                // Pass 2: Kbar = k A, Qbar = scale q A, Ktil = k / A over k, q, g in place; with
+                // Pass 2: Kbar = k A, Qbar = scale q A, Ktil = k / A over k, q, g in place.  With
                 // L2-normalised rows (preprocessing) k and q are first scaled by their rows'
-                // inverse norms
+                // inverse norms; with the sigmoid gate the running products are D = 1 / A.
                 auto pass2 = [&](auto norm, auto sig) {
                     constexpr bool kNorm = decltype(norm)::value;
                     constexpr bool kSig = decltype(sig)::value;
@@ -807,14 +779,14 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_tc_kernel(const __grid_
                         for (int e = 0; e < 2; ++e) {
                             const uint32_t off = swz(r0 + rr + e, cc);
                             uint64_t a01, a23, aq01, aq23, r01, r23;
-                            if constexpr (kSig) {  // the products are D = 1 / A
+                            if constexpr (kSig) {
                                 r01 = mul2(m01, A01[rr + e]);
                                 r23 = mul2(m23, A23[rr + e]);
                                 const float2 fr01 = uf2(r01), fr23 = uf2(r23);
                                 a01 = f2(rcp_approx(fr01.x), rcp_approx(fr01.y));
                                 a23 = f2(rcp_approx(fr23.x), rcp_approx(fr23.y));
-                                aq01 = mul2(a01, SC2);
-                                aq23 = mul2(a23, SC2);
+                                aq01 = mul2(a01, f2(sc, sc));
+                                aq23 = mul2(a23, f2(sc, sc));
                             } else {
                                 a01 = mul2(m01, A01[rr + e]);
                                 a23 = mul2(m23, A23[rr + e]);
@@ -827,12 +799,11 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_tc_kernel(const __grid_
                             uint64_t k01 = bf2x(kw[e].x), k23 = bf2x(kw[e].y);
                             uint64_t q01 = bf2x(qw[e].x), q23 = bf2x(qw[e].y);
                             if constexpr (kNorm) {
-                                const float rk = s_rn[s][0][r0 + rr + e], rq = s_rn[s][1][r0 + rr + e];
-                                const uint64_t RK = f2(rk, rk), RQ = f2(rq, rq);
-                                k01 = mul2(k01, RK);
-                                k23 = mul2(k23, RK);
-                                q01 = mul2(q01, RQ);
-                                q23 = mul2(q23, RQ);
+                                const float rk = s_rn[0][r0 + rr + e], rq = s_rn[1][r0 + rr + e];
+                                k01 = mul2(k01, f2(rk, rk));
+                                k23 = mul2(k23, f2(rk, rk));
+                                q01 = mul2(q01, f2(rq, rq));
+                                q23 = mul2(q23, f2(rq, rq));
                             }
                             *reinterpret_cast<uint2 *>(Rk + off) = make_uint2(pk2(mul2(k01, a01)), pk2(mul2(k23, a23)));
                             *reinterpret_cast<uint2 *>(Rq + off) = make_uint2(pk2(mul2(q01, aq01)), pk2(mul2(q23, aq23)));
@@ -841,7 +812,10 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_tc_kernel(const __grid_
                     }
                 };
                 float4 ac;  // A_C of the chunk (segment 7 holds the last products)
-                if constexpr (kPrep) {
+                if constexpr (!kPrep) {
+                    pass2(std::false_type{}, std::false_type{});
+                    ac = make_float4(m.x * p0, m.y * p1, m.z * p2, m.w * p3);
+                } else {
                     if (norms) {
                         if (sig_gate) pass2(std::true_type{}, std::true_type{});
                         else pass2(std::true_type{}, std::false_type{});
@@ -849,14 +823,8 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_tc_kernel(const __grid_
                         if (sig_gate) pass2(std::false_type{}, std::true_type{});
                         else pass2(std::false_type{}, std::false_type{});
                     }
-                    if (sig_gate)
-                        ac = make_float4(rcp_approx(m.x * p0), rcp_approx(m.y * p1), rcp_approx(m.z * p2),
-                                         rcp_approx(m.w * p3));
-                    else
-                        ac = make_float4(m.x * p0, m.y * p1, m.z * p2, m.w * p3);
-                } else {
-                    pass2(std::false_type{}, std::false_type{});
-                    ac = make_float4(m.x * p0, m.y * p1, m.z * p2, m.w * p3);
+                    const float4 x = make_float4(m.x * p0, m.y * p1, m.z * p2, m.w * p3);
+                    ac = sig_gate ? make_float4(rcp_approx(x.x), rcp_approx(x.y), rcp_approx(x.z), rcp_approx(x.w)) : x;
                 }
                 if (seg == 7) {
                     if (!(ac.x >= kMinDecay) || !(ac.y >= kMinDecay) || !(ac.z >= kMinDecay) || !(ac.w >= kMinDecay))
