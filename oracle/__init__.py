@@ -11,6 +11,9 @@ float64 (an exact upcast of bf16/fp32 data) and exposes:
 * ``forward``  -- packed varlen prefill: o and final state.
 * ``decode``   -- one token per sequence on a slot-indexed state pool.
 * ``replay``   -- accepted tokens re-applied to committed states (no output).
+* ``backward`` -- gradients of a loss with respect to every input, given its
+  gradients with respect to o and the final states (reverse mode of the same
+  token-by-token recurrence).
 
 Decode and replay are the same recurrence as ``forward`` (the speculative-
 decoding paragraph of "Kimi K3 on Fireworks: Fast RL at frontier scale" replays
@@ -62,6 +65,11 @@ def _load():
             lib.kda_oracle_prep.restype = ctypes.c_int
             lib.kda_oracle_prep.argtypes = [dp, dp, dp, dp, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
                                             ctypes.c_double, ctypes.c_int]
+            lib.kda_oracle_backward.restype = ctypes.c_int
+            lib.kda_oracle_backward.argtypes = [dp, dp, dp, dp, dp, dp, ctypes.POINTER(ctypes.c_int64),
+                                                ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                                                ctypes.c_double, ctypes.c_int, dp, dp, dp, dp, dp, dp, dp, dp,
+                                                ctypes.c_int]
             lib.kda_oracle_max_threads.restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -173,3 +181,31 @@ def replay(k, v, g, beta, cu_accept, state_pool, slots=None, threads: int = 1, p
                     prep_flags=prep_flags & ~PREP_L2NORM_Q, prep_eps=prep_eps)
     pool[sl] = fs
     return pool
+
+
+def backward(q, k, v, g, beta, cu_seqlens, init_state, d_o, d_final=None, scale: float = 1.0,
+             gate_is_alpha: bool = False, threads: int = 1):
+    """Reverse mode of ``forward`` in fp64 (kda_oracle_backward).
+
+    Given dL/do [T, H, dv] and dL/d(final_state) [N, H, dk, dv] (None = 0), returns a
+    dict of float64 arrays: dq, dk, dg [T, H, dk] (dg with respect to the log-gates,
+    or to alpha with ``gate_is_alpha``), dv [T, H, dv], dbeta [T, H] and d_init
+    [N, H, dk, dv].
+    """
+    lib = _load()
+    q64, k64, v64, g64, b64 = _f64(q), _f64(k), _f64(v), _f64(g), _f64(beta)
+    cu = np.ascontiguousarray(np.asarray(_f64(cu_seqlens), dtype=np.int64))
+    T, H, dk = k64.shape
+    dv = v64.shape[2]
+    N = cu.shape[0] - 1
+    s0, do64, df64 = _f64(init_state), _f64(d_o), _f64(d_final)
+    out = {"dq": np.zeros((T, H, dk)), "dk": np.zeros((T, H, dk)), "dv": np.zeros((T, H, dv)),
+           "dg": np.zeros((T, H, dk)), "dbeta": np.zeros((T, H)), "d_init": np.zeros((N, H, dk, dv))}
+    rc = lib.kda_oracle_backward(_ptr(q64), _ptr(k64), _ptr(v64), _ptr(g64), _ptr(b64), _ptr(s0),
+                                 cu.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)), N, H, dk, dv, float(scale),
+                                 int(bool(gate_is_alpha)), _ptr(do64), _ptr(df64), _ptr(out["dq"]),
+                                 _ptr(out["dk"]), _ptr(out["dv"]), _ptr(out["dg"]), _ptr(out["dbeta"]),
+                                 _ptr(out["d_init"]), int(threads))
+    if rc != 0:
+        raise RuntimeError(f"kda_oracle_backward failed with code {rc}")
+    return out

@@ -157,6 +157,168 @@ int kda_oracle_prep(double *q, double *k, double *g, double *beta, int64_t T, in
     return KDA_ORACLE_OK;
 }
 
+/*
+ * Backward (reverse mode) of kda_oracle_forward, for training: given the
+ * gradients of a loss with respect to the outputs o (d_o, [T,H,dv]) and to the
+ * final states (d_final, [N,H,dk,dv] or NULL = zero), the gradients with
+ * respect to q, k, v, g (log-gates; with gate_is_alpha, alpha itself), beta and
+ * the initial states.  The KDA paragraph quotes a backward kernel (its speedup
+ * over FLA) but no formula; this is the adjoint of exactly the three steps the
+ * forward takes per token, applied in reverse token order:
+ *
+ *   forward   S' = Diag(a) S_prev;  y = S'^T k;  u = beta (v - y);  S = S' + k u^T;
+ *             o = S^T (scale q)
+ *   reverse   dS += (scale q) do^T;   dq = scale S do
+ *             du = dS^T k;  dk = dS u;  dbeta = du . (v - y);  dv = beta du;  dy = -beta du
+ *             dS' = dS + k dy^T;  dk += S' dy
+ *             da_i = sum_j dS'_ij S_prev,ij;  dg_i = da_i a_i (log-gates);  dS_prev = Diag(a) dS'
+ *
+ * The state before every token's decay is kept (stored on the way forward), so
+ * each reverse step recomputes S', y, u and S from it in double precision.
+ * Outputs dq, dk, dg [T,H,dk], dv [T,H,dv], dbeta [T,H] are written for every
+ * token; d_init [N,H,dk,dv] may be NULL.
+ */
+static void oracle_chain_bwd(const double *q, const double *k, const double *v, const double *g,
+                             const double *beta, int64_t bos, int64_t eos, int64_t h, int64_t H,
+                             int64_t dk, int64_t dv, double scale, int gate_is_alpha, const double *d_o,
+                             double *Sall, double *dS, double *Sp, double *dSp, double *y, double *u,
+                             double *du, double *dy, double *dq, double *dkk, double *dvv, double *dg,
+                             double *dbeta)
+{
+    const int64_t L = eos - bos, sz = dk * dv;
+    /* forward, keeping the state before each token: Sall[l] = S before token bos + l */
+    for (int64_t l = 0; l < L; ++l) {
+        const int64_t t = bos + l;
+        const double *kt = k + (t * H + h) * dk, *gt = g + (t * H + h) * dk, *vt = v + (t * H + h) * dv;
+        const double bt = beta[t * H + h];
+        double *S = Sall + (l + 1) * sz;
+        memcpy(S, Sall + l * sz, sizeof(double) * (size_t)sz);
+        for (int64_t i = 0; i < dk; ++i) {
+            const double a = gate_is_alpha ? gt[i] : exp(gt[i]);
+            for (int64_t j = 0; j < dv; ++j) S[i * dv + j] *= a;
+        }
+        for (int64_t j = 0; j < dv; ++j) y[j] = 0.0;
+        for (int64_t i = 0; i < dk; ++i)
+            for (int64_t j = 0; j < dv; ++j) y[j] += kt[i] * S[i * dv + j];
+        for (int64_t j = 0; j < dv; ++j) u[j] = bt * (vt[j] - y[j]);
+        for (int64_t i = 0; i < dk; ++i)
+            for (int64_t j = 0; j < dv; ++j) S[i * dv + j] += kt[i] * u[j];
+    }
+    /* reverse; dS holds the gradient with respect to the state after token t */
+    for (int64_t l = L - 1; l >= 0; --l) {
+        const int64_t t = bos + l;
+        const double *qt = q + (t * H + h) * dk, *kt = k + (t * H + h) * dk, *gt = g + (t * H + h) * dk;
+        const double *vt = v + (t * H + h) * dv, *dot = d_o + (t * H + h) * dv;
+        const double bt = beta[t * H + h];
+        const double *Sprev = Sall + l * sz, *S = Sall + (l + 1) * sz;
+        double *dqt = dq + (t * H + h) * dk, *dkt = dkk + (t * H + h) * dk, *dgt = dg + (t * H + h) * dk;
+        double *dvt = dvv + (t * H + h) * dv;
+        /* recompute S' = Diag(a) S_prev, y, u */
+        for (int64_t i = 0; i < dk; ++i) {
+            const double a = gate_is_alpha ? gt[i] : exp(gt[i]);
+            for (int64_t j = 0; j < dv; ++j) Sp[i * dv + j] = a * Sprev[i * dv + j];
+        }
+        for (int64_t j = 0; j < dv; ++j) y[j] = 0.0;
+        for (int64_t i = 0; i < dk; ++i)
+            for (int64_t j = 0; j < dv; ++j) y[j] += kt[i] * Sp[i * dv + j];
+        for (int64_t j = 0; j < dv; ++j) u[j] = bt * (vt[j] - y[j]);
+        /* o = S^T (scale q) */
+        for (int64_t i = 0; i < dk; ++i) {
+            double acc = 0.0;
+            for (int64_t j = 0; j < dv; ++j) acc += S[i * dv + j] * dot[j];
+            dqt[i] = scale * acc;
+            for (int64_t j = 0; j < dv; ++j) dS[i * dv + j] += scale * qt[i] * dot[j];
+        }
+        /* S = S' + k u^T */
+        for (int64_t j = 0; j < dv; ++j) du[j] = 0.0;
+        for (int64_t i = 0; i < dk; ++i) {
+            double acc = 0.0;
+            for (int64_t j = 0; j < dv; ++j) {
+                acc += dS[i * dv + j] * u[j];
+                du[j] += dS[i * dv + j] * kt[i];
+            }
+            dkt[i] = acc;
+        }
+        /* u = beta (v - y) */
+        double db = 0.0;
+        for (int64_t j = 0; j < dv; ++j) {
+            db += du[j] * (vt[j] - y[j]);
+            dvt[j] = bt * du[j];
+            dy[j] = -bt * du[j];
+        }
+        dbeta[t * H + h] = db;
+        /* y = S'^T k:  dS' = dS + k dy^T,  dk += S' dy */
+        for (int64_t i = 0; i < dk; ++i) {
+            double acc = 0.0;
+            for (int64_t j = 0; j < dv; ++j) {
+                dSp[i * dv + j] = dS[i * dv + j] + kt[i] * dy[j];
+                acc += Sp[i * dv + j] * dy[j];
+            }
+            dkt[i] += acc;
+        }
+        /* S' = Diag(a) S_prev */
+        for (int64_t i = 0; i < dk; ++i) {
+            const double a = gate_is_alpha ? gt[i] : exp(gt[i]);
+            double da = 0.0;
+            for (int64_t j = 0; j < dv; ++j) {
+                da += dSp[i * dv + j] * Sprev[i * dv + j];
+                dS[i * dv + j] = a * dSp[i * dv + j];
+            }
+            dgt[i] = gate_is_alpha ? da : da * a;
+        }
+    }
+}
+
+int kda_oracle_backward(const double *q, const double *k, const double *v, const double *g,
+                        const double *beta, const double *init_state, const int64_t *cu_seqlens,
+                        int64_t N, int64_t H, int64_t dk, int64_t dv, double scale, int gate_is_alpha,
+                        const double *d_o, const double *d_final, double *dq, double *dk_out,
+                        double *dv_out, double *dg, double *dbeta, double *d_init, int nthreads)
+{
+    if (N < 0 || H <= 0 || dk <= 0 || dv <= 0 || !cu_seqlens || !q || !k || !v || !g || !beta || !d_o ||
+        !dq || !dk_out || !dv_out || !dg || !dbeta)
+        return KDA_ORACLE_BAD_ARGS;
+    if (N > 0 && cu_seqlens[0] != 0) return KDA_ORACLE_BAD_ARGS;
+    for (int64_t n = 0; n < N; ++n)
+        if (cu_seqlens[n + 1] < cu_seqlens[n]) return KDA_ORACLE_BAD_ARGS;
+
+    const int64_t pairs = N * H, sz = dk * dv;
+    int failed = 0;
+#ifdef _OPENMP
+    if (nthreads <= 0) nthreads = omp_get_max_threads();
+#pragma omp parallel for schedule(dynamic, 1) num_threads(nthreads) reduction(| : failed)
+#endif
+    for (int64_t p = 0; p < pairs; ++p) {
+        const int64_t n = p / H, h = p % H;
+        const int64_t L = cu_seqlens[n + 1] - cu_seqlens[n];
+        double *Sall = (double *)malloc(sizeof(double) * (size_t)((L + 1) * sz));
+        double *work = (double *)malloc(sizeof(double) * (size_t)(3 * sz + 4 * dv));
+        if (!Sall || !work) {
+            free(Sall);
+            free(work);
+            failed |= 1;
+            continue;
+        }
+        double *dS = work, *Sp = work + sz, *dSp = work + 2 * sz, *y = work + 3 * sz, *u = y + dv, *du = u + dv,
+               *dy = du + dv;
+        if (init_state)
+            memcpy(Sall, init_state + p * sz, sizeof(double) * (size_t)sz);
+        else
+            memset(Sall, 0, sizeof(double) * (size_t)sz);
+        if (d_final)
+            memcpy(dS, d_final + p * sz, sizeof(double) * (size_t)sz);
+        else
+            memset(dS, 0, sizeof(double) * (size_t)sz);
+        oracle_chain_bwd(q, k, v, g, beta, cu_seqlens[n], cu_seqlens[n + 1], h, H, dk, dv, scale, gate_is_alpha,
+                         d_o, Sall, dS, Sp, dSp, y, u, du, dy, dq, dk_out, dv_out, dg, dbeta);
+        if (d_init) memcpy(d_init + p * sz, dS, sizeof(double) * (size_t)sz);
+        free(Sall);
+        free(work);
+    }
+    (void)nthreads;
+    return failed ? KDA_ORACLE_NO_MEMORY : KDA_ORACLE_OK;
+}
+
 /* Threads the OpenMP runtime would use by default (1 without OpenMP). */
 int kda_oracle_max_threads(void)
 {

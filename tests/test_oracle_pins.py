@@ -423,3 +423,84 @@ def test_prep_forward_reduces_to_plain_forward():
     o_c, _ = oracle.forward(q, k, v, xg, beta, cu, s0, prep_flags=oracle.PREP_SIGMOID_GATE)
     o_d, _ = oracle.forward(q, k, v, np.zeros(k.shape), beta, cu, np.zeros_like(s0))
     np.testing.assert_allclose(o_c[:9], o_d[:9], rtol=1e-13, atol=1e-13)
+
+
+# ------------------------------------------------------------------------------------------------
+# Backward (reverse mode of the recurrence): pinned against the forward by central finite
+# differences, against a closed form, and by linearity.
+# ------------------------------------------------------------------------------------------------
+
+def _bwd_case(seed, lens=(5, 3, 0, 4), H=2, dk=3, dv=4):
+    rng = np.random.default_rng(seed)
+    T = sum(lens)
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int64)
+    N = len(lens)
+    d = dict(q=rng.standard_normal((T, H, dk)), k=rng.standard_normal((T, H, dk)),
+             v=rng.standard_normal((T, H, dv)), g=-np.abs(rng.standard_normal((T, H, dk))) * 0.5,
+             b=rng.uniform(0.1, 0.9, (T, H)), s0=rng.standard_normal((N, H, dk, dv)) * 0.3)
+    Wo, Ws = rng.standard_normal((T, H, dv)), rng.standard_normal((N, H, dk, dv))
+    return cu, d, Wo, Ws
+
+
+@pytest.mark.parametrize("gate_is_alpha", [False, True])
+def test_backward_matches_finite_differences_of_forward(gate_is_alpha):
+    """L = sum(o * Wo) + sum(final * Ws): every gradient the backward returns equals the
+    central difference of the forward's L (step 1e-6, fp64) to 1e-7 relative."""
+    cu, d, Wo, Ws = _bwd_case(11 + gate_is_alpha)
+    if gate_is_alpha:
+        d["g"] = np.exp(d["g"])
+    sc = 0.7
+
+    def loss(q, k, v, g, b, s0):
+        o, fs = oracle.forward(q, k, v, g, b, cu, s0, scale=sc, gate_is_alpha=gate_is_alpha)
+        return float((o * Wo).sum() + (fs * Ws).sum())
+
+    G = oracle.backward(d["q"], d["k"], d["v"], d["g"], d["b"], cu, d["s0"], Wo, Ws, scale=sc,
+                        gate_is_alpha=gate_is_alpha)
+    h = 1e-6
+    for name, key in (("q", "dq"), ("k", "dk"), ("v", "dv"), ("g", "dg"), ("b", "dbeta"), ("s0", "d_init")):
+        arr = d[name]
+        num = np.zeros_like(arr)
+        for idx in np.ndindex(arr.shape):
+            plus, minus = dict(d), dict(d)
+            plus[name] = arr.copy()
+            plus[name][idx] += h
+            minus[name] = arr.copy()
+            minus[name][idx] -= h
+            num[idx] = (loss(**plus) - loss(**minus)) / (2 * h)
+        err = np.abs(num - G[key]).max() / np.abs(num).max()
+        assert err < 1e-7, (name, err)
+
+
+def test_backward_closed_form_without_delta_step():
+    """beta = 0: S_t = Diag(A_t) S_0 with A_t the running product of exp(g), o_t = S_t^T (s q_t).
+    Then dq_t = s Diag(A_t) S_0 do_t, d_init = sum_t Diag(A_t) (s q_t) do_t^T,
+    dg_{u,i} = sum_{t >= u} s q_{t,i} A_{t,i} (S_0 do_t)_i, dk = dv = 0."""
+    rng = np.random.default_rng(5)
+    T, H, dk, dv, s = 6, 1, 3, 2, 0.9
+    q, k, v = rng.standard_normal((T, H, dk)), rng.standard_normal((T, H, dk)), rng.standard_normal((T, H, dv))
+    g = -rng.uniform(0.0, 0.7, (T, H, dk))
+    b = np.zeros((T, H))
+    s0 = rng.standard_normal((1, H, dk, dv))
+    do = rng.standard_normal((T, H, dv))
+    G = oracle.backward(q, k, v, g, b, np.array([0, T]), s0, do, None, scale=s)
+    A = np.exp(np.cumsum(g[:, 0, :], axis=0))            # [T, dk]
+    S0 = s0[0, 0]
+    S0do = do[:, 0, :] @ S0.T                            # [T, dk]: (S_0 do_t)
+    np.testing.assert_allclose(G["dq"][:, 0, :], s * A * S0do, rtol=1e-12, atol=1e-12)
+    dinit = sum(np.outer(A[t] * s * q[t, 0], do[t, 0]) for t in range(T))
+    np.testing.assert_allclose(G["d_init"][0, 0], dinit, rtol=1e-12, atol=1e-12)
+    contrib = s * q[:, 0, :] * A * S0do                  # [T, dk], term of token t
+    dg = np.cumsum(contrib[::-1], axis=0)[::-1]          # sum over t >= u
+    np.testing.assert_allclose(G["dg"][:, 0, :], dg, rtol=1e-12, atol=1e-12)
+    assert np.abs(G["dk"]).max() == 0.0 and np.abs(G["dv"]).max() == 0.0
+
+
+def test_backward_is_linear_in_the_output_gradients_and_empty_sequences_pass_through():
+    cu, d, Wo, Ws = _bwd_case(7)
+    G1 = oracle.backward(d["q"], d["k"], d["v"], d["g"], d["b"], cu, d["s0"], Wo, Ws)
+    G2 = oracle.backward(d["q"], d["k"], d["v"], d["g"], d["b"], cu, d["s0"], -2.5 * Wo, -2.5 * Ws)
+    for key in G1:
+        np.testing.assert_allclose(G2[key], -2.5 * G1[key], rtol=1e-12, atol=1e-12)
+    # sequence 2 is empty: its initial-state gradient is the final-state gradient
+    np.testing.assert_array_equal(G1["d_init"][2], Ws[2])
