@@ -225,6 +225,71 @@ kda_status kda_replay(float *state_pool, int64_t num_slots, const int32_t *slots
                            0.f, workspace, ws_bytes, stream);
 }
 
+// Backward workspace: header | checkpoints (floor(T/64) + N + 1 slots of H states) |
+// per-(sequence, head) scratch of the backward kernel.
+static size_t bwd_ckpt_bytes(int N, int64_t T_total, int H, int dk, int dv) {
+    return static_cast<size_t>(T_total / 64 + N + 1) * H * dk * dv * sizeof(float);
+}
+
+size_t kda_chunk_bwd_workspace_size(int N, int64_t T_total, int H, int dk, int dv) {
+    if (N < 0 || T_total < 0 || H <= 0 || !dim_ok(dk) || !dim_ok(dv)) return 0;
+    return KDA_WS_HEADER_BYTES + bwd_ckpt_bytes(N, T_total, H, dk, dv) +
+           static_cast<size_t>(N) * H * kda::bwd_scratch_floats(dk, dv) * sizeof(float);
+}
+
+kda_status kda_chunk_bwd(const void *q, const void *k, const void *v, const void *g, const void *beta,
+                         kda_dtype dtype, const float *init_state, const int32_t *cu_seqlens, int N,
+                         int64_t T_total, int H, int dk, int dv, float scale, const void *d_o,
+                         const float *d_final_state, void *dq, void *dk_out, void *dv_out, void *dg, void *dbeta,
+                         float *d_init_state, void *workspace, size_t ws_bytes, void *stream) {
+    if (!dtype_ok(dtype) || !dim_ok(dk) || !dim_ok(dv)) return KDA_ERR_UNSUPPORTED;
+    if (N < 0 || T_total < 0 || H <= 0) return KDA_ERR_INVALID_ARGUMENT;
+    if (!workspace || !aligned16(workspace)) return KDA_ERR_WORKSPACE;
+    if (ws_bytes < kda_chunk_bwd_workspace_size(N, T_total, H, dk, dv)) return KDA_ERR_WORKSPACE;
+    const size_t es = elem_size(dtype);
+    if (T_total > 0) {
+        if (!q || !k || !v || !g || !beta || !d_o || !dq || !dk_out || !dv_out || !dg || !dbeta)
+            return KDA_ERR_INVALID_ARGUMENT;
+        for (const void *ptr : {q, k, v, g, beta, d_o, static_cast<const void *>(dq),
+                                static_cast<const void *>(dk_out), static_cast<const void *>(dv_out),
+                                static_cast<const void *>(dg), static_cast<const void *>(dbeta)})
+            if (!aligned_to(ptr, es)) return KDA_ERR_INVALID_ARGUMENT;
+    }
+    if ((init_state && !aligned16(init_state)) || (d_final_state && !aligned_to(d_final_state, 4)) ||
+        (d_init_state && !aligned_to(d_init_state, 4)))
+        return KDA_ERR_INVALID_ARGUMENT;
+    if (!cu_seqlens && N > 0 && (T_total % N) != 0) return KDA_ERR_INVALID_ARGUMENT;
+    if (!cu_seqlens && N == 0 && T_total != 0) return KDA_ERR_INVALID_ARGUMENT;
+    if (cu_seqlens && !aligned_to(cu_seqlens, 4)) return KDA_ERR_INVALID_ARGUMENT;
+
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    kda_status st = clear_status(workspace, s);
+    if (st != KDA_OK) return st;
+    if (N == 0) return KDA_OK;
+    uint32_t *status = static_cast<uint32_t *>(workspace);
+    float *ckpt = reinterpret_cast<float *>(static_cast<char *>(workspace) + KDA_WS_HEADER_BYTES);
+    float *scratch = reinterpret_cast<float *>(static_cast<char *>(workspace) + KDA_WS_HEADER_BYTES +
+                                               bwd_ckpt_bytes(N, T_total, H, dk, dv));
+    const int64_t fixed_len = cu_seqlens ? 0 : T_total / N;
+
+    // forward pass for the chunk-start states (token-sequential, no outputs)
+    kda::SeqParams sp{};
+    sp.q = q; sp.k = k; sp.v = v; sp.g = g; sp.beta = beta; sp.o = nullptr;
+    sp.N = N; sp.H = H; sp.scale = scale; sp.mode = kda::SEQ_MODE_PREFILL;
+    sp.cu = cu_seqlens; sp.T_total = T_total; sp.seq_len_fixed = fixed_len; sp.chunk_skip = 0;
+    sp.state_in = init_state; sp.state_out = nullptr; sp.chunk_state = nullptr;
+    sp.slots = nullptr; sp.num_slots = 0; sp.status = status; sp.ckpt = ckpt;
+    if (kda::launch_seq(sp, dk, dv, static_cast<int>(dtype), s) != cudaSuccess) return KDA_ERR_CUDA;
+
+    kda::BwdParams bp{};
+    bp.q = q; bp.k = k; bp.v = v; bp.g = g; bp.beta = beta; bp.d_o = d_o; bp.d_final = d_final_state;
+    bp.dq = dq; bp.dk = dk_out; bp.dv = dv_out; bp.dg = dg; bp.dbeta = dbeta; bp.d_init = d_init_state;
+    bp.ckpt = ckpt; bp.scratch = scratch; bp.cu = cu_seqlens; bp.T_total = T_total; bp.seq_len_fixed = fixed_len;
+    bp.N = N; bp.H = H; bp.scale = scale; bp.status = status;
+    if (kda::launch_bwd(bp, dk, dv, static_cast<int>(dtype), s) != cudaSuccess) return KDA_ERR_CUDA;
+    return KDA_OK;
+}
+
 kda_status kda_device_status(const void *workspace, void *stream) {
     if (!workspace) return KDA_ERR_WORKSPACE;
     cudaStream_t s = static_cast<cudaStream_t>(stream);

@@ -42,7 +42,15 @@ struct SeqParams {
     uint32_t *status;           // device status word
     int prep;                   // input preprocessing flags (PREP_*), 0 = inputs used as given
     float prep_eps;             // epsilon of the L2 normalisation
+    // prefill only, or null: the state at the start of every 64-token chunk of sequence n
+    // goes to slot (ckpt_base(n) + c) * H + h, ckpt_base(n) = floor(first token / 64) + n
+    float *ckpt;
 };
+
+// First checkpoint slot of a sequence starting at token `bos` (sequence index n): the
+// ranges [base, base + ceil(len / 64)) of consecutive sequences do not overlap, and
+// floor(T_total / 64) + N + 1 slots cover every sequence.
+__host__ __device__ inline int64_t ckpt_base(int64_t bos, int64_t n) { return bos / 64 + n; }
 
 // T-segment merge after a split chunked launch (kda_merge.cu): o on segment-1 tokens
 // += S1^T o_phi, then state <- phi state + psi.  o, o_phi: [T, H, 128] bf16.
@@ -60,6 +68,24 @@ cudaError_t launch_merge(const MergeParams &p, cudaStream_t stream);
 
 // dtype: 0 = bf16, 1 = fp32 (kda_dtype).  Returns the launch error.
 cudaError_t launch_seq(const SeqParams &p, int dk, int dv, int dtype, cudaStream_t stream);
+
+// Backward of the packed prefill (kda_bwd.cu): one CTA per (sequence, head) walks the
+// 64-token chunks in reverse from the checkpoints of the forward pass.
+struct BwdParams {
+    const void *q, *k, *v, *g, *beta, *d_o;
+    const float *d_final;       // may be null (zero)
+    void *dq, *dk, *dv, *dg, *dbeta;
+    float *d_init;              // may be null
+    const float *ckpt;          // states at chunk starts (see ckpt_base)
+    float *scratch;             // per (sequence, head): bwd_scratch_floats(dk, dv) floats
+    const int32_t *cu;
+    int64_t T_total, seq_len_fixed;
+    int N, H;
+    float scale;
+    uint32_t *status;
+};
+size_t bwd_scratch_floats(int dk, int dv);
+cudaError_t launch_bwd(const BwdParams &p, int dk, int dv, int dtype, cudaStream_t stream);
 
 // Arguments of the chunked (64-token WY, tcgen05) kernel: bf16, dk = dv = 128.
 struct ChunkParams {

@@ -101,8 +101,8 @@ __device__ __forceinline__ float4 f4_shfl_xor(float4 a, int m) {
                        __shfl_xor_sync(0xffffffffu, a.z, m), __shfl_xor_sync(0xffffffffu, a.w, m));
 }
 
-// PREP: the instance that applies the input preprocessing of p.prep (the other one
-// carries none of its code).
+// PREP: the extended instance -- it applies the input preprocessing of p.prep and
+// writes the chunk-start checkpoints of p.ckpt (the other one carries none of that code).
 template <int DK, int DV, typename Tin, bool WRITE_O, bool PREP>
 __global__ void __launch_bounds__(kSeqThreads, 6) kda_seq_kernel(SeqParams p) {
     constexpr int CB = kColBlock;         // columns of this CTA
@@ -254,9 +254,20 @@ __global__ void __launch_bounds__(kSeqThreads, 6) kda_seq_kernel(SeqParams p) {
     }
     __syncthreads();
 
+    int64_t ck = 0;  // checkpoint slot of the chunk that starts at t0 (backward's forward pass)
+    if constexpr (PREP) {
+        if (p.ckpt) ck = (ckpt_base(t0, n) * H + h) * DK * DV + col0 + 4 * cg;
+    }
     int it = 0;
     for (int64_t t = t0; t < t1; ++t, ++it) {
         const int b = it % 3, r = it & 1;
+        if constexpr (PREP) {
+            if (p.ckpt && (it & 63) == 0) {  // state before the first token of each chunk
+                float *dstc = p.ckpt + ck + static_cast<int64_t>(it >> 6) * H * DK * DV;
+#pragma unroll
+                for (int s = 0; s < NS; ++s) *reinterpret_cast<float4 *>(dstc + (s * RPS + row0) * DV) = S[s];
+            }
+        }
         const bool has_next = (t + 1 < t1);
         float ng = 0.f, nk = 0.f, nq = 0.f, nv = 0.f, nb = 0.f;
         if (has_next) load_raw(t + 1, ng, nk, nq, nv, nb);
@@ -339,12 +350,12 @@ cudaError_t launch_typed(const SeqParams &p, cudaStream_t stream) {
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     const dim3 grid(static_cast<unsigned>(blocks));
     if (p.o) {
-        if (p.prep)
+        if (p.prep || p.ckpt)
             kda_seq_kernel<DK, DV, Tin, true, true><<<grid, kSeqThreads, 0, stream>>>(p);
         else
             kda_seq_kernel<DK, DV, Tin, true, false><<<grid, kSeqThreads, 0, stream>>>(p);
     } else {
-        if (p.prep)
+        if (p.prep || p.ckpt)
             kda_seq_kernel<DK, DV, Tin, false, true><<<grid, kSeqThreads, 0, stream>>>(p);
         else
             kda_seq_kernel<DK, DV, Tin, false, false><<<grid, kSeqThreads, 0, stream>>>(p);

@@ -56,6 +56,9 @@ _SIGS = {
                                     _vp]),
     "kda_replay_prep": (_int, [_vp, _i64, _vp, _vp, _vp, _vp, _vp, _int, _vp, _int, _i64, _int, _int, _int,
                                ctypes.c_uint32, ctypes.c_float, _vp, ctypes.c_size_t, _vp]),
+    "kda_chunk_bwd_workspace_size": (ctypes.c_size_t, [_int, _i64, _int, _int, _int]),
+    "kda_chunk_bwd": (_int, [_vp, _vp, _vp, _vp, _vp, _int, _vp, _vp, _int, _i64, _int, _int, _int, ctypes.c_float,
+                             _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp]),
     "kda_device_status": (_int, [_vp, _vp]),
     "kda_status_string": (ctypes.c_char_p, [_int]),
     "kda_version": (_int, []),
@@ -321,6 +324,46 @@ def _replay(state_pool, k, v, g, beta, cu_accept, slots, workspace, stream, prep
         _check(lib.kda_replay(*common, *tail), "kda_replay")
     else:
         _check(lib.kda_replay_prep(*common, prep, l2_eps, *tail), "kda_replay_prep")
+
+
+def kda_chunk_bwd_workspace_size(N: int, T_total: int, H: int, dk: int, dv: int) -> int:
+    return int(load_library().kda_chunk_bwd_workspace_size(N, T_total, H, dk, dv))
+
+
+def kda_chunk_bwd(q, k, v, g, beta, d_o, cu_seqlens=None, init_state=None, d_final_state=None,
+                  scale: float = 1.0, want_d_init: bool = True, workspace=None, stream=None) -> dict:
+    """Backward of kda_chunk_fwd: returns a dict with dq, dk, dg [T, H, dk], dv [T, H, dv],
+    dbeta [T, H] (input dtype) and d_init [N, H, dk, dv] fp32 (None unless ``want_d_init``),
+    given d_o [T, H, dv] and d_final_state [N, H, dk, dv] fp32 (None = zero)."""
+    lib = load_library()
+    dt = q.dtype
+    T, H, dk = q.shape
+    dv = v.shape[2]
+    for name, t, shp in (("q", q, (T, H, dk)), ("k", k, (T, H, dk)), ("v", v, (T, H, dv)),
+                         ("g", g, (T, H, dk)), ("beta", beta, (T, H)), ("d_o", d_o, (T, H, dv))):
+        _need(t, name, dt, shp)
+    if cu_seqlens is None:
+        N = 1
+    else:
+        _need(cu_seqlens, "cu_seqlens", torch.int32)
+        N = cu_seqlens.numel() - 1
+    if init_state is not None:
+        _need(init_state, "init_state", torch.float32, (N, H, dk, dv))
+    if d_final_state is not None:
+        _need(d_final_state, "d_final_state", torch.float32, (N, H, dk, dv))
+    out = {"dq": torch.empty_like(q), "dk": torch.empty_like(k), "dv": torch.empty_like(v),
+           "dg": torch.empty_like(g), "dbeta": torch.empty_like(beta),
+           "d_init": torch.empty(N, H, dk, dv, dtype=torch.float32, device=q.device) if want_d_init else None}
+    need = kda_chunk_bwd_workspace_size(N, T, H, dk, dv)
+    if workspace is None:
+        workspace = new_workspace(need, q.device)
+    rc = lib.kda_chunk_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _dtype_code(q), _ptr(init_state),
+                           _ptr(cu_seqlens), N, T, H, dk, dv, float(scale), _ptr(d_o), _ptr(d_final_state),
+                           _ptr(out["dq"]), _ptr(out["dk"]), _ptr(out["dv"]), _ptr(out["dg"]),
+                           _ptr(out["dbeta"]), _ptr(out["d_init"]), _ptr(workspace),
+                           workspace.numel() * workspace.element_size(), _stream_handle(stream))
+    _check(rc, "kda_chunk_bwd")
+    return out
 
 
 def _pool_shape(state_pool):

@@ -232,6 +232,36 @@ kda_status kda_replay_prep(float *state_pool, int64_t num_slots, const int32_t *
                            float l2_eps, void *workspace, size_t ws_bytes, void *stream);
 
 /*
+ * Backward of kda_chunk_fwd (training): the gradients of a loss with respect to
+ * q, k, v, g (the log-gates), beta and the initial states, given its gradients
+ * with respect to o (d_o [T_total, H, dv]) and to the final states
+ * (d_final_state [N, H, dk, dv] fp32, or NULL = zero).  The KDA paragraph of
+ * "Kimi K3 on Fireworks: Fast RL at frontier scale" quotes a backward kernel but
+ * no formula; this is the reverse mode of the same recurrence, evaluated on the
+ * 64-token chunked form: a forward pass stores the state at every chunk start
+ * in the workspace, then one CTA per (sequence, head) walks the chunks in
+ * reverse.
+ *
+ * Inputs as for kda_chunk_fwd (same dtype, layouts, cu_seqlens, init_state,
+ * scale).  Outputs, all in the input dtype: d_q, d_k, d_g [T_total, H, dk],
+ * d_v [T_total, H, dv], d_beta [T_total, H]; d_init_state [N, H, dk, dv] fp32 or
+ * NULL.  Every output element is written (they need no clearing).
+ * Workspace: at least kda_chunk_bwd_workspace_size(N, T_total, H, dk, dv) bytes,
+ * 16-byte aligned, owned by the caller, not read back.  Errors as for
+ * kda_chunk_fwd: KDA_ERR_UNSUPPORTED (dtype, dk, dv), KDA_ERR_INVALID_ARGUMENT
+ * (NULL or misaligned pointers, N not dividing T_total without cu_seqlens),
+ * KDA_ERR_WORKSPACE; invalid cu_seqlens and a chunk decay below 2^-100 are
+ * reported through kda_device_status (KDA_ERR_BAD_SEQLENS, KDA_ERR_GATE_RANGE).
+ */
+size_t kda_chunk_bwd_workspace_size(int N, int64_t T_total, int H, int dk, int dv);
+
+kda_status kda_chunk_bwd(const void *q, const void *k, const void *v, const void *g, const void *beta,
+                         kda_dtype dtype, const float *init_state, const int32_t *cu_seqlens, int N,
+                         int64_t T_total, int H, int dk, int dv, float scale, const void *d_o,
+                         const float *d_final_state, void *d_q, void *d_k, void *d_v, void *d_g, void *d_beta,
+                         float *d_init_state, void *workspace, size_t ws_bytes, void *stream);
+
+/*
  * Synchronizes `stream`, then reads the device status word of `workspace`
  * (errors from the last call that used it).  Returns KDA_OK or the first of
  * BAD_SEQLENS, BAD_SLOT, GATE_RANGE, TIMEOUT that was raised; KDA_ERR_CUDA if
