@@ -304,6 +304,40 @@ def measure_state_kernels(kda, dev, hbm_peak, n_seq=128, H=32, d=128, reps=50):
     return out
 
 
+def measure_backward(kda, case, dev, hbm_peak, reps=3):
+    """kda_chunk_bwd on the same workload: d_o ~ N(0, 1), no final-state gradient.
+    Algorithmic bytes per token-head: q, k, v, g, d_o and beta read, dq, dk, dv, dg and
+    dbeta written (10 d + 2 values of the input dtype), plus the initial state read and
+    its gradient written per (sequence, head)."""
+    q, k, v, g, b = (x.to(dev) for x in (case.q, case.k, case.v, case.g, case.beta))
+    cu = case.cu_seqlens.to(dev)
+    s0 = None if case.init_state is None else case.init_state.to(dev)
+    d_o = torch.randn(case.T_total, case.H, case.dv, generator=torch.Generator().manual_seed(9)).to(q.dtype).to(dev)
+    ws = kda.new_workspace(kda.kda_chunk_bwd_workspace_size(case.N, case.T_total, case.H, case.dk, case.dv), dev)
+
+    def call():
+        kda.kda_chunk_bwd(q, k, v, g, b, d_o, cu_seqlens=cu, init_state=s0, scale=case.scale, workspace=ws)
+
+    call()
+    torch.cuda.synchronize()
+    st = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(st)
+    for _ in range(reps):
+        call()
+    e1.record(st)
+    torch.cuda.synchronize()
+    if kda.kda_device_status(ws) != kda.KDA_OK:
+        raise RuntimeError("backward device status")
+    ms = e0.elapsed_time(e1) / reps
+    es = q.element_size()
+    nbytes = case.T_total * case.H * (10 * case.dk + 2) * es + 2 * case.N * case.H * case.dk * case.dv * 4
+    gbs = nbytes / (ms / 1e3) / 1e9
+    return {"ms_per_call": ms, "tokens_per_s": case.T_total / (ms / 1e3), "achieved_GBs": gbs,
+            "frac_of_hbm": gbs / hbm_peak, "algorithmic_bytes": nbytes, "calls": reps,
+            "launches_per_call": 2}
+
+
 def run_gpu(args, world, rank, local):
     import gated_linear_attention_chunk_gb300 as kda
 
@@ -449,6 +483,7 @@ def run_gpu(args, world, rank, local):
                            " and the partial-chunk launch)"})
 
     state_kernels = measure_state_kernels(kda, dev, hbm_peak) if not args.no_state_kernels else None
+    backward = measure_backward(kda, case, dev, hbm_peak) if not (args.no_backward or args.prep) else None
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -460,7 +495,7 @@ def run_gpu(args, world, rank, local):
                 "vs_baseline": None, "dtype": "bf16" if q.dtype == torch.bfloat16 else "f32",
                 "data": "synthetic", "config": config_dict(args, case), "roofline": roof,
                 "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches_per_step * args.steps,
-                "clocks": clk, "state_kernels": state_kernels}
+                "clocks": clk, "state_kernels": state_kernels, "backward": backward}
         print(json.dumps(line), flush=True)
     if distributed:
         dist.destroy_process_group()
@@ -479,6 +514,7 @@ def main(argv=None):
     ap.add_argument("--no-state-kernels", action="store_true", help="skip the decode/replay bandwidth check")
     ap.add_argument("--plain-workspace", action="store_true",
                     help="minimum workspace: kda_chunk_fwd runs without the T-segment split")
+    ap.add_argument("--no-backward", action="store_true", help="skip the kda_chunk_bwd measurement")
     ap.add_argument("--prep", action="store_true",
                     help="raw inputs through kda_chunk_fwd_prep with every preprocessing flag")
     args = ap.parse_args(argv)

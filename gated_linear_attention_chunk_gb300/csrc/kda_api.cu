@@ -225,16 +225,33 @@ kda_status kda_replay(float *state_pool, int64_t num_slots, const int32_t *slots
                            0.f, workspace, ws_bytes, stream);
 }
 
-// Backward workspace: header | checkpoints (floor(T/64) + N + 1 slots of H states) |
-// per-(sequence, head) scratch of the backward kernel.
-static size_t bwd_ckpt_bytes(int N, int64_t T_total, int H, int dk, int dv) {
-    return static_cast<size_t>(T_total / 64 + N + 1) * H * dk * dv * sizeof(float);
+// Backward workspace: header | checkpoints | records (both nslots x H) | staging states
+// (N x H) | persistent-CTA scratch (kBwdMaxCtas) | two states per (sequence, head).
+constexpr int kBwdMaxCtas = 256;
+
+static int64_t bwd_slots(int N, int64_t T_total) { return T_total / 64 + N + 1; }
+
+static size_t bwd_layout(int N, int64_t T_total, int H, int dk, int dv, size_t *ckpt_off, size_t *rec_off,
+                         size_t *stage_off, size_t *scratch_off) {
+    const size_t st = static_cast<size_t>(dk) * dv * sizeof(float);
+    const size_t slots = static_cast<size_t>(bwd_slots(N, T_total)) * H;
+    size_t off = KDA_WS_HEADER_BYTES;
+    *ckpt_off = off;
+    off += slots * st;
+    *rec_off = off;
+    off += slots * kda::bwd_record_floats(dk, dv) * sizeof(float);
+    *stage_off = off;
+    off += static_cast<size_t>(N) * H * st;
+    *scratch_off = off;
+    off += static_cast<size_t>(kBwdMaxCtas) * kda::bwd_scratch_floats(dk, dv) * sizeof(float) +
+           static_cast<size_t>(N) * H * 2 * st;
+    return off;
 }
 
 size_t kda_chunk_bwd_workspace_size(int N, int64_t T_total, int H, int dk, int dv) {
     if (N < 0 || T_total < 0 || H <= 0 || !dim_ok(dk) || !dim_ok(dv)) return 0;
-    return KDA_WS_HEADER_BYTES + bwd_ckpt_bytes(N, T_total, H, dk, dv) +
-           static_cast<size_t>(N) * H * kda::bwd_scratch_floats(dk, dv) * sizeof(float);
+    size_t a, b, c, d;
+    return bwd_layout(N, T_total, H, dk, dv, &a, &b, &c, &d);
 }
 
 kda_status kda_chunk_bwd(const void *q, const void *k, const void *v, const void *g, const void *beta,
@@ -250,9 +267,10 @@ kda_status kda_chunk_bwd(const void *q, const void *k, const void *v, const void
     if (T_total > 0) {
         if (!q || !k || !v || !g || !beta || !d_o || !dq || !dk_out || !dv_out || !dg || !dbeta)
             return KDA_ERR_INVALID_ARGUMENT;
-        for (const void *ptr : {q, k, v, g, beta, d_o, static_cast<const void *>(dq),
-                                static_cast<const void *>(dk_out), static_cast<const void *>(dv_out),
-                                static_cast<const void *>(dg), static_cast<const void *>(dbeta)})
+        if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(g)) return KDA_ERR_INVALID_ARGUMENT;
+        for (const void *ptr : {beta, d_o, static_cast<const void *>(dq), static_cast<const void *>(dk_out),
+                                static_cast<const void *>(dv_out), static_cast<const void *>(dg),
+                                static_cast<const void *>(dbeta)})
             if (!aligned_to(ptr, es)) return KDA_ERR_INVALID_ARGUMENT;
     }
     if ((init_state && !aligned16(init_state)) || (d_final_state && !aligned_to(d_final_state, 4)) ||
@@ -266,25 +284,46 @@ kda_status kda_chunk_bwd(const void *q, const void *k, const void *v, const void
     kda_status st = clear_status(workspace, s);
     if (st != KDA_OK) return st;
     if (N == 0) return KDA_OK;
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
+        return KDA_ERR_CUDA;
     uint32_t *status = static_cast<uint32_t *>(workspace);
-    float *ckpt = reinterpret_cast<float *>(static_cast<char *>(workspace) + KDA_WS_HEADER_BYTES);
-    float *scratch = reinterpret_cast<float *>(static_cast<char *>(workspace) + KDA_WS_HEADER_BYTES +
-                                               bwd_ckpt_bytes(N, T_total, H, dk, dv));
+    size_t ckpt_off, rec_off, stage_off, scratch_off;
+    bwd_layout(N, T_total, H, dk, dv, &ckpt_off, &rec_off, &stage_off, &scratch_off);
+    char *ws = static_cast<char *>(workspace);
+    float *ckpt = reinterpret_cast<float *>(ws + ckpt_off);
     const int64_t fixed_len = cu_seqlens ? 0 : T_total / N;
 
-    // forward pass for the chunk-start states (token-sequential, no outputs)
-    kda::SeqParams sp{};
-    sp.q = q; sp.k = k; sp.v = v; sp.g = g; sp.beta = beta; sp.o = nullptr;
-    sp.N = N; sp.H = H; sp.scale = scale; sp.mode = kda::SEQ_MODE_PREFILL;
-    sp.cu = cu_seqlens; sp.T_total = T_total; sp.seq_len_fixed = fixed_len; sp.chunk_skip = 0;
-    sp.state_in = init_state; sp.state_out = nullptr; sp.chunk_state = nullptr;
-    sp.slots = nullptr; sp.num_slots = 0; sp.status = status; sp.ckpt = ckpt;
-    if (kda::launch_seq(sp, dk, dv, static_cast<int>(dtype), s) != cudaSuccess) return KDA_ERR_CUDA;
+    // forward pass leaving the chunk-start states: the tensor-core kernel (no outputs) where
+    // it serves the shape, else the token-sequential kernel
+    if (kda::chunk_tc_supported(dk, dv, static_cast<int>(dtype)) && T_total <= 0x7fffffffLL) {
+        kda::ChunkParams cp{};
+        cp.q = q; cp.k = k; cp.v = v; cp.g = g; cp.beta = beta; cp.o = nullptr;
+        cp.N = N; cp.H = H; cp.scale = scale; cp.cu = cu_seqlens; cp.T_total = T_total;
+        cp.seq_len_fixed = fixed_len; cp.init_state = init_state;
+        cp.state_out = reinterpret_cast<float *>(ws + stage_off); cp.status = status; cp.split = 0;
+        cp.ckpt = ckpt;
+        if (kda::launch_chunk_tc(cp, s) != cudaSuccess) return KDA_ERR_CUDA;
+    } else {
+        kda::SeqParams sp{};
+        sp.q = q; sp.k = k; sp.v = v; sp.g = g; sp.beta = beta; sp.o = nullptr;
+        sp.N = N; sp.H = H; sp.scale = scale; sp.mode = kda::SEQ_MODE_PREFILL;
+        sp.cu = cu_seqlens; sp.T_total = T_total; sp.seq_len_fixed = fixed_len; sp.chunk_skip = 0;
+        sp.state_in = init_state; sp.state_out = nullptr; sp.chunk_state = nullptr;
+        sp.slots = nullptr; sp.num_slots = 0; sp.status = status; sp.ckpt = ckpt;
+        if (kda::launch_seq(sp, dk, dv, static_cast<int>(dtype), s) != cudaSuccess) return KDA_ERR_CUDA;
+    }
 
     kda::BwdParams bp{};
-    bp.q = q; bp.k = k; bp.v = v; bp.g = g; bp.beta = beta; bp.d_o = d_o; bp.d_final = d_final_state;
+    bp.q = q; bp.k = k; bp.v = v; bp.g = g; bp.beta = beta; bp.d_o = d_o;
+    bp.init_state = init_state; bp.d_final = d_final_state;
     bp.dq = dq; bp.dk = dk_out; bp.dv = dv_out; bp.dg = dg; bp.dbeta = dbeta; bp.d_init = d_init_state;
-    bp.ckpt = ckpt; bp.scratch = scratch; bp.cu = cu_seqlens; bp.T_total = T_total; bp.seq_len_fixed = fixed_len;
+    bp.ckpt = ckpt; bp.rec = reinterpret_cast<float *>(ws + rec_off);
+    bp.scratch = reinterpret_cast<float *>(ws + scratch_off);
+    bp.ctas = sms < kBwdMaxCtas ? sms : kBwdMaxCtas;
+    bp.nslots = bwd_slots(N, T_total);
+    bp.cu = cu_seqlens; bp.T_total = T_total; bp.seq_len_fixed = fixed_len;
     bp.N = N; bp.H = H; bp.scale = scale; bp.status = status;
     if (kda::launch_bwd(bp, dk, dv, static_cast<int>(dtype), s) != cudaSuccess) return KDA_ERR_CUDA;
     return KDA_OK;

@@ -81,6 +81,7 @@ struct TcParams {
     float *phi, *psi;             // per pair: segment-1 transition and zero-start state
     __nv_bfloat16 *o_phi;         // [T, H, 128]: segment-1 outputs of the transition run
     int split;
+    float *ckpt;                  // chunk-end state checkpoints (backward's forward pass), or null
     int prep;                     // input preprocessing flags (PREP_*)
     float prep_eps;               // epsilon of the L2 normalisation
     int64_t T_total, seq_len_fixed;
@@ -216,8 +217,8 @@ __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, const 
     return __shfl_sync(0xffffffffu, ok, 0) != 0;
 }
 
-// kPrep: the instance that applies the input preprocessing of p.prep (the other
-// instance carries none of its code).
+// kPrep: the extended instance -- it applies the input preprocessing of p.prep and
+// writes the chunk-end checkpoints of p.ckpt (the other instance carries none of that code).
 template <bool kPrep>
 __global__ void __launch_bounds__(kThreads, 1) kda_chunk_tc_kernel(const __grid_constant__ TcParams p) {
     extern __shared__ uint8_t dsmem_raw[];
@@ -532,6 +533,9 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_tc_kernel(const __grid_
         uint32_t opk[32];          // previous chunk's O row block, bf16 pairs (r, r+1)
         int64_t o_t0 = -1;
         auto store_o = [&](int64_t t0) {
+            if constexpr (kPrep) {
+                if (!obase) return;  // checkpoint-only forward
+            }
             __nv_bfloat16 *orow = obase + (t0 * H + h) * kD + j;
             const int64_t rs = H * kD;
 #pragma unroll
@@ -637,6 +641,16 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_tc_kernel(const __grid_
                     for (int e = 0; e < 16; ++e) {
                         sout[(cc + e) * kD + j] = __uint_as_float(a[e]);
                         sout[(cc + 16 + e) * kD + j] = __uint_as_float(b[e]);
+                    }
+                }
+                if constexpr (kPrep) {
+                    if (p.ckpt) {  // the state at the start of chunk c + 1 (slot c + 1 of the sequence)
+                        float *ck = p.ckpt + ((ckpt_base(bos, n) + c + 1) * H + h) * kD * kD;
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) {
+                            ck[(cc + e) * kD + j] = __uint_as_float(a[e]);
+                            ck[(cc + 16 + e) * kD + j] = __uint_as_float(b[e]);
+                        }
                     }
                 }
             }
@@ -1118,6 +1132,7 @@ cudaError_t launch_chunk_tc(const ChunkParams &cp, cudaStream_t stream) {
     p.phi = cp.phi;
     p.psi = cp.psi;
     p.o_phi = static_cast<__nv_bfloat16 *>(cp.o_phi);
+    p.ckpt = cp.ckpt;
     static bool attr_set = false;
     if (!attr_set) {
         for (auto fn : {kda_chunk_tc_kernel<false>, kda_chunk_tc_kernel<true>}) {
@@ -1130,7 +1145,7 @@ cudaError_t launch_chunk_tc(const ChunkParams &cp, cudaStream_t stream) {
         }
         attr_set = true;
     }
-    if (p.prep)
+    if (p.prep || p.ckpt)
         kda_chunk_tc_kernel<true><<<static_cast<unsigned>(blocks), kThreads, kDynSmem, stream>>>(p);
     else
         kda_chunk_tc_kernel<false><<<static_cast<unsigned>(blocks), kThreads, kDynSmem, stream>>>(p);

@@ -69,15 +69,23 @@ cudaError_t launch_merge(const MergeParams &p, cudaStream_t stream);
 // dtype: 0 = bf16, 1 = fp32 (kda_dtype).  Returns the launch error.
 cudaError_t launch_seq(const SeqParams &p, int dk, int dv, int dtype, cudaStream_t stream);
 
-// Backward of the packed prefill (kda_bwd.cu): one CTA per (sequence, head) walks the
-// 64-token chunks in reverse from the checkpoints of the forward pass.
+// Backward of the packed prefill (kda_bwd.cu), in three launches after the forward pass
+// that leaves the chunk-start states in `ckpt` (slot ckpt_base(bos, n) + c for chunk c;
+// slot 0 of each sequence is not read, the initial state is): (A) chunk-local work of
+// every chunk, (B) the reverse chain of state gradients per (sequence, head), (C) the
+// gradients of every chunk.  A and C run on `ctas` persistent CTAs with their own
+// scratch; `rec` holds bwd_record_floats per (slot, head).
 struct BwdParams {
     const void *q, *k, *v, *g, *beta, *d_o;
+    const float *init_state;    // may be null (zero)
     const float *d_final;       // may be null (zero)
     void *dq, *dk, *dv, *dg, *dbeta;
     float *d_init;              // may be null
-    const float *ckpt;          // states at chunk starts (see ckpt_base)
-    float *scratch;             // per (sequence, head): bwd_scratch_floats(dk, dv) floats
+    const float *ckpt;
+    float *rec;                 // per (slot, head) records
+    float *scratch;             // per persistent CTA: bwd_scratch_floats; then per chain: 2 states
+    int ctas;                   // persistent CTAs of phases A and C
+    int64_t nslots;             // checkpoint / record slots: floor(T_total / 64) + N + 1
     const int32_t *cu;
     int64_t T_total, seq_len_fixed;
     int N, H;
@@ -85,6 +93,7 @@ struct BwdParams {
     uint32_t *status;
 };
 size_t bwd_scratch_floats(int dk, int dv);
+size_t bwd_record_floats(int dk, int dv);
 cudaError_t launch_bwd(const BwdParams &p, int dk, int dv, int dtype, cudaStream_t stream);
 
 // Arguments of the chunked (64-token WY, tcgen05) kernel: bf16, dk = dv = 128.
@@ -107,6 +116,9 @@ struct ChunkParams {
     void *o_phi;
     int prep;                   // input preprocessing flags (PREP_*)
     float prep_eps;
+    // or null: the state after every full chunk c goes to checkpoint slot
+    // (ckpt_base(bos, n) + c + 1) * H + h (needs split == 0); o may then be null
+    float *ckpt;
 };
 
 // True when the chunked tensor-core kernel is compiled in and supports the shape.
