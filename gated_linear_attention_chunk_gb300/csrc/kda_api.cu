@@ -227,7 +227,7 @@ kda_status kda_replay(float *state_pool, int64_t num_slots, const int32_t *slots
 
 // Backward workspace: header | checkpoints | records (both nslots x H) | staging states
 // (N x H) | persistent-CTA scratch (kBwdMaxCtas) | two states per (sequence, head).
-constexpr int kBwdMaxCtas = 256;
+constexpr int kBwdMaxCtas = 320;  // two per SM
 
 static int64_t bwd_slots(int N, int64_t T_total) { return T_total / 64 + N + 1; }
 
@@ -321,7 +321,7 @@ kda_status kda_chunk_bwd(const void *q, const void *k, const void *v, const void
     bp.dq = dq; bp.dk = dk_out; bp.dv = dv_out; bp.dg = dg; bp.dbeta = dbeta; bp.d_init = d_init_state;
     bp.ckpt = ckpt; bp.rec = reinterpret_cast<float *>(ws + rec_off);
     bp.scratch = reinterpret_cast<float *>(ws + scratch_off);
-    bp.ctas = sms < kBwdMaxCtas ? sms : kBwdMaxCtas;
+    bp.ctas = 2 * sms < kBwdMaxCtas ? 2 * sms : kBwdMaxCtas;
     bp.nslots = bwd_slots(N, T_total);
     bp.cu = cu_seqlens; bp.T_total = T_total; bp.seq_len_fixed = fixed_len;
     bp.N = N; bp.H = H; bp.scale = scale; bp.status = status;

@@ -37,7 +37,7 @@
 //   (B) every (sequence, head): the chain of dS, two small products per chunk,
 //       leaving dS_next and dR in the records;
 //   (C) every (chunk, head), in parallel: all the gradients of the chunk.
-// A and C run on one persistent CTA per SM, each with its own scratch.  Every
+// A and C run on two persistent CTAs per SM, each with its own scratch.  Every
 // product is a CTA-wide fp32 matrix product over global (L2-resident) operands,
 // staged through shared memory in 16-deep slices with the next slice fetched
 // into registers while the current one is multiplied.
@@ -288,7 +288,7 @@ __device__ void tri_inverse(const float *Mr, const float *s_beta, float *s_buf, 
 
 // ---------------------------------------------------------------------------- phase A
 template <int DK, int DV, typename Tin>
-__global__ void __launch_bounds__(kBT, 1) kda_bwd_chunk_kernel(BwdParams p) {
+__global__ void __launch_bounds__(kBT, 2) kda_bwd_chunk_kernel(BwdParams p) {
     using S = Scr<DK, DV>;
     using RC = Rec<DK, DV>;
     __shared__ __align__(16) float s_buf[SmemBuf<DK>::kFloats];
@@ -328,44 +328,67 @@ __global__ void __launch_bounds__(kBT, 1) kda_bwd_chunk_kernel(BwdParams p) {
 }
 
 // ---------------------------------------------------------------------------- phase B
+// The columns of dS follow independent recurrences (dR and the update of column j read
+// column j only), so each (sequence, head) chain is split into DV / kChainCols CTAs.
+constexpr int kChainCols = 32;
+
 template <int DK, int DV>
 __global__ void __launch_bounds__(kBT, 1) kda_bwd_chain_kernel(BwdParams p) {
     using S = Scr<DK, DV>;
     using RC = Rec<DK, DV>;
+    constexpr int kCB = kChainCols, kBlocks = DV / kCB;
     __shared__ __align__(16) float s_buf[SmemBuf<DK>::kFloats];
     const int tid = threadIdx.x;
-    const int64_t pair = blockIdx.x;
+    const int64_t pair = blockIdx.x / kBlocks;
+    const int col0 = static_cast<int>(blockIdx.x % kBlocks) * kCB;
     const int n = static_cast<int>(pair / p.H), h = static_cast<int>(pair % p.H);
     int64_t bos, eos;
     if (!seq_range(p, n, bos, eos)) {
-        if (tid == 0 && h == 0) atomicOr(p.status, DEV_ERR_SEQLENS);
+        if (tid == 0 && h == 0 && col0 == 0) atomicOr(p.status, DEV_ERR_SEQLENS);
         return;
     }
-    float *dS = p.scratch + static_cast<int64_t>(p.ctas) * S::kTotal + pair * 2 * DK * DV;
+    // this CTA's columns of the chain's two DK x DV states (row stride DV)
+    float *dS = p.scratch + static_cast<int64_t>(p.ctas) * S::kTotal + pair * 2 * DK * DV + col0;
     float *dSn = dS + DK * DV;
-    for (int e = tid; e < DK * DV; e += kBT) dS[e] = p.d_final ? p.d_final[pair * DK * DV + e] : 0.f;
+    for (int e = tid; e < DK * kCB; e += kBT) {
+        const int i = e / kCB, j = e % kCB;
+        dS[i * DV + j] = p.d_final ? p.d_final[pair * DK * DV + i * DV + col0 + j] : 0.f;
+    }
     __syncthreads();
     const int nch = static_cast<int>((eos - bos + kC - 1) / kC);
     const int64_t base = ckpt_base(bos, n);
     for (int c = nch - 1; c >= 0; --c) {
         float *rec = p.rec + ((base + c) * p.H + h) * RC::kTotal;
-        cta_copy(rec + RC::kdSn, dS, DK * DV);
-        cta_copy(rec + RC::kdR, rec + RC::kF, kC * DV);
-        cta_copy(dSn, rec + RC::kE, DK * DV);
+        for (int e = tid; e < DK * kCB; e += kBT) {
+            const int i = e / kCB, j = e % kCB;
+            rec[RC::kdSn + i * DV + col0 + j] = dS[i * DV + j];
+            dSn[i * DV + j] = rec[RC::kE + i * DV + col0 + j];
+        }
+        for (int e = tid; e < kC * kCB; e += kBT) {
+            const int r = e / kCB, j = e % kCB;
+            rec[RC::kdR + r * DV + col0 + j] = rec[RC::kF + r * DV + col0 + j];
+        }
         __syncthreads();
-        // dR = G dS_next + F;  dS = Diag(A_C) dS_next + E - Kbar^T dR
-        cta_gemm<kC, DV, DK, false, false>(rec + RC::kdR, DV, rec + RC::kG, DK, dS, DV, 1.f, true, 0, s_buf);
-        cta_gemm<DK, DV, kC, true, false>(dSn, DV, rec + RC::kKb, DK, rec + RC::kdR, DV, -1.f, true, 0, s_buf);
-        for (int e = tid; e < DK * DV; e += kBT) dS[e] = fmaf(rec[RC::kAC + e / DV], dS[e], dSn[e]);
+        // dR = G dS_next + F;  dS = Diag(A_C) dS_next + E - Kbar^T dR   (this CTA's columns)
+        cta_gemm<kC, kCB, DK, false, false>(rec + RC::kdR + col0, DV, rec + RC::kG, DK, dS, DV, 1.f, true, 0, s_buf);
+        cta_gemm<DK, kCB, kC, true, false>(dSn, DV, rec + RC::kKb, DK, rec + RC::kdR + col0, DV, -1.f, true, 0,
+                                            s_buf);
+        for (int e = tid; e < DK * kCB; e += kBT) {
+            const int i = e / kCB, j = e % kCB;
+            dS[i * DV + j] = fmaf(rec[RC::kAC + i], dS[i * DV + j], dSn[i * DV + j]);
+        }
         __syncthreads();
     }
     if (p.d_init)
-        for (int e = tid; e < DK * DV; e += kBT) p.d_init[pair * DK * DV + e] = dS[e];
+        for (int e = tid; e < DK * kCB; e += kBT) {
+            const int i = e / kCB, j = e % kCB;
+            p.d_init[pair * DK * DV + i * DV + col0 + j] = dS[i * DV + j];
+        }
 }
 
 // ---------------------------------------------------------------------------- phase C
 template <int DK, int DV, typename Tin>
-__global__ void __launch_bounds__(kBT, 1) kda_bwd_grad_kernel(BwdParams p) {
+__global__ void __launch_bounds__(kBT, 2) kda_bwd_grad_kernel(BwdParams p) {
     using S = Scr<DK, DV>;
     using RC = Rec<DK, DV>;
     __shared__ __align__(16) float s_buf[SmemBuf<DK>::kFloats];
@@ -500,7 +523,7 @@ cudaError_t launch_typed(const BwdParams &p, cudaStream_t stream) {
     if (chains <= 0) return cudaSuccess;
     if (chains > 0x7fffffffLL || p.ctas <= 0) return cudaErrorInvalidConfiguration;
     kda_bwd_chunk_kernel<DK, DV, Tin><<<p.ctas, kBT, 0, stream>>>(p);
-    kda_bwd_chain_kernel<DK, DV><<<static_cast<unsigned>(chains), kBT, 0, stream>>>(p);
+    kda_bwd_chain_kernel<DK, DV><<<static_cast<unsigned>(chains * (DV / kChainCols)), kBT, 0, stream>>>(p);
     kda_bwd_grad_kernel<DK, DV, Tin><<<p.ctas, kBT, 0, stream>>>(p);
     return cudaGetLastError();
 }
