@@ -39,9 +39,9 @@ METRIC = "KDA chunk_fwd tokens/s at T=4K-128K (1 GB300) and % of roofline"
 UNIT = "tokens/s"
 
 # DRAM bytes (read + write) of one kda_chunk_tc_kernel launch on prefill_4k, from the
-# ncu capture summarised in profiles/kda_chunk_tc_prefill_4k.md (546.7 MB read +
-# 117.2 MB written).  Reset to None whenever that kernel changes until it is re-captured.
-DOMINANT_TRAFFIC = {"prefill_4k": 663934208}
+# ncu capture summarised in profiles/kda_chunk_tc_prefill_4k.md (546.65 MB read +
+# 117.82 MB written).  Reset to None whenever that kernel changes until it is re-captured.
+DOMINANT_TRAFFIC = {"prefill_4k": 664470272}
 
 # every preprocessing flag (KDA_PREP_L2NORM_Q | _L2NORM_K | _SIGMOID_GATE | _SIGMOID_BETA)
 PREP_ALL, PREP_EPS = 15, 1e-6
@@ -335,7 +335,7 @@ def measure_backward(kda, case, dev, hbm_peak, reps=3):
     gbs = nbytes / (ms / 1e3) / 1e9
     return {"ms_per_call": ms, "tokens_per_s": case.T_total / (ms / 1e3), "achieved_GBs": gbs,
             "frac_of_hbm": gbs / hbm_peak, "algorithmic_bytes": nbytes, "calls": reps,
-            "launches_per_call": 2}
+            "launches_per_call": 4}
 
 
 def run_gpu(args, world, rank, local):

@@ -133,6 +133,9 @@ def make_case(lengths: List[int], H: int, dk: int, dv: int, dtype: torch.dtype =
 NAMED_WORKLOADS = {
     "tiny_fp32": dict(desc="B=1 T=256 H=2 dk=dv=64 fp32, zero initial state, seed 0",
                       lengths=[256], H=2, dk=64, dv=64, dtype="f32", init=False, g_mu=3.0, seed=0),
+    "prefill_1k": dict(desc="B=4 T=1024 H=32 dk=dv=128 bf16, N(0,0.02) initial state (small profiling case,"
+                            " inputs just above L2)",
+                       lengths=[1024] * 4, H=32, dk=128, dv=128, dtype="bf16", init=True, g_mu=3.0, seed=5),
     "prefill_4k": dict(desc="B=4 T=4096 H=32 dk=dv=128 bf16, N(0,0.02) initial state",
                        lengths=[4096] * 4, H=32, dk=128, dv=128, dtype="bf16", init=True, g_mu=3.0, seed=1),
     "varlen_64": dict(desc="64 sequences, log-normal lengths (median 4096, sigma 0.5, clipped to"
