@@ -20,7 +20,7 @@ def test_exports_every_declared_symbol(lib):
     assert {"kda_chunk_fwd", "kda_decode_step", "kda_replay", "kda_device_status",
             "kda_chunk_fwd_workspace_size", "kda_status_string", "kda_version", "kda_chunk_fwd_prep",
             "kda_decode_step_prep", "kda_replay_prep", "kda_state_fork", "kda_state_offload",
-            "kda_state_restore", "kda_chunk_fwd_noalloc"} <= set(names)
+            "kda_state_restore", "kda_chunk_fwd_noalloc", "kda_chunk_bwd", "kda_chunk_bwd_workspace_size"} <= set(names)
     for n in names:
         assert hasattr(lib, n), n
 
@@ -126,3 +126,32 @@ def test_prep_flag_host_errors(lib):
     assert r(FAKE, 4, None, FAKE, FAKE, FAKE, FAKE, 0, FAKE, 2, 8, 2, 128, 128, 64, 1e-6, FAKE, 256, None) == 1
     assert r(FAKE, 4, None, FAKE, FAKE, FAKE, FAKE, 0, FAKE, 2, 8, 2, 128, 128, 15, -2.0, FAKE, 256, None) == 1
     assert r(FAKE, 4, None, FAKE, FAKE, FAKE, FAKE, 0, FAKE, 2, 8, 2, 128, 128, 15, 1e-6, None, 256, None) == 3
+
+
+def test_bwd_workspace_size_and_host_errors(lib):
+    """Backward workspace: header, checkpoints and records per (64-token slot, head),
+    staging states and the persistent-CTA scratch; host-detectable errors return early."""
+    from gated_linear_attention_chunk_gb300 import kda
+    small = kda.kda_chunk_bwd_workspace_size(1, 64, 1, 64, 64)
+    big = kda.kda_chunk_bwd_workspace_size(1, 6400, 1, 64, 64)
+    assert small > 256 and big > small
+    # 99 more slots, each a 64x64 checkpoint (16 KiB) and a record of the same size per slot
+    per_slot = (big - small) // 99
+    assert (big - small) % 99 == 0 and per_slot > 64 * 64 * 4
+    assert kda.kda_chunk_bwd_workspace_size(1, 64, 1, 96, 64) == 0
+    assert kda.kda_chunk_bwd_workspace_size(-1, 64, 1, 64, 64) == 0
+    b = lib.kda_chunk_bwd
+    args = lambda **kw: tuple(kw.get(n, d) for n, d in (
+        ("q", FAKE), ("k", FAKE), ("v", FAKE), ("g", FAKE), ("beta", FAKE), ("dtype", 0), ("init", None),
+        ("cu", None), ("N", 1), ("T", 64), ("H", 1), ("dk", 64), ("dv", 64), ("scale", 1.0), ("d_o", FAKE),
+        ("d_fin", None), ("dq", FAKE), ("dkk", FAKE), ("dvv", FAKE), ("dg", FAKE), ("db", FAKE), ("dinit", None),
+        ("ws", FAKE), ("wsb", small), ("stream", None)))
+    assert b(*args(dk=96)) == 2                   # UNSUPPORTED
+    assert b(*args(dtype=5)) == 2
+    assert b(*args(H=0)) == 1                     # INVALID_ARGUMENT
+    assert b(*args(d_o=None)) == 1
+    assert b(*args(dg=None)) == 1
+    assert b(*args(k=FAKE + 4)) == 1              # misaligned
+    assert b(*args(N=3, wsb=big)) == 1            # equal lengths need N | T
+    assert b(*args(ws=None)) == 3                 # WORKSPACE
+    assert b(*args(wsb=small - 1)) == 3
