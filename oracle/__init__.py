@@ -11,6 +11,8 @@ float64 (an exact upcast of bf16/fp32 data) and exposes:
 * ``forward``  -- packed varlen prefill: o and final state.
 * ``decode``   -- one token per sequence on a slot-indexed state pool.
 * ``replay``   -- accepted tokens re-applied to committed states (no output).
+* ``conv``     -- the short causal convolution (+ SiLU) of the input projections,
+  with the convolution state carried across calls.
 * ``backward`` -- gradients of a loss with respect to every input, given its
   gradients with respect to o and the final states (reverse mode of the same
   token-by-token recurrence).
@@ -70,6 +72,9 @@ def _load():
                                                 ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
                                                 ctypes.c_double, ctypes.c_int, dp, dp, dp, dp, dp, dp, dp, dp,
                                                 ctypes.c_int]
+            lib.kda_oracle_conv.restype = ctypes.c_int
+            lib.kda_oracle_conv.argtypes = [dp, dp, dp, ctypes.POINTER(ctypes.c_int64), ctypes.c_int64,
+                                            ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, dp, dp]
             lib.kda_oracle_max_threads.restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -209,3 +214,23 @@ def backward(q, k, v, g, beta, cu_seqlens, init_state, d_o, d_final=None, scale:
     if rc != 0:
         raise RuntimeError(f"kda_oracle_backward failed with code {rc}")
     return out
+
+
+def conv(x, w, cu_seqlens, state_in=None):
+    """Short causal depthwise convolution + SiLU (kda_oracle_conv).
+
+    x [T, H, C]; w [H, C, W]; state_in [N, W-1, H, C] (previous inputs, oldest first) or
+    None.  Returns ``(y [T, H, C], state_out [N, W-1, H, C])`` as float64 arrays."""
+    lib = _load()
+    x64, w64, s64 = _f64(x), _f64(w), _f64(state_in)
+    cu = np.ascontiguousarray(np.asarray(_f64(cu_seqlens), dtype=np.int64))
+    T, H, C = x64.shape
+    W = w64.shape[2]
+    N = cu.shape[0] - 1
+    y = np.zeros((T, H, C))
+    so = np.zeros((N, max(W - 1, 0), H, C))
+    rc = lib.kda_oracle_conv(_ptr(x64), _ptr(w64), _ptr(s64), cu.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)),
+                             N, H, C, W, _ptr(y), _ptr(so) if W > 1 else None)
+    if rc != 0:
+        raise RuntimeError(f"kda_oracle_conv failed with code {rc}")
+    return y, so

@@ -319,6 +319,66 @@ int kda_oracle_backward(const double *q, const double *k, const double *v, const
     return failed ? KDA_ORACLE_NO_MEMORY : KDA_ORACLE_OK;
 }
 
+/*
+ * Short causal convolution of the input projections, with the convolution state
+ * carried across calls.  "Kimi K3 on Fireworks: Fast RL at frontier scale"
+ * (disaggregated-serving paragraph) says a handoff must move KDA's recurrent
+ * and convolution state; the pages define neither.  The reading taken: a
+ * depthwise causal 1-D convolution of width W over the tokens of each sequence,
+ * one weight vector per channel, followed by SiLU:
+ *
+ *   pre_t[c] = sum_{i=0}^{W-1} w[h][c][i] * x_{t-(W-1)+i}[c],   y_t[c] = pre / (1 + exp(-pre))
+ *
+ * where tokens before the sequence's first come from its convolution state, the
+ * W-1 previous inputs oldest first (zeros when state_in is NULL).  state_out
+ * receives the last W-1 inputs of (state ++ tokens).
+ * Layouts: x, y [T, H, C]; w [H, C, W]; state [N, W-1, H, C].
+ */
+int kda_oracle_conv(const double *x, const double *w, const double *state_in, const int64_t *cu_seqlens,
+                    int64_t N, int64_t H, int64_t C, int64_t W, double *y, double *state_out)
+{
+    if (N < 0 || H <= 0 || C <= 0 || W < 1 || !x || !w || !y || !cu_seqlens) return KDA_ORACLE_BAD_ARGS;
+    for (int64_t n = 0; n < N; ++n) {
+        const int64_t bos = cu_seqlens[n], eos = cu_seqlens[n + 1];
+        if (eos < bos) return KDA_ORACLE_BAD_ARGS;
+        for (int64_t h = 0; h < H; ++h) {
+            for (int64_t c = 0; c < C; ++c) {
+                /* value of input j positions back from token t (j >= 1 may reach into the state) */
+                for (int64_t t = bos; t < eos; ++t) {
+                    double pre = 0.0;
+                    for (int64_t i = 0; i < W; ++i) {
+                        const int64_t src = t - (W - 1) + i;
+                        double xv;
+                        if (src >= bos)
+                            xv = x[(src * H + h) * C + c];
+                        else {
+                            const int64_t back = bos - src; /* 1 .. W-1 positions before the first token */
+                            xv = state_in ? state_in[((n * (W - 1) + (W - 1 - back)) * H + h) * C + c] : 0.0;
+                        }
+                        pre += w[(h * C + c) * W + i] * xv;
+                    }
+                    y[(t * H + h) * C + c] = pre / (1.0 + exp(-pre));
+                }
+                if (state_out) {
+                    for (int64_t j = 0; j < W - 1; ++j) {
+                        /* slot j of the new state: the input W-1-j positions before the end */
+                        const int64_t src = eos - (W - 1) + j;
+                        double xv;
+                        if (src >= bos)
+                            xv = x[(src * H + h) * C + c];
+                        else {
+                            const int64_t back = bos - src;
+                            xv = state_in ? state_in[((n * (W - 1) + (W - 1 - back)) * H + h) * C + c] : 0.0;
+                        }
+                        state_out[((n * (W - 1) + j) * H + h) * C + c] = xv;
+                    }
+                }
+            }
+        }
+    }
+    return KDA_ORACLE_OK;
+}
+
 /* Threads the OpenMP runtime would use by default (1 without OpenMP). */
 int kda_oracle_max_threads(void)
 {

@@ -504,3 +504,60 @@ def test_backward_is_linear_in_the_output_gradients_and_empty_sequences_pass_thr
         np.testing.assert_allclose(G2[key], -2.5 * G1[key], rtol=1e-12, atol=1e-12)
     # sequence 2 is empty: its initial-state gradient is the final-state gradient
     np.testing.assert_array_equal(G1["d_init"][2], Ws[2])
+
+
+# ------------------------------------------------------------------------------------------------
+# Short convolution of the input projections (depthwise, causal, width W, then SiLU), with
+# the convolution state carried across calls.
+# ------------------------------------------------------------------------------------------------
+
+def _silu(x):
+    return x / (1.0 + np.exp(-x))
+
+
+def test_conv_matches_numpy_convolve_per_channel():
+    """Each channel is numpy's valid-mode convolution of [state, x] with the reversed
+    weights (w[W-1] weighs the current token), one value per token, then SiLU."""
+    rng = np.random.default_rng(21)
+    lens, H, C, W = [7, 0, 3, 5], 2, 3, 4
+    T = sum(lens)
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int64)
+    x = rng.standard_normal((T, H, C))
+    w = rng.standard_normal((H, C, W))
+    st = rng.standard_normal((len(lens), W - 1, H, C))
+    y, so = oracle.conv(x, w, cu, st)
+    for n in range(len(lens)):
+        b, e = cu[n], cu[n + 1]
+        for h in range(H):
+            for c in range(C):
+                full = np.concatenate([st[n, :, h, c], x[b:e, h, c]])
+                ref = np.convolve(full, w[h, c, ::-1], mode="valid")   # one value per token
+                np.testing.assert_allclose(y[b:e, h, c], _silu(ref), rtol=1e-12, atol=1e-12)
+                np.testing.assert_array_equal(so[n, :, h, c], full[len(full) - (W - 1):])
+
+
+def test_conv_impulse_response_and_zero_state():
+    """A unit impulse at token 0 with no state gives SiLU(w reversed) on tokens 0..W-1, then SiLU(0) = 0."""
+    W, T = 4, 7
+    x = np.zeros((T, 1, 1))
+    x[0, 0, 0] = 1.0
+    w = np.array([[[0.5, -1.0, 2.0, 3.0]]])
+    y, so = oracle.conv(x, w, np.array([0, T]))
+    np.testing.assert_allclose(y[:W, 0, 0], _silu(w[0, 0, ::-1]), rtol=1e-14)
+    np.testing.assert_array_equal(y[W:, 0, 0], np.zeros(T - W))
+    np.testing.assert_array_equal(so[0, :, 0, 0], np.zeros(W - 1))
+
+
+def test_conv_state_carries_across_a_split():
+    """conv over a sequence == conv over its first part, then the rest from the carried state."""
+    rng = np.random.default_rng(22)
+    T, H, C, W = 11, 2, 5, 4
+    x = rng.standard_normal((T, H, C))
+    w = rng.standard_normal((H, C, W))
+    st = rng.standard_normal((1, W - 1, H, C))
+    y, so = oracle.conv(x, w, np.array([0, T]), st)
+    for cut in (1, 2, 3, 6):
+        y1, s1 = oracle.conv(x[:cut], w, np.array([0, cut]), st)
+        y2, s2 = oracle.conv(x[cut:], w, np.array([0, T - cut]), s1)
+        np.testing.assert_array_equal(np.concatenate([y1, y2]), y)
+        np.testing.assert_array_equal(s2, so)
