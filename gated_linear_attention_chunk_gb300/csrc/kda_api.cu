@@ -141,12 +141,14 @@ kda_status kda_chunk_fwd(const void *q, const void *k, const void *v, const void
                               0.f, o, final_state, workspace, ws_bytes, stream);
 }
 
-kda_status kda_decode_step_prep(const void *q, const void *k, const void *v, const void *g, const void *beta,
-                                kda_dtype dtype, float *state_pool, int64_t num_slots, const int32_t *slots,
-                                int N, int H, int dk, int dv, float scale, uint32_t prep, float l2_eps, void *o,
-                                void *workspace, size_t ws_bytes, void *stream) {
+static kda_status decode_impl(const void *q, const void *k, const void *v, const void *g, const void *beta,
+                              kda_dtype dtype, float *state_pool, int64_t num_slots, const int32_t *slots, int N,
+                              int H, int dk, int dv, float scale, uint32_t prep, float l2_eps, const float *conv_w,
+                              float *conv_pool, void *o, void *workspace, size_t ws_bytes, void *stream) {
     if (!dtype_ok(dtype) || !dim_ok(dk) || !dim_ok(dv)) return KDA_ERR_UNSUPPORTED;
     if (!prep_ok(prep, l2_eps)) return KDA_ERR_INVALID_ARGUMENT;
+    if (conv_w && (!conv_pool || !aligned_to(conv_w, 4) || !aligned_to(conv_pool, 4)))
+        return KDA_ERR_INVALID_ARGUMENT;
     if (N < 0 || H <= 0 || num_slots < 0) return KDA_ERR_INVALID_ARGUMENT;
     if (!workspace || !aligned16(workspace) || ws_bytes < KDA_WS_HEADER_BYTES) return KDA_ERR_WORKSPACE;
     if (N > 0) {
@@ -170,8 +172,28 @@ kda_status kda_decode_step_prep(const void *q, const void *k, const void *v, con
     sp.state_in = state_pool; sp.state_out = state_pool; sp.chunk_state = nullptr;
     sp.slots = slots; sp.num_slots = num_slots; sp.status = static_cast<uint32_t *>(workspace);
     sp.prep = static_cast<int>(prep); sp.prep_eps = l2_eps;
+    sp.conv_w = conv_w; sp.conv_state = conv_pool;
     if (kda::launch_seq(sp, dk, dv, static_cast<int>(dtype), s) != cudaSuccess) return KDA_ERR_CUDA;
     return KDA_OK;
+}
+
+kda_status kda_decode_step_prep(const void *q, const void *k, const void *v, const void *g, const void *beta,
+                                kda_dtype dtype, float *state_pool, int64_t num_slots, const int32_t *slots,
+                                int N, int H, int dk, int dv, float scale, uint32_t prep, float l2_eps, void *o,
+                                void *workspace, size_t ws_bytes, void *stream) {
+    return decode_impl(q, k, v, g, beta, dtype, state_pool, num_slots, slots, N, H, dk, dv, scale, prep, l2_eps,
+                       nullptr, nullptr, o, workspace, ws_bytes, stream);
+}
+
+kda_status kda_decode_step_conv(const void *q, const void *k, const void *v, const void *g, const void *beta,
+                                kda_dtype dtype, float *state_pool, int64_t num_slots, const int32_t *slots,
+                                int N, int H, int dk, int dv, float scale, const float *conv_weight,
+                                int conv_width, float *conv_pool, uint32_t prep, float l2_eps, void *o,
+                                void *workspace, size_t ws_bytes, void *stream) {
+    if (conv_width != KDA_CONV_WIDTH) return KDA_ERR_UNSUPPORTED;
+    if (!conv_weight || !conv_pool) return KDA_ERR_INVALID_ARGUMENT;
+    return decode_impl(q, k, v, g, beta, dtype, state_pool, num_slots, slots, N, H, dk, dv, scale, prep, l2_eps,
+                       conv_weight, conv_pool, o, workspace, ws_bytes, stream);
 }
 
 kda_status kda_decode_step(const void *q, const void *k, const void *v, const void *g, const void *beta,
@@ -182,12 +204,16 @@ kda_status kda_decode_step(const void *q, const void *k, const void *v, const vo
                                 o, workspace, ws_bytes, stream);
 }
 
-kda_status kda_replay_prep(float *state_pool, int64_t num_slots, const int32_t *slots, const void *k,
-                           const void *v, const void *g, const void *beta, kda_dtype dtype,
-                           const int32_t *cu_accept, int N, int64_t A_total, int H, int dk, int dv, uint32_t prep,
-                           float l2_eps, void *workspace, size_t ws_bytes, void *stream) {
+static kda_status replay_impl(float *state_pool, int64_t num_slots, const int32_t *slots, const void *q,
+                              const void *k, const void *v, const void *g, const void *beta, kda_dtype dtype,
+                              const int32_t *cu_accept, int N, int64_t A_total, int H, int dk, int dv,
+                              uint32_t prep, float l2_eps, const float *conv_w, float *conv_pool, void *workspace,
+                              size_t ws_bytes, void *stream) {
     if (!dtype_ok(dtype) || !dim_ok(dk) || !dim_ok(dv)) return KDA_ERR_UNSUPPORTED;
     if (!prep_ok(prep, l2_eps)) return KDA_ERR_INVALID_ARGUMENT;
+    if (conv_w && (!conv_pool || !aligned_to(conv_w, 4) || !aligned_to(conv_pool, 4)))
+        return KDA_ERR_INVALID_ARGUMENT;
+    if (conv_w && A_total > 0 && (!q || !aligned16(q))) return KDA_ERR_INVALID_ARGUMENT;
     if (N < 0 || A_total < 0 || H <= 0 || num_slots < 0) return KDA_ERR_INVALID_ARGUMENT;
     if (!workspace || !aligned16(workspace) || ws_bytes < KDA_WS_HEADER_BYTES) return KDA_ERR_WORKSPACE;
     if (N > 0) {
@@ -206,14 +232,66 @@ kda_status kda_replay_prep(float *state_pool, int64_t num_slots, const int32_t *
     if (st != KDA_OK || N == 0) return st;
 
     kda::SeqParams sp{};
-    sp.q = nullptr; sp.k = k; sp.v = v; sp.g = g; sp.beta = beta; sp.o = nullptr;
+    sp.q = conv_w ? q : nullptr; sp.k = k; sp.v = v; sp.g = g; sp.beta = beta; sp.o = nullptr;
     sp.N = N; sp.H = H; sp.scale = 1.0f;
     sp.mode = kda::SEQ_MODE_REPLAY;
     sp.cu = cu_accept; sp.T_total = A_total; sp.seq_len_fixed = 0; sp.chunk_skip = 0;
     sp.state_in = state_pool; sp.state_out = state_pool; sp.chunk_state = nullptr;
     sp.slots = slots; sp.num_slots = num_slots; sp.status = static_cast<uint32_t *>(workspace);
     sp.prep = static_cast<int>(prep & ~static_cast<uint32_t>(KDA_PREP_L2NORM_Q)); sp.prep_eps = l2_eps;  // no q in replay
+    sp.conv_w = conv_w; sp.conv_state = conv_pool;  // q only advances the convolution state
     if (kda::launch_seq(sp, dk, dv, static_cast<int>(dtype), s) != cudaSuccess) return KDA_ERR_CUDA;
+    return KDA_OK;
+}
+
+kda_status kda_replay_prep(float *state_pool, int64_t num_slots, const int32_t *slots, const void *k,
+                           const void *v, const void *g, const void *beta, kda_dtype dtype,
+                           const int32_t *cu_accept, int N, int64_t A_total, int H, int dk, int dv, uint32_t prep,
+                           float l2_eps, void *workspace, size_t ws_bytes, void *stream) {
+    return replay_impl(state_pool, num_slots, slots, nullptr, k, v, g, beta, dtype, cu_accept, N, A_total, H, dk, dv,
+                       prep, l2_eps, nullptr, nullptr, workspace, ws_bytes, stream);
+}
+
+kda_status kda_replay_conv(float *state_pool, int64_t num_slots, const int32_t *slots, const void *q, const void *k,
+                           const void *v, const void *g, const void *beta, kda_dtype dtype,
+                           const int32_t *cu_accept, int N, int64_t A_total, int H, int dk, int dv,
+                           const float *conv_weight, int conv_width, float *conv_pool, uint32_t prep, float l2_eps,
+                           void *workspace, size_t ws_bytes, void *stream) {
+    if (conv_width != KDA_CONV_WIDTH) return KDA_ERR_UNSUPPORTED;
+    if (!conv_weight || !conv_pool) return KDA_ERR_INVALID_ARGUMENT;
+    return replay_impl(state_pool, num_slots, slots, q, k, v, g, beta, dtype, cu_accept, N, A_total, H, dk, dv, prep,
+                       l2_eps, conv_weight, conv_pool, workspace, ws_bytes, stream);
+}
+
+kda_status kda_conv_fwd(const void *q, const void *k, const void *v, kda_dtype dtype, const float *conv_weight,
+                        int conv_width, const float *conv_state_in, const int32_t *cu_seqlens, int N, int64_t T_total,
+                        int H, int dk, int dv, void *q_out, void *k_out, void *v_out, float *conv_state_out,
+                        void *workspace, size_t ws_bytes, void *stream) {
+    if (!dtype_ok(dtype) || !dim_ok(dk) || !dim_ok(dv) || conv_width != KDA_CONV_WIDTH) return KDA_ERR_UNSUPPORTED;
+    if (N < 0 || T_total < 0 || H <= 0) return KDA_ERR_INVALID_ARGUMENT;
+    if (!workspace || !aligned16(workspace) || ws_bytes < KDA_WS_HEADER_BYTES) return KDA_ERR_WORKSPACE;
+    if (!conv_weight || !aligned_to(conv_weight, 4)) return KDA_ERR_INVALID_ARGUMENT;
+    const size_t es = elem_size(dtype);
+    if (T_total > 0) {
+        if (!q || !k || !v || !q_out || !k_out || !v_out) return KDA_ERR_INVALID_ARGUMENT;
+        for (const void *ptr : {q, k, v, static_cast<const void *>(q_out), static_cast<const void *>(k_out),
+                                static_cast<const void *>(v_out)})
+            if (!aligned_to(ptr, es)) return KDA_ERR_INVALID_ARGUMENT;
+    }
+    if ((conv_state_in && !aligned_to(conv_state_in, 4)) || (conv_state_out && !aligned_to(conv_state_out, 4)))
+        return KDA_ERR_INVALID_ARGUMENT;
+    if (!cu_seqlens && N > 0 && (T_total % N) != 0) return KDA_ERR_INVALID_ARGUMENT;
+    if (!cu_seqlens && N == 0 && T_total != 0) return KDA_ERR_INVALID_ARGUMENT;
+    if (cu_seqlens && !aligned_to(cu_seqlens, 4)) return KDA_ERR_INVALID_ARGUMENT;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    kda_status st = clear_status(workspace, s);
+    if (st != KDA_OK || N == 0) return st;
+    kda::ConvParams cp{};
+    cp.q = q; cp.k = k; cp.v = v; cp.q_out = q_out; cp.k_out = k_out; cp.v_out = v_out;
+    cp.weight = conv_weight; cp.state_in = conv_state_in; cp.state_out = conv_state_out;
+    cp.cu = cu_seqlens; cp.T_total = T_total; cp.seq_len_fixed = cu_seqlens ? 0 : T_total / N;
+    cp.N = N; cp.H = H; cp.dk = dk; cp.dv = dv; cp.status = static_cast<uint32_t *>(workspace);
+    if (kda::launch_conv(cp, static_cast<int>(dtype), s) != cudaSuccess) return KDA_ERR_CUDA;
     return KDA_OK;
 }
 

@@ -45,7 +45,31 @@ struct SeqParams {
     // prefill only, or null: the state at the start of every 64-token chunk of sequence n
     // goes to slot (ckpt_base(n) + c) * H + h, ckpt_base(n) = floor(first token / 64) + n
     float *ckpt;
+    // decode / replay only, or null: short convolution of q, k, v (width kConvW, then SiLU)
+    // before everything else, weights [H, 2dk + dv, kConvW], states [slots, kConvW - 1, H,
+    // 2dk + dv] indexed like the recurrent pool and updated in place
+    const float *conv_w;
+    float *conv_state;
 };
+
+// Width of the short convolution of the input projections (kda_conv.cu).
+constexpr int kConvW = 4;
+
+// Prefill form of the short convolution: q, k, v -> q_out, k_out, v_out (same dtype),
+// state_in / state_out [N, kConvW - 1, H, 2dk + dv] fp32 (either may be null; they may be
+// the same buffer).
+struct ConvParams {
+    const void *q, *k, *v;
+    void *q_out, *k_out, *v_out;
+    const float *weight;        // [H, 2dk + dv, kConvW]
+    const float *state_in;
+    float *state_out;
+    const int32_t *cu;
+    int64_t T_total, seq_len_fixed;
+    int N, H, dk, dv;
+    uint32_t *status;
+};
+cudaError_t launch_conv(const ConvParams &p, int dtype, cudaStream_t stream);
 
 // First checkpoint slot of a sequence starting at token `bos` (sequence index n): the
 // ranges [base, base + ceil(len / 64)) of consecutive sequences do not overlap, and

@@ -132,6 +132,7 @@ __global__ void __launch_bounds__(kSeqThreads, 6) kda_seq_kernel(SeqParams p) {
     int64_t t0, t1;
     const float *src;
     float *dst;
+    float *cst = nullptr;  // this sequence's short-convolution state (decode / replay with conv_w)
     if (p.mode == SEQ_MODE_DECODE) {
         t0 = n;
         t1 = n + 1;
@@ -168,6 +169,9 @@ __global__ void __launch_bounds__(kSeqThreads, 6) kda_seq_kernel(SeqParams p) {
         }
         src = p.state_in + (slot * H + h) * DK * DV;
         dst = p.state_out + (slot * H + h) * DK * DV;
+        if constexpr (PREP) {
+            if (p.conv_w) cst = p.conv_state + slot * (kConvW - 1) * H * (2 * DK + DV);
+        }
     }
 
     const Tin *Q = static_cast<const Tin *>(p.q);
@@ -191,7 +195,7 @@ __global__ void __launch_bounds__(kSeqThreads, 6) kda_seq_kernel(SeqParams p) {
             const int64_t base = (t * H + h) * DK + tid;
             rg = ld_in(G, base);
             rk = ld_in(K, base);
-            if (WRITE_O) rq = ld_in(Q, base);
+            if (WRITE_O || (PREP && cst)) rq = ld_in(Q, base);
         }
         if (tid < CB) rv = ld_in(V, (t * H + h) * DV + col0 + tid);
         if (tid == kSeqThreads - 1) rb = ld_in(B, t * H + h);
@@ -200,7 +204,49 @@ __global__ void __launch_bounds__(kSeqThreads, 6) kda_seq_kernel(SeqParams p) {
     // sigmoid(x_beta), and k / q rows divided by sqrt(sum of squares + eps); the row sums
     // are reduced here per warp (a xor butterfly gives every lane the same bits) and the
     // inverse norms are applied where k and q are read.
+    // Short convolution (extended instance, decode / replay with conv_w): each thread keeps
+    // its channel's last kConvW - 1 raw inputs and the kConvW weights in registers; the sum
+    // runs oldest first with round-to-nearest multiply-adds, then SiLU.
+    constexpr int Ct = 2 * DK + DV;
+    float hq[kConvW - 1], hk[kConvW - 1], hv[kConvW - 1], wq[kConvW], wk[kConvW], wv[kConvW];
+    if constexpr (PREP) {
+        if (cst) {
+#pragma unroll
+            for (int j = 0; j < kConvW - 1; ++j) {
+                const float *row = cst + (static_cast<int64_t>(j) * H + h) * Ct;
+                hq[j] = tid < DK ? row[tid] : 0.f;
+                hk[j] = tid < DK ? row[DK + tid] : 0.f;
+                hv[j] = tid < CB ? row[2 * DK + col0 + tid] : 0.f;
+            }
+            const float *wrow = p.conv_w + static_cast<int64_t>(h) * Ct * kConvW;
+#pragma unroll
+            for (int i = 0; i < kConvW; ++i) {
+                wq[i] = tid < DK ? wrow[tid * kConvW + i] : 0.f;
+                wk[i] = tid < DK ? wrow[(DK + tid) * kConvW + i] : 0.f;
+                wv[i] = tid < CB ? wrow[(2 * DK + col0 + tid) * kConvW + i] : 0.f;
+            }
+        }
+    }
+    auto conv_step = [&](float (&hist)[kConvW - 1], const float (&w)[kConvW], float x) {
+        float pre = 0.f;
+#pragma unroll
+        for (int i = 0; i < kConvW - 1; ++i) pre = __fmaf_rn(w[i], hist[i], pre);
+        pre = __fmaf_rn(w[kConvW - 1], x, pre);
+#pragma unroll
+        for (int i = 0; i < kConvW - 2; ++i) hist[i] = hist[i + 1];
+        hist[kConvW - 2] = x;
+        return __fdiv_rn(pre, __fadd_rn(1.f, expf(-pre)));
+    };
     auto stage = [&](int buf, float rg, float rk, float rq, float rv, float rb) {
+        if constexpr (PREP) {
+            if (cst) {
+                if (tid < DK) {
+                    rq = conv_step(hq, wq, rq);
+                    rk = conv_step(hk, wk, rk);
+                }
+                if (tid < CB) rv = conv_step(hv, wv, rv);
+            }
+        }
         if (tid < DK) {
             tok_a[buf][tid] = (PREP && (p.prep & PREP_SIGMOID_GATE)) ? __fdiv_rn(1.f, __fadd_rn(1.f, expf(-rg)))
                                                                        : expf(rg);
@@ -334,6 +380,19 @@ __global__ void __launch_bounds__(kSeqThreads, 6) kda_seq_kernel(SeqParams p) {
         }
     }
 
+    if constexpr (PREP) {  // the advanced convolution state (q, k once per head; v per column block)
+        if (cst) {
+#pragma unroll
+            for (int j = 0; j < kConvW - 1; ++j) {
+                float *row = cst + (static_cast<int64_t>(j) * H + h) * Ct;
+                if (tid < DK && cb == 0) {
+                    row[tid] = hq[j];
+                    row[DK + tid] = hk[j];
+                }
+                if (tid < CB) row[2 * DK + col0 + tid] = hv[j];
+            }
+        }
+    }
     if (dst) {
 #pragma unroll
         for (int s = 0; s < NS; ++s) {
@@ -350,12 +409,12 @@ cudaError_t launch_typed(const SeqParams &p, cudaStream_t stream) {
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     const dim3 grid(static_cast<unsigned>(blocks));
     if (p.o) {
-        if (p.prep || p.ckpt)
+        if (p.prep || p.ckpt || p.conv_w)
             kda_seq_kernel<DK, DV, Tin, true, true><<<grid, kSeqThreads, 0, stream>>>(p);
         else
             kda_seq_kernel<DK, DV, Tin, true, false><<<grid, kSeqThreads, 0, stream>>>(p);
     } else {
-        if (p.prep || p.ckpt)
+        if (p.prep || p.ckpt || p.conv_w)
             kda_seq_kernel<DK, DV, Tin, false, true><<<grid, kSeqThreads, 0, stream>>>(p);
         else
             kda_seq_kernel<DK, DV, Tin, false, false><<<grid, kSeqThreads, 0, stream>>>(p);

@@ -36,6 +36,7 @@ KDA_PREP_L2NORM_Q = 1
 KDA_PREP_L2NORM_K = 2
 KDA_PREP_SIGMOID_GATE = 4
 KDA_PREP_SIGMOID_BETA = 8
+KDA_CONV_WIDTH = 4
 
 _vp = ctypes.c_void_p
 _i64 = ctypes.c_int64
@@ -59,6 +60,13 @@ _SIGS = {
     "kda_chunk_bwd_workspace_size": (ctypes.c_size_t, [_int, _i64, _int, _int, _int]),
     "kda_chunk_bwd": (_int, [_vp, _vp, _vp, _vp, _vp, _int, _vp, _vp, _int, _i64, _int, _int, _int, ctypes.c_float,
                              _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp]),
+    "kda_conv_fwd": (_int, [_vp, _vp, _vp, _int, _vp, _int, _vp, _vp, _int, _i64, _int, _int, _int, _vp, _vp, _vp,
+                            _vp, _vp, ctypes.c_size_t, _vp]),
+    "kda_decode_step_conv": (_int, [_vp, _vp, _vp, _vp, _vp, _int, _vp, _i64, _vp, _int, _int, _int, _int,
+                                    ctypes.c_float, _vp, _int, _vp, ctypes.c_uint32, ctypes.c_float, _vp, _vp,
+                                    ctypes.c_size_t, _vp]),
+    "kda_replay_conv": (_int, [_vp, _i64, _vp, _vp, _vp, _vp, _vp, _vp, _int, _vp, _int, _i64, _int, _int, _int,
+                               _vp, _int, _vp, ctypes.c_uint32, ctypes.c_float, _vp, ctypes.c_size_t, _vp]),
     "kda_device_status": (_int, [_vp, _vp]),
     "kda_status_string": (ctypes.c_char_p, [_int]),
     "kda_version": (_int, []),
@@ -364,6 +372,105 @@ def kda_chunk_bwd(q, k, v, g, beta, d_o, cu_seqlens=None, init_state=None, d_fin
                            workspace.numel() * workspace.element_size(), _stream_handle(stream))
     _check(rc, "kda_chunk_bwd")
     return out
+
+
+def _conv_check(conv_weight, H, dk, dv):
+    _need(conv_weight, "conv_weight", torch.float32, (H, 2 * dk + dv, KDA_CONV_WIDTH))
+
+
+def kda_conv_fwd(q, k, v, conv_weight, cu_seqlens=None, conv_state_in=None, conv_state_out=None,
+                 want_state: bool = True, workspace=None, stream=None):
+    """Short causal convolution (width 4) + SiLU of the raw projections q, k, v [T, H, d].
+    conv_weight [H, 2dk+dv, 4] fp32 (channels q | k | v); conv_state_in / out [N, 3, H, 2dk+dv]
+    fp32.  Returns ``(q_out, k_out, v_out, conv_state_out)``."""
+    lib = load_library()
+    dt = q.dtype
+    T, H, dk = q.shape
+    dv = v.shape[2]
+    for name, t, shp in (("q", q, (T, H, dk)), ("k", k, (T, H, dk)), ("v", v, (T, H, dv))):
+        _need(t, name, dt, shp)
+    _conv_check(conv_weight, H, dk, dv)
+    N = 1 if cu_seqlens is None else cu_seqlens.numel() - 1
+    if cu_seqlens is not None:
+        _need(cu_seqlens, "cu_seqlens", torch.int32)
+    cs = (N, KDA_CONV_WIDTH - 1, H, 2 * dk + dv)
+    if conv_state_in is not None:
+        _need(conv_state_in, "conv_state_in", torch.float32, cs)
+    if conv_state_out is None and want_state:
+        conv_state_out = torch.empty(cs, dtype=torch.float32, device=q.device)
+    if conv_state_out is not None:
+        _need(conv_state_out, "conv_state_out", torch.float32, cs)
+    qo, ko, vo = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    if workspace is None:
+        workspace = new_workspace(KDA_WS_HEADER_BYTES, q.device)
+    rc = lib.kda_conv_fwd(_ptr(q), _ptr(k), _ptr(v), _dtype_code(q), _ptr(conv_weight), KDA_CONV_WIDTH,
+                          _ptr(conv_state_in), _ptr(cu_seqlens), N, T, H, dk, dv, _ptr(qo), _ptr(ko), _ptr(vo),
+                          _ptr(conv_state_out), _ptr(workspace), workspace.numel() * workspace.element_size(),
+                          _stream_handle(stream))
+    _check(rc, "kda_conv_fwd")
+    return qo, ko, vo, conv_state_out
+
+
+def kda_decode_step_conv(q, k, v, g, beta, state_pool, conv_weight, conv_pool, prep: int = 0,
+                         l2_eps: float = 1e-6, slots=None, scale: float = 1.0, o=None, workspace=None,
+                         stream=None) -> torch.Tensor:
+    """kda_decode_step on raw projections with the short convolution fused (conv_pool
+    [S, 3, H, 2dk+dv] fp32, advanced in place) and optional KDA_PREP_* flags."""
+    lib = load_library()
+    dt = q.dtype
+    N, H, dk = q.shape
+    dv = v.shape[2]
+    for name, t, shp in (("q", q, (N, H, dk)), ("k", k, (N, H, dk)), ("v", v, (N, H, dv)),
+                         ("g", g, (N, H, dk)), ("beta", beta, (N, H))):
+        _need(t, name, dt, shp)
+    _need(state_pool, "state_pool", torch.float32)
+    if tuple(state_pool.shape[1:]) != (H, dk, dv):
+        raise ValueError(f"state_pool shape {tuple(state_pool.shape)} != [S, {H}, {dk}, {dv}]")
+    _conv_check(conv_weight, H, dk, dv)
+    _need(conv_pool, "conv_pool", torch.float32, (state_pool.shape[0], KDA_CONV_WIDTH - 1, H, 2 * dk + dv))
+    if slots is not None:
+        _need(slots, "slots", torch.int32, (N,))
+    if o is None:
+        o = torch.empty(N, H, dv, dtype=dt, device=q.device)
+    _need(o, "o", dt, (N, H, dv))
+    if workspace is None:
+        workspace = new_workspace(KDA_WS_HEADER_BYTES, q.device)
+    rc = lib.kda_decode_step_conv(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _dtype_code(q), _ptr(state_pool),
+                                  state_pool.shape[0], _ptr(slots), N, H, dk, dv, float(scale), _ptr(conv_weight),
+                                  KDA_CONV_WIDTH, _ptr(conv_pool), int(prep), float(l2_eps), _ptr(o),
+                                  _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                  _stream_handle(stream))
+    _check(rc, "kda_decode_step_conv")
+    return o
+
+
+def kda_replay_conv(state_pool, q, k, v, g, beta, cu_accept, conv_weight, conv_pool, prep: int = 0,
+                    l2_eps: float = 1e-6, slots=None, workspace=None, stream=None) -> None:
+    """kda_replay on raw projections with the short convolution fused: the accepted
+    tokens' q, k, v advance conv_pool and their convolved k, v the recurrent states."""
+    lib = load_library()
+    dt = k.dtype
+    A, H, dk = k.shape
+    dv = v.shape[2]
+    for name, t, shp in (("q", q, (A, H, dk)), ("k", k, (A, H, dk)), ("v", v, (A, H, dv)),
+                         ("g", g, (A, H, dk)), ("beta", beta, (A, H))):
+        _need(t, name, dt, shp)
+    _need(cu_accept, "cu_accept", torch.int32)
+    N = cu_accept.numel() - 1
+    _need(state_pool, "state_pool", torch.float32)
+    if tuple(state_pool.shape[1:]) != (H, dk, dv):
+        raise ValueError(f"state_pool shape {tuple(state_pool.shape)} != [S, {H}, {dk}, {dv}]")
+    _conv_check(conv_weight, H, dk, dv)
+    _need(conv_pool, "conv_pool", torch.float32, (state_pool.shape[0], KDA_CONV_WIDTH - 1, H, 2 * dk + dv))
+    if slots is not None:
+        _need(slots, "slots", torch.int32, (N,))
+    if workspace is None:
+        workspace = new_workspace(KDA_WS_HEADER_BYTES, k.device)
+    rc = lib.kda_replay_conv(_ptr(state_pool), state_pool.shape[0], _ptr(slots), _ptr(q), _ptr(k), _ptr(v), _ptr(g),
+                             _ptr(beta), _dtype_code(k), _ptr(cu_accept), N, A, H, dk, dv, _ptr(conv_weight),
+                             KDA_CONV_WIDTH, _ptr(conv_pool), int(prep), float(l2_eps), _ptr(workspace),
+                             workspace.numel() * workspace.element_size(), _stream_handle(stream))
+    _check(rc, "kda_replay_conv")
 
 
 def _pool_shape(state_pool):

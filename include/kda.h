@@ -262,6 +262,50 @@ kda_status kda_chunk_bwd(const void *q, const void *k, const void *v, const void
                          float *d_init_state, void *workspace, size_t ws_bytes, void *stream);
 
 /*
+ * Short convolution of the input projections, with its state carried across calls
+ * (the disaggregated-serving paragraph of "Kimi K3 on Fireworks: Fast RL at
+ * frontier scale" lists KDA's convolution state beside its recurrent state; the
+ * pages define neither).  The reading implemented: a depthwise causal convolution
+ * of width KDA_CONV_WIDTH over the tokens of each sequence, one weight vector per
+ * channel, then SiLU:
+ *   pre_t[c] = sum_{i=0}^{3} w[h][c][i] x_{t-3+i}[c],   y_t[c] = pre / (1 + exp(-pre)),
+ * applied to q, k and v before everything else (the _prep flags act on its output).
+ * Channels of a head are packed (q 0..dk-1 | k dk..2dk-1 | v 2dk..2dk+dv-1):
+ *   conv_weight [H, 2dk+dv, KDA_CONV_WIDTH] fp32;
+ *   a convolution state [KDA_CONV_WIDTH-1, H, 2dk+dv] fp32 per sequence holds its
+ *   previous raw inputs, oldest first (zeros for a new sequence).
+ *
+ * kda_conv_fwd: the prefill form.  q, k, v [T_total, H, d] raw -> q_out, k_out,
+ * v_out (same dtype and layout; then call kda_chunk_fwd(_prep) on them);
+ * conv_state_in / conv_state_out [N, 3, H, 2dk+dv] (either NULL = zeros / not
+ * written; they may be the same buffer).
+ * kda_decode_step_conv / kda_replay_conv: the decode and replay forms, the
+ * convolution fused into the token-sequential kernel; conv_pool [num_slots, 3, H,
+ * 2dk+dv] is indexed by the same slots as state_pool and advanced in place.  Replay
+ * takes q too: the accepted tokens' q advances the convolution state.
+ * conv_width must be KDA_CONV_WIDTH (else KDA_ERR_UNSUPPORTED); other errors as
+ * for the calls without convolution.
+ */
+#define KDA_CONV_WIDTH 4
+
+kda_status kda_conv_fwd(const void *q, const void *k, const void *v, kda_dtype dtype, const float *conv_weight,
+                        int conv_width, const float *conv_state_in, const int32_t *cu_seqlens, int N, int64_t T_total,
+                        int H, int dk, int dv, void *q_out, void *k_out, void *v_out, float *conv_state_out,
+                        void *workspace, size_t ws_bytes, void *stream);
+
+kda_status kda_decode_step_conv(const void *q, const void *k, const void *v, const void *g, const void *beta,
+                                kda_dtype dtype, float *state_pool, int64_t num_slots, const int32_t *slots,
+                                int N, int H, int dk, int dv, float scale, const float *conv_weight,
+                                int conv_width, float *conv_pool, uint32_t prep, float l2_eps, void *o,
+                                void *workspace, size_t ws_bytes, void *stream);
+
+kda_status kda_replay_conv(float *state_pool, int64_t num_slots, const int32_t *slots, const void *q, const void *k,
+                           const void *v, const void *g, const void *beta, kda_dtype dtype,
+                           const int32_t *cu_accept, int N, int64_t A_total, int H, int dk, int dv,
+                           const float *conv_weight, int conv_width, float *conv_pool, uint32_t prep, float l2_eps,
+                           void *workspace, size_t ws_bytes, void *stream);
+
+/*
  * Synchronizes `stream`, then reads the device status word of `workspace`
  * (errors from the last call that used it).  Returns KDA_OK or the first of
  * BAD_SEQLENS, BAD_SLOT, GATE_RANGE, TIMEOUT that was raised; KDA_ERR_CUDA if

@@ -20,7 +20,8 @@ def test_exports_every_declared_symbol(lib):
     assert {"kda_chunk_fwd", "kda_decode_step", "kda_replay", "kda_device_status",
             "kda_chunk_fwd_workspace_size", "kda_status_string", "kda_version", "kda_chunk_fwd_prep",
             "kda_decode_step_prep", "kda_replay_prep", "kda_state_fork", "kda_state_offload",
-            "kda_state_restore", "kda_chunk_fwd_noalloc", "kda_chunk_bwd", "kda_chunk_bwd_workspace_size"} <= set(names)
+            "kda_state_restore", "kda_chunk_fwd_noalloc", "kda_chunk_bwd", "kda_chunk_bwd_workspace_size", "kda_conv_fwd", "kda_decode_step_conv",
+            "kda_replay_conv"} <= set(names)
     for n in names:
         assert hasattr(lib, n), n
 
@@ -155,3 +156,27 @@ def test_bwd_workspace_size_and_host_errors(lib):
     assert b(*args(N=3, wsb=big)) == 1            # equal lengths need N | T
     assert b(*args(ws=None)) == 3                 # WORKSPACE
     assert b(*args(wsb=small - 1)) == 3
+
+
+def test_conv_host_errors(lib):
+    """The convolution calls reject a width other than KDA_CONV_WIDTH and missing weights on the host."""
+    c = lib.kda_conv_fwd
+    base = dict(q=FAKE, k=FAKE, v=FAKE, dtype=0, w=FAKE, width=4, sin=None, cu=None, N=1, T=8, H=1, dk=64, dv=64,
+                qo=FAKE, ko=FAKE, vo=FAKE, sout=None, ws=FAKE, wsb=256, stream=None)
+    call = lambda **kw: c(*({**base, **kw}).values())
+    assert call(width=3) == 2                    # UNSUPPORTED
+    assert call(dk=96) == 2
+    assert call(w=None) == 1                     # INVALID_ARGUMENT
+    assert call(qo=None) == 1
+    assert call(N=3) == 1                        # equal lengths need N | T
+    assert call(ws=None) == 3                    # WORKSPACE
+    d = lib.kda_decode_step_conv
+    assert d(FAKE, FAKE, FAKE, FAKE, FAKE, 0, FAKE, 4, None, 2, 2, 128, 128, 1.0, FAKE, 5, FAKE, 0, 0.0, FAKE,
+             FAKE, 256, None) == 2
+    assert d(FAKE, FAKE, FAKE, FAKE, FAKE, 0, FAKE, 4, None, 2, 2, 128, 128, 1.0, None, 4, FAKE, 0, 0.0, FAKE,
+             FAKE, 256, None) == 1
+    r = lib.kda_replay_conv
+    assert r(FAKE, 4, None, FAKE, FAKE, FAKE, FAKE, FAKE, 0, FAKE, 2, 8, 2, 128, 128, FAKE, 4, None, 0, 0.0, FAKE,
+             256, None) == 1
+    assert r(FAKE, 4, None, None, FAKE, FAKE, FAKE, FAKE, 0, FAKE, 2, 8, 2, 128, 128, FAKE, 4, FAKE, 0, 0.0, FAKE,
+             256, None) == 1                     # the accepted tokens' q is needed for the convolution state
