@@ -253,12 +253,20 @@ def measure_state_kernels(kda, dev, hbm_peak, n_seq=128, H=32, d=128, reps=50):
     cu = torch.arange(0, 4 * n_seq + 1, 4, dtype=torch.int32, device=dev)
     state_bytes = 2 * pool.numel() * 4
     out = {}
-    for name in ("decode", "replay"):
+    # the same with the short convolution fused (raw projections, every preprocessing flag)
+    cw = torch.randn(H, 3 * d, kda.KDA_CONV_WIDTH, device=dev) * 0.5
+    cpool = torch.zeros(n_seq, kda.KDA_CONV_WIDTH - 1, H, 3 * d, device=dev)
+    for name in ("decode", "replay", "decode_conv", "replay_conv"):
         def call():
             if name == "decode":
                 kda.kda_decode_step(q[:n_seq], k[:n_seq], v[:n_seq], g[:n_seq], b[:n_seq], pool, o=o, workspace=ws)
-            else:
+            elif name == "replay":
                 kda.kda_replay(pool, k, v, g, b, cu, workspace=ws)
+            elif name == "decode_conv":
+                kda.kda_decode_step_conv(q[:n_seq], k[:n_seq], v[:n_seq], g[:n_seq], b[:n_seq], pool, cw, cpool,
+                                         prep=15, o=o, workspace=ws)
+            else:
+                kda.kda_replay_conv(pool, q, k, v, g, b, cu, cw, cpool, prep=15, workspace=ws)
         for _ in range(3):
             call()
         torch.cuda.synchronize()
@@ -270,10 +278,12 @@ def measure_state_kernels(kda, dev, hbm_peak, n_seq=128, H=32, d=128, reps=50):
         e1.record(st)
         torch.cuda.synchronize()
         ms = e0.elapsed_time(e1) / reps
-        tok_bytes = (n_seq if name == "decode" else 4 * n_seq) * H * (4 * d * 2 + 2)
-        gbs = (state_bytes + tok_bytes) / (ms / 1e3) / 1e9
+        ntok = n_seq if name.startswith("decode") else 4 * n_seq
+        tok_bytes = ntok * H * (4 * d * 2 + 2) + (ntok * H * d * 2 if name == "replay_conv" else 0)  # + q
+        conv_bytes = 2 * cpool.numel() * 4 if name.endswith("conv") else 0
+        gbs = (state_bytes + conv_bytes + tok_bytes) / (ms / 1e3) / 1e9
         out[name] = {"ms_per_call": ms, "achieved_GBs": gbs, "frac_of_hbm": gbs / hbm_peak,
-                     "states": n_seq * H, "tokens_per_seq": 1 if name == "decode" else 4}
+                     "states": n_seq * H, "tokens_per_seq": 1 if name.startswith("decode") else 4}
     # state-pool operations on the same pool: fork half the slots onto the other half
     # (read + write of 64 states x H heads), offload them to pinned host memory (write)
     half = n_seq // 2
@@ -302,6 +312,45 @@ def measure_state_kernels(kda, dev, hbm_peak, n_seq=128, H=32, d=128, reps=50):
     if kda.kda_device_status(ws) != kda.KDA_OK:
         raise RuntimeError("decode/replay/pool device status")
     return out
+
+
+def measure_conv(kda, case, dev, hbm_peak, reps=20):
+    """kda_conv_fwd (short convolution + SiLU of q, k, v) on the same workload: q, k, v
+    read and written once, plus the convolution states read and written."""
+    q, k, v = (x.to(dev) for x in (case.q, case.k, case.v))
+    cu = case.cu_seqlens.to(dev)
+    H, dk, dv = case.H, case.dk, case.dv
+    w = torch.randn(H, 2 * dk + dv, kda.KDA_CONV_WIDTH, device=dev) * 0.5
+    st = torch.zeros(case.N, kda.KDA_CONV_WIDTH - 1, H, 2 * dk + dv, device=dev)
+    ws = kda.new_workspace(kda.KDA_WS_HEADER_BYTES, dev)
+    outs = (torch.empty_like(q), torch.empty_like(k), torch.empty_like(v))
+
+    def call():
+        lib = kda.load_library()
+        rc = lib.kda_conv_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), 0 if q.dtype == torch.bfloat16 else 1,
+                              w.data_ptr(), kda.KDA_CONV_WIDTH, st.data_ptr(), cu.data_ptr(), case.N, case.T_total,
+                              H, dk, dv, outs[0].data_ptr(), outs[1].data_ptr(), outs[2].data_ptr(), st.data_ptr(),
+                              ws.data_ptr(), ws.numel(), torch.cuda.current_stream().cuda_stream)
+        if rc != 0:
+            raise RuntimeError(f"kda_conv_fwd: {kda.kda_status_string(rc)}")
+
+    for _ in range(3):
+        call()
+    torch.cuda.synchronize()
+    st_ = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(st_)
+    for _ in range(reps):
+        call()
+    e1.record(st_)
+    torch.cuda.synchronize()
+    if kda.kda_device_status(ws) != kda.KDA_OK:
+        raise RuntimeError("conv device status")
+    ms = e0.elapsed_time(e1) / reps
+    nbytes = 2 * case.T_total * H * (2 * dk + dv) * q.element_size() + 2 * st.numel() * 4
+    gbs = nbytes / (ms / 1e3) / 1e9
+    return {"ms_per_call": ms, "achieved_GBs": gbs, "frac_of_hbm": gbs / hbm_peak, "algorithmic_bytes": nbytes,
+            "launches_per_call": 2}
 
 
 def measure_backward(kda, case, dev, hbm_peak, reps=3):
@@ -484,6 +533,7 @@ def run_gpu(args, world, rank, local):
 
     state_kernels = measure_state_kernels(kda, dev, hbm_peak) if not args.no_state_kernels else None
     backward = measure_backward(kda, case, dev, hbm_peak) if not (args.no_backward or args.prep) else None
+    conv = measure_conv(kda, case, dev, hbm_peak) if not (args.no_state_kernels or args.prep) else None
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -495,7 +545,7 @@ def run_gpu(args, world, rank, local):
                 "vs_baseline": None, "dtype": "bf16" if q.dtype == torch.bfloat16 else "f32",
                 "data": "synthetic", "config": config_dict(args, case), "roofline": roof,
                 "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches_per_step * args.steps,
-                "clocks": clk, "state_kernels": state_kernels, "backward": backward}
+                "clocks": clk, "state_kernels": state_kernels, "backward": backward, "conv_fwd": conv}
         print(json.dumps(line), flush=True)
     if distributed:
         dist.destroy_process_group()

@@ -271,12 +271,11 @@ kda_status kda_conv_fwd(const void *q, const void *k, const void *v, kda_dtype d
     if (N < 0 || T_total < 0 || H <= 0) return KDA_ERR_INVALID_ARGUMENT;
     if (!workspace || !aligned16(workspace) || ws_bytes < KDA_WS_HEADER_BYTES) return KDA_ERR_WORKSPACE;
     if (!conv_weight || !aligned_to(conv_weight, 4)) return KDA_ERR_INVALID_ARGUMENT;
-    const size_t es = elem_size(dtype);
     if (T_total > 0) {
         if (!q || !k || !v || !q_out || !k_out || !v_out) return KDA_ERR_INVALID_ARGUMENT;
         for (const void *ptr : {q, k, v, static_cast<const void *>(q_out), static_cast<const void *>(k_out),
                                 static_cast<const void *>(v_out)})
-            if (!aligned_to(ptr, es)) return KDA_ERR_INVALID_ARGUMENT;
+            if (!aligned16(ptr)) return KDA_ERR_INVALID_ARGUMENT;  // 16-byte vector accesses
     }
     if ((conv_state_in && !aligned_to(conv_state_in, 4)) || (conv_state_out && !aligned_to(conv_state_out, 4)))
         return KDA_ERR_INVALID_ARGUMENT;

@@ -14,7 +14,9 @@
 //
 // This file is the prefill form (two launches: outputs, then states); decode and
 // replay apply the same convolution token by token inside the token-sequential
-// kernel.  Every sum runs in the order i = 0..3 with round-to-nearest intrinsics.
+// kernel.  Every sum runs in the order i = 0..3 with round-to-nearest intrinsics; the
+// prefill form takes SiLU with the fast exp / divide intrinsics (its outputs are rounded
+// to the input dtype), the fused form with correctly rounded ones.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -73,30 +75,118 @@ __device__ __forceinline__ float conv_input(const ConvParams &p, int64_t src, in
     return p.state_in[((static_cast<int64_t>(n) * (kConvW - 1) + (kConvW - 1 - back)) * H + h) * Ct + c];
 }
 
-// One thread per (token, head, packed channel).
+// Eight consecutive channels of one row as floats (16-byte aligned rows).
+__device__ __forceinline__ void ld8(const float *p, float (&x)[8]) {
+    const float4 a = *reinterpret_cast<const float4 *>(p), b = *reinterpret_cast<const float4 *>(p + 4);
+    x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w; x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+}
+__device__ __forceinline__ void ld8(const __nv_bfloat16 *p, float (&x)[8]) {
+    const uint4 u = *reinterpret_cast<const uint4 *>(p);
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        x[2 * e] = __uint_as_float(w[e] << 16);
+        x[2 * e + 1] = __uint_as_float(w[e] & 0xffff0000u);
+    }
+}
+__device__ __forceinline__ void st8(float *p, const float (&y)[8]) {
+    *reinterpret_cast<float4 *>(p) = make_float4(y[0], y[1], y[2], y[3]);
+    *reinterpret_cast<float4 *>(p + 4) = make_float4(y[4], y[5], y[6], y[7]);
+}
+__device__ __forceinline__ void st8(__nv_bfloat16 *p, const float (&y)[8]) {
+    uint32_t w[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        const __nv_bfloat162 v = __floats2bfloat162_rn(y[2 * e], y[2 * e + 1]);
+        w[e] = *reinterpret_cast<const uint32_t *>(&v);
+    }
+    *reinterpret_cast<uint4 *>(p) = make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// A thread owns 8 consecutive channels (all in one of q, k, v) of one head and slides the
+// width-4 window down a block of kConvBlock tokens, so every input is loaded once with
+// 16-byte loads (a warp reads 512 contiguous bytes per token).  The window restarts from
+// the sequence's state where a sequence begins inside the block.  Grid: token blocks x
+// groups of kConvThreads (head, channel group) pairs.
+constexpr int kConvBlock = 64;
+constexpr int kConvThreads = 256;
+
 template <typename Tin>
-__global__ void __launch_bounds__(kThreads) conv_out_kernel(ConvParams p) {
-    const int Ct = 2 * p.dk + p.dv;
-    const int64_t idx = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x;
-    if (idx >= p.T_total * p.H * Ct) return;
-    const int c = static_cast<int>(idx % Ct);
-    const int h = static_cast<int>((idx / Ct) % p.H);
-    const int64_t t = idx / (static_cast<int64_t>(Ct) * p.H);
-    const int n = seq_of(p, t);
+__global__ void __launch_bounds__(kConvThreads) conv_out_kernel(ConvParams p) {
+    const int Ct = 2 * p.dk + p.dv, G = Ct / 8;
+    const int u = static_cast<int>(blockIdx.y) * kConvThreads + threadIdx.x;
+    if (u >= p.H * G) return;
+    const int h = u / G, c0 = (u % G) * 8;
+    const int64_t H = p.H;
+    // which tensor the group lies in, its channel offset there and row length
+    const Tin *X;
+    Tin *Y;
+    int cx, d;
+    if (c0 < p.dk) { X = static_cast<const Tin *>(p.q); Y = static_cast<Tin *>(p.q_out); cx = c0; d = p.dk; }
+    else if (c0 < 2 * p.dk) { X = static_cast<const Tin *>(p.k); Y = static_cast<Tin *>(p.k_out); cx = c0 - p.dk; d = p.dk; }
+    else { X = static_cast<const Tin *>(p.v); Y = static_cast<Tin *>(p.v_out); cx = c0 - 2 * p.dk; d = p.dv; }
+    float w[8][kConvW];
+#pragma unroll
+    for (int e = 0; e < 8; ++e)
+#pragma unroll
+        for (int i = 0; i < kConvW; ++i) w[e][i] = p.weight[(static_cast<int64_t>(h) * Ct + c0 + e) * kConvW + i];
+    const int64_t t_begin = static_cast<int64_t>(blockIdx.x) * kConvBlock;
+    const int64_t t_end = t_begin + kConvBlock < p.T_total ? t_begin + kConvBlock : p.T_total;
+    int n = seq_of(p, t_begin);
     int64_t bos, eos;
-    if (!seq_bounds(p, n, bos, eos) || t < bos || t >= eos) {
-        if (c == 0 && h == 0) atomicOr(p.status, DEV_ERR_SEQLENS);
+    if (!seq_bounds(p, n, bos, eos)) {
+        if (u == 0) atomicOr(p.status, DEV_ERR_SEQLENS);
         return;
     }
-    const float *w = p.weight + (static_cast<int64_t>(h) * Ct + c) * kConvW;
-    float pre = 0.f;
+    float hw[kConvW - 1][8];  // the window: inputs t-3, t-2, t-1
+    auto window_at = [&](int64_t t) {
 #pragma unroll
-    for (int i = 0; i < kConvW; ++i) pre = __fmaf_rn(w[i], conv_input<Tin>(p, t - (kConvW - 1) + i, bos, n, h, c, Ct), pre);
-    const float y = __fdiv_rn(pre, __fadd_rn(1.f, expf(-pre)));
-    const int64_t H = p.H;
-    if (c < p.dk) st_out(static_cast<Tin *>(p.q_out), (t * H + h) * p.dk + c, y);
-    else if (c < 2 * p.dk) st_out(static_cast<Tin *>(p.k_out), (t * H + h) * p.dk + c - p.dk, y);
-    else st_out(static_cast<Tin *>(p.v_out), (t * H + h) * p.dv + c - 2 * p.dk, y);
+        for (int j = 0; j < kConvW - 1; ++j) {
+            const int64_t src = t - (kConvW - 1) + j;
+            if (src >= bos) {
+                ld8(X + (src * H + h) * d + cx, hw[j]);
+            } else if (p.state_in) {
+                const int64_t back = bos - src;
+                const float *sp = p.state_in + ((static_cast<int64_t>(n) * (kConvW - 1) + (kConvW - 1 - back)) * H + h) * Ct + c0;
+#pragma unroll
+                for (int e = 0; e < 8; ++e) hw[j][e] = sp[e];
+            } else {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) hw[j][e] = 0.f;
+            }
+        }
+    };
+    window_at(t_begin);
+    float xn[8];  // the next token's inputs, loaded one step ahead
+    ld8(X + (t_begin * H + h) * d + cx, xn);
+    for (int64_t t = t_begin; t < t_end; ++t) {
+        if (t >= eos) {  // the next sequence (skipping empty ones) starts here
+            while (n + 1 < p.N && t >= eos) {
+                ++n;
+                if (!seq_bounds(p, n, bos, eos)) {
+                    if (u == 0) atomicOr(p.status, DEV_ERR_SEQLENS);
+                    return;
+                }
+            }
+            window_at(t);
+        }
+        float x[8], y[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) x[e] = xn[e];
+        if (t + 1 < t_end) ld8(X + ((t + 1) * H + h) * d + cx, xn);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            float pre = __fmaf_rn(w[e][0], hw[0][e], 0.f);
+            pre = __fmaf_rn(w[e][1], hw[1][e], pre);
+            pre = __fmaf_rn(w[e][2], hw[2][e], pre);
+            pre = __fmaf_rn(w[e][3], x[e], pre);
+            y[e] = __fdividef(pre, 1.f + __expf(-pre));  // SiLU (fast intrinsics; the outputs are rounded to Tin)
+            hw[0][e] = hw[1][e];
+            hw[1][e] = hw[2][e];
+            hw[2][e] = x[e];
+        }
+        st8(Y + (t * H + h) * d + cx, y);
+    }
 }
 
 // One thread per (sequence, head, packed channel): the new state, slots in increasing
@@ -121,10 +211,12 @@ __global__ void __launch_bounds__(kThreads) conv_state_kernel(ConvParams p) {
 template <typename Tin>
 cudaError_t launch_typed(const ConvParams &p, cudaStream_t s) {
     const int64_t Ct = 2 * p.dk + p.dv;
-    const int64_t n_out = p.T_total * p.H * Ct, n_state = static_cast<int64_t>(p.N) * p.H * Ct;
-    const int64_t b_out = (n_out + kThreads - 1) / kThreads, b_state = (n_state + kThreads - 1) / kThreads;
-    if (b_out > 0x7fffffffLL || b_state > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    if (b_out > 0) conv_out_kernel<Tin><<<static_cast<unsigned>(b_out), kThreads, 0, s>>>(p);
+    const int64_t n_state = static_cast<int64_t>(p.N) * p.H * Ct;
+    const int64_t b_out = (p.T_total + kConvBlock - 1) / kConvBlock, b_state = (n_state + kThreads - 1) / kThreads;
+    const int64_t b_grp = (static_cast<int64_t>(p.H) * (Ct / 8) + kConvThreads - 1) / kConvThreads;
+    if (b_out > 0x7fffffffLL || b_state > 0x7fffffffLL || b_grp > 65535) return cudaErrorInvalidConfiguration;
+    if (b_out > 0)
+        conv_out_kernel<Tin><<<dim3(static_cast<unsigned>(b_out), static_cast<unsigned>(b_grp)), kConvThreads, 0, s>>>(p);
     if (p.state_out && b_state > 0) conv_state_kernel<Tin><<<static_cast<unsigned>(b_state), kThreads, 0, s>>>(p);
     return cudaGetLastError();
 }
