@@ -1,5 +1,7 @@
 /*
- * libkda -- Kimi Delta Attention (KDA) forward on one GB300 (sm_103a).
+ * libkda -- Kimi Delta Attention (KDA) on one GB300 (sm_103a): packed prefill,
+ * decode, ReplaySSM replay, state-pool operations, input preprocessing and the
+ * short convolution, and the backward of the prefill.
  *
  * What is computed.  The KDA paragraph of "Kimi K3 on Fireworks: Fast RL at
  * frontier scale" (kernels section) describes KDA as linear attention that
@@ -18,16 +20,18 @@
  *
  * Conventions shared by every call
  * --------------------------------
- * - All tensor arguments are DEVICE pointers to caller-owned memory.  The
- *   library never allocates or frees device memory; its only scratch is the
- *   caller's workspace.
+ * - All tensor arguments are DEVICE pointers to caller-owned memory (the
+ *   state-pool offload / restore calls also take page-locked host memory).  The
+ *   library never allocates or frees device memory; its scratch is the caller's
+ *   workspace (kda_chunk_fwd_noalloc: one fixed array of its own).
  * - Token-major packed layouts, C-contiguous:
  *     q, k, g  [T, H, dk]     v, o [T, H, dv]     beta [T, H]
  *   of dtype `kda_dtype` (bf16 or fp32; o uses the same dtype as the inputs).
  *   States are always fp32, [.., H, dk, dv] with dv contiguous.
  * - g holds log-gates (alpha = exp(g) in [0, 1]); g = -inf erases the state.
  * - dk and dv must each be 64 or 128 (KDA_ERR_UNSUPPORTED otherwise).
- * - Pointers must be 16-byte aligned (beta: element-aligned).
+ * - Pointers must be 16-byte aligned (beta: element-aligned; each call's
+ *   section names its exceptions).
  * - `stream` is a cudaStream_t (NULL = legacy default stream).  Every call is
  *   asynchronous on `stream`; none synchronizes except kda_device_status.
  * - Errors the host can see (NULL pointers, bad sizes, dtype, alignment, small
