@@ -24,6 +24,19 @@ bool prep_ok(uint32_t prep, float eps) {
 
 size_t staging_offset() { return KDA_WS_HEADER_BYTES; }
 
+// Launch order (longest sequences first) for batches of more (sequence, head) chains than
+// one wave of chunked-kernel CTAs (one per SM; 152 on GB300): N int32 after the staging
+// states, when the workspace has room for them.
+constexpr int64_t kWaveChains = 152;
+constexpr int kOrderMaxSeqs = 8192;
+bool order_shape(int N, int H) {
+    return N >= 2 && N <= kOrderMaxSeqs && static_cast<int64_t>(N) * H > kWaveChains;
+}
+size_t order_offset(int N, int H, int dk, int dv) {
+    return staging_offset() + static_cast<size_t>(N) * H * dk * dv * sizeof(float);
+}
+size_t order_bytes(int N) { return (static_cast<size_t>(N) * sizeof(int32_t) + 15) & ~static_cast<size_t>(15); }
+
 size_t state_bytes(int N, int H, int dk, int dv) {
     return static_cast<size_t>(N) * static_cast<size_t>(H) * dk * dv * sizeof(float);
 }
@@ -56,6 +69,7 @@ extern "C" {
 size_t kda_chunk_fwd_workspace_size(int N, int64_t T_total, int H, int dk, int dv) {
     if (N < 0 || T_total < 0 || H <= 0 || !dim_ok(dk) || !dim_ok(dv)) return 0;
     if (split_shape(N, T_total, H, dk, dv)) return split_workspace(N, T_total, H, dk, dv);
+    if (order_shape(N, H)) return order_offset(N, H, dk, dv) + order_bytes(N);
     return staging_offset() + state_bytes(N, H, dk, dv);
 }
 
@@ -103,6 +117,11 @@ kda_status kda_chunk_fwd_prep(const void *q, const void *k, const void *v, const
         cp.cu = cu_seqlens; cp.T_total = T_total; cp.seq_len_fixed = fixed_len;
         cp.init_state = init_state; cp.state_out = chunk_state; cp.status = status;
         cp.prep = static_cast<int>(prep); cp.prep_eps = l2_eps;
+        if (!split && cu_seqlens && order_shape(N, H) && ws_bytes >= order_offset(N, H, dk, dv) + order_bytes(N)) {
+            int32_t *order = reinterpret_cast<int32_t *>(static_cast<char *>(workspace) + order_offset(N, H, dk, dv));
+            if (kda::launch_order(cu_seqlens, N, order, s) != cudaSuccess) return KDA_ERR_CUDA;
+            cp.order = order;
+        }
         if (split) {
             char *base = static_cast<char *>(workspace) + staging_offset() + state_bytes(N, H, dk, dv);
             cp.split = 1;

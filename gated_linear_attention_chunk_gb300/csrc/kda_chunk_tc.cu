@@ -73,6 +73,7 @@ struct TcParams {
     CUtensorMap tm_q, tm_k, tm_g, tm_v;
     const __nv_bfloat16 *beta;
     __nv_bfloat16 *o;
+    const int32_t *order;         // launch order of the sequences, or null
     const int32_t *cu;
     const float *init_state;
     float *state_out;
@@ -244,7 +245,9 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_tc_kernel(const __grid_
     // 1 from the identity with v = 0 (outputs Phi_t^T (scale q_t), transition Phi).
     const int64_t npairs = static_cast<int64_t>(p.N) * p.H;
     const int role = p.split ? static_cast<int>(blockIdx.x / npairs) : 0;
-    const int64_t pair = p.split ? static_cast<int64_t>(blockIdx.x) % npairs : static_cast<int64_t>(blockIdx.x);
+    const int64_t slot = p.split ? static_cast<int64_t>(blockIdx.x) % npairs : static_cast<int64_t>(blockIdx.x);
+    // with a launch order, consecutive CTAs take the heads of the longest sequences first
+    const int64_t pair = p.order ? static_cast<int64_t>(p.order[slot / p.H]) * p.H + slot % p.H : slot;
     const int n = static_cast<int>(pair / p.H), h = static_cast<int>(pair % p.H);
     const int64_t H = p.H;
 
@@ -1104,6 +1107,27 @@ bool encode_tile_map(CUtensorMap *map, const void *base, int64_t T, int H) {
 
 }  // namespace
 
+namespace {
+// order[rank] = n: rank = sequences with more full chunks, or as many and a lower index.
+__global__ void __launch_bounds__(256) order_kernel(const int32_t *cu, int N, int32_t *order) {
+    const int n = static_cast<int>(blockIdx.x) * 256 + static_cast<int>(threadIdx.x);
+    if (n >= N) return;
+    const int64_t cn = (static_cast<int64_t>(cu[n + 1]) - cu[n]) / kC;
+    int r = 0;
+    for (int m = 0; m < N; ++m) {
+        const int64_t cm = (static_cast<int64_t>(cu[m + 1]) - cu[m]) / kC;
+        r += (cm > cn || (cm == cn && m < n)) ? 1 : 0;
+    }
+    order[r] = n;
+}
+}  // namespace
+
+cudaError_t launch_order(const int32_t *cu, int N, int32_t *order, cudaStream_t stream) {
+    if (N <= 0) return cudaSuccess;
+    order_kernel<<<static_cast<unsigned>((N + 255) / 256), 256, 0, stream>>>(cu, N, order);
+    return cudaGetLastError();
+}
+
 bool chunk_tc_supported(int dk, int dv, int dtype) { return dk == 128 && dv == 128 && dtype == 0; }
 
 cudaError_t launch_chunk_tc(const ChunkParams &cp, cudaStream_t stream) {
@@ -1133,6 +1157,7 @@ cudaError_t launch_chunk_tc(const ChunkParams &cp, cudaStream_t stream) {
     p.psi = cp.psi;
     p.o_phi = static_cast<__nv_bfloat16 *>(cp.o_phi);
     p.ckpt = cp.ckpt;
+    p.order = cp.split ? nullptr : cp.order;
     static bool attr_set = false;
     if (!attr_set) {
         for (auto fn : {kda_chunk_tc_kernel<false>, kda_chunk_tc_kernel<true>}) {

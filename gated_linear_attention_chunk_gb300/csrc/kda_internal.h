@@ -143,7 +143,13 @@ struct ChunkParams {
     // or null: the state after every full chunk c goes to checkpoint slot
     // (ckpt_base(bos, n) + c + 1) * H + h (needs split == 0); o may then be null
     float *ckpt;
+    // or null: launch order of the sequences (a permutation of 0..N-1, longest first), so
+    // that a batch of more chains than one wave of CTAs starts its longest chains first
+    // (needs split == 0)
+    const int32_t *order;
 };
+// order[rank] = n, sequences ranked by full chunks (descending, ties by index).
+cudaError_t launch_order(const int32_t *cu, int N, int32_t *order, cudaStream_t stream);
 
 // True when the chunked tensor-core kernel is compiled in and supports the shape.
 bool chunk_tc_supported(int dk, int dv, int dtype);

@@ -95,6 +95,13 @@ typedef enum kda_dtype {
  * header, which this function then includes; with a smaller (but sufficient)
  * workspace the call runs unsplit.  Results agree within floating-point
  * rounding either way.
+ *
+ * Launch order: when a batch has more (sequence, head) chains than one wave of
+ * chunked-kernel CTAs (N*H > 152, 2 <= N <= 8192, cu_seqlens given), the call
+ * ranks the sequences by length on the device and starts the longest chains
+ * first, which shortens the tail of a variable-length batch.  It needs N int32
+ * (rounded up to 16 bytes) after the staging states, which this function then
+ * includes; the results are bit-identical with or without it.
  */
 size_t kda_chunk_fwd_workspace_size(int N, int64_t T_total, int H, int dk, int dv);
 

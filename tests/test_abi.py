@@ -44,6 +44,10 @@ def test_workspace_size(lib):
     assert kda.kda_chunk_fwd_workspace_size(1, 4095, 2, 128, 128) == 256 + 2 * 65536    # too short: no split
     assert kda.kda_chunk_fwd_workspace_size(1, 8192, 2, 64, 64) == 256 + 2 * 16384      # d = 64: no split
     assert kda.kda_chunk_fwd_workspace_size(0, 0, 1, 64, 64) == 256
+    # more chains than one wave of CTAs: room for the launch order (N int32, 16-byte rounded)
+    assert kda.kda_chunk_fwd_workspace_size(64, 300000, 32, 128, 128) == 256 + 64 * 32 * 65536 + 256
+    assert kda.kda_chunk_fwd_workspace_size(39, 5000, 4, 64, 64) == 256 + 39 * 4 * 16384 + 160
+    assert kda.kda_chunk_fwd_workspace_size(38, 5000, 4, 64, 64) == 256 + 38 * 4 * 16384        # 152 chains: one wave
     assert kda.kda_chunk_fwd_workspace_size(1, 10, 2, 96, 128) == 0
     assert kda.kda_chunk_fwd_workspace_size(-1, 10, 2, 64, 128) == 0
 

@@ -260,3 +260,27 @@ def test_empty_sequences_copy_state(kda):
     assert torch.equal(fs[0].cpu(), case.init_state[0]) and torch.equal(fs[2].cpu(), case.init_state[2])
     o_ref, fs_ref = _oracle(case)
     assert_close(fs, fs_ref, "final_state")
+
+
+def test_launch_order_for_many_chains_is_bit_identical(kda):
+    """More chains than one wave (40 x 4 = 160): with the full workspace the call starts the
+    longest sequences first; the results equal the oracle and, bit for bit, the same call
+    with the minimum workspace (natural order)."""
+    gen = torch.Generator().manual_seed(9)
+    lengths = [int(x) for x in torch.randint(1, 400, (40,), generator=gen)]
+    lengths[3], lengths[17] = 0, 64
+    case = workloads.make_case(lengths, H=4, dk=128, dv=128, seed=75)
+    d = to_dev(case)
+    N, T = case.N, case.T_total
+    full = kda.new_workspace(kda.kda_chunk_fwd_workspace_size(N, T, 4, 128, 128), "cuda")
+    o1, fs1 = kda.kda_chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], cu_seqlens=d["cu_seqlens"],
+                                init_state=d["init_state"], workspace=full)
+    small = kda.new_workspace(kda.KDA_WS_HEADER_BYTES, "cuda")
+    o2, fs2 = kda.kda_chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], cu_seqlens=d["cu_seqlens"],
+                                init_state=d["init_state"], workspace=small)
+    torch.cuda.synchronize()
+    assert kda.kda_device_status(full) == kda.KDA_OK and kda.kda_device_status(small) == kda.KDA_OK
+    assert torch.equal(_bits(o1), _bits(o2)) and torch.equal(_bits(fs1), _bits(fs2))
+    o_ref, fs_ref = _oracle(case)
+    assert_close(o1, o_ref, "o")
+    assert_close(fs1, fs_ref, "final_state")
