@@ -39,9 +39,9 @@ METRIC = "KDA chunk_fwd tokens/s at T=4K-128K (1 GB300) and % of roofline"
 UNIT = "tokens/s"
 
 # DRAM bytes (read + write) of one kda_chunk_tc_kernel launch on prefill_4k, from the
-# ncu capture summarised in profiles/kda_chunk_tc_prefill_4k.md (546.65 MB read +
-# 117.82 MB written).  Reset to None whenever that kernel changes until it is re-captured.
-DOMINANT_TRAFFIC = {"prefill_4k": 664470272}
+# ncu capture summarised in profiles/kda_chunk_tc_prefill_4k.md (546.59 MB read +
+# 118.15 MB written).  Reset to None whenever that kernel changes until it is re-captured.
+DOMINANT_TRAFFIC = {"prefill_4k": 664739328}
 
 # every preprocessing flag (KDA_PREP_L2NORM_Q | _L2NORM_K | _SIGMOID_GATE | _SIGMOID_BETA)
 PREP_ALL, PREP_EPS = 15, 1e-6
