@@ -7,7 +7,6 @@ unsplit.  Both are checked against the fp64 oracle, including a sequence too
 short to have a second segment and sequences with a partial-chunk tail.
 """
 import pytest
-import torch
 
 import oracle
 import workloads
