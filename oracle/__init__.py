@@ -189,14 +189,34 @@ def replay(k, v, g, beta, cu_accept, state_pool, slots=None, threads: int = 1, p
 
 
 def backward(q, k, v, g, beta, cu_seqlens, init_state, d_o, d_final=None, scale: float = 1.0,
-             gate_is_alpha: bool = False, threads: int = 1):
+             gate_is_alpha: bool = False, threads: int = 1, prep_flags: int = 0, prep_eps: float = 1e-6):
     """Reverse mode of ``forward`` in fp64 (kda_oracle_backward).
 
     Given dL/do [T, H, dv] and dL/d(final_state) [N, H, dk, dv] (None = 0), returns a
     dict of float64 arrays: dq, dk, dg [T, H, dk] (dg with respect to the log-gates,
     or to alpha with ``gate_is_alpha``), dv [T, H, dv], dbeta [T, H] and d_init
-    [N, H, dk, dv].
+    [N, H, dk, dv].  With ``prep_flags`` the inputs are raw (see ``prep``) and the
+    gradients are taken with respect to them: the recurrence's gradients are carried
+    back through the L2 normalisation (dx = r (dxn - xn (xn . dxn)), r = (sum x^2 +
+    eps)^-1/2, xn = r x), alpha = sigmoid(x_g) (dx = dalpha alpha (1 - alpha)) and
+    beta = sigmoid(x_beta) (dx = dbeta beta (1 - beta)).
     """
+    if prep_flags:
+        qn, kn, gn, bn = prep(q, k, g, beta, prep_flags, prep_eps)
+        sig_gate = bool(prep_flags & PREP_SIGMOID_GATE)
+        G = backward(qn, kn, v, gn, bn, cu_seqlens, init_state, d_o, d_final, scale=scale,
+                     gate_is_alpha=sig_gate or gate_is_alpha, threads=threads)
+        for flag, name, raw, xn in ((PREP_L2NORM_Q, "dq", q, qn), (PREP_L2NORM_K, "dk", k, kn)):
+            if prep_flags & flag:
+                x = _f64(raw)
+                r = 1.0 / np.sqrt((x * x).sum(-1, keepdims=True) + prep_eps)
+                dxn = G[name]
+                G[name] = r * (dxn - xn * (xn * dxn).sum(-1, keepdims=True))
+        if sig_gate:
+            G["dg"] = G["dg"] * gn * (1.0 - gn)
+        if prep_flags & PREP_SIGMOID_BETA:
+            G["dbeta"] = G["dbeta"] * bn * (1.0 - bn)
+        return G
     lib = _load()
     q64, k64, v64, g64, b64 = _f64(q), _f64(k), _f64(v), _f64(g), _f64(beta)
     cu = np.ascontiguousarray(np.asarray(_f64(cu_seqlens), dtype=np.int64))

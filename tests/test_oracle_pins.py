@@ -562,3 +562,33 @@ def test_conv_state_carries_across_a_split():
         y2, s2 = oracle.conv(x[cut:], w, np.array([0, T - cut]), s1)
         np.testing.assert_array_equal(np.concatenate([y1, y2]), y)
         np.testing.assert_array_equal(s2, so)
+
+
+
+def test_backward_with_preprocessing_matches_finite_differences():
+    """With every preprocessing flag the backward returns the gradients with respect to the
+    raw inputs: central differences of the forward with the same flags (1e-6 relative)."""
+    cu, d, Wo, Ws = _bwd_case(31, lens=(4, 3), H=1, dk=3, dv=2)
+    d["g"] = np.random.default_rng(3).standard_normal(d["g"].shape) + 2.0   # raw gate logits
+    d["b"] = np.random.default_rng(4).standard_normal(d["b"].shape)          # raw beta logits
+    sc, flags, eps = 0.8, 15, 1e-3
+
+    def loss(q, k, v, g, b, s0):
+        o, fs = oracle.forward(q, k, v, g, b, cu, s0, scale=sc, prep_flags=flags, prep_eps=eps)
+        return float((o * Wo).sum() + (fs * Ws).sum())
+
+    G = oracle.backward(d["q"], d["k"], d["v"], d["g"], d["b"], cu, d["s0"], Wo, Ws, scale=sc, prep_flags=flags,
+                        prep_eps=eps)
+    h = 1e-6
+    for name, key in (("q", "dq"), ("k", "dk"), ("v", "dv"), ("g", "dg"), ("b", "dbeta"), ("s0", "d_init")):
+        arr = d[name]
+        num = np.zeros_like(arr)
+        for idx in np.ndindex(arr.shape):
+            plus, minus = dict(d), dict(d)
+            plus[name] = arr.copy()
+            plus[name][idx] += h
+            minus[name] = arr.copy()
+            minus[name][idx] -= h
+            num[idx] = (loss(**plus) - loss(**minus)) / (2 * h)
+        err = np.abs(num - G[key]).max() / np.abs(num).max()
+        assert err < 1e-6, (name, err)
