@@ -350,12 +350,14 @@ size_t kda_chunk_bwd_workspace_size(int N, int64_t T_total, int H, int dk, int d
     return bwd_layout(N, T_total, H, dk, dv, &a, &b, &c, &d);
 }
 
-kda_status kda_chunk_bwd(const void *q, const void *k, const void *v, const void *g, const void *beta,
-                         kda_dtype dtype, const float *init_state, const int32_t *cu_seqlens, int N,
-                         int64_t T_total, int H, int dk, int dv, float scale, const void *d_o,
-                         const float *d_final_state, void *dq, void *dk_out, void *dv_out, void *dg, void *dbeta,
-                         float *d_init_state, void *workspace, size_t ws_bytes, void *stream) {
+kda_status kda_chunk_bwd_prep(const void *q, const void *k, const void *v, const void *g, const void *beta,
+                              kda_dtype dtype, const float *init_state, const int32_t *cu_seqlens, int N,
+                              int64_t T_total, int H, int dk, int dv, float scale, uint32_t prep, float l2_eps,
+                              const void *d_o, const float *d_final_state, void *dq, void *dk_out, void *dv_out,
+                              void *dg, void *dbeta, float *d_init_state, void *workspace, size_t ws_bytes,
+                              void *stream) {
     if (!dtype_ok(dtype) || !dim_ok(dk) || !dim_ok(dv)) return KDA_ERR_UNSUPPORTED;
+    if (!prep_ok(prep, l2_eps)) return KDA_ERR_INVALID_ARGUMENT;
     if (N < 0 || T_total < 0 || H <= 0) return KDA_ERR_INVALID_ARGUMENT;
     if (!workspace || !aligned16(workspace)) return KDA_ERR_WORKSPACE;
     if (ws_bytes < kda_chunk_bwd_workspace_size(N, T_total, H, dk, dv)) return KDA_ERR_WORKSPACE;
@@ -399,7 +401,7 @@ kda_status kda_chunk_bwd(const void *q, const void *k, const void *v, const void
         cp.N = N; cp.H = H; cp.scale = scale; cp.cu = cu_seqlens; cp.T_total = T_total;
         cp.seq_len_fixed = fixed_len; cp.init_state = init_state;
         cp.state_out = reinterpret_cast<float *>(ws + stage_off); cp.status = status; cp.split = 0;
-        cp.ckpt = ckpt;
+        cp.ckpt = ckpt; cp.prep = static_cast<int>(prep); cp.prep_eps = l2_eps;
         if (kda::launch_chunk_tc(cp, s) != cudaSuccess) return KDA_ERR_CUDA;
     } else {
         kda::SeqParams sp{};
@@ -408,6 +410,7 @@ kda_status kda_chunk_bwd(const void *q, const void *k, const void *v, const void
         sp.cu = cu_seqlens; sp.T_total = T_total; sp.seq_len_fixed = fixed_len; sp.chunk_skip = 0;
         sp.state_in = init_state; sp.state_out = nullptr; sp.chunk_state = nullptr;
         sp.slots = nullptr; sp.num_slots = 0; sp.status = status; sp.ckpt = ckpt;
+        sp.prep = static_cast<int>(prep); sp.prep_eps = l2_eps;
         if (kda::launch_seq(sp, dk, dv, static_cast<int>(dtype), s) != cudaSuccess) return KDA_ERR_CUDA;
     }
 
@@ -421,8 +424,19 @@ kda_status kda_chunk_bwd(const void *q, const void *k, const void *v, const void
     bp.nslots = bwd_slots(N, T_total);
     bp.cu = cu_seqlens; bp.T_total = T_total; bp.seq_len_fixed = fixed_len;
     bp.N = N; bp.H = H; bp.scale = scale; bp.status = status;
+    bp.prep = static_cast<int>(prep); bp.prep_eps = l2_eps;
     if (kda::launch_bwd(bp, dk, dv, static_cast<int>(dtype), s) != cudaSuccess) return KDA_ERR_CUDA;
     return KDA_OK;
+}
+
+kda_status kda_chunk_bwd(const void *q, const void *k, const void *v, const void *g, const void *beta,
+                         kda_dtype dtype, const float *init_state, const int32_t *cu_seqlens, int N,
+                         int64_t T_total, int H, int dk, int dv, float scale, const void *d_o,
+                         const float *d_final_state, void *dq, void *dk_out, void *dv_out, void *dg, void *dbeta,
+                         float *d_init_state, void *workspace, size_t ws_bytes, void *stream) {
+    return kda_chunk_bwd_prep(q, k, v, g, beta, dtype, init_state, cu_seqlens, N, T_total, H, dk, dv, scale, 0u, 0.f,
+                              d_o, d_final_state, dq, dk_out, dv_out, dg, dbeta, d_init_state, workspace, ws_bytes,
+                              stream);
 }
 
 kda_status kda_device_status(const void *workspace, void *stream) {

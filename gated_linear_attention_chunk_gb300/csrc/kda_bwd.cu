@@ -212,10 +212,13 @@ __device__ bool slot_chunk(const BwdParams &p, int64_t slot, int &n, int &c, int
 }
 
 // Chunk inputs of (t0, Lc, h) into the CTA scratch: A, Kbar, Ktil, Khat, Qbar (C x DK),
-// V (optional) and dO (C x DV), beta and A_C into shared memory.
+// V (optional) and dO (C x DV), beta and A_C into shared memory.  With preprocessing
+// (p.prep) the raw inputs are mapped as the forward maps them: alpha = sigmoid(x_g),
+// beta = sigmoid(x_beta), k and q rows scaled by their inverse L2 norms (s_rk, s_rq; 1
+// when the flag is off).
 template <int DK, int DV, typename Tin>
 __device__ void load_chunk(const BwdParams &p, int64_t t0, int Lc, int h, float *W, bool want_v, float *s_buf,
-                           float *s_beta, float *s_ac) {
+                           float *s_beta, float *s_ac, float *s_rk, float *s_rq) {
     using S = Scr<DK, DV>;
     const int tid = threadIdx.x;
     const int64_t H = p.H;
@@ -226,12 +229,35 @@ __device__ void load_chunk(const BwdParams &p, int64_t t0, int Lc, int h, float 
         const int r = e / DK, i = e % DK;
         s_buf[e] = r < Lc ? ld_in(G, ((t0 + r) * H + h) * DK + i) : 0.f;
     }
-    if (tid < kC) s_beta[tid] = tid < Lc ? ld_in(B, (t0 + tid) * H + h) : 0.f;
+    if (tid < kC) {
+        float b = tid < Lc ? ld_in(B, (t0 + tid) * H + h) : 0.f;
+        if ((p.prep & PREP_SIGMOID_BETA) && tid < Lc) b = 1.f / (1.f + expf(-b));
+        s_beta[tid] = b;
+    }
+    if (tid >= 128 && tid < 128 + 2 * kC) {  // inverse row norms of k (rows 0-63) and q (rows 64-127)
+        const int r = (tid - 128) % kC;
+        const bool is_q = tid - 128 >= kC;
+        const int flag = is_q ? PREP_L2NORM_Q : PREP_L2NORM_K;
+        float inv = 1.f;
+        if ((p.prep & flag) && r < Lc) {
+            const Tin *X = is_q ? static_cast<const Tin *>(p.q) : static_cast<const Tin *>(p.k);
+            float ss = 0.f;
+#pragma unroll 8
+            for (int i = 0; i < DK; ++i) {
+                const float x = ld_in(X, ((t0 + r) * H + h) * DK + i);
+                ss = fmaf(x, x, ss);
+            }
+            inv = rsqrtf(ss + p.prep_eps);
+        }
+        (is_q ? s_rq : s_rk)[r] = inv;
+    }
     __syncthreads();
     if (tid < DK) {
+        const bool sig = (p.prep & PREP_SIGMOID_GATE) != 0;
         float a = 1.f;
         for (int r = 0; r < kC; ++r) {
-            a *= expf(s_buf[r * DK + tid]);
+            const float x = s_buf[r * DK + tid];
+            if (r < Lc) a *= sig ? 1.f / (1.f + expf(-x)) : expf(x);  // padding rows: alpha = 1
             W[S::kA + r * DK + tid] = a;
         }
         s_ac[tid] = a;
@@ -241,8 +267,8 @@ __device__ void load_chunk(const BwdParams &p, int64_t t0, int Lc, int h, float 
     for (int e = tid; e < kC * DK; e += kBT) {
         const int r = e / DK, i = e % DK;
         const bool ok = r < Lc;
-        const float kk = ok ? ld_in(K, ((t0 + r) * H + h) * DK + i) : 0.f;
-        const float qq = ok ? ld_in(Q, ((t0 + r) * H + h) * DK + i) : 0.f;
+        const float kk = ok ? ld_in(K, ((t0 + r) * H + h) * DK + i) * s_rk[r] : 0.f;
+        const float qq = ok ? ld_in(Q, ((t0 + r) * H + h) * DK + i) * s_rq[r] : 0.f;
         const float a = W[S::kA + e];
         W[S::kKb + e] = kk * a;
         W[S::kKt + e] = kk / a;
@@ -292,7 +318,7 @@ __global__ void __launch_bounds__(kBT, 2) kda_bwd_chunk_kernel(BwdParams p) {
     using S = Scr<DK, DV>;
     using RC = Rec<DK, DV>;
     __shared__ __align__(16) float s_buf[SmemBuf<DK>::kFloats];
-    __shared__ float s_beta[kC], s_ac[DK];
+    __shared__ float s_beta[kC], s_ac[DK], s_rk[kC], s_rq[kC];
     float *W = p.scratch + static_cast<int64_t>(blockIdx.x) * S::kTotal;
     const int64_t items = p.nslots * p.H;
     for (int64_t item = blockIdx.x; item < items; item += gridDim.x) {
@@ -304,7 +330,7 @@ __global__ void __launch_bounds__(kBT, 2) kda_bwd_chunk_kernel(BwdParams p) {
         const int64_t t0 = bos + static_cast<int64_t>(c) * kC;
         const int Lc = static_cast<int>(eos - t0 < kC ? eos - t0 : kC);
         float *rec = p.rec + item * RC::kTotal;
-        load_chunk<DK, DV, Tin>(p, t0, Lc, h, W, false, s_buf, s_beta, s_ac);
+        load_chunk<DK, DV, Tin>(p, t0, Lc, h, W, false, s_buf, s_beta, s_ac, s_rk, s_rq);
         if (threadIdx.x < DK) {
             rec[RC::kAC + threadIdx.x] = s_ac[threadIdx.x];
             if (!(s_ac[threadIdx.x] >= kMinDecay)) atomicOr(p.status, DEV_ERR_GATE);
@@ -392,7 +418,7 @@ __global__ void __launch_bounds__(kBT, 2) kda_bwd_grad_kernel(BwdParams p) {
     using S = Scr<DK, DV>;
     using RC = Rec<DK, DV>;
     __shared__ __align__(16) float s_buf[SmemBuf<DK>::kFloats];
-    __shared__ float s_beta[kC], s_dbeta[kC], s_ac[DK], s_red[kBT];
+    __shared__ float s_beta[kC], s_dbeta[kC], s_ac[DK], s_red[kBT], s_rk[kC], s_rq[kC];
     const int tid = threadIdx.x;
     float *W = p.scratch + static_cast<int64_t>(blockIdx.x) * S::kTotal;
     const int64_t H = p.H;
@@ -420,7 +446,7 @@ __global__ void __launch_bounds__(kBT, 2) kda_bwd_grad_kernel(BwdParams p) {
         float *Mr = W + S::kMr, *Pr = W + S::kPr, *P = W + S::kP, *Tp = W + S::kTp, *dP = W + S::kdP;
         float *dTp = W + S::kdTp, *X = W + S::kX, *dM = W + S::kdM;
 
-        load_chunk<DK, DV, Tin>(p, t0, Lc, h, W, true, s_buf, s_beta, s_ac);
+        load_chunk<DK, DV, Tin>(p, t0, Lc, h, W, true, s_buf, s_beta, s_ac, s_rk, s_rq);
         cta_gemm<kC, kC, DK, false, true>(Mr, kC, Kb, DK, Kt, DK, 1.f, false, 0, s_buf);
         cta_gemm<kC, kC, DK, false, true>(Pr, kC, Qb, DK, Kt, DK, 1.f, false, 0, s_buf);
         for (int e = tid; e < kC * kC; e += kBT) {
@@ -487,13 +513,17 @@ __global__ void __launch_bounds__(kBT, 2) kda_bwd_grad_kernel(BwdParams p) {
         }
         __syncthreads();
         // per element: dK, dQ and dlogA_r (into shared memory for the reverse sums)
+        const bool norms = (p.prep & (PREP_L2NORM_K | PREP_L2NORM_Q)) != 0;
         for (int e = tid; e < kC * DK; e += kBT) {
             const int r = e / DK, i = e % DK;
             const float a = A_[e];
             const float gk = dKb[e] * a + dKt[e] / a + dKh[e] * (s_ac[i] / a);
             const float gq = sc * dQb[e] * a;
             s_buf[e] = dKb[e] * Kb[e] - dKt[e] * Kt[e] + dQb[e] * Qb[e] - dKh[e] * Kh[e];
-            if (r < Lc) {
+            if (norms) {  // gradients of the normalised rows, carried back below
+                dKb[e] = gk;
+                dQb[e] = gq;
+            } else if (r < Lc) {
                 const int64_t o = ((t0 + r) * H + h) * DK + i;
                 st_out(DK_, o, gk);
                 st_out(DQ, o, gq);
@@ -504,15 +534,45 @@ __global__ void __launch_bounds__(kBT, 2) kda_bwd_grad_kernel(BwdParams p) {
             if (r < Lc) st_out(DV_, ((t0 + r) * H + h) * DV + j, dR[e]);
         }
         __syncthreads();
-        if (tid < DK) {  // dg_s = dlogA_C + sum_{r >= s} dlogA_r
+        if (tid < DK) {  // dg_s = dlogA_C + sum_{r >= s} dlogA_r (raw gate x: times 1 - sigmoid(x))
+            const bool sig = (p.prep & PREP_SIGMOID_GATE) != 0;
+            const Tin *G = static_cast<const Tin *>(p.g);
             float acc = 0.f;
             for (int gi = 0; gi < kBT / DK; ++gi) acc += s_red[tid + gi * DK];
             for (int r = kC - 1; r >= 0; --r) {
                 acc += s_buf[r * DK + tid];
-                if (r < Lc) st_out(DG, ((t0 + r) * H + h) * DK + tid, acc);
+                if (r < Lc) {
+                    const int64_t o = ((t0 + r) * H + h) * DK + tid;
+                    st_out(DG, o, sig ? acc * (1.f - 1.f / (1.f + expf(-ld_in(G, o)))) : acc);
+                }
             }
         }
-        if (tid < Lc) st_out(DB, (t0 + tid) * H + h, s_dbeta[tid]);
+        if (tid < Lc) {
+            const float b = s_beta[tid];
+            st_out(DB, (t0 + tid) * H + h, (p.prep & PREP_SIGMOID_BETA) ? s_dbeta[tid] * b * (1.f - b) : s_dbeta[tid]);
+        }
+        if (norms && tid >= 128 && tid < 128 + 2 * kC) {
+            // dx = r (dxn - xn (xn . dxn)) with xn = r x, per row of k (rows 0-63) or q (64-127)
+            const int r = (tid - 128) % kC;
+            const bool is_q = tid - 128 >= kC;
+            if (r < Lc) {
+                const Tin *X = is_q ? static_cast<const Tin *>(p.q) : static_cast<const Tin *>(p.k);
+                const float *gx = (is_q ? dQb : dKb) + r * DK;
+                const bool on = (p.prep & (is_q ? PREP_L2NORM_Q : PREP_L2NORM_K)) != 0;
+                const float inv = is_q ? s_rq[r] : s_rk[r];
+                const int64_t o = ((t0 + r) * H + h) * DK;
+                float dot = 0.f;
+                if (on) {
+#pragma unroll 8
+                    for (int i = 0; i < DK; ++i) dot = fmaf(ld_in(X, o + i) * inv, gx[i], dot);
+                }
+#pragma unroll 8
+                for (int i = 0; i < DK; ++i) {
+                    const float out = on ? inv * (gx[i] - ld_in(X, o + i) * inv * dot) : gx[i];
+                    st_out(is_q ? DQ : DK_, o + i, out);
+                }
+            }
+        }
         __syncthreads();
     }
 }

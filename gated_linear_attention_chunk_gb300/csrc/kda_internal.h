@@ -115,6 +115,8 @@ struct BwdParams {
     int N, H;
     float scale;
     uint32_t *status;
+    int prep;                   // input preprocessing of the forward (PREP_*): gradients are then taken
+    float prep_eps;             // with respect to the raw inputs
 };
 size_t bwd_scratch_floats(int dk, int dv);
 size_t bwd_record_floats(int dk, int dv);

@@ -67,6 +67,9 @@ _SIGS = {
                                     ctypes.c_size_t, _vp]),
     "kda_replay_conv": (_int, [_vp, _i64, _vp, _vp, _vp, _vp, _vp, _vp, _int, _vp, _int, _i64, _int, _int, _int,
                                _vp, _int, _vp, ctypes.c_uint32, ctypes.c_float, _vp, ctypes.c_size_t, _vp]),
+    "kda_chunk_bwd_prep": (_int, [_vp, _vp, _vp, _vp, _vp, _int, _vp, _vp, _int, _i64, _int, _int, _int,
+                                  ctypes.c_float, ctypes.c_uint32, ctypes.c_float, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
+                                  _vp, _vp, ctypes.c_size_t, _vp]),
     "kda_device_status": (_int, [_vp, _vp]),
     "kda_status_string": (ctypes.c_char_p, [_int]),
     "kda_version": (_int, []),
@@ -343,6 +346,21 @@ def kda_chunk_bwd(q, k, v, g, beta, d_o, cu_seqlens=None, init_state=None, d_fin
     """Backward of kda_chunk_fwd: returns a dict with dq, dk, dg [T, H, dk], dv [T, H, dv],
     dbeta [T, H] (input dtype) and d_init [N, H, dk, dv] fp32 (None unless ``want_d_init``),
     given d_o [T, H, dv] and d_final_state [N, H, dk, dv] fp32 (None = zero)."""
+    return _chunk_bwd(q, k, v, g, beta, d_o, cu_seqlens, init_state, d_final_state, scale, want_d_init,
+                      workspace, stream, None, 0.0)
+
+
+def kda_chunk_bwd_prep(q, k, v, g, beta, d_o, prep: int, l2_eps: float = 1e-6, cu_seqlens=None, init_state=None,
+                       d_final_state=None, scale: float = 1.0, want_d_init: bool = True, workspace=None,
+                       stream=None) -> dict:
+    """kda_chunk_bwd for a forward taken with kda_chunk_fwd_prep (raw inputs, same flags):
+    the gradients are with respect to the raw inputs."""
+    return _chunk_bwd(q, k, v, g, beta, d_o, cu_seqlens, init_state, d_final_state, scale, want_d_init,
+                      workspace, stream, int(prep), float(l2_eps))
+
+
+def _chunk_bwd(q, k, v, g, beta, d_o, cu_seqlens, init_state, d_final_state, scale, want_d_init, workspace,
+               stream, prep, l2_eps):
     lib = load_library()
     dt = q.dtype
     T, H, dk = q.shape
@@ -365,12 +383,15 @@ def kda_chunk_bwd(q, k, v, g, beta, d_o, cu_seqlens=None, init_state=None, d_fin
     need = kda_chunk_bwd_workspace_size(N, T, H, dk, dv)
     if workspace is None:
         workspace = new_workspace(need, q.device)
-    rc = lib.kda_chunk_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _dtype_code(q), _ptr(init_state),
-                           _ptr(cu_seqlens), N, T, H, dk, dv, float(scale), _ptr(d_o), _ptr(d_final_state),
-                           _ptr(out["dq"]), _ptr(out["dk"]), _ptr(out["dv"]), _ptr(out["dg"]),
-                           _ptr(out["dbeta"]), _ptr(out["d_init"]), _ptr(workspace),
-                           workspace.numel() * workspace.element_size(), _stream_handle(stream))
-    _check(rc, "kda_chunk_bwd")
+    head = (_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _dtype_code(q), _ptr(init_state), _ptr(cu_seqlens), N,
+            T, H, dk, dv, float(scale))
+    tail = (_ptr(d_o), _ptr(d_final_state), _ptr(out["dq"]), _ptr(out["dk"]), _ptr(out["dv"]), _ptr(out["dg"]),
+            _ptr(out["dbeta"]), _ptr(out["d_init"]), _ptr(workspace), workspace.numel() * workspace.element_size(),
+            _stream_handle(stream))
+    if prep is None:
+        _check(lib.kda_chunk_bwd(*head, *tail), "kda_chunk_bwd")
+    else:
+        _check(lib.kda_chunk_bwd_prep(*head, prep, l2_eps, *tail), "kda_chunk_bwd_prep")
     return out
 
 

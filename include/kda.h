@@ -272,6 +272,18 @@ kda_status kda_chunk_bwd(const void *q, const void *k, const void *v, const void
                          const float *d_final_state, void *d_q, void *d_k, void *d_v, void *d_g, void *d_beta,
                          float *d_init_state, void *workspace, size_t ws_bytes, void *stream);
 
+/* kda_chunk_bwd for a forward taken with kda_chunk_fwd_prep: the inputs are the raw
+ * ones given to the forward, with the same prep flags and l2_eps, and the gradients
+ * are taken with respect to those raw inputs (carried back through the L2
+ * normalisation, alpha = sigmoid(x_g) and beta = sigmoid(x_beta)).  prep = 0 is
+ * kda_chunk_bwd. */
+kda_status kda_chunk_bwd_prep(const void *q, const void *k, const void *v, const void *g, const void *beta,
+                              kda_dtype dtype, const float *init_state, const int32_t *cu_seqlens, int N,
+                              int64_t T_total, int H, int dk, int dv, float scale, uint32_t prep, float l2_eps,
+                              const void *d_o, const float *d_final_state, void *d_q, void *d_k, void *d_v,
+                              void *d_g, void *d_beta, float *d_init_state, void *workspace, size_t ws_bytes,
+                              void *stream);
+
 /*
  * Short convolution of the input projections, with its state carried across calls
  * (the disaggregated-serving paragraph of "Kimi K3 on Fireworks: Fast RL at

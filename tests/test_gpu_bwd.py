@@ -119,3 +119,33 @@ def test_bwd_full_size_prefill_4k_sampled_heads(kda):
         got = {key: out[key][ts, heads] for key in ("dq", "dk", "dv", "dg", "dbeta")}
         got["d_init"] = out["d_init"][n:n + 1, heads]
         _check(got, ref, f" (sequence {n})")
+
+
+@pytest.mark.parametrize("dk,dv,dtype", [(128, 128, torch.bfloat16), (64, 64, torch.float32)])
+def test_bwd_prep_matches_oracle(kda, dk, dv, dtype):
+    """Raw inputs with every preprocessing flag: the gradients with respect to the raw
+    q, k, gate and beta logits (and v, the initial state) equal the oracle's."""
+    case = workloads.make_case(LENGTHS, H=2, dk=dk, dv=dv, dtype=dtype, seed=76 + dk, raw=True, q_scale=False,
+                               scale=dk ** -0.5)
+    d_o, d_fin = _grads_out(case, seed=7)
+    d = to_dev(case)
+    out = kda.kda_chunk_bwd_prep(d["q"], d["k"], d["v"], d["g"], d["beta"], d_o.cuda(), 15, 1e-6,
+                                 cu_seqlens=d["cu_seqlens"], init_state=d["init_state"],
+                                 d_final_state=d_fin.cuda(), scale=case.scale)
+    torch.cuda.synchronize()
+    ref = oracle.backward(case.q, case.k, case.v, case.g, case.beta, case.cu_seqlens, case.init_state, d_o, d_fin,
+                          scale=case.scale, threads=0, prep_flags=15, prep_eps=1e-6)
+    _check(out, ref, f" (prep, {dk}x{dv} {dtype})")
+
+
+def test_bwd_prep_zero_is_the_plain_call(kda):
+    case = workloads.make_case([150, 64, 9], H=2, dk=128, dv=128, seed=77)
+    d_o, d_fin = _grads_out(case, seed=8)
+    d = to_dev(case)
+    args = (d["q"], d["k"], d["v"], d["g"], d["beta"], d_o.cuda())
+    kw = dict(cu_seqlens=d["cu_seqlens"], init_state=d["init_state"], d_final_state=d_fin.cuda())
+    a = kda.kda_chunk_bwd(*args, **kw)
+    b = kda.kda_chunk_bwd_prep(*args, 0, 0.0, **kw)
+    torch.cuda.synchronize()
+    for key in ("dq", "dk", "dv", "dg", "dbeta", "d_init"):
+        assert torch.equal(a[key], b[key]), key
