@@ -453,7 +453,10 @@ def run_gpu(args, world, rank, local):
     # kernels of ours per kda_chunk_fwd: the chunked tensor-core kernel (when it serves this shape)
     # plus the token-sequential partial-chunk kernel
     # (with the T-segment split, also the two merge kernels)
-    launches_per_step = 1 + int(kda.kda_chunk_fwd_uses_tensor_cores(dk, dv, q.dtype)) + (2 if split else 0)
+    # (and, for more chains than one wave of CTAs, the kernel that orders the sequences longest first)
+    uses_tc = bool(kda.kda_chunk_fwd_uses_tensor_cores(dk, dv, q.dtype))
+    ordered = uses_tc and not split and not args.plain_workspace and 2 <= N <= 8192 and N * H > 152
+    launches_per_step = 1 + int(uses_tc) + (2 if split else 0) + int(ordered)
     clocks = ClockSampler(local)
     for _ in range(args.warmup):
         step()
