@@ -37,10 +37,27 @@ import workloads  # noqa: E402
 METRIC = "KDA chunk_fwd tokens/s at T=4K-128K (1 GB300) and % of roofline"
 UNIT = "tokens/s"
 
-# DRAM bytes (read + write) of one kda_chunk_tc_kernel launch on prefill_4k, from the
-# ncu capture summarised in profiles/kda_chunk_tc_prefill_4k.md (546.59 MB read +
-# 118.15 MB written).  Reset to None whenever that kernel changes until it is re-captured.
-DOMINANT_TRAFFIC = {"prefill_4k": 664739328}
+# DRAM bytes (read + write) of one launch of the chunked kernel on prefill_4k, from one ncu
+# capture (dram__bytes_read.sum + dram__bytes_write.sum), with the first 16 hex digits of the
+# sha256 of the kernel's source file at the time of the capture: the figure is reported only
+# while that file is unchanged, and as null otherwise (until it is captured again).
+DOMINANT_TRAFFIC = {"prefill_4k": (664739328, "43a8ef819ac3f667")}
+DOMINANT_SRC = os.path.join(ROOT, "gated_linear_attention_chunk_gb300", "csrc", "kda_chunk_tc.cu")
+
+
+def source_sha16(path: str) -> str:
+    import hashlib
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def dominant_traffic(workload: str):
+    entry = DOMINANT_TRAFFIC.get(workload)
+    if not entry:
+        return None
+    nbytes, sha = entry
+    return nbytes if source_sha16(DOMINANT_SRC) == sha else None
+
 
 # every preprocessing flag (KDA_PREP_L2NORM_Q | _L2NORM_K | _SIGMOID_GATE | _SIGMOID_BETA)
 PREP_ALL, PREP_EPS = 15, 1e-6
@@ -109,35 +126,114 @@ def max_over_ranks(value: float, device=None) -> float:
 # clocks sampled during the timed region
 # ------------------------------------------------------------------------------------------------
 
+class _Nvml:
+    """Read-only NVML queries through ctypes (SM clock, its maximum, power, clock-event reasons)."""
+    SW_POWER_CAP, HW_SLOWDOWN, SW_THERMAL, HW_THERMAL = 0x4, 0x8, 0x20, 0x40
+
+    def __init__(self, device_index: int):
+        import ctypes
+        self.ct = ctypes
+        lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if lib.nvmlInit_v2() != 0:
+            raise RuntimeError("nvmlInit failed")
+        self.lib = lib
+        props = torch.cuda.get_device_properties(device_index)
+        self.handle = ctypes.c_void_p()
+        ok = False
+        for fmt in ("{:08X}:{:02X}:{:02X}.0", "{:04X}:{:02X}:{:02X}.0"):
+            bus = fmt.format(props.pci_domain_id, props.pci_bus_id, props.pci_device_id).encode()
+            if lib.nvmlDeviceGetHandleByPciBusId_v2(bus, ctypes.byref(self.handle)) == 0:
+                ok = True
+                break
+        if not ok:
+            raise RuntimeError("no NVML handle for this device")
+        self.reasons_fn = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            getattr(lib, "nvmlDeviceGetCurrentClocksThrottleReasons")
+        m = ctypes.c_uint()
+        self.sm_max = float(m.value) if lib.nvmlDeviceGetMaxClockInfo(self.handle, 1, ctypes.byref(m)) == 0 else None
+
+    def sample(self):
+        ct = self.ct
+        clk, pw, rs = ct.c_uint(), ct.c_uint(), ct.c_ulonglong()
+        if self.lib.nvmlDeviceGetClockInfo(self.handle, 1, ct.byref(clk)) != 0:  # NVML_CLOCK_SM
+            return None
+        self.lib.nvmlDeviceGetPowerUsage(self.handle, ct.byref(pw))
+        self.reasons_fn(self.handle, ct.byref(rs))
+        names = []
+        for bit, name in ((self.HW_SLOWDOWN, "hw_slowdown"), (self.HW_THERMAL, "hw_thermal_slowdown"),
+                          (self.SW_THERMAL, "sw_thermal_slowdown"), (self.SW_POWER_CAP, "sw_power_cap")):
+            if rs.value & bit:
+                names.append(name)
+        return float(clk.value), self.sm_max, pw.value / 1e3, names
+
+
 class ClockSampler:
+    """SM clocks, power and clock-event reasons sampled while the GPU works: NVML (read-only
+    queries, through ctypes) about every millisecond, so that even a few-millisecond timed region
+    holds samples; nvidia-smi every 100 ms where NVML cannot be loaded.  ``summary(t0, t1)``
+    keeps the samples taken between two wall-clock times."""
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, device_index: int = 0):
-        self.samples = []
+    def __init__(self, device_index: int = 0, period_s: float = 0.001):
+        self.samples = []  # (time, sm_mhz, sm_max_mhz, power_w, reasons)
         self.proc = None
+        self.source = None
+        self._stop = threading.Event()
+        try:
+            nv = _Nvml(device_index)
+            self.source = "nvml"
+
+            def loop():
+                while not self._stop.is_set():
+                    r = nv.sample()
+                    if r is not None:
+                        self.samples.append((time.time(), *r))
+                    time.sleep(period_s)
+            self.thread = threading.Thread(target=loop, daemon=True)
+            self.thread.start()
+        except Exception:
+            self._start_smi(device_index)
+
+    def _start_smi(self, device_index):
         sel = []
         try:
-            bus = torch.cuda.get_device_properties(device_index).pci_bus_id
-            if bus:
-                sel = ["-i", str(bus)]
+            p = torch.cuda.get_device_properties(device_index)
+            sel = ["-i", "{:08X}:{:02X}:{:02X}.0".format(p.pci_domain_id, p.pci_bus_id, p.pci_device_id)]
         except Exception:
             sel = []
         try:
             self.proc = subprocess.Popen(["nvidia-smi", *sel, f"--query-gpu={self.FIELDS}",
                                           "--format=csv,noheader,nounits", "-lms", "100"],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.source = "nvidia-smi"
+            self.thread = threading.Thread(target=self._read_smi, daemon=True)
             self.thread.start()
         except Exception:
             self.proc = None
 
-    def _read(self):
+    def _read_smi(self):
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for line in self.proc.stdout:
-            self.samples.append((time.time(), line.strip()))
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm, smax = float(parts[0]), float(parts[1])
+                pw = float(parts[2]) if parts[2] not in ("", "[N/A]") else None
+            except ValueError:
+                continue
+            rs = [n for n, v in zip(names, parts[4:8]) if v.lower().startswith("active")]
+            self.samples.append((time.time(), sm, smax, pw, rs))
+
+    def wait_first(self, timeout_s: float = 3.0):
+        t = time.time()
+        while not self.samples and time.time() - t < timeout_s:
+            time.sleep(0.005)
 
     def stop(self):
+        self._stop.set()
         if self.proc is not None:
             self.proc.terminate()
             try:
@@ -146,29 +242,15 @@ class ClockSampler:
                 self.proc.kill()
 
     def summary(self, t0: float, t1: float):
-        rows = [s for ts, s in self.samples if t0 <= ts <= t1]
-        if not rows and self.samples:  # region shorter than the sampling period: nearest samples
-            mid = 0.5 * (t0 + t1)
-            rows = [min(self.samples, key=lambda x: abs(x[0] - mid))[1]]
-        sm, smax, reasons = [], None, set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for r in rows:
-            parts = [p.strip() for p in r.split(",")]
-            if len(parts) < 8:
-                continue
-            try:
-                sm.append(float(parts[0]))
-                smax = float(parts[1])
-            except ValueError:
-                continue
-            for n, v in zip(names, parts[4:8]):
-                if v.lower().startswith("active"):
-                    reasons.add(n)
-        if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
-        sm.sort()
-        return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": smax, "reasons": sorted(reasons),
-                "samples": len(sm)}
+        rows = [r for r in list(self.samples) if t0 <= r[0] <= t1]
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0, "source": self.source}
+        sm = sorted(r[1] for r in rows)
+        reasons = sorted({n for r in rows for n in r[4]})
+        pw = [r[3] for r in rows if r[3] is not None]
+        return {"sm_mhz": sm[len(sm) // 2], "sm_mhz_min": sm[0], "sm_max_mhz": rows[-1][2], "reasons": reasons,
+                "samples": len(rows), "power_w_max": max(pw) if pw else None, "source": self.source,
+                "region_s": t1 - t0}
 
 
 # ------------------------------------------------------------------------------------------------
@@ -411,6 +493,128 @@ def measure_backward(kda, case, dev, hbm_peak, reps=3):
             "launches_per_call": 4}
 
 
+def _median_ms(call, reps: int, warm: int = 3) -> float:
+    """Median per-call CUDA-event time of ``call`` on the current stream."""
+    for _ in range(warm):
+        call()
+    torch.cuda.synchronize()
+    st = torch.cuda.current_stream()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+    for a, b in ev:
+        a.record(st)
+        call()
+        b.record(st)
+    torch.cuda.synchronize()
+    ms = sorted(a.elapsed_time(b) for a, b in ev)
+    return ms[len(ms) // 2]
+
+
+def measure_workload(kda, name, dev, hbm_peak, tf_peak, reps=10):
+    """kda_chunk_fwd tokens/s and roofline fraction on another named prefill workload (inputs
+    drawn on the device with the same recipe; full workspace, so every path of the call is
+    enabled: the T-segment split for few long chains, the longest-first launch order for
+    more chains than one wave)."""
+    case = workloads.named_case(name, device=dev)
+    N, T, H, dk, dv = case.N, case.T_total, case.H, case.dk, case.dv
+    o = torch.empty(T, H, dv, dtype=case.q.dtype, device=dev)
+    fs = torch.empty(N, H, dk, dv, dtype=torch.float32, device=dev)
+    ws = kda.new_workspace(kda.kda_chunk_fwd_workspace_size(N, T, H, dk, dv), dev)
+
+    def call():
+        kda.kda_chunk_fwd(case.q, case.k, case.v, case.g, case.beta, cu_seqlens=case.cu_seqlens,
+                          init_state=case.init_state, scale=case.scale, o=o, final_state=fs, workspace=ws)
+
+    ms = _median_ms(call, reps)
+    if kda.kda_device_status(ws) != kda.KDA_OK:
+        raise RuntimeError(f"{name}: device status")
+    nbytes, flops = algorithmic_bytes(case), algorithmic_flops(case)
+    roof_ms = 1e3 * max(nbytes / (hbm_peak * 1e9), flops / (tf_peak * 1e12))
+    gbs = nbytes / (ms / 1e3) / 1e9
+    out = {"tokens_per_s": T / (ms / 1e3), "ms_per_call": ms, "tokens": T, "sequences": N, "heads": H,
+           "achieved_GBs": gbs, "frac_of_hbm": gbs / hbm_peak, "roofline_ms": roof_ms, "frac": roof_ms / ms,
+           "algorithmic_bytes": nbytes, "calls": reps,
+           "inputs": "drawn on the device (same recipe, CUDA generator)", "desc": workloads.NAMED_WORKLOADS[name]["desc"]}
+    del case, o, fs, ws
+    torch.cuda.empty_cache()
+    return out
+
+
+def measure_spec_rollout(kda, dev, hbm_peak, steps=64, loops=3):
+    """The speculative rollout loop: a 2048-token prefill of 128 sequences into a state pool,
+    then ``steps`` x (4-token verify kda_chunk_fwd from the committed states, no final state
+    + kda_replay of the accepted prefix, U{1..4} tokens per sequence).  Every step's tokens,
+    accept lengths and packed accepted tokens are prepared before the timed loop (inputs
+    resident in HBM); the pool is reset to the prefill's states before each timed loop."""
+    case = workloads.named_case("spec_rollout", device=dev)
+    N, T, H, dk, dv = case.N, case.T_total, case.H, case.dk, case.dv
+    pool = torch.empty(N, H, dk, dv, dtype=torch.float32, device=dev)
+    o_p = torch.empty(T, H, dv, dtype=case.q.dtype, device=dev)
+    ws_p = kda.new_workspace(kda.kda_chunk_fwd_workspace_size(N, T, H, dk, dv), dev)
+
+    def prefill():
+        kda.kda_chunk_fwd(case.q, case.k, case.v, case.g, case.beta, cu_seqlens=case.cu_seqlens, init_state=None,
+                          scale=case.scale, o=o_p, final_state=pool, workspace=ws_p)
+
+    prefill_ms = _median_ms(prefill, 5)
+    pool0 = pool.clone()
+    del case, o_p, ws_p
+    q, k, v, g, b = workloads.make_decode_tokens(4 * N * steps, H, dk, dv, torch.bfloat16, seed=4004, device=dev)
+    q, k, v, g, b = (x.view(steps, 4 * N, *x.shape[1:]) for x in (q, k, v, g, b))
+    acc = workloads.make_accept_lengths(steps, N, 4, seed=404)
+    packed = []
+    for s in range(steps):
+        a = acc[s]
+        sel = torch.cat([torch.arange(4 * i, 4 * i + int(a[i])) for i in range(N)]).to(dev)
+        cu_a = torch.zeros(N + 1, dtype=torch.int32)
+        cu_a[1:] = torch.cumsum(a, 0)
+        packed.append((k[s][sel].contiguous(), v[s][sel].contiguous(), g[s][sel].contiguous(),
+                       b[s][sel].contiguous(), cu_a.to(dev)))
+    cu4 = torch.arange(0, 4 * N + 1, 4, dtype=torch.int32, device=dev)
+    o_v = torch.empty(4 * N, H, dv, dtype=torch.bfloat16, device=dev)
+    ws_v = kda.new_workspace(kda.kda_chunk_fwd_workspace_size(N, 4 * N, H, dk, dv), dev)
+    ws_r = kda.new_workspace(kda.KDA_WS_HEADER_BYTES, dev)
+
+    def loop():
+        for s in range(steps):
+            kda.kda_chunk_fwd(q[s], k[s], v[s], g[s], b[s], cu_seqlens=cu4, init_state=pool, output_final_state=False,
+                              o=o_v, workspace=ws_v)
+            ka, va, ga, ba, cua = packed[s]
+            kda.kda_replay(pool, ka, va, ga, ba, cua, workspace=ws_r)
+
+    pool.copy_(pool0)
+    loop()
+    torch.cuda.synchronize()
+    if kda.kda_device_status(ws_v) != kda.KDA_OK or kda.kda_device_status(ws_r) != kda.KDA_OK:
+        raise RuntimeError("spec rollout: device status")
+    st = torch.cuda.current_stream()
+    times = []
+    for _ in range(loops):
+        pool.copy_(pool0)
+        a_, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a_.record(st)
+        loop()
+        b_.record(st)
+        torch.cuda.synchronize()
+        times.append(a_.elapsed_time(b_))
+    ms = sorted(times)[len(times) // 2]
+    accepted = int(acc.sum())
+    state = N * H * dk * dv * 4
+    tok_v = 4 * N * H * ((3 * dk + dv + 1) * 2 + dv * 2)          # q, k, g, v, beta in; o out
+    tok_r = accepted * H * (2 * dk + dv + 1) * 2                 # k, g, v, beta of accepted tokens
+    nbytes = steps * (state + 2 * state) + steps * tok_v + tok_r
+    roof_ms = 1e3 * nbytes / (hbm_peak * 1e9)
+    out = {"accepted_tokens_per_s": accepted / (ms / 1e3), "ms_per_loop": ms, "steps": steps,
+           "ms_per_step": ms / steps, "accepted_tokens": accepted, "sequences": N, "heads": H,
+           "prefill_ms": prefill_ms, "prefill_tokens_per_s": T / (prefill_ms / 1e3),
+           "algorithmic_bytes_per_loop": nbytes, "achieved_GBs": nbytes / (ms / 1e3) / 1e9,
+           "roofline_ms_per_step": roof_ms / steps, "frac": roof_ms / ms, "loops_timed": loops,
+           "launches_per_step": 3,
+           "inputs": "drawn on the device (same recipe, CUDA generator); accept lengths U{1..4}, seed 404"}
+    del q, k, v, g, b, packed, pool, pool0, o_v, ws_v
+    torch.cuda.empty_cache()
+    return out
+
+
 def run_gpu(args, world, rank, local):
     import gated_linear_attention_chunk_gb300 as kda
 
@@ -458,6 +662,7 @@ def run_gpu(args, world, rank, local):
     ordered = uses_tc and not split and not args.plain_workspace and 2 <= N <= 8192 and N * H > 152
     launches_per_step = 1 + int(uses_tc) + (2 if split else 0) + int(ordered)
     clocks = ClockSampler(local)
+    clocks.wait_first()
     for _ in range(args.warmup):
         step()
     st = kda.kda_device_status(ws)
@@ -494,47 +699,37 @@ def run_gpu(args, world, rank, local):
     if st != kda.KDA_OK:
         raise RuntimeError(f"device status {kda.kda_status_string(st)}")
 
-    # end to end through the public API with host buffers: H2D inputs, call, D2H outputs
+    # End to end through the public API with host buffers: every step copies the inputs in from
+    # pinned host memory and o and the final states out, with the copies of one sequence group
+    # overlapping the other groups' compute (HostPrefill, one kda_chunk_fwd per group).
+    from gated_linear_attention_chunk_gb300.host_pipeline import HostPrefill
+    pipe = HostPrefill(case.q, case.k, case.v, case.g, case.beta, case.cu_seqlens, case.init_state,
+                       scale=case.scale, groups=min(N, 4), device=dev)
+    if prep:
+        pipe = None  # the pipelined helper runs the plain call; --prep reports no end-to-end number
     e2e = None
-    host = {n: x.pin_memory() for n, x in (("q", case.q), ("k", case.k), ("v", case.v), ("g", case.g),
-                                           ("beta", case.beta), ("cu", case.cu_seqlens))}
-    if case.init_state is not None:
-        host["s0"] = case.init_state.pin_memory()
-    host_o = torch.empty(T, H, dv, dtype=q.dtype).pin_memory()
-    host_fs = torch.empty(N, H, dk, dv, dtype=torch.float32).pin_memory()
-    dq, dk_, dvv, dg, db = (torch.empty_like(x) for x in (q, k, v, g, b))
-    dcu = torch.empty_like(cu)
-    ds0 = None if s0 is None else torch.empty_like(s0)
-    h2d = sum(x.numel() * x.element_size() for x in host.values())
-    d2h = host_o.numel() * host_o.element_size() + host_fs.numel() * 4
-    e2e_steps = max(1, min(args.steps, 20))
-
-    def e2e_step():
-        dq.copy_(host["q"], non_blocking=True)
-        dk_.copy_(host["k"], non_blocking=True)
-        dvv.copy_(host["v"], non_blocking=True)
-        dg.copy_(host["g"], non_blocking=True)
-        db.copy_(host["beta"], non_blocking=True)
-        dcu.copy_(host["cu"], non_blocking=True)
-        if ds0 is not None:
-            ds0.copy_(host["s0"], non_blocking=True)
-        call(dq, dk_, dvv, dg, db, dcu, ds0)
-        host_o.copy_(o, non_blocking=True)
-        host_fs.copy_(fs, non_blocking=True)
-
-    e2e_step()
-    torch.cuda.synchronize()
-    if distributed:
-        dist.barrier()
-    a, bb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record(stream)
-    for _ in range(e2e_steps):
-        e2e_step()
-    bb.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = max_over_ranks(a.elapsed_time(bb), dev)
-    e2e = {"value": world * T * e2e_steps / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
-           "d2h_bytes_per_step": int(d2h), "steps": e2e_steps}
+    if pipe is not None:
+        e2e_steps = max(1, min(args.steps, 20))
+        pipe.run()
+        torch.cuda.synchronize()
+        if pipe.status() != kda.KDA_OK:
+            raise RuntimeError("e2e device status")
+        if distributed:
+            dist.barrier()
+        a, bb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(e2e_steps):
+            pipe.run()
+        bb.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = max_over_ranks(a.elapsed_time(bb), dev)
+        h2d, d2h = pipe.h2d_bytes, pipe.d2h_bytes
+        e2e = {"value": world * T * e2e_steps / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+               "d2h_bytes_per_step": int(d2h), "steps": e2e_steps, "ms_per_step": e2e_ms / e2e_steps,
+               "host_link_GBs": (h2d + d2h) * e2e_steps / (e2e_ms / 1e3) / 1e9,
+               "pipeline": f"{len(pipe.groups)} sequence groups; H2D, compute and D2H on three streams"}
+        del pipe
+        torch.cuda.empty_cache()
 
     hbm_peak, tf_peak, peak_src = measured_peaks()
     nbytes = algorithmic_bytes(case)
@@ -543,7 +738,7 @@ def run_gpu(args, world, rank, local):
     t_hbm = nbytes / (hbm_peak * 1e9)
     t_tc = flops / (tf_peak * 1e12)
     bound = "hbm" if t_hbm >= t_tc else "tensor"
-    traffic = None if prep else (DOMINANT_TRAFFIC or {}).get(args.workload)  # captured on preprocessed inputs
+    traffic = None if prep else dominant_traffic(args.workload)  # captured on preprocessed inputs
     if bound == "hbm":
         achieved = nbytes / (kern_ms / 1e3) / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
@@ -558,6 +753,12 @@ def run_gpu(args, world, rank, local):
                  "timing": "median per-step CUDA-event time of kda_chunk_fwd (includes the status-word memset"
                            " and the partial-chunk launch)"})
 
+    # the rest of the metric's 4K-128K range and the speculative rollout loop (default workload only)
+    workloads_sub = None
+    if args.workload == "prefill_4k" and not (args.prep or args.no_sub_workloads):
+        workloads_sub = {name: measure_workload(kda, name, dev, hbm_peak, tf_peak)
+                         for name in ("long_128k", "varlen_64")}
+        workloads_sub["spec_rollout"] = measure_spec_rollout(kda, dev, hbm_peak)
     state_kernels = measure_state_kernels(kda, dev, hbm_peak) if not args.no_state_kernels else None
     backward = measure_backward(kda, case, dev, hbm_peak) if not (args.no_backward or args.prep) else None
     conv = measure_conv(kda, case, dev, hbm_peak) if not (args.no_state_kernels or args.prep) else None
@@ -572,7 +773,8 @@ def run_gpu(args, world, rank, local):
                 "vs_baseline": None, "dtype": "bf16" if q.dtype == torch.bfloat16 else "f32",
                 "data": "synthetic", "config": config_dict(args, case), "roofline": roof,
                 "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches_per_step * args.steps,
-                "clocks": clk, "state_kernels": state_kernels, "backward": backward, "conv_fwd": conv}
+                "clocks": clk, "workloads": workloads_sub, "state_kernels": state_kernels, "backward": backward,
+                "conv_fwd": conv}
         print(json.dumps(line), flush=True)
     if distributed:
         dist.destroy_process_group()
@@ -592,12 +794,24 @@ def main(argv=None):
     ap.add_argument("--plain-workspace", action="store_true",
                     help="minimum workspace: kda_chunk_fwd runs without the T-segment split")
     ap.add_argument("--no-backward", action="store_true", help="skip the kda_chunk_bwd measurement")
+    ap.add_argument("--no-sub-workloads", action="store_true",
+                    help="skip the long_128k / varlen_64 / spec_rollout sub-records")
+    ap.add_argument("--state-kernels-only", action="store_true",
+                    help="only the decode / replay / pool measurements (a short command for profiling them)")
+    ap.add_argument("--state-reps", type=int, default=50, help="timed calls per state kernel")
     ap.add_argument("--prep", action="store_true",
                     help="raw inputs through kda_chunk_fwd_prep with every preprocessing flag")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     world, rank, local = dist_env()
+    if args.state_kernels_only:
+        import gated_linear_attention_chunk_gb300 as kda
+        torch.cuda.set_device(local)
+        dev = torch.device("cuda", local)
+        out = measure_state_kernels(kda, dev, measured_peaks()[0], reps=args.state_reps)
+        print(json.dumps({"state_kernels": out}), flush=True)
+        return 0
     if args.impl == "reference":
         return run_reference(args, world, rank)
     return run_gpu(args, world, rank, local)

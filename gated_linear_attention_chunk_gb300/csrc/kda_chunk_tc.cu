@@ -37,6 +37,7 @@
 #include <cudaTypedefs.h>
 #include <stdint.h>
 
+#include <atomic>
 #include <type_traits>
 
 #include "kda_internal.h"
@@ -1158,18 +1159,24 @@ cudaError_t launch_chunk_tc(const ChunkParams &cp, cudaStream_t stream) {
     p.o_phi = static_cast<__nv_bfloat16 *>(cp.o_phi);
     p.ckpt = cp.ckpt;
     p.order = cp.split ? nullptr : cp.order;
-    static bool attr_set = false;
-    if (!attr_set) {
-        for (auto fn : {kda_chunk_tc_kernel<false>, kda_chunk_tc_kernel<true>}) {
+    // The register split assumes 96 registers per thread at launch (a property of the compiled
+    // image, checked once).  The dynamic shared-memory limit is a function attribute of the device
+    // that is current when it is set, so it is set on every launch (a host-side call that
+    // allocates nothing and does not synchronize).
+    static std::atomic<int> regs_ok{0};  // 0 unknown, 1 as assumed, 2 not
+    for (auto fn : {kda_chunk_tc_kernel<false>, kda_chunk_tc_kernel<true>}) {
+        if (regs_ok.load(std::memory_order_acquire) == 0) {
             cudaFuncAttributes fa{};
-            if (cudaFuncGetAttributes(&fa, fn) != cudaSuccess || fa.numRegs != 96)
-                return cudaErrorInvalidConfiguration;  // the register split assumes 96 per thread at launch
-            cudaError_t e =
-                cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kDynSmem));
-            if (e != cudaSuccess) return e;
+            if (cudaFuncGetAttributes(&fa, fn) != cudaSuccess) return cudaErrorInvalidConfiguration;
+            if (fa.numRegs != 96) regs_ok.store(2, std::memory_order_release);
         }
-        attr_set = true;
+        if (regs_ok.load(std::memory_order_acquire) == 2) return cudaErrorInvalidConfiguration;
+        const cudaError_t e =
+            cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kDynSmem));
+        if (e != cudaSuccess) return e;
     }
+    int unknown = 0;
+    regs_ok.compare_exchange_strong(unknown, 1);
     if (p.prep || p.ckpt)
         kda_chunk_tc_kernel<true><<<static_cast<unsigned>(blocks), kThreads, kDynSmem, stream>>>(p);
     else

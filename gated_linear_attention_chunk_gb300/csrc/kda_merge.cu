@@ -319,16 +319,14 @@ cudaError_t launch_merge(const MergeParams &p, cudaStream_t stream) {
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return cudaErrorInvalidValue;
     const size_t smem_s = static_cast<size_t>(2 * kD * kLdS) * sizeof(float);
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(merge_o_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(kMoSmem));
-        if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(merge_state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     static_cast<int>(smem_s));
-        if (e != cudaSuccess) return e;
-        attr_set = true;
-    }
+    // The dynamic shared-memory limit is a function attribute of the device that is current
+    // when it is set, so it is set on every launch (a host-side call that allocates nothing).
+    cudaError_t e = cudaFuncSetAttribute(merge_o_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(kMoSmem));
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(merge_state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(smem_s));
+    if (e != cudaSuccess) return e;
     const int64_t grid_o = pairs * mo.parts;
     if (grid_o > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     merge_o_kernel<<<static_cast<unsigned>(grid_o), kMoThreads, kMoSmem, stream>>>(mo);

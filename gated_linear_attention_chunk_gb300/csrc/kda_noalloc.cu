@@ -12,8 +12,11 @@
 // The array is a file-scope __device__ variable, so every GPU that loads this
 // library keeps it (kStaticWorkspaceBytes) until the process exits.  In host
 // code its name is only a host-side stand-in; its device address is looked up
-// with cudaGetSymbolAddress once per device, on the first call made while that
-// device is current.
+// with cudaGetSymbolAddress, with the caller's device current.  The lookup is
+// repeated on every call made outside stream capture (it is cheap and
+// allocates nothing), so a reset device or another context never sees a stale
+// address; during capture the address last looked up on that device is used,
+// which is why the first call on a device must come before any capture.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -31,17 +34,20 @@ static __device__ __align__(256) unsigned char g_static_workspace[kStaticWorkspa
 std::mutex g_mutex;
 void *g_device_ptr[kMaxDevices] = {};
 
-// Device address of the scratch array on the current device (set up once per device).
-kda_status static_workspace(void **out) {
+// Device address of the scratch array on the current device.
+kda_status static_workspace(cudaStream_t stream, void **out) {
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess) return KDA_ERR_CUDA;
     if (dev < 0 || dev >= kMaxDevices) return KDA_ERR_UNSUPPORTED;
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess) return KDA_ERR_CUDA;
     std::lock_guard<std::mutex> lock(g_mutex);
-    if (!g_device_ptr[dev]) {
+    if (cap == cudaStreamCaptureStatusNone) {
         void *ptr = nullptr;
         if (cudaGetSymbolAddress(&ptr, g_static_workspace) != cudaSuccess || !ptr) return KDA_ERR_CUDA;
         g_device_ptr[dev] = ptr;
     }
+    if (!g_device_ptr[dev]) return KDA_ERR_CUDA;  // first call on this device made during capture
     *out = g_device_ptr[dev];
     return KDA_OK;
 }
@@ -63,7 +69,7 @@ extern "C" kda_status kda_chunk_fwd_noalloc(const void *q, const void *k, const 
     const size_t need = KDA_WS_HEADER_BYTES + (final_state ? 0 : states);
     if (need > kStaticWorkspaceBytes) return KDA_ERR_WORKSPACE;
     void *ws = nullptr;
-    const kda_status st = static_workspace(&ws);
+    const kda_status st = static_workspace(static_cast<cudaStream_t>(stream), &ws);
     if (st != KDA_OK) return st;
     if (status_workspace) *status_workspace = ws;
     // kda_chunk_fwd clears the status word first; the staging area is written before it is read.

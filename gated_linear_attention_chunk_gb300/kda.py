@@ -252,9 +252,11 @@ def kda_chunk_fwd_noalloc(q, k, v, g, beta, o, cu_seqlens=None, init_state=None,
     if final_state is not None:
         _need(final_state, "final_state", torch.float32, (N, H, dk, dv))
     ws = ctypes.c_void_p()
-    rc = lib.kda_chunk_fwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _dtype_code(q),
-                                   _ptr(init_state), _ptr(cu_seqlens), N, T, H, dk, dv, float(scale), _ptr(o),
-                                   _ptr(final_state), ctypes.byref(ws), _stream_handle(stream))
+    # the library's scratch and the default stream are those of the current device
+    with torch.cuda.device(q.device):
+        rc = lib.kda_chunk_fwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _dtype_code(q),
+                                       _ptr(init_state), _ptr(cu_seqlens), N, T, H, dk, dv, float(scale), _ptr(o),
+                                       _ptr(final_state), ctypes.byref(ws), _stream_handle(stream))
     _check(rc, "kda_chunk_fwd_noalloc")
     return int(ws.value)
 

@@ -350,15 +350,21 @@ kda_status kda_device_status(const void *workspace, void *stream);
  *
  * Scratch: one array of KDA_NOALLOC_WORKSPACE_BYTES in the library's own
  * device memory; every GPU that loads libkda holds it until the process exits.
- * - The first call on a device (with that device current) looks up the
- *   array's device address; make that first call before any stream capture.
+ * - Each call made outside stream capture looks up the array's device
+ *   address on the current device; a call made during capture reuses the
+ *   address last looked up there, so make the first call on a device before
+ *   any stream capture (it returns KDA_ERR_CUDA otherwise).
  * - Every call shares the array: calls that could run at the same time on the
  *   GPU (other streams, other host threads on the same device) race on it and
  *   must be serialized by the caller.  The status word is cleared by each call.
- * - With final_state != NULL only the 256-byte header is used and any size is
- *   accepted.  With final_state == NULL the states are staged in the array, so
- *   N*H*dk*dv*4 must not exceed 8 MiB; larger requests return
+ * - With final_state != NULL the size limit below does not apply and any
+ *   batch is accepted.  With final_state == NULL the states are staged in the
+ *   array, so N*H*dk*dv*4 must not exceed 8 MiB; larger requests return
  *   KDA_ERR_WORKSPACE and launch nothing.
+ * - The call hands the whole array to kda_chunk_fwd as its workspace, so
+ *   whatever of that call's optional buffers fit (the T-segment split's
+ *   buffers, the launch order) are placed in the array too; overlapping calls
+ *   race on all of it, not only on the status word and staged states.
  *
  *   status_workspace  optional out: receives the array's device address, which
  *                     kda_device_status() accepts to read this call's status.

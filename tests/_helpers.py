@@ -27,10 +27,18 @@ def max_abs(got, ref) -> float:
     return float(np.max(np.abs(got - ref))) if got.size else 0.0
 
 
+# Every comparison made by assert_close, as (test id, what, rel_l2, max_abs, tolerance);
+# conftest writes them to the file named by KDA_PARITY_REPORT at the end of the session.
+RECORDS = []
+CURRENT_TEST = [""]
+
+
 def assert_close(got, ref, what: str, rel=REL_L2, mab=MAX_ABS):
     if isinstance(got, torch.Tensor):
         got = got.detach().to("cpu", torch.float64).numpy()
     r, m = rel_l2(got, ref), max_abs(got, ref)
+    RECORDS.append({"test": CURRENT_TEST[0], "what": what, "rel_l2": r, "max_abs": m, "tol_rel_l2": rel,
+                    "tol_max_abs": mab})
     assert np.all(np.isfinite(got)), f"{what}: non-finite values"
     assert r <= rel and m <= mab, f"{what}: rel_l2={r:.3e} (<= {rel}), max_abs={m:.3e} (<= {mab})"
     return r, m

@@ -22,29 +22,46 @@ def kda():
 
 def _chain_oracle(case, n, h):
     """fp64 oracle for one (sequence, head) chain of a packed case."""
-    b, e = int(case.cu_seqlens[n]), int(case.cu_seqlens[n + 1])
-    sl = slice(b, e)
-    pick = lambda x: x[sl, h:h + 1]
-    s0 = None if case.init_state is None else case.init_state[n:n + 1, h:h + 1]
-    o, fs = oracle.forward(pick(case.q), pick(case.k), pick(case.v), pick(case.g), case.beta[sl, h:h + 1],
-                           np.array([0, e - b]), s0, scale=case.scale)
-    return o[:, 0], fs[0, 0]
+    return _chains_oracle(case, [(n, h)])[(n, h)]
 
 
-def _check_chains(case, o, fs, chains):
+def _chains_oracle(case, chains, threads=8):
+    """fp64 oracle for several (sequence, head) chains in one call: each chain becomes a
+    sequence of a one-head packed batch, so the oracle runs them on parallel threads."""
+    cu = case.cu_seqlens.tolist()
+    parts = {name: [] for name in ("q", "k", "v", "g", "beta")}
+    bounds, s0 = [0], []
     for n, h in chains:
-        o_ref, fs_ref = _chain_oracle(case, n, h)
+        b, e = int(cu[n]), int(cu[n + 1])
+        for name in parts:
+            t = getattr(case, name)
+            parts[name].append(t[b:e, h:h + 1])
+        bounds.append(bounds[-1] + e - b)
+        if case.init_state is not None:
+            s0.append(case.init_state[n:n + 1, h:h + 1])
+    cat = {name: torch.cat(x) for name, x in parts.items()}
+    o, fs = oracle.forward(cat["q"], cat["k"], cat["v"], cat["g"], cat["beta"], np.array(bounds),
+                           torch.cat(s0) if s0 else None, scale=case.scale, threads=threads)
+    return {c: (o[bounds[i]:bounds[i + 1], 0], fs[i, 0]) for i, c in enumerate(chains)}
+
+
+def _check_chains(case, o, fs, chains, tag):
+    refs = _chains_oracle(case, chains)
+    for n, h in chains:
+        o_ref, fs_ref = refs[(n, h)]
         b, e = int(case.cu_seqlens[n]), int(case.cu_seqlens[n + 1])
-        assert_close(o[b:e, h].float().cpu(), o_ref, f"o chain ({n},{h})")
-        assert_close(fs[n, h].cpu(), fs_ref, f"final_state chain ({n},{h})")
+        assert_close(o[b:e, h].float().cpu(), o_ref, f"{tag} o chain ({n},{h})")
+        assert_close(fs[n, h].cpu(), fs_ref, f"{tag} final_state chain ({n},{h})")
 
 
 def _run(kda, case):
+    """kda_chunk_fwd with the full workspace, as the benchmark calls it."""
     d = to_dev(case)
+    ws = kda.new_workspace(kda.kda_chunk_fwd_workspace_size(case.N, case.T_total, case.H, case.dk, case.dv),
+                           "cuda")
     o, fs = kda.kda_chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], cu_seqlens=d["cu_seqlens"],
-                              init_state=d["init_state"], scale=case.scale)
-    ws = kda.new_workspace(256, "cuda")
-    torch.cuda.synchronize()
+                              init_state=d["init_state"], scale=case.scale, workspace=ws)
+    assert kda.kda_device_status(ws) == kda.KDA_OK
     return o, fs
 
 
@@ -63,10 +80,11 @@ def test_multi_chunk_varlen(kda, lengths):
 
 
 def test_prefill_4k_full_size_sampled(kda):
+    """Eight chains of the 4 x 4096 benchmark batch, the first and the last (sequence, head) among them."""
     case = workloads.named_case("prefill_4k")
     o, fs = _run(kda, case)
     assert torch.isfinite(o.float()).all() and torch.isfinite(fs).all()
-    _check_chains(case, o, fs, [(0, 0), (1, 7), (2, 19), (3, 31)])
+    _check_chains(case, o, fs, [(0, 0), (0, 31), (1, 7), (1, 16), (2, 19), (2, 2), (3, 0), (3, 31)], "prefill_4k")
 
 
 def test_varlen_64_full_size_sampled(kda):
@@ -74,30 +92,33 @@ def test_varlen_64_full_size_sampled(kda):
     o, fs = _run(kda, case)
     lens = np.diff(case.cu_seqlens.numpy())
     longest, shortest = int(np.argmax(lens)), int(np.argmin(lens))
-    _check_chains(case, o, fs, [(longest, 3), (shortest, 30), (17, 12)])
+    _check_chains(case, o, fs, [(longest, 3), (longest, 31), (shortest, 30), (17, 12), (0, 0), (63, 31)],
+                  "varlen_64")
 
 
 def test_long_128k_full_size_sampled(kda):
+    """Eight of the 32 chains of 131072 tokens (T-segment split path), head 31 among them."""
     case = workloads.named_case("long_128k")
     o, fs = _run(kda, case)
-    _check_chains(case, o, fs, [(0, 0), (0, 21)])
+    _check_chains(case, o, fs, [(0, h) for h in (0, 5, 9, 14, 21, 26, 30, 31)], "long_128k")
 
 
 def test_spec_rollout_committed_states(kda):
-    """2048-token prefill of 128 sequences, then verify (4 tokens) + replay of the accepted
-    prefix, repeated; committed states and verify outputs checked on sampled chains."""
-    steps = 8
+    """The rollout workload in full: a 2048-token prefill of 128 sequences, then 64 x (4-token
+    verify from the committed states + replay of the accepted prefix, U{1..4} tokens).  Verify
+    outputs and committed states are checked against the oracle on sampled chains at every step."""
+    steps = 64
     case = workloads.named_case("spec_rollout")
     d = to_dev(case)
     N, H, dk, dv = case.N, case.H, case.dk, case.dv
     pool = torch.zeros(N, H, dk, dv, dtype=torch.float32, device="cuda")
     kda.kda_chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], cu_seqlens=d["cu_seqlens"], final_state=pool)
     acc = workloads.make_accept_lengths(steps, N, 4, seed=404)
-    sample = [(0, 0), (57, 13), (127, 31)]
-    ref = {}
-    for n, h in sample:
-        _, fs = _chain_oracle(case, n, h)
-        ref[(n, h)] = fs
+    sample = [(0, 0), (31, 31), (57, 13), (64, 1), (100, 22), (127, 31)]
+    prefill_refs = _chains_oracle(case, sample)
+    ref = {c: prefill_refs[c][1] for c in sample}
+    for c in sample:
+        assert_close(pool[c[0], c[1]].cpu(), ref[c], f"spec_rollout prefill state chain {c}")
     cu4 = torch.arange(0, 4 * N + 1, 4, dtype=torch.int32, device="cuda")
     ws_v = kda.new_workspace(kda.kda_chunk_fwd_workspace_size(N, 4 * N, H, dk, dv), "cuda")
     for s in range(steps):
@@ -117,12 +138,12 @@ def test_spec_rollout_committed_states(kda):
             pk = lambda x: x[sl, h:h + 1].cpu()
             o_ref, _ = oracle.forward(pk(q), pk(k), pk(v), pk(g), b[sl, h:h + 1].cpu(), np.array([0, 4]),
                                       ref[(n, h)][None, None])
-            assert_close(o_v[sl, h].float().cpu(), o_ref[:, 0], f"verify o step {s} chain ({n},{h})")
+            assert_close(o_v[sl, h].float().cpu(), o_ref[:, 0], f"spec_rollout verify o step {s} chain ({n},{h})")
             na = int(a[n])
             _, fs = oracle.forward(None, pk(k)[:na], pk(v)[:na], pk(g)[:na], b[sl, h:h + 1].cpu()[:na],
                                    np.array([0, na]), ref[(n, h)][None, None], want_o=False)
             ref[(n, h)] = fs[0, 0]
-            assert_close(pool[n, h].cpu(), ref[(n, h)], f"committed state step {s} chain ({n},{h})")
+            assert_close(pool[n, h].cpu(), ref[(n, h)], f"spec_rollout committed state step {s} chain ({n},{h})")
 
 
 def test_gate_range_violation_is_reported(kda):

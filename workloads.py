@@ -22,7 +22,11 @@ library standardises on):
   alpha = sigmoid(x_g) and beta = sigmoid(x_beta)); the caller passes
   scale = 1/sqrt(dk).
 
-All draws use a CPU ``torch.Generator`` seeded with the case seed.
+All draws use a CPU ``torch.Generator`` seeded with the case seed, so the oracle
+and the library see the same bytes.  ``device="cuda"`` draws the same recipe with
+a CUDA generator seeded the same way (other bytes, same distributions): the
+benchmark uses it for its large timing-only workloads, where no oracle compares.
+Sequence lengths and accept lengths are always drawn on the CPU.
 """
 from __future__ import annotations
 
@@ -77,8 +81,8 @@ class KdaCase:
         return n
 
 
-def _gen(seed: int) -> torch.Generator:
-    g = torch.Generator(device="cpu")
+def _gen(seed: int, device="cpu") -> torch.Generator:
+    g = torch.Generator(device=device)
     g.manual_seed(int(seed))
     return g
 
@@ -92,11 +96,12 @@ def varlen_lengths(n_seq: int, median: int, sigma: float, lo: int, hi: int, gen:
 
 def _draw_tokens(T: int, H: int, dk: int, dv: int, dtype: torch.dtype, gen: torch.Generator,
                  g_mu: float, q_scale: bool = True, raw: bool = False):
-    q = torch.randn(T, H, dk, generator=gen, dtype=torch.float32)
-    k = torch.randn(T, H, dk, generator=gen, dtype=torch.float32)
-    v = torch.randn(T, H, dv, generator=gen, dtype=torch.float32)
-    xg = torch.randn(T, H, dk, generator=gen, dtype=torch.float32) + g_mu
-    xb = torch.randn(T, H, generator=gen, dtype=torch.float32)
+    dev = gen.device
+    q = torch.randn(T, H, dk, generator=gen, dtype=torch.float32, device=dev)
+    k = torch.randn(T, H, dk, generator=gen, dtype=torch.float32, device=dev)
+    v = torch.randn(T, H, dv, generator=gen, dtype=torch.float32, device=dev)
+    xg = torch.randn(T, H, dk, generator=gen, dtype=torch.float32, device=dev) + g_mu
+    xb = torch.randn(T, H, generator=gen, dtype=torch.float32, device=dev)
     if raw:
         return (q.to(dtype), k.to(dtype), v.to(dtype), xg.to(dtype), xb.to(dtype))
     k = k / k.norm(dim=-1, keepdim=True).clamp_min(1e-12)
@@ -109,22 +114,25 @@ def _draw_tokens(T: int, H: int, dk: int, dv: int, dtype: torch.dtype, gen: torc
 
 def make_case(lengths: List[int], H: int, dk: int, dv: int, dtype: torch.dtype = torch.bfloat16,
               seed: int = 0, init: bool = True, g_mu: float = 3.0, init_std: float = 0.02,
-              q_scale: bool = True, scale: float = 1.0, raw: bool = False) -> KdaCase:
+              q_scale: bool = True, scale: float = 1.0, raw: bool = False, device="cpu") -> KdaCase:
     """Packed varlen case with the given per-sequence lengths.
 
     ``q_scale`` folds 1/sqrt(dk) into q (then ``scale`` is normally 1.0);
     ``q_scale=False`` leaves q raw so the caller passes ``scale=1/sqrt(dk)``.
     ``raw`` returns the un-preprocessed draws (see the module docstring).
+    ``device`` is where the draws are made and kept (see the module docstring).
     """
-    gen = _gen(seed)
+    gen = _gen(seed, device)
     T = int(sum(lengths))
     q, k, v, g, beta = _draw_tokens(T, H, dk, dv, dtype, gen, g_mu, q_scale, raw)
     cu = torch.zeros(len(lengths) + 1, dtype=torch.int32)
     if lengths:
         cu[1:] = torch.cumsum(torch.tensor(lengths, dtype=torch.int64), 0).to(torch.int32)
+    cu = cu.to(device)
     s0 = None
     if init:
-        s0 = (torch.randn(len(lengths), H, dk, dv, generator=gen, dtype=torch.float32) * init_std)
+        s0 = (torch.randn(len(lengths), H, dk, dv, generator=gen, dtype=torch.float32, device=gen.device)
+              * init_std)
     return KdaCase(q, k, v, g, beta, cu, s0, float(scale), list(lengths))
 
 
@@ -154,9 +162,11 @@ def _torch_dtype(name: str) -> torch.dtype:
     return {"bf16": torch.bfloat16, "f32": torch.float32}[name]
 
 
-def named_case(name: str, lengths_override: Optional[List[int]] = None, raw: bool = False) -> KdaCase:
+def named_case(name: str, lengths_override: Optional[List[int]] = None, raw: bool = False,
+               device="cpu") -> KdaCase:
     """Build one of ``NAMED_WORKLOADS`` (the prefill part for ``spec_rollout``); ``raw``
-    gives the same draws before preprocessing, with scale = 1/sqrt(dk)."""
+    gives the same draws before preprocessing, with scale = 1/sqrt(dk); ``device`` as in
+    ``make_case``."""
     w = NAMED_WORKLOADS[name]
     seed = w["seed"]
     if lengths_override is not None:
@@ -167,13 +177,13 @@ def named_case(name: str, lengths_override: Optional[List[int]] = None, raw: boo
         lengths = list(w["lengths"])
     return make_case(lengths, w["H"], w["dk"], w["dv"], _torch_dtype(w["dtype"]), seed=seed,
                      init=w["init"], g_mu=w["g_mu"], q_scale=not raw, scale=w["dk"] ** -0.5 if raw else 1.0,
-                     raw=raw)
+                     raw=raw, device=device)
 
 
 def make_decode_tokens(n_tok: int, H: int, dk: int, dv: int, dtype: torch.dtype, seed: int,
-                       g_mu: float = 3.0, raw: bool = False):
+                       g_mu: float = 3.0, raw: bool = False, device="cpu"):
     """Per-token inputs (q, k, v, g, beta) for ``n_tok`` decode/verify tokens."""
-    return _draw_tokens(n_tok, H, dk, dv, dtype, _gen(seed), g_mu, True, raw)
+    return _draw_tokens(n_tok, H, dk, dv, dtype, _gen(seed, device), g_mu, True, raw)
 
 
 def make_accept_lengths(n_steps: int, n_seq: int, max_accept: int, seed: int) -> torch.Tensor:
