@@ -56,6 +56,12 @@ size_t split_workspace(int N, int64_t T_total, int H, int dk, int dv) {
     return staging_offset() + 3 * state_bytes(N, H, dk, dv) + static_cast<size_t>(T_total) * H * dv * 2;
 }
 
+// Strong-decay fallback: one byte per (sequence, head) chain, after everything else the call
+// uses, when the workspace has room for it.  A chain whose chunk decays below the factored
+// form's range is then flagged by the chunked kernel and recomputed token by token.
+size_t align16(size_t x) { return (x + 15) & ~static_cast<size_t>(15); }
+size_t fallback_bytes(int N, int H) { return align16(static_cast<size_t>(N) * static_cast<size_t>(H)); }
+
 // Clears the status word at the start of the workspace (asynchronously on the stream).
 kda_status clear_status(void *workspace, cudaStream_t s) {
     if (cudaMemsetAsync(workspace, 0, sizeof(uint32_t), s) != cudaSuccess) return KDA_ERR_CUDA;
@@ -68,9 +74,12 @@ extern "C" {
 
 size_t kda_chunk_fwd_workspace_size(int N, int64_t T_total, int H, int dk, int dv) {
     if (N < 0 || T_total < 0 || H <= 0 || !dim_ok(dk) || !dim_ok(dv)) return 0;
-    if (split_shape(N, T_total, H, dk, dv)) return split_workspace(N, T_total, H, dk, dv);
-    if (order_shape(N, H)) return order_offset(N, H, dk, dv) + order_bytes(N);
-    return staging_offset() + state_bytes(N, H, dk, dv);
+    size_t used = staging_offset() + state_bytes(N, H, dk, dv);
+    if (split_shape(N, T_total, H, dk, dv))
+        used = split_workspace(N, T_total, H, dk, dv);
+    else if (order_shape(N, H))
+        used = order_offset(N, H, dk, dv) + order_bytes(N);
+    return align16(used) + fallback_bytes(N, H);
 }
 
 kda_status kda_chunk_fwd_prep(const void *q, const void *k, const void *v, const void *g, const void *beta,
@@ -109,18 +118,32 @@ kda_status kda_chunk_fwd_prep(const void *q, const void *k, const void *v, const
                              ? final_state
                              : reinterpret_cast<float *>(static_cast<char *>(workspace) + staging_offset());
 
+    uint8_t *fallback = nullptr;
     if (use_tc) {
         const bool split = split_shape(N, T_total, H, dk, dv) && ws_bytes >= split_workspace(N, T_total, H, dk, dv);
+        const bool ordered = !split && cu_seqlens && order_shape(N, H) &&
+                             ws_bytes >= order_offset(N, H, dk, dv) + order_bytes(N);
+        size_t used = KDA_WS_HEADER_BYTES + (final_state ? 0 : state_bytes(N, H, dk, dv));
+        if (split) used = split_workspace(N, T_total, H, dk, dv);
+        if (ordered) used = order_offset(N, H, dk, dv) + order_bytes(N);
+        if (ws_bytes >= align16(used) + fallback_bytes(N, H)) {
+            fallback = reinterpret_cast<uint8_t *>(static_cast<char *>(workspace) + align16(used));
+            if (cudaMemsetAsync(fallback, 0, static_cast<size_t>(N) * H, s) != cudaSuccess) return KDA_ERR_CUDA;
+        }
         kda::ChunkParams cp{};
         cp.q = q; cp.k = k; cp.v = v; cp.g = g; cp.beta = beta; cp.o = o;
         cp.N = N; cp.H = H; cp.scale = scale;
         cp.cu = cu_seqlens; cp.T_total = T_total; cp.seq_len_fixed = fixed_len;
         cp.init_state = init_state; cp.state_out = chunk_state; cp.status = status;
         cp.prep = static_cast<int>(prep); cp.prep_eps = l2_eps;
-        if (!split && cu_seqlens && order_shape(N, H) && ws_bytes >= order_offset(N, H, dk, dv) + order_bytes(N)) {
+        cp.fallback = fallback;
+        if (ordered) {
             int32_t *order = reinterpret_cast<int32_t *>(static_cast<char *>(workspace) + order_offset(N, H, dk, dv));
             if (kda::launch_order(cu_seqlens, N, order, s) != cudaSuccess) return KDA_ERR_CUDA;
             cp.order = order;
+            // Sequences with a full chunk rank first and at most T_total / 64 of them exist, so the
+            // CTAs of later ranks would find nothing to do (a batch of short verify sequences).
+            cp.n_active = static_cast<int>(T_total / 64 < N ? T_total / 64 : N);
         }
         if (split) {
             char *base = static_cast<char *>(workspace) + staging_offset() + state_bytes(N, H, dk, dv);
@@ -148,6 +171,7 @@ kda_status kda_chunk_fwd_prep(const void *q, const void *k, const void *v, const
     sp.state_in = init_state; sp.state_out = final_state; sp.chunk_state = chunk_state;
     sp.slots = nullptr; sp.num_slots = 0; sp.status = status;
     sp.prep = static_cast<int>(prep); sp.prep_eps = l2_eps;
+    sp.fallback = fallback;
     if (kda::launch_seq(sp, dk, dv, static_cast<int>(dtype), s) != cudaSuccess) return KDA_ERR_CUDA;
     return KDA_OK;
 }

@@ -45,6 +45,10 @@ struct SeqParams {
     // prefill only, or null: the state at the start of every 64-token chunk of sequence n
     // goes to slot (ckpt_base(n) + c) * H + h, ckpt_base(n) = floor(first token / 64) + n
     float *ckpt;
+    // prefill with chunk_skip, or null: per (sequence, head), 1 when the chunked kernel met a
+    // chunk it cannot factor (decay below its range); such a chain is recomputed here from its
+    // initial state, token by token, over the whole sequence
+    const uint8_t *fallback;
     // decode / replay only, or null: short convolution of q, k, v (width kConvW, then SiLU)
     // before everything else, weights [H, 2dk + dv, kConvW], states [slots, kConvW - 1, H,
     // 2dk + dv] indexed like the recurrent pool and updated in place
@@ -149,6 +153,13 @@ struct ChunkParams {
     // that a batch of more chains than one wave of CTAs starts its longest chains first
     // (needs split == 0)
     const int32_t *order;
+    // or null: per (sequence, head) flag set (instead of the gate-range error) when a chunk's
+    // decay leaves the range the factored form supports; the partial-chunk kernel then
+    // recomputes the chain token by token
+    uint8_t *fallback;
+    // with an order: CTAs are launched for the first n_active ranks only (sequences with a full
+    // chunk rank first, and at most T_total / 64 of them exist; 0 launches none)
+    int n_active;
 };
 // order[rank] = n, sequences ranked by full chunks (descending, ties by index).
 cudaError_t launch_order(const int32_t *cu, int N, int32_t *order, cudaStream_t stream);

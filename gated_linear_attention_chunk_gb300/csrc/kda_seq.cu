@@ -152,7 +152,8 @@ __global__ void __launch_bounds__(kSeqThreads, 6) kda_seq_kernel(SeqParams p) {
     }
     if (p.mode == SEQ_MODE_PREFILL) {
         const int64_t len = t1 - t0;
-        const int64_t nfull = p.chunk_skip ? len / 64 : 0;
+        const bool redo = p.fallback && p.fallback[pair];  // the chunked kernel gave this chain up
+        const int64_t nfull = (p.chunk_skip && !redo) ? len / 64 : 0;
         if (nfull > 0) {
             if (len % 64 == 0) return;  // the chunked kernel already left the final state
             src = p.chunk_state + pair * DK * DV;

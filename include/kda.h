@@ -61,7 +61,8 @@ typedef enum kda_status {
     KDA_ERR_UNSUPPORTED = 2,      /* dk/dv not in {64,128}, unknown dtype                     */
     KDA_ERR_WORKSPACE = 3,        /* workspace NULL or smaller than required                  */
     KDA_ERR_CUDA = 4,             /* a CUDA runtime call or launch failed                     */
-    KDA_ERR_GATE_RANGE = 5,       /* device: a 64-token chunk decays a channel below 2^-100  */
+    KDA_ERR_GATE_RANGE = 5,       /* device: a chunk decays below 2^-100 and the workspace has
+                                     no room to recompute its chain (see kda_chunk_fwd)       */
     KDA_ERR_TIMEOUT = 6,          /* device: a bounded wait gave up                           */
     KDA_ERR_BAD_SEQLENS = 7,      /* device: cu_seqlens / cu_accept not a valid partition     */
     KDA_ERR_BAD_SLOT = 8          /* device: slot index outside [0, num_slots)                */
@@ -101,7 +102,18 @@ typedef enum kda_dtype {
  * ranks the sequences by length on the device and starts the longest chains
  * first, which shortens the tail of a variable-length batch.  It needs N int32
  * (rounded up to 16 bytes) after the staging states, which this function then
- * includes; the results are bit-identical with or without it.
+ * includes; the results are bit-identical with or without it.  With it, chunked-kernel
+ * CTAs are launched only for the first floor(T_total / 64) sequences of that order
+ * (the others have no full chunk), which keeps a batch of short sequences (a
+ * speculative verify step) from paying for thousands of empty CTAs.
+ *
+ * Strong decay: the chunked kernel factors each chunk's decay through prefix
+ * products and needs every channel's product over a 64-token chunk to stay at or
+ * above 2^-100.  With N*H bytes (rounded up to 16) after everything above, which
+ * this function includes, a (sequence, head) chain that leaves that range is
+ * flagged and recomputed from its initial state by the token-sequential kernel,
+ * which takes any gate (g = -inf included); without that room the call reports
+ * KDA_ERR_GATE_RANGE instead.
  */
 size_t kda_chunk_fwd_workspace_size(int N, int64_t T_total, int H, int dk, int dv);
 
@@ -126,7 +138,9 @@ size_t kda_chunk_fwd_workspace_size(int N, int64_t T_total, int H, int dk, int d
  * the other dtype/size combinations run through the token-sequential kernel,
  * which is the same routine kda_decode_step and kda_replay use: a 1-token
  * sequence here gives the same bits as kda_decode_step on the same state.
- * An empty sequence copies init_state to final_state.
+ * An empty sequence copies init_state to final_state.  A chain whose chunk
+ * decays below the chunked kernel's range is recomputed token by token (see
+ * kda_chunk_fwd_workspace_size), so any gate values are accepted.
  */
 kda_status kda_chunk_fwd(const void *q, const void *k, const void *v, const void *g, const void *beta,
                          kda_dtype dtype, const float *init_state, const int32_t *cu_seqlens, int N,

@@ -36,18 +36,20 @@ def test_status_strings_and_version(lib):
 
 def test_workspace_size(lib):
     from gated_linear_attention_chunk_gb300 import kda
-    assert kda.kda_chunk_fwd_workspace_size(4, 16384, 32, 128, 128) == 256 + 4 * 32 * 128 * 128 * 4
+    fb = lambda N, H: (N * H + 15) // 16 * 16  # strong-decay fallback flags, one byte per chain
+    assert kda.kda_chunk_fwd_workspace_size(4, 16384, 32, 128, 128) == 256 + 4 * 32 * 128 * 128 * 4 + fb(4, 32)
     # few chains and long sequences: room for the T-segment split (three state sets + bf16 outputs)
-    assert kda.kda_chunk_fwd_workspace_size(1, 131072, 32, 128, 128) == 256 + 3 * 32 * 65536 + 131072 * 32 * 256
-    assert kda.kda_chunk_fwd_workspace_size(6, 4096, 8, 128, 128) == 256 + 3 * 48 * 65536 + 4096 * 8 * 256
-    assert kda.kda_chunk_fwd_workspace_size(7, 4096, 7, 128, 128) == 256 + 49 * 65536   # 49 chains: no split
-    assert kda.kda_chunk_fwd_workspace_size(1, 4095, 2, 128, 128) == 256 + 2 * 65536    # too short: no split
-    assert kda.kda_chunk_fwd_workspace_size(1, 8192, 2, 64, 64) == 256 + 2 * 16384      # d = 64: no split
+    assert kda.kda_chunk_fwd_workspace_size(1, 131072, 32, 128, 128) == \
+        256 + 3 * 32 * 65536 + 131072 * 32 * 256 + fb(1, 32)
+    assert kda.kda_chunk_fwd_workspace_size(6, 4096, 8, 128, 128) == 256 + 3 * 48 * 65536 + 4096 * 8 * 256 + fb(6, 8)
+    assert kda.kda_chunk_fwd_workspace_size(7, 4096, 7, 128, 128) == 256 + 49 * 65536 + fb(7, 7)  # 49 chains: no split
+    assert kda.kda_chunk_fwd_workspace_size(1, 4095, 2, 128, 128) == 256 + 2 * 65536 + fb(1, 2)  # too short: no split
+    assert kda.kda_chunk_fwd_workspace_size(1, 8192, 2, 64, 64) == 256 + 2 * 16384 + fb(1, 2)  # d = 64: no split
     assert kda.kda_chunk_fwd_workspace_size(0, 0, 1, 64, 64) == 256
     # more chains than one wave of CTAs: room for the launch order (N int32, 16-byte rounded)
-    assert kda.kda_chunk_fwd_workspace_size(64, 300000, 32, 128, 128) == 256 + 64 * 32 * 65536 + 256
-    assert kda.kda_chunk_fwd_workspace_size(39, 5000, 4, 64, 64) == 256 + 39 * 4 * 16384 + 160
-    assert kda.kda_chunk_fwd_workspace_size(38, 5000, 4, 64, 64) == 256 + 38 * 4 * 16384        # 152 chains: one wave
+    assert kda.kda_chunk_fwd_workspace_size(64, 300000, 32, 128, 128) == 256 + 64 * 32 * 65536 + 256 + fb(64, 32)
+    assert kda.kda_chunk_fwd_workspace_size(39, 5000, 4, 64, 64) == 256 + 39 * 4 * 16384 + 160 + fb(39, 4)
+    assert kda.kda_chunk_fwd_workspace_size(38, 5000, 4, 64, 64) == 256 + 38 * 4 * 16384 + fb(38, 4)  # one wave
     assert kda.kda_chunk_fwd_workspace_size(1, 10, 2, 96, 128) == 0
     assert kda.kda_chunk_fwd_workspace_size(-1, 10, 2, 64, 128) == 0
 

@@ -170,18 +170,28 @@ def test_prefill_prep_tail_is_bit_exact_with_decode_prep_steps(kda, r):
     assert torch.equal(_bits(state), _bits(fs_full))
 
 
-def test_sigmoid_gate_range_reported(kda):
-    """A raw gate so negative that a chunk's decay product falls below the supported
-    range is reported as KDA_ERR_GATE_RANGE, as with log-gates (tensor-core chunks)."""
+def test_sigmoid_gate_beyond_the_chunked_range(kda):
+    """A raw gate so negative that a chunk's decay product falls below the range the chunked
+    kernel factors (sigmoid(-6)^64 is about 2^-222): with the full workspace the chain is
+    recomputed token by token and matches the oracle; with only the status header the call
+    reports KDA_ERR_GATE_RANGE, as with log-gates."""
     case = _raw_case([128], H=1, seed=66)
-    case.g = torch.full_like(case.g, -6.0)   # sigmoid(-6)^64 is about 2^-222
+    case.g = torch.full_like(case.g, -6.0)
     d = to_dev(case)
     ws = kda.new_workspace(kda.kda_chunk_fwd_workspace_size(1, 128, 1, 128, 128), "cuda")
+    o, fs = kda.kda_chunk_fwd_prep(d["q"], d["k"], d["v"], d["g"], d["beta"], ALL, EPS, cu_seqlens=d["cu_seqlens"],
+                                   init_state=d["init_state"], scale=case.scale, workspace=ws)
+    assert kda.kda_device_status(ws) == kda.KDA_OK
+    o_ref, fs_ref = oracle.forward(case.q, case.k, case.v, case.g, case.beta, case.cu_seqlens, case.init_state,
+                                   scale=case.scale, prep_flags=ALL, prep_eps=EPS)
+    assert_close(o, o_ref, "o (strong sigmoid gate, recomputed)")
+    assert_close(fs, fs_ref, "final_state (strong sigmoid gate, recomputed)")
+    small = kda.new_workspace(kda.KDA_WS_HEADER_BYTES, "cuda")
     kda.kda_chunk_fwd_prep(d["q"], d["k"], d["v"], d["g"], d["beta"], ALL, EPS, cu_seqlens=d["cu_seqlens"],
-                           init_state=d["init_state"], scale=case.scale, workspace=ws)
-    assert kda.kda_device_status(ws) == kda.KDA_ERR_GATE_RANGE
+                           init_state=d["init_state"], scale=case.scale, workspace=small)
+    assert kda.kda_device_status(small) == kda.KDA_ERR_GATE_RANGE
     case.g = torch.full_like(case.g, 2.0)
     d = to_dev(case)
     kda.kda_chunk_fwd_prep(d["q"], d["k"], d["v"], d["g"], d["beta"], ALL, EPS, cu_seqlens=d["cu_seqlens"],
-                           init_state=d["init_state"], scale=case.scale, workspace=ws)
-    assert kda.kda_device_status(ws) == kda.KDA_OK
+                           init_state=d["init_state"], scale=case.scale, workspace=small)
+    assert kda.kda_device_status(small) == kda.KDA_OK

@@ -79,6 +79,24 @@ def test_multi_chunk_varlen(kda, lengths):
     assert_close(fs, fs_ref, "final_state")
 
 
+@pytest.mark.parametrize("lengths", [
+    [4] * 17 + [64] + [4] * 10 + [130, 70] + [4] * 9 + [200],   # verify-like: few full chunks among short sequences
+    [64, 0, 64] + [0] * 48 + [64],                              # exactly floor(T / 64) sequences with a full chunk
+    [3] * 60,                                                   # no full chunk at all (T >= 64)
+    [1] * 50,                                                   # T < 64
+])
+def test_many_short_sequences_launch_only_needed_ctas(kda, lengths):
+    """With more chains than one wave the sequences are ordered longest first and chunked CTAs are
+    launched only for the first floor(T / 64) ranks; every sequence still matches the oracle."""
+    case = workloads.make_case(lengths, H=4, dk=128, dv=128, seed=len(lengths))
+    assert case.N * case.H > 152
+    o, fs = _run(kda, case)
+    o_ref, fs_ref = oracle.forward(case.q, case.k, case.v, case.g, case.beta, case.cu_seqlens, case.init_state,
+                                   threads=0)
+    assert_close(o, o_ref, "o")
+    assert_close(fs, fs_ref, "final_state")
+
+
 def test_prefill_4k_full_size_sampled(kda):
     """Eight chains of the 4 x 4096 benchmark batch, the first and the last (sequence, head) among them."""
     case = workloads.named_case("prefill_4k")
