@@ -14,21 +14,19 @@
 //   U = Utl - W S,   O = Qbar S + P U,   S <- Diag(A_C) (S + Ktil^T U)
 //
 // Every factor stays bounded except Ktil (<= 1/A_C); the kernel therefore
-// requires A_C >= 2^-100 per channel and chunk (checked; KDA_ERR_GATE_RANGE).
+// requires A_C >= 2^-100 per channel and chunk (checked: such a chain is flagged
+// for the token-sequential kernel, or KDA_ERR_GATE_RANGE without room for the flag).
 //
 // One CTA per (sequence, head) walks its full chunks in order.  Warp roles:
-//   warp 0       TMA producer: v tiles (SW128) into a ring of two, L2 prefetch of later chunks
+//   warp 0       TMA producer: q, k, g, v tiles (SW128) + beta, 2-stage ring
 //   warp 1       chain MMA issuer (and TMEM owner)
 //   warp 2       prep MMA issuer (polls both prep products)
 //   warps 4-7    chain group: W tile from W^T, U and state epilogues in TMEM, O to HBM
-//   warps 8-15   decay group: raw q, k, g rows and beta from global memory into registers,
-//                prefix products, Kbar / Qbar / Ktil written into the stage once it is free
+//   warps 8-15   decay group: prefix products, Kbar / Qbar / Ktil in place
 //   warps 16-19  solve group: M and P from the accumulator, T' = (I+M)^-1 Diag(beta)
 // Registers are split per warpgroup with setmaxnreg (the control warps need few).
-// Three stages hold the Kbar / W, Qbar and Ktil tiles of three chunks.  The decay group
-// computes a chunk while the chain still holds that chunk's stage (the chunk three
-// before), so releasing a stage only costs the tiles' stores; the solve group runs
-// ahead of the chain by up to the W / Utl product.  The state lives in TMEM transposed (lane = value
+// The decay group runs up to one chunk ahead of the solve group, which runs one
+// chunk ahead of the chain.  The state lives in TMEM transposed (lane = value
 // column j, column = channel c) as an fp32 master plus a bf16 copy that feeds
 // the next chunk's MMAs as the A operand straight from TMEM.
 //
@@ -57,31 +55,24 @@ constexpr int kThreads = 640;   // 20 warps
 constexpr uint64_t kWaitNs = 1000000000ull;
 
 // dynamic shared memory map (offsets from a 1024-byte aligned base)
-#ifndef KDA_STAGES
-#define KDA_STAGES 3
-#endif
-constexpr int kStages = KDA_STAGES;                // chunks whose tiles are resident at once
-constexpr uint32_t kStage = 49152;                 // per stage: R (Kbar | Qbar, 32K), G (Ktil, 16K)
-constexpr uint32_t OFF_R = 0, OFF_G = 32768;
+constexpr uint32_t kStage = 65536;                 // per-stage: R (k|q, 32K), G (16K), V (16K)
+constexpr uint32_t OFF_R = 0, OFF_G = 32768, OFF_V = 49152;
 // The W tile of a chunk (MN-major, row = channel) is written over the Kbar half of
 // its R tile once Kbar's last reader (the W / Utl product) has completed.
-constexpr uint32_t OFF_VR = kStages * kStage;      // 2 x 16K   V tiles, ring of two (read by the W / Utl product only)
-constexpr uint32_t OFF_P = OFF_VR + 2 * 16384;     // 2 x 8K    P (K-major: row = token), by chunk parity
-constexpr uint32_t OFF_TT = OFF_P + 2 * 8192;      // 8K        T' (K-major)
-constexpr int kLdM = 68;                           // row stride (floats) of the fp32 M / T buffer (16-byte rows)
-// One fp32 64 x 64 buffer holds M and then T = (I + M)^-1: each block of T is written over the
-// block of M it replaces once that block has been read; rows 0-31, columns 32-63 (never used
-// by M, whose first 32 rows need only 32 columns) hold the block-product scratch.
-constexpr uint32_t OFF_M = OFF_TT + 8192;
-constexpr uint32_t kDynSmem = OFF_M + 64 * kLdM * 4 + 1024;
-static_assert(OFF_VR % 1024 == 0 && OFF_P % 1024 == 0 && OFF_TT % 1024 == 0, "swizzled tiles need 1024-byte alignment");
+constexpr uint32_t OFF_P = 2 * kStage;             // 2 x 8K    P (K-major: row = token)
+constexpr uint32_t OFF_TT = OFF_P + 2 * 8192;      // 2 x 8K    T' (K-major), by chunk parity
+constexpr int kLdM = 68;                           // row stride (floats) of the fp32 M buffer (16-byte rows)
+constexpr int kLdT = 72;                           // row stride of the fp32 T buffer (16-byte rows)
+constexpr int kLdX = 40;                           // row stride of the block-product scratch
+constexpr uint32_t OFF_M = OFF_TT + 2 * 8192;      // fp32 64 x kLdM
+constexpr uint32_t OFF_T = OFF_M + 64 * kLdM * 4;  // fp32 64 x kLdT
+constexpr uint32_t kDynSmem = OFF_T + 64 * kLdT * 4 + 1024;
 
 // TMEM columns (512 allocated)
 constexpr uint32_t TM_S = 0, TM_SB = 128, TM_U = 192, TM_W = 256, TM_UB = 320, TM_O = 352, TM_PREP = 416;
 
 struct TcParams {
     CUtensorMap tm_q, tm_k, tm_g, tm_v;
-    const __nv_bfloat16 *q, *k, *g;   // raw rows, read by the decay group
     const __nv_bfloat16 *beta;
     __nv_bfloat16 *o;
     const int32_t *order;         // launch order of the sequences, or null
@@ -125,6 +116,22 @@ __device__ __forceinline__ void mma_tf32(float (&c)[4], float a0, float a1, floa
         : "r"(__float_as_uint(a0)), "r"(__float_as_uint(a1)), "r"(__float_as_uint(a2)), "r"(__float_as_uint(a3)),
           "r"(__float_as_uint(b0)), "r"(__float_as_uint(b1)));
 }
+// Four 8x8 bf16 tiles from shared memory (lanes 8i .. 8i+7 give the row addresses of tile i).
+__device__ __forceinline__ void ldmatrix_x4(uint32_t (&r)[4], uint32_t addr) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr)
+                 : "memory");
+}
+// One m16n8k16 bf16 tile product c += a b, fp32 accumulation.
+__device__ __forceinline__ void mma_bf16_16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
 // Packed fp32 pairs: two floats in one 64-bit register pair, multiplied with one
 // f32x2 instruction (the decay and state-scaling loops are issue-bound).
 __device__ __forceinline__ uint64_t f2(float x, float y) {
@@ -167,33 +174,11 @@ __device__ __forceinline__ float ex2_approx(float x) {
     return r;
 }
 // Per-warpgroup register budgets (all four warps of a warpgroup execute the same one).
-template <int kRegs>
-__device__ __forceinline__ void regs_dec() { asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegs) : "memory"); }
-template <int kRegs>
-__device__ __forceinline__ void regs_inc() { asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegs) : "memory"); }
-// Register budgets per warpgroup: launched with 96 per thread (61440 for 640 threads, checked
-// on the host); control warps + chain + two decay warpgroups + solve add up to the same total.
-constexpr int kRegsCtl = 40, kRegsChain = 112, kRegsDecay = 104, kRegsSolve = 120;
-static_assert((kRegsCtl + kRegsChain + 2 * kRegsDecay + kRegsSolve) * 128 == kThreads * 96, "register split");
+__device__ __forceinline__ void regs_dec_48() { asm volatile("setmaxnreg.dec.sync.aligned.u32 48;" ::: "memory"); }
+__device__ __forceinline__ void regs_inc_120() { asm volatile("setmaxnreg.inc.sync.aligned.u32 120;" ::: "memory"); }
 __device__ __forceinline__ void named_bar(int id, int n) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
-
-// Opt-in timeline, compiled only with -DKDA_TIMELINE (never in the library's normal build): SM-clock
-// stamps of every hand-off of the first CTA's chunks, read back with kda_debug_timeline().
-#ifdef KDA_TIMELINE
-constexpr int kTlEvents = 24, kTlChunks = 64, kTlCtas = 1024;
-__device__ unsigned long long g_tl[kTlEvents][kTlChunks];
-__device__ unsigned long long g_tl_cta[kTlCtas][2];  // global-timer start and end of each CTA
-#define KDA_TL(ev, c)                                                                           \
-    do {                                                                                        \
-        if (blockIdx.x == 0 && (c) < kTlChunks) g_tl[ev][c] = static_cast<unsigned long long>(clock64()); \
-    } while (0)
-#else
-#define KDA_TL(ev, c) \
-    do {              \
-    } while (0)
-#endif
 
 struct Ctl {
     volatile int *abort;
@@ -242,11 +227,12 @@ template <bool kPrep>
 __global__ void __launch_bounds__(kThreads, 1) kda_chunk_tc_kernel(const __grid_constant__ TcParams p) {
     extern __shared__ uint8_t dsmem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(dsmem_raw) + 1023) & ~uintptr_t(1023));
-    __shared__ __align__(16) float s_beta[kStages][kC];
-    __shared__ __align__(16) float s_ac[4][kD];  // per-chunk A_C, ring of four
+    __shared__ __align__(16) float s_beta[2][kC];
+    __shared__ __align__(16) float s_ac[3][kD];  // per-chunk A_C, ring of three
+    __shared__ __align__(16) float s_x[32 * kLdX];
     __shared__ __align__(16) float s_tot[8][kD];
     __shared__ float s_rn[2][kC];  // inverse L2 norms of this chunk's k and q rows (preprocessing)
-    __shared__ uint64_t bar_vfull[2], bar_vfree[2], bar_free[kStages];
+    __shared__ uint64_t bar_full[2], bar_free[2];
     __shared__ uint64_t bar_elem, bar_mma1, bar_mfree, bar_tready, bar_mma2, bar_ready, bar_wfree, bar_c1, bar_uready,
         bar_c3;
     __shared__ uint64_t bar_drain[2];
@@ -297,10 +283,9 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_tc_kernel(const __grid_
 
     if (tid == 0) {
         for (int s = 0; s < 2; ++s) {
-            mbar_init(&bar_vfull[s], 1);
-            mbar_init(&bar_vfree[s], 1);
+            mbar_init(&bar_full[s], 2);
+            mbar_init(&bar_free[s], 1);
         }
-        for (int s = 0; s < kStages; ++s) mbar_init(&bar_free[s], 1);
         mbar_init(&bar_elem, 1);
         mbar_init(&bar_mma1, 1);
         mbar_init(&bar_mfree, 1);
@@ -323,69 +308,80 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_tc_kernel(const __grid_
         tmem_alloc(&s_tmem, 512);
         tmem_relinquish();
     }
-    if (role == 2) {  // the transition run has v = 0: both V tiles of the ring stay zero
-        for (int i = tid; i < 2 * 16384 / 16; i += kThreads)
-            reinterpret_cast<uint4 *>(sm + OFF_VR)[i] = make_uint4(0u, 0u, 0u, 0u);
+    if (role == 2) {  // the transition run has v = 0: both stages' V tiles stay zero
+        for (int i = tid; i < 2 * 16384 / 16; i += kThreads) {
+            const int st = i / (16384 / 16), w = i % (16384 / 16);
+            reinterpret_cast<uint4 *>(sm + st * kStage + OFF_V)[w] = make_uint4(0u, 0u, 0u, 0u);
+        }
         fence_proxy_async_smem();
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-#ifdef KDA_TIMELINE
-    if (tid == 0 && blockIdx.x < kTlCtas) g_tl_cta[blockIdx.x][0] = globaltimer_ns();
-#endif
     const uint32_t tmem = s_tmem;
     const Ctl ctl{&s_abort, p.status};
     const uint32_t sm_base = smem_u32(sm);
 
     // Register split per warpgroup (setmaxnreg; each warpgroup's four warps take the same
     // share): launched with 96 per thread, 61440 for 640 threads (checked on the host);
-    // control warps 40, chain group 112, the two decay warpgroups 104, solve group 120:
-    // (40 + 112 + 104 + 104 + 120) x 128 = 61440.
+    // control warps 48, chain and solve groups 120, the two decay warpgroups 96:
+    // (48 + 120 + 96 + 96 + 120) x 128 = 61440.
     if (warp < 4) {
-        regs_dec<kRegsCtl>();
+        regs_dec_48();
         if (warp == 0) {
             // ------------------------------------------------------------------ TMA producer
-            // The V tile of each chunk into the V ring (the decay group writes the other tiles)
-            // and L2 prefetches of the rows the decay group reads two chunks later.
             const bool v_zero = (role == 2);
             int issued0 = -1, issued1 = -1;
-            auto prefetch = [&](int c) {
-                const int t = static_cast<int>(bos + static_cast<int64_t>(c) * kC);
-                for (int x = 0; x < 128; x += 64) {
-                    tma_prefetch_l2_3d(&p.tm_q, x, h, t);
-                    tma_prefetch_l2_3d(&p.tm_k, x, h, t);
-                    tma_prefetch_l2_3d(&p.tm_g, x, h, t);
-                    if (!v_zero) tma_prefetch_l2_3d(&p.tm_v, x, h, t);
-                }
-            };
-            if (lane == 0 && nfull > 1) prefetch(1);
             for (int c = 0; c < nfull; ++c) {
                 const int s = c & 1;
                 const int t0 = static_cast<int>(bos + static_cast<int64_t>(c) * kC);
-                // the slot held chunk c - 2's V until its W / Utl product completed
-                if (c >= 2 && !warp_wait(&bar_vfree[s], ((c >> 1) - 1) & 1, ctl, lane)) break;
-                if (lane == 0) KDA_TL(21, c);
-                uint8_t *vt = sm + OFF_VR + s * 16384;
-                if (lane == 0) {
-                    if (v_zero) {
-                        mbar_arrive(&bar_vfull[s]);
-                    } else {
-                        mbar_arrive_expect_tx(&bar_vfull[s], 16384);
-                        tma_load_3d(vt + 0, &p.tm_v, 0, h, t0, &bar_vfull[s]);
-                        tma_load_3d(vt + 8192, &p.tm_v, 64, h, t0, &bar_vfull[s]);
+                // beta for this chunk: loaded before waiting for the stage, so its latency overlaps the wait
+                float b_lo = __bfloat162float(p.beta[(static_cast<int64_t>(t0) + lane) * H + h]);
+                float b_hi = __bfloat162float(p.beta[(static_cast<int64_t>(t0) + lane + 32) * H + h]);
+                if constexpr (kPrep) {
+                    if (p.prep & PREP_SIGMOID_BETA) {  // beta = sigmoid(x_beta)
+                        b_lo = 1.f / (1.f + __expf(-b_lo));
+                        b_hi = 1.f / (1.f + __expf(-b_hi));
                     }
-                    if (c + 2 < nfull) prefetch(c + 2);
+                }
+                if (c >= 2 && !warp_wait(&bar_free[s], ((c >> 1) - 1) & 1, ctl, lane)) break;
+                uint8_t *st = sm + s * kStage;
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(&bar_full[s], v_zero ? kStage - 16384 : kStage);
+                    tma_load_3d(st + OFF_R + 0, &p.tm_k, 0, h, t0, &bar_full[s]);
+                    tma_load_3d(st + OFF_R + 16384, &p.tm_k, 64, h, t0, &bar_full[s]);
+                    tma_load_3d(st + OFF_R + 8192, &p.tm_q, 0, h, t0, &bar_full[s]);
+                    tma_load_3d(st + OFF_R + 24576, &p.tm_q, 64, h, t0, &bar_full[s]);
+                    tma_load_3d(st + OFF_G + 0, &p.tm_g, 0, h, t0, &bar_full[s]);
+                    tma_load_3d(st + OFF_G + 8192, &p.tm_g, 64, h, t0, &bar_full[s]);
+                    if (!v_zero) {
+                        tma_load_3d(st + OFF_V + 0, &p.tm_v, 0, h, t0, &bar_full[s]);
+                        tma_load_3d(st + OFF_V + 8192, &p.tm_v, 64, h, t0, &bar_full[s]);
+                    }
+                    // warm L2 with the chunk that will reuse this stage, so its load is short
+                    if (c + 2 < nfull) {
+                        const int t2 = t0 + 2 * kC;
+                        for (int x = 0; x < 128; x += 64) {
+                            tma_prefetch_l2_3d(&p.tm_q, x, h, t2);
+                            tma_prefetch_l2_3d(&p.tm_k, x, h, t2);
+                            tma_prefetch_l2_3d(&p.tm_g, x, h, t2);
+                            if (!v_zero) tma_prefetch_l2_3d(&p.tm_v, x, h, t2);
+                        }
+                    }
                 }
                 if (s == 0) issued0 = c; else issued1 = c;
+                s_beta[s][lane] = b_lo;
+                s_beta[s][lane + 32] = b_hi;
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bar_full[s]);
             }
             // make sure no TMA copy is still landing in shared memory when the CTA exits
             const uint64_t deadline = globaltimer_ns() + kWaitNs;
             if (issued0 >= 0)
-                while (!mbar_try_wait(&bar_vfull[0], (issued0 >> 1) & 1) && globaltimer_ns() < deadline) {
+                while (!mbar_try_wait(&bar_full[0], (issued0 >> 1) & 1) && globaltimer_ns() < deadline) {
                 }
             if (issued1 >= 0)
-                while (!mbar_try_wait(&bar_vfull[1], (issued1 >> 1) & 1) && globaltimer_ns() < deadline) {
+                while (!mbar_try_wait(&bar_full[1], (issued1 >> 1) & 1) && globaltimer_ns() < deadline) {
                 }
         } else if (warp == 1) {
             // ------------------------------------------------------------------ chain MMA issuer
@@ -394,28 +390,25 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_tc_kernel(const __grid_
                 const uint32_t idO = idesc_bf16(128, 64, false, false);         // O  = S^T Qbar^T, += U^T P^T
                 const uint32_t idS = idesc_bf16(128, 128, false, true);         // S += U^T Ktil (Ktil MN-major)
                 for (int c = 0; c < nfull; ++c) {
-                    const int s = c % kStages;
+                    const int s = c & 1;
                     if (!wait_bar(&bar_ready, c & 1, ctl)) break;
-                    KDA_TL(17, c);
                     tc_fence_after();
                     const uint32_t st = sm_base + s * kStage;
                     // descriptors built once per chunk; k-steps add constant start offsets
                     const uint64_t dW = sdesc_sw128(st + OFF_R, 8192, 1024);          // W over Kbar, MN-major
                     const uint64_t dQ = sdesc_sw128(st + OFF_R + 8192, 16, 1024);     // Qbar, K-major
-                    const uint64_t dP = sdesc_sw128(sm_base + OFF_P + (c & 1) * 8192, 16, 1024);
+                    const uint64_t dP = sdesc_sw128(sm_base + OFF_P + s * 8192, 16, 1024);
                     const uint64_t dG = sdesc_sw128(st + OFF_G, 8192, 1024);          // Ktil, MN-major
 #pragma unroll
                     for (int ks = 0; ks < 8; ++ks)
                         mma_bf16_ts(tmem + TM_U, tmem + TM_SB + 8 * ks, dW + (((ks >> 2) * 16384 + (ks & 3) * 2048) >> 4),
                                     idU, 1u);
                     mma_commit(&bar_c1);  // U is on the critical path: release its epilogue first
-                    KDA_TL(18, c);
 #pragma unroll
                     for (int ks = 0; ks < 8; ++ks)
                         mma_bf16_ts(tmem + TM_O, tmem + TM_SB + 8 * ks, dQ + (((ks >> 2) * 16384 + (ks & 3) * 32) >> 4),
                                     idO, ks > 0 ? 1u : 0u);
                     if (!wait_bar(&bar_uready, c & 1, ctl)) break;
-                    KDA_TL(19, c);
                     tc_fence_after();
 #pragma unroll
                     for (int ks = 0; ks < 4; ++ks)
@@ -424,7 +417,6 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_tc_kernel(const __grid_
                     for (int ks = 0; ks < 4; ++ks)
                         mma_bf16_ts(tmem + TM_O, tmem + TM_UB + 8 * ks, dP + ((ks * 32) >> 4), idO, 1u);
                     mma_commit(&bar_c3);
-                    KDA_TL(20, c);
                     mma_commit(&bar_free[s]);
                 }
                 // drain: every MMA this thread issued completes before the TMEM is freed
@@ -448,7 +440,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_tc_kernel(const __grid_
                     if (c1 < nfull && mbar_test_wait(&bar_elem, c1 & 1) &&
                         (c1 == 0 || mbar_test_wait(&bar_mfree, (c1 - 1) & 1))) {
                         tc_fence_after();
-                        const uint32_t st = sm_base + (c1 % kStages) * kStage;
+                        const uint32_t st = sm_base + (c1 & 1) * kStage;
                         const uint64_t dA = sdesc_sw128(st + OFF_R, 16, 1024);   // [Kbar; Qbar], K-major
                         const uint64_t dB = sdesc_sw128(st + OFF_G, 16, 1024);   // Ktil, K-major
 #pragma unroll
@@ -456,17 +448,16 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_tc_kernel(const __grid_
                             mma_bf16_ss(tmem + TM_PREP, dA + (((ks >> 2) * 16384 + (ks & 3) * 32) >> 4),
                                         dB + (((ks >> 2) * 8192 + (ks & 3) * 32) >> 4), id1, ks > 0 ? 1u : 0u);
                         mma_commit(&bar_mma1);
-                        KDA_TL(4, c1);
                         ++c1;
                         progress = true;
                     }
-                    if (c2 < c1 && mbar_test_wait(&bar_tready, c2 & 1) && mbar_test_wait(&bar_vfull[c2 & 1], (c2 >> 1) & 1) &&
+                    if (c2 < c1 && mbar_test_wait(&bar_tready, c2 & 1) &&
                         (c2 == 0 || (mbar_test_wait(&bar_wfree, (c2 - 1) & 1) && mbar_test_wait(&bar_uready, (c2 - 1) & 1)))) {
                         tc_fence_after();
-                        const uint32_t st = sm_base + (c2 % kStages) * kStage;
+                        const uint32_t st = sm_base + (c2 & 1) * kStage;
                         const uint64_t dK = sdesc_sw128(st + OFF_R, 16384, 1024);  // Kbar^T, MN-major
-                        const uint64_t dV = sdesc_sw128(sm_base + OFF_VR + (c2 & 1) * 16384, 8192, 1024);  // V^T, MN-major
-                        const uint64_t dT = sdesc_sw128(sm_base + OFF_TT, 16, 1024);  // T', K-major
+                        const uint64_t dV = sdesc_sw128(st + OFF_V, 8192, 1024);   // V^T, MN-major
+                        const uint64_t dT = sdesc_sw128(sm_base + OFF_TT + (c2 & 1) * 8192, 16, 1024);  // T', K-major
 #pragma unroll
                         for (int ks = 0; ks < 4; ++ks)
                             mma_bf16_ss(tmem + TM_W, dK + ((ks * 2048) >> 4), dT + ((ks * 32) >> 4), id2, ks > 0 ? 1u : 0u);
@@ -474,8 +465,6 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_tc_kernel(const __grid_
                         for (int ks = 0; ks < 4; ++ks)
                             mma_bf16_ss(tmem + TM_U, dV + ((ks * 2048) >> 4), dT + ((ks * 32) >> 4), id2, ks > 0 ? 1u : 0u);
                         mma_commit(&bar_mma2);
-                        KDA_TL(5, c2);
-                        mma_commit(&bar_vfree[c2 & 1]);  // the V slot may take chunk c2 + 2
                         ++c2;
                         progress = true;
                     }
@@ -501,7 +490,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_tc_kernel(const __grid_
             }
         }
     } else if (warp < 8) {
-        regs_inc<kRegsChain>();
+        regs_inc_120();
         // ------------------------------------------------------------------ chain group
         const int j = tid - 128;  // TMEM lane: value column j (state, U, O); channel j (W^T)
         int gseq = 0;
@@ -564,13 +553,12 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_tc_kernel(const __grid_
         };
         bool done = true;
         for (int c = 0; c < nfull; ++c) {
-            const int s = c % kStages;
+            const int s = c & 1;
             // W^T (lane = channel) -> bf16 W tile, MN-major (row = channel, 64 tokens)
             if (!group_wait(&bar_mma2, c & 1, ctl, &s_grp_fail[1], 2, 128, gseq)) {
                 done = false;
                 break;
             }
-            if (j == 0) KDA_TL(11, c);
             tc_fence_after();
             {
                 uint8_t *W = sm + s * kStage + OFF_R + (j >> 6) * 16384;  // over Kbar
@@ -597,7 +585,6 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_tc_kernel(const __grid_
             named_bar(2, 128);
             if (j == 0) {
                 mbar_arrive(&bar_ready);   // W(c) written and the state of chunk c-1 final
-                KDA_TL(12, c);
                 mbar_arrive(&bar_wfree);   // W^T columns may take the next chunk's product
             }
             if (o_t0 >= 0) store_o(o_t0);  // previous chunk's O while C1 runs
@@ -607,7 +594,6 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_tc_kernel(const __grid_
                 done = false;
                 break;
             }
-            if (j == 0) KDA_TL(13, c);
             tc_fence_after();
             {
                 const uint32_t tU = tmem + lane_base + TM_U;
@@ -625,17 +611,13 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_tc_kernel(const __grid_
             }
             tc_fence_before();
             named_bar(2, 128);
-            if (j == 0) {
-                mbar_arrive(&bar_uready);
-                KDA_TL(14, c);
-            }
+            if (j == 0) mbar_arrive(&bar_uready);
 
             // state: S <- Diag(A_C)(S + Ktil^T U) with its bf16 copy; O into registers
             if (!group_wait(&bar_c3, c & 1, ctl, &s_grp_fail[1], 2, 128, gseq)) {
                 done = false;
                 break;
             }
-            if (j == 0) KDA_TL(15, c);
             tc_fence_after();
             const bool last = (c == nfull - 1);
             float *sout = (role == 0 ? p.state_out : role == 1 ? p.psi : p.phi) + pair * kD * kD;
@@ -646,7 +628,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_tc_kernel(const __grid_
                 tmem_ld_wait();
 #pragma unroll
                 for (int e = 0; e < 16; e += 4) {
-                    const float4 fa = ld4(&s_ac[c & 3][cc + e]), fb = ld4(&s_ac[c & 3][cc + 16 + e]);
+                    const float4 fa = ld4(&s_ac[c % 3][cc + e]), fb = ld4(&s_ac[c % 3][cc + 16 + e]);
                     scale2(a[e], a[e + 1], fa.x, fa.y);
                     scale2(a[e + 2], a[e + 3], fa.z, fa.w);
                     scale2(b[e], b[e + 1], fb.x, fb.y);
@@ -690,232 +672,191 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_tc_kernel(const __grid_
             }
             o_t0 = bos + static_cast<int64_t>(c) * kC;
             tmem_st_wait();
-            if (j == 0) KDA_TL(16, c);
             tc_fence_before();
             named_bar(2, 128);
         }
         if (done && o_t0 >= 0) store_o(o_t0);
     } else if (warp >= 8 && warp < 16) {
         // ------------------------------------------------------------------ decay group (warps 8-15)
-        // Decay factors and the scaled operand tiles.  Thread = (8-token segment = its warp in the
-        // group, channels 4 lane .. 4 lane + 3).  A chunk's raw k, q, g rows and beta are read from
-        // global memory into registers one chunk ahead (one warp instruction reads one 256-byte
-        // row), and the whole pass runs in registers: alpha = exp(g), prefix products within the
-        // segment, the earlier segments' totals carried in, Kbar = k A, Qbar = scale q A,
-        // Ktil = k / A.  Only the finished bf16 tiles go into the stage, once the chain has
-        // released it, so the pass overlaps the chain's work on the earlier chunks instead of
-        // sitting between the stage's release and the next chunk's products.
-        if constexpr (kRegsDecay > 96) regs_inc<kRegsDecay>();
-        if constexpr (kRegsDecay < 96) regs_dec<kRegsDecay>();
+        // Decay factors and the scaled operand tiles, one chunk ahead of the solve group.
+        // Thread = (8-token segment, 4 channels): alpha = exp(g), prefix products within
+        // the segment, the earlier segments' totals carried in, then Kbar, Qbar, Ktil
+        // written over k, q, g in place.
         const int pt = tid - 256;
-        const int seg = pt >> 5;
-        const int kb = lane >> 4, cc = 4 * (lane & 15), ch = 4 * lane;
-        const int r0 = 8 * seg;
         int gseq = 0;
         const float kMinDecay = 7.888609052210118e-31f;  // 2^-100
-        const uint2 *Kg = reinterpret_cast<const uint2 *>(p.k);
-        const uint2 *Qg = reinterpret_cast<const uint2 *>(p.q);
-        const uint2 *Gg = reinterpret_cast<const uint2 *>(p.g);
-        uint2 kr[8], qr[8], gr[8];  // raw rows r0 .. r0 + 7 of the next chunk, 4 channels each
-        float br = 0.f;             // beta of token r0 + lane (lanes 0-7)
-        auto load_raw = [&](int c) {
-            const int64_t t0 = bos + static_cast<int64_t>(c) * kC + r0;
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                const int64_t row = ((t0 + e) * H + h) * (kD / 4) + lane;  // in 8-byte units
-                gr[e] = __ldg(Gg + row);
-                kr[e] = __ldg(Kg + row);
-                qr[e] = __ldg(Qg + row);
-            }
-            if (lane < 8) br = __bfloat162float(p.beta[(t0 + lane) * H + h]);
-        };
-        bool sig_gate = false, norms = false, sig_beta = false;
-        if constexpr (kPrep) {
-            sig_gate = (p.prep & PREP_SIGMOID_GATE) != 0;
-            norms = (p.prep & (PREP_L2NORM_K | PREP_L2NORM_Q)) != 0;
-            sig_beta = (p.prep & PREP_SIGMOID_BETA) != 0;
-        }
         for (int c = 0; c < nfull; ++c) {
-            load_raw(c);
-            if (pt == 0) KDA_TL(0, c);
-            const int s = c % kStages;
-            // Pass 1: running products along the segment.  alpha = exp(g) = 2^(g log2 e),
-            // A_r = alpha_1 ... alpha_r.  With the sigmoid gate (preprocessing) alpha =
-            // 1 / (1 + 2^(-x log2 e)) and the running product is that of the denominators,
-            // D_r = 1 / A_r, so no reciprocal is taken per element here.
-            uint64_t A01[8], A23[8];
-            uint64_t P01 = f2(1.f, 1.f), P23 = f2(1.f, 1.f);
-            auto pass1 = [&](auto sig) {
-                constexpr bool kSig = decltype(sig)::value;
-                const float l2e = kSig ? -1.4426950408889634f : 1.4426950408889634f;
-                const uint64_t L2E = f2(l2e, l2e);
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const float2 l01 = uf2(mul2(bf2x(gr[e].x), L2E)), l23 = uf2(mul2(bf2x(gr[e].y), L2E));
-                    const uint64_t e01 = f2(ex2_approx(l01.x), ex2_approx(l01.y));
-                    const uint64_t e23 = f2(ex2_approx(l23.x), ex2_approx(l23.y));
-                    if constexpr (kSig) {
-                        P01 = fma2(P01, e01, P01);  // D *= 1 + e
-                        P23 = fma2(P23, e23, P23);
-                    } else {
-                        P01 = mul2(P01, e01);
-                        P23 = mul2(P23, e23);
-                    }
-                    A01[e] = P01;
-                    A23[e] = P23;
-                }
-            };
-            if (sig_gate)
-                pass1(std::true_type{});
-            else
-                pass1(std::false_type{});
-            if constexpr (kPrep) {
-                // Row norms (preprocessing): the warp's 32 lanes hold all 128 channels of its 8
-                // tokens, so the 16 sums of squares (k and q of each token) are reduced across the
-                // warp by a xor reduce-scatter (16 shuffles; lanes 2j and 2j + 1 end with sum j,
-                // j = 8 (lane bit 4) + 4 (bit 3) + 2 (bit 2) + (bit 1)); the even lane of each pair
-                // writes the inverse norm.
-                if (norms) {
-                    float v[16];
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        const float2 k01 = uf2(bf2x(kr[e].x)), k23 = uf2(bf2x(kr[e].y));
-                        const float2 q01 = uf2(bf2x(qr[e].x)), q23 = uf2(bf2x(qr[e].y));
-                        v[e] = fmaf(k23.y, k23.y, fmaf(k23.x, k23.x, fmaf(k01.y, k01.y, k01.x * k01.x)));
-                        v[8 + e] = fmaf(q23.y, q23.y, fmaf(q23.x, q23.x, fmaf(q01.y, q01.y, q01.x * q01.x)));
-                    }
-                    const bool b4 = (lane >> 4) & 1, b3 = (lane >> 3) & 1, b2 = (lane >> 2) & 1, b1 = (lane >> 1) & 1;
-                    float w[8], x[4], y[2];
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        const float send = b4 ? v[i] : v[8 + i], keep = b4 ? v[8 + i] : v[i];
-                        w[i] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
-                    }
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const float send = b3 ? w[i] : w[4 + i], keep = b3 ? w[4 + i] : w[i];
-                        x[i] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
-                    }
-#pragma unroll
-                    for (int i = 0; i < 2; ++i) {
-                        const float send = b2 ? x[i] : x[2 + i], keep = b2 ? x[2 + i] : x[i];
-                        y[i] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
-                    }
-                    float z = (b1 ? y[1] : y[0]) + __shfl_xor_sync(0xffffffffu, b1 ? y[0] : y[1], 2);
-                    z += __shfl_xor_sync(0xffffffffu, z, 1);
-                    if ((lane & 1) == 0) {
-                        const int j = 8 * b4 + 4 * b3 + 2 * b2 + b1;
-                        const bool on = (p.prep & (j < 8 ? PREP_L2NORM_K : PREP_L2NORM_Q)) != 0;
-                        s_rn[j >> 3][r0 + (j & 7)] = on ? rsqrtf(z + p.prep_eps) : 1.f;
-                    }
-                    __syncwarp();
-                }
-            }
-            const float2 pp01 = uf2(P01), pp23 = uf2(P23);
-            const float p0 = pp01.x, p1 = pp01.y, p2 = pp23.x, p3 = pp23.y;
-            st4(&s_tot[seg][ch], make_float4(p0, p1, p2, p3));
-            named_bar(1, 256);
-            float4 m = make_float4(1.f, 1.f, 1.f, 1.f);  // product of the earlier segments' totals
-            for (int q = 0; q < seg; ++q) {
-                const float4 t = ld4(&s_tot[q][ch]);
-                m = make_float4(m.x * t.x, m.y * t.y, m.z * t.z, m.w * t.w);
-            }
-            const float sc = p.scale;
-            const uint64_t m01 = f2(m.x, m.y), m23 = f2(m.z, m.w);
-            const uint64_t ms01 = f2(m.x * sc, m.y * sc), ms23 = f2(m.z * sc, m.w * sc);
-            // Pass 2: Kbar = k A, Qbar = scale q A, Ktil = k / A, into registers.  With
-            // L2-normalised rows (preprocessing) k and q are first scaled by their rows' inverse
-            // norms; with the sigmoid gate the running products are D = 1 / A.
-            uint2 ok[8], oq[8], og[8];
-            auto pass2 = [&](auto norm, auto sig) {
-                constexpr bool kNorm = decltype(norm)::value;
-                constexpr bool kSig = decltype(sig)::value;
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    uint64_t a01, a23, aq01, aq23, r01, r23;
-                    if constexpr (kSig) {
-                        r01 = mul2(m01, A01[e]);
-                        r23 = mul2(m23, A23[e]);
-                        const float2 fr01 = uf2(r01), fr23 = uf2(r23);
-                        a01 = f2(rcp_approx(fr01.x), rcp_approx(fr01.y));
-                        a23 = f2(rcp_approx(fr23.x), rcp_approx(fr23.y));
-                        aq01 = mul2(a01, f2(sc, sc));
-                        aq23 = mul2(a23, f2(sc, sc));
-                    } else {
-                        a01 = mul2(m01, A01[e]);
-                        a23 = mul2(m23, A23[e]);
-                        aq01 = mul2(ms01, A01[e]);
-                        aq23 = mul2(ms23, A23[e]);
-                        const float2 fa01 = uf2(a01), fa23 = uf2(a23);
-                        r01 = f2(rcp_approx(fa01.x), rcp_approx(fa01.y));
-                        r23 = f2(rcp_approx(fa23.x), rcp_approx(fa23.y));
-                    }
-                    uint64_t k01 = bf2x(kr[e].x), k23 = bf2x(kr[e].y);
-                    uint64_t q01 = bf2x(qr[e].x), q23 = bf2x(qr[e].y);
-                    if constexpr (kNorm) {
-                        const float rk = s_rn[0][r0 + e], rq = s_rn[1][r0 + e];
-                        k01 = mul2(k01, f2(rk, rk));
-                        k23 = mul2(k23, f2(rk, rk));
-                        q01 = mul2(q01, f2(rq, rq));
-                        q23 = mul2(q23, f2(rq, rq));
-                    }
-                    ok[e] = make_uint2(pk2(mul2(k01, a01)), pk2(mul2(k23, a23)));
-                    oq[e] = make_uint2(pk2(mul2(q01, aq01)), pk2(mul2(q23, aq23)));
-                    og[e] = make_uint2(pk2(mul2(k01, r01)), pk2(mul2(k23, r23)));
-                }
-            };
-            float4 ac;  // A_C of the chunk (segment 7 holds the last products)
-            if constexpr (!kPrep) {
-                pass2(std::false_type{}, std::false_type{});
-                ac = make_float4(m.x * p0, m.y * p1, m.z * p2, m.w * p3);
-            } else {
-                if (norms) {
-                    if (sig_gate) pass2(std::true_type{}, std::true_type{});
-                    else pass2(std::true_type{}, std::false_type{});
-                } else {
-                    if (sig_gate) pass2(std::false_type{}, std::true_type{});
-                    else pass2(std::false_type{}, std::false_type{});
-                }
-                const float4 x = make_float4(m.x * p0, m.y * p1, m.z * p2, m.w * p3);
-                ac = sig_gate ? make_float4(rcp_approx(x.x), rcp_approx(x.y), rcp_approx(x.z), rcp_approx(x.w)) : x;
-            }
-            if (pt == 0) KDA_TL(1, c);
-            // The stage of chunk c held chunk c - 3 until the chain's last products on it completed
-            // (which also means that chunk c - 4's state epilogue, the last reader of s_ac[c & 3],
-            // has finished: chunk c - 3's products started after it).
-            if (c >= kStages && !group_wait(&bar_free[s], (c / kStages - 1) & 1, ctl, &s_grp_fail[0], 1, 256, gseq))
-                break;
-            if (pt == 0) KDA_TL(2, c);
+            const int s = c & 1;
+            uint8_t *st = sm + s * kStage;
+            if (!group_wait(&bar_full[s], (c >> 1) & 1, ctl, &s_grp_fail[0], 1, 256, gseq)) break;
             {
-                uint8_t *st = sm + s * kStage;
+                // thread = (token segment of 8, channel quad): 64-bit shared accesses
+                const int cq = pt & 31, seg = pt >> 5;
+                const int kb = cq >> 4, cc = 4 * (cq & 15), ch = kb * 64 + cc;
                 uint8_t *Rk = st + OFF_R + kb * 16384;
                 uint8_t *Rq = Rk + 8192;
                 uint8_t *G = st + OFF_G + kb * 8192;
+                const int r0 = 8 * seg;
+                uint64_t A01[8], A23[8];
+                uint64_t P01 = f2(1.f, 1.f), P23 = f2(1.f, 1.f);
+                // Pass 1: running products along the segment.  alpha = exp(g) = 2^(g log2 e),
+                // A_r = alpha_1 ... alpha_r.  With the sigmoid gate (preprocessing) alpha =
+                // 1 / (1 + 2^(-x log2 e)) and the running product is that of the denominators,
+                // D_r = 1 / A_r, so no reciprocal is taken per element here.
+                auto pass1 = [&](auto sig) {
+                    constexpr bool kSig = decltype(sig)::value;
+                    const float l2e = kSig ? -1.4426950408889634f : 1.4426950408889634f;
+                    const uint64_t L2E = f2(l2e, l2e);
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const uint32_t off = swz(r0 + e, cc);
-                    *reinterpret_cast<uint2 *>(Rk + off) = ok[e];
-                    *reinterpret_cast<uint2 *>(Rq + off) = oq[e];
-                    *reinterpret_cast<uint2 *>(G + off) = og[e];
-                }
-            }
-            if (lane < 8) {
-                float b = br;
+                    for (int rr = 0; rr < 8; rr += 4) {
+                        uint2 gw[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) gw[e] = *reinterpret_cast<const uint2 *>(G + swz(r0 + rr + e, cc));
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const float2 l01 = uf2(mul2(bf2x(gw[e].x), L2E)), l23 = uf2(mul2(bf2x(gw[e].y), L2E));
+                            const uint64_t e01 = f2(ex2_approx(l01.x), ex2_approx(l01.y));
+                            const uint64_t e23 = f2(ex2_approx(l23.x), ex2_approx(l23.y));
+                            if constexpr (kSig) {
+                                P01 = fma2(P01, e01, P01);  // D *= 1 + e
+                                P23 = fma2(P23, e23, P23);
+                            } else {
+                                P01 = mul2(P01, e01);
+                                P23 = mul2(P23, e23);
+                            }
+                            A01[rr + e] = P01;
+                            A23[rr + e] = P23;
+                        }
+                    }
+                };
+                bool sig_gate = false, norms = false;
                 if constexpr (kPrep) {
-                    if (sig_beta) b = 1.f / (1.f + __expf(-b));  // beta = sigmoid(x_beta)
+                    sig_gate = (p.prep & PREP_SIGMOID_GATE) != 0;
+                    norms = (p.prep & (PREP_L2NORM_K | PREP_L2NORM_Q)) != 0;
                 }
-                s_beta[s][r0 + lane] = b;
-            }
-            if (seg == 7) {
-                if (!(ac.x >= kMinDecay) || !(ac.y >= kMinDecay) || !(ac.z >= kMinDecay) || !(ac.w >= kMinDecay)) {
-                    // out of the factored form's range: the token-sequential kernel redoes the chain
-                    // (its results here are discarded), or, without room for that flag, an error
-                    if (p.fallback)
-                        p.fallback[pair] = 1;
-                    else
-                        atomicOr(p.status, DEV_ERR_GATE);
+                // Row norms (preprocessing): each of the eight warps takes one 16-row block of k
+                // (warps 0-3) or q (warps 4-7) and forms the diagonal of its Gram block with
+                // m16n8k16 tensor-core tiles: a 16 x 16 slice loaded by ldmatrix is the A operand
+                // and, for each 8-row half, the B operand.  Issued before the first pass so that
+                // their latency overlaps it.
+                float nc0[4] = {0.f, 0.f, 0.f, 0.f}, nc1[4] = {0.f, 0.f, 0.f, 0.f};
+                const int ntq = seg >> 2, nblk = seg & 3;
+                if constexpr (kPrep) {
+                    if (norms) {
+                        const uint32_t nbase = sm_base + s * kStage + OFF_R + ntq * 8192;
+                        const int nrow = 16 * nblk + (cq & 7) + ((cq >> 3) & 1) * 8;
+#pragma unroll
+                        for (int nk = 0; nk < 8; ++nk) {
+                            uint32_t fa[4];
+                            ldmatrix_x4(fa, nbase + (nk >> 2) * 16384 + chunk16(nrow, 2 * (nk & 3) + (cq >> 4)));
+                            mma_bf16_16816(nc0, fa, fa[0], fa[2]);  // block x its rows 0-7
+                            mma_bf16_16816(nc1, fa, fa[1], fa[3]);  // block x its rows 8-15
+                        }
+                    }
                 }
-                st4(&s_ac[c & 3][ch], ac);
+                if (sig_gate)
+                    pass1(std::true_type{});
+                else
+                    pass1(std::false_type{});
+                if constexpr (kPrep) {
+                    // lane (g, g / 2) of the m16n8 accumulator layout holds rows g and g + 8 of the diagonal
+                    const int g8 = cq >> 2;
+                    if (norms && (cq & 3) == (g8 >> 1)) {
+                        const bool on = (p.prep & (ntq == 0 ? PREP_L2NORM_K : PREP_L2NORM_Q)) != 0;
+                        const float lo = (g8 & 1) ? nc0[1] : nc0[0], hi = (g8 & 1) ? nc1[3] : nc1[2];
+                        s_rn[ntq][16 * nblk + g8] = on ? rsqrtf(lo + p.prep_eps) : 1.f;
+                        s_rn[ntq][16 * nblk + g8 + 8] = on ? rsqrtf(hi + p.prep_eps) : 1.f;
+                    }
+                }
+                const float2 pp01 = uf2(P01), pp23 = uf2(P23);
+                const float p0 = pp01.x, p1 = pp01.y, p2 = pp23.x, p3 = pp23.y;
+                st4(&s_tot[seg][ch], make_float4(p0, p1, p2, p3));
+                named_bar(1, 256);
+                float4 m = make_float4(1.f, 1.f, 1.f, 1.f);  // product of the earlier segments' totals
+                for (int q = 0; q < seg; ++q) {
+                    const float4 t = ld4(&s_tot[q][ch]);
+                    m = make_float4(m.x * t.x, m.y * t.y, m.z * t.z, m.w * t.w);
+                }
+                const float sc = p.scale;
+                const uint64_t m01 = f2(m.x, m.y), m23 = f2(m.z, m.w);
+                const uint64_t ms01 = f2(m.x * sc, m.y * sc), ms23 = f2(m.z * sc, m.w * sc);
+                // Pass 2: Kbar = k A, Qbar = scale q A, Ktil = k / A over k, q, g in place.  With
+                // L2-normalised rows (preprocessing) k and q are first scaled by their rows'
+                // inverse norms; with the sigmoid gate the running products are D = 1 / A.
+                auto pass2 = [&](auto norm, auto sig) {
+                    constexpr bool kNorm = decltype(norm)::value;
+                    constexpr bool kSig = decltype(sig)::value;
+#pragma unroll
+                    for (int rr = 0; rr < 8; rr += 2) {
+                        uint2 kw[2], qw[2];
+#pragma unroll
+                        for (int e = 0; e < 2; ++e) {
+                            const uint32_t off = swz(r0 + rr + e, cc);
+                            kw[e] = *reinterpret_cast<const uint2 *>(Rk + off);
+                            qw[e] = *reinterpret_cast<const uint2 *>(Rq + off);
+                        }
+#pragma unroll
+                        for (int e = 0; e < 2; ++e) {
+                            const uint32_t off = swz(r0 + rr + e, cc);
+                            uint64_t a01, a23, aq01, aq23, r01, r23;
+                            if constexpr (kSig) {
+                                r01 = mul2(m01, A01[rr + e]);
+                                r23 = mul2(m23, A23[rr + e]);
+                                const float2 fr01 = uf2(r01), fr23 = uf2(r23);
+                                a01 = f2(rcp_approx(fr01.x), rcp_approx(fr01.y));
+                                a23 = f2(rcp_approx(fr23.x), rcp_approx(fr23.y));
+                                aq01 = mul2(a01, f2(sc, sc));
+                                aq23 = mul2(a23, f2(sc, sc));
+                            } else {
+                                a01 = mul2(m01, A01[rr + e]);
+                                a23 = mul2(m23, A23[rr + e]);
+                                aq01 = mul2(ms01, A01[rr + e]);
+                                aq23 = mul2(ms23, A23[rr + e]);
+                                const float2 fa01 = uf2(a01), fa23 = uf2(a23);
+                                r01 = f2(rcp_approx(fa01.x), rcp_approx(fa01.y));
+                                r23 = f2(rcp_approx(fa23.x), rcp_approx(fa23.y));
+                            }
+                            uint64_t k01 = bf2x(kw[e].x), k23 = bf2x(kw[e].y);
+                            uint64_t q01 = bf2x(qw[e].x), q23 = bf2x(qw[e].y);
+                            if constexpr (kNorm) {
+                                const float rk = s_rn[0][r0 + rr + e], rq = s_rn[1][r0 + rr + e];
+                                k01 = mul2(k01, f2(rk, rk));
+                                k23 = mul2(k23, f2(rk, rk));
+                                q01 = mul2(q01, f2(rq, rq));
+                                q23 = mul2(q23, f2(rq, rq));
+                            }
+                            *reinterpret_cast<uint2 *>(Rk + off) = make_uint2(pk2(mul2(k01, a01)), pk2(mul2(k23, a23)));
+                            *reinterpret_cast<uint2 *>(Rq + off) = make_uint2(pk2(mul2(q01, aq01)), pk2(mul2(q23, aq23)));
+                            *reinterpret_cast<uint2 *>(G + off) = make_uint2(pk2(mul2(k01, r01)), pk2(mul2(k23, r23)));
+                        }
+                    }
+                };
+                float4 ac;  // A_C of the chunk (segment 7 holds the last products)
+                if constexpr (!kPrep) {
+                    pass2(std::false_type{}, std::false_type{});
+                    ac = make_float4(m.x * p0, m.y * p1, m.z * p2, m.w * p3);
+                } else {
+                    if (norms) {
+                        if (sig_gate) pass2(std::true_type{}, std::true_type{});
+                        else pass2(std::true_type{}, std::false_type{});
+                    } else {
+                        if (sig_gate) pass2(std::false_type{}, std::true_type{});
+                        else pass2(std::false_type{}, std::false_type{});
+                    }
+                    const float4 x = make_float4(m.x * p0, m.y * p1, m.z * p2, m.w * p3);
+                    ac = sig_gate ? make_float4(rcp_approx(x.x), rcp_approx(x.y), rcp_approx(x.z), rcp_approx(x.w)) : x;
+                }
+                if (seg == 7) {
+                    if (!(ac.x >= kMinDecay) || !(ac.y >= kMinDecay) || !(ac.z >= kMinDecay) || !(ac.w >= kMinDecay)) {
+                        // out of the factored form's range: the token-sequential kernel redoes the chain
+                        // (its results here are discarded), or, without room for that flag, an error
+                        if (p.fallback)
+                            p.fallback[pair] = 1;
+                        else
+                            atomicOr(p.status, DEV_ERR_GATE);
+                    }
+                    st4(&s_ac[c % 3][ch], ac);
+                }
             }
             fence_proxy_async_smem();
             named_bar(1, 256);
@@ -923,37 +864,28 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_tc_kernel(const __grid_
                 // at most one chunk ahead of the MMA that consumes these tiles
                 if (c > 0) wait_bar(&bar_mma1, (c - 1) & 1, ctl);
                 mbar_arrive(&bar_elem);
-                KDA_TL(3, c);
             }
         }
     } else if (warp >= 16) {
-        regs_inc<kRegsSolve>();
+        regs_inc_120();
         // ------------------------------------------------------------------ solve group (warps 16-19)
         const int pt = tid - 512;
         const int wq = warp & 3;
         int gseq = 0;
-        // M and then T in one fp32 buffer (row stride kLdM); the block-product scratch X sits in
-        // its rows 0-31, columns 32-63, which neither M nor T uses.
         float *Mb = reinterpret_cast<float *>(sm + OFF_M);
-        float *Tb = Mb;
-        float *s_x = Mb + 32;
-        constexpr int kLdT = kLdM, kLdX = kLdM;
-        for (int i = pt; i < 2 * 8192 / 16; i += 128)  // T' blocks above the diagonal stay zero; likewise
-            reinterpret_cast<uint4 *>(sm + OFF_P)[i] = make_uint4(0u, 0u, 0u, 0u);  // P's columns 32-63 of rows 0-31
-        for (int i = pt; i < 8192 / 16; i += 128) reinterpret_cast<uint4 *>(sm + OFF_TT)[i] = make_uint4(0u, 0u, 0u, 0u);
+        float *Tb = reinterpret_cast<float *>(sm + OFF_T);
+        for (int i = pt; i < 64 * kLdT; i += 128) Tb[i] = 0.f;  // blocks above the diagonal stay zero
+        for (int i = pt; i < 2 * 8192 / 16; i += 128) {         // likewise in both T' tiles; both P tiles
+            reinterpret_cast<uint4 *>(sm + OFF_TT)[i] = make_uint4(0u, 0u, 0u, 0u);
+            reinterpret_cast<uint4 *>(sm + OFF_P)[i] = make_uint4(0u, 0u, 0u, 0u);
+        }
         named_bar(3, 128);
-        uint8_t *TT = sm + OFF_TT;  // T' = T Diag(beta), bf16, one chunk at a time
         for (int c = 0; c < nfull; ++c) {
-            const int s = c % kStages;
+            const int s = c & 1;
+            uint8_t *TT = sm + OFF_TT + (c & 1) * 8192;  // this chunk's T' = T Diag(beta), bf16
             // (2) M (fp32, rows scaled by beta, strictly lower) and P (bf16, lower incl.).
             // Accumulator lane x: rows 0-63 = Kbar . Ktil, 64-127 = Qbar . Ktil.
-            // P's buffer (c & 1) held chunk c - 2's P until that chunk's last products completed.
-            if (c >= 2 && !group_wait(&bar_free[(c - 2) % kStages], ((c - 2) / kStages) & 1, ctl, &s_grp_fail[2], 3,
-                                      128, gseq))
-                break;
-            if (pt == 0) KDA_TL(22, c);
             if (!group_wait(&bar_mma1, c & 1, ctl, &s_grp_fail[2], 3, 128, gseq)) break;
-            if (pt == 0) KDA_TL(6, c);
             tc_fence_after();
             {
                 // Warps 0 / 2 of the group hold rows 0-31 of M / P, which need only columns 0-31
@@ -988,7 +920,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_tc_kernel(const __grid_
                 } else {
                     // P = (Qbar Ktil^T)[r, :] for i <= r, bf16
                     const int r = x - 64;
-                    uint8_t *P = sm + OFF_P + (c & 1) * 8192;
+                    uint8_t *P = sm + OFF_P + s * 8192;
                     auto put8 = [&](int q8, bool masked) {
                         uint4 v;
                         uint32_t *vw = reinterpret_cast<uint32_t *>(&v);
@@ -1015,14 +947,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_tc_kernel(const __grid_
             fence_proxy_async_smem();
             tc_fence_before();
             named_bar(3, 128);
-            if (pt == 0) {
-                mbar_arrive(&bar_mfree);  // PREP columns may take the next chunk's product
-                KDA_TL(7, c);
-            }
-            // T' is written block by block below; its one tile held the previous chunk's T' until
-            // that chunk's W / Utl product completed.
-            if (c > 0 && !group_wait(&bar_mma2, (c - 1) & 1, ctl, &s_grp_fail[2], 3, 128, gseq)) break;
-            if (pt == 0) KDA_TL(23, c);
+            if (pt == 0) mbar_arrive(&bar_mfree);  // PREP columns may take the next chunk's product
 
             // (3) T = (I + M)^-1, blocked: the four 16x16 diagonal blocks D_b by forward
             // substitution, column-oriented (warp = block, lane = column, so the four blocks run
@@ -1050,7 +975,6 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_tc_kernel(const __grid_
                     }
                 }
                 const float bm = s_beta[s][R0 + mm];
-                __syncwarp(0x0000ffffu);  // D_b is written over M's diagonal block, which every lane has read
 #pragma unroll
                 for (int l = 0; l < 16; ++l) {
                     Tb[(R0 + l) * kLdT + R0 + mm] = xv[l];
@@ -1058,7 +982,6 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_tc_kernel(const __grid_
                 }
             }
             named_bar(3, 128);
-            if (pt == 0) KDA_TL(8, c);
             // ... then the off-diagonal blocks as tf32 tensor-core tiles (m16n8k8; each warp
             // owns output tiles): fragment row gq = lane / 4, column tq = lane % 4.
             const int gq = lane >> 2, tq = lane & 3;
@@ -1098,17 +1021,14 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_tc_kernel(const __grid_
                 *reinterpret_cast<uint32_t *>(TT + swz(Ra + gq + 8, cl)) = pack_bf16x2(-d[2] * b0, -d[3] * b1);
             }
             named_bar(3, 128);
-            if (pt == 0) KDA_TL(9, c);
             {
                 // lower-left quadrant T[32:64, 0:32] = -T22 (M[32:64, 0:32] T11); T11 = T[0:32, 0:32],
-                // T22 = T[32:64, 32:64].  Warp: 16 rows x 16 cols.  The upper-right 16 x 16 blocks of
-                // T11 and T22 are zero and are skipped (their place in the buffer still holds M).
+                // T22 = T[32:64, 32:64] (their upper-right blocks are zero).  Warp: 16 rows x 16 cols.
                 const int mt = wq >> 1, nh = wq & 1;
                 const int r0 = 16 * mt;
                 float c[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks) {
-                    if (nh == 1 && ks < 2) continue;  // T11[0:16, 16:32] = 0
                     const int k0 = 8 * ks;
                     const float a0 = Mb[(32 + r0 + gq) * kLdM + k0 + tq], a1 = Mb[(40 + r0 + gq) * kLdM + k0 + tq];
                     const float a2 = Mb[(32 + r0 + gq) * kLdM + k0 + tq + 4], a3 = Mb[(40 + r0 + gq) * kLdM + k0 + tq + 4];
@@ -1130,7 +1050,6 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_tc_kernel(const __grid_
                 float d[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks) {
-                    if (mt == 0 && ks >= 2) continue;  // T22[0:16, 16:32] = 0
                     const int k0 = 8 * ks;
                     const float a0 = Tb[(32 + r0 + gq) * kLdT + 32 + k0 + tq], a1 = Tb[(40 + r0 + gq) * kLdT + 32 + k0 + tq];
                     const float a2 = Tb[(32 + r0 + gq) * kLdT + 36 + k0 + tq], a3 = Tb[(40 + r0 + gq) * kLdT + 36 + k0 + tq];
@@ -1150,22 +1069,19 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_tc_kernel(const __grid_
                         pack_bf16x2(-d[nt][2] * b0, -d[nt][3] * b1);
                 }
             }
-            // T' is complete (the previous chunk's W / Utl product, which consumed the previous
-            // announcement, completed before it was written, so the barrier phases cannot alias).
+            // T' was written block by block above (its tile's previous content, chunk c-2,
+            // was consumed before the previous chunk announced its T').  Announce this
+            // chunk's T' only once the previous chunk's W / Utl product has completed: that
+            // product consumed the previous announcement, so the barrier phases cannot alias.
+            if (c > 0 && !group_wait(&bar_mma2, (c - 1) & 1, ctl, &s_grp_fail[2], 3, 128, gseq)) break;
             fence_proxy_async_smem();
             named_bar(3, 128);
-            if (pt == 0) {
-                mbar_arrive(&bar_tready);
-                KDA_TL(10, c);
-            }
+            if (pt == 0) mbar_arrive(&bar_tready);
         }
     }
 
     tc_fence_before();
     __syncthreads();
-#ifdef KDA_TIMELINE
-    if (tid == 0 && blockIdx.x < kTlCtas) g_tl_cta[blockIdx.x][1] = globaltimer_ns();
-#endif
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem, 512);
@@ -1215,16 +1131,6 @@ __global__ void __launch_bounds__(256) order_kernel(const int32_t *cu, int N, in
 }
 }  // namespace
 
-#ifdef KDA_TIMELINE
-// Copies the timeline of the last launch (kTlEvents x kTlChunks SM-clock stamps) to the host.
-extern "C" int kda_debug_timeline(unsigned long long *host, int n) {
-    if (n < kTlEvents * kTlChunks + 2 * kTlCtas) return -1;
-    if (cudaMemcpyFromSymbol(host, g_tl, sizeof(g_tl)) != cudaSuccess) return -2;
-    if (cudaMemcpyFromSymbol(host + kTlEvents * kTlChunks, g_tl_cta, sizeof(g_tl_cta)) != cudaSuccess) return -2;
-    return kTlEvents * kTlChunks + 2 * kTlCtas;
-}
-#endif
-
 cudaError_t launch_order(const int32_t *cu, int N, int32_t *order, cudaStream_t stream) {
     if (N <= 0) return cudaSuccess;
     order_kernel<<<static_cast<unsigned>((N + 255) / 256), 256, 0, stream>>>(cu, N, order);
@@ -1243,9 +1149,6 @@ cudaError_t launch_chunk_tc(const ChunkParams &cp, cudaStream_t stream) {
     if (!encode_tile_map(&p.tm_q, cp.q, cp.T_total, cp.H) || !encode_tile_map(&p.tm_k, cp.k, cp.T_total, cp.H) ||
         !encode_tile_map(&p.tm_g, cp.g, cp.T_total, cp.H) || !encode_tile_map(&p.tm_v, cp.v, cp.T_total, cp.H))
         return cudaErrorInvalidValue;
-    p.q = static_cast<const __nv_bfloat16 *>(cp.q);
-    p.k = static_cast<const __nv_bfloat16 *>(cp.k);
-    p.g = static_cast<const __nv_bfloat16 *>(cp.g);
     p.beta = static_cast<const __nv_bfloat16 *>(cp.beta);
     p.o = static_cast<__nv_bfloat16 *>(cp.o);
     p.cu = cp.cu;
