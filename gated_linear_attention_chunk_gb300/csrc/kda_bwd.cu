@@ -38,14 +38,18 @@
 //       leaving dS_next and dR in the records;
 //   (C) every (chunk, head), in parallel: all the gradients of the chunk.
 // A and C run on two persistent CTAs per SM, each with its own scratch.  Every
-// product is a CTA-wide fp32 matrix product over global (L2-resident) operands,
-// staged through shared memory in 16-deep slices with the next slice fetched
-// into registers while the current one is multiplied.
+// product runs on the tcgen05 tensor cores (kda_tc_gemm.cuh: tf32 operands staged
+// from the global scratch and records into swizzled shared-memory tiles, fp32
+// accumulation in TMEM), in the order and with the masks the equations above give.
+// The work between products is a string of round trips through L2 and DRAM, so every
+// CTA-wide loop issues all of its loads before its first store, and the chain
+// prefetches the next chunk's records into L2 while it works on the current one.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
 #include "kda_internal.h"
+#include "kda_tc_gemm.cuh"
 
 namespace kda {
 namespace {
@@ -60,93 +64,94 @@ __device__ __forceinline__ float ld_in(const __nv_bfloat16 *p, int64_t i) { retu
 __device__ __forceinline__ void st_out(float *p, int64_t i, float x) { p[i] = x; }
 __device__ __forceinline__ void st_out(__nv_bfloat16 *p, int64_t i, float x) { p[i] = __float2bfloat16_rn(x); }
 
-// C (M x N, row stride ldc) = alpha op(A) op(B), or += when `acc`.  op(A) is M x K: A is
-// stored M x K (row stride lda), or K x M when TA.  op(B) is K x N: B is stored K x N, or
-// N x K when TB.  mask 1 keeps entries i >= j, mask 2 entries i > j (the others become 0,
-// or stay unchanged when accumulating).  All threads of the CTA take part; ends with a
-// barrier, so the result is visible to the whole CTA.
-template <int M, int N, int K, bool TA, bool TB>
-__device__ void cta_gemm(float *C, int ldc, const float *A, int lda, const float *B, int ldb, float alpha, bool acc,
-                         int mask, float *sm) {
-    static_assert(M % 16 == 0 && N % 16 == 0 && K % 16 == 0 && M <= 128 && N <= 128, "shape");
-    static_assert((16 * M) % kBT == 0 && (16 * N) % kBT == 0, "slice split");
-    constexpr int MB = M / 16, NB = N / 16, PA = M + 4, PB = N + 4, EA = 16 * M / kBT, EB = 16 * N / kBT;
-    float *As = sm;            // [16][PA]: op(A) slice, k-major
-    float *Bs = sm + 16 * PA;  // [16][PB]
-    const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
-    float ra[EA], rb[EB];
-    auto fetch = [&](int k0) {
+// Eight consecutive inputs p[i .. i + 7] as floats: one or two 16-byte loads when `vec` (the
+// address is 16-byte aligned), else element by element.
+__device__ __forceinline__ void ld8(const __nv_bfloat16 *p, int64_t i, bool vec, float *x) {
+    if (vec) {
+        const uint4 u = __ldg(reinterpret_cast<const uint4 *>(p + i));
+        const __nv_bfloat162 *b = reinterpret_cast<const __nv_bfloat162 *>(&u);
 #pragma unroll
-        for (int u = 0; u < EA; ++u) {
-            const int e = tid + u * kBT;
-            ra[u] = TA ? A[(k0 + e / M) * lda + e % M] : A[(e >> 4) * lda + k0 + (e & 15)];
+        for (int t = 0; t < 4; ++t) {
+            const float2 f = __bfloat1622float2(b[t]);
+            x[2 * t] = f.x;
+            x[2 * t + 1] = f.y;
         }
+    } else {
 #pragma unroll
-        for (int u = 0; u < EB; ++u) {
-            const int e = tid + u * kBT;
-            rb[u] = TB ? B[(e >> 4) * ldb + k0 + (e & 15)] : B[(k0 + e / N) * ldb + e % N];
-        }
-    };
-    auto stash = [&]() {
+        for (int t = 0; t < 8; ++t) x[t] = __bfloat162float(p[i + t]);
+    }
+}
+__device__ __forceinline__ void ld8(const float *p, int64_t i, bool vec, float *x) {
+    if (vec) {
+        const float4 a = __ldg(reinterpret_cast<const float4 *>(p + i)), b = __ldg(reinterpret_cast<const float4 *>(p + i + 4));
+        x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w; x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+    } else {
 #pragma unroll
-        for (int u = 0; u < EA; ++u) {
-            const int e = tid + u * kBT;
-            if (TA)
-                As[(e / M) * PA + e % M] = ra[u];
-            else
-                As[(e & 15) * PA + (e >> 4)] = ra[u];
-        }
+        for (int t = 0; t < 8; ++t) x[t] = p[i + t];
+    }
+}
+__device__ __forceinline__ void st4(float *p, float4 v) { *reinterpret_cast<float4 *>(p) = v; }
+__device__ __forceinline__ float4 ld4(const float *p) { return __ldcg(reinterpret_cast<const float4 *>(p)); }
+
+// dst[r * ldd + j] = src[r * lds + j] for r < R, j < NC (global memory, 16-byte aligned rows,
+// NC a multiple of 4); all loads are issued before the first store.
+template <int R, int NC>
+__device__ __forceinline__ void cta_copy(float *dst, int ldd, const float *src, int lds) {
+    constexpr int kVec = R * NC / 4, kIt = (kVec + kBT - 1) / kBT;
+    float4 v[kIt];
 #pragma unroll
-        for (int u = 0; u < EB; ++u) {
-            const int e = tid + u * kBT;
-            if (TB)
-                Bs[(e & 15) * PB + (e >> 4)] = rb[u];
-            else
-                Bs[(e / N) * PB + e % N] = rb[u];
-        }
-    };
-    float c[MB][NB];
-#pragma unroll
-    for (int x = 0; x < MB; ++x)
-#pragma unroll
-        for (int y = 0; y < NB; ++y) c[x][y] = 0.f;
-    fetch(0);
-    for (int k0 = 0; k0 < K; k0 += 16) {
-        stash();
-        __syncthreads();
-        if (k0 + 16 < K) fetch(k0 + 16);  // in flight while this slice is multiplied
-#pragma unroll
-        for (int kk = 0; kk < 16; ++kk) {
-            float a[MB], b[NB];
-#pragma unroll
-            for (int x = 0; x < MB; ++x) a[x] = As[kk * PA + ty + 16 * x];
-#pragma unroll
-            for (int y = 0; y < NB; ++y) b[y] = Bs[kk * PB + tx + 16 * y];
-#pragma unroll
-            for (int x = 0; x < MB; ++x)
-#pragma unroll
-                for (int y = 0; y < NB; ++y) c[x][y] = fmaf(a[x], b[y], c[x][y]);
-        }
-        __syncthreads();
+    for (int it = 0; it < kIt; ++it) {
+        const int e = threadIdx.x + it * kBT;
+        if (kVec % kBT == 0 || e < kVec)
+            v[it] = __ldcg(reinterpret_cast<const float4 *>(src + (e / (NC / 4)) * lds + (e % (NC / 4)) * 4));
     }
 #pragma unroll
-    for (int x = 0; x < MB; ++x)
-#pragma unroll
-        for (int y = 0; y < NB; ++y) {
-            const int i = ty + 16 * x, j = tx + 16 * y;
-            const bool keep = mask == 0 || (mask == 1 ? i >= j : i > j);
-            float *o = C + i * ldc + j;
-            if (acc) {
-                if (keep) *o += alpha * c[x][y];
-            } else {
-                *o = keep ? alpha * c[x][y] : 0.f;
-            }
-        }
-    __syncthreads();
+    for (int it = 0; it < kIt; ++it) {
+        const int e = threadIdx.x + it * kBT;
+        if (kVec % kBT == 0 || e < kVec) *reinterpret_cast<float4 *>(dst + (e / (NC / 4)) * ldd + (e % (NC / 4)) * 4) = v[it];
+    }
 }
 
-__device__ __forceinline__ void cta_copy(float *dst, const float *src, int n) {
-    for (int e = threadIdx.x; e < n; e += kBT) dst[e] = src[e];
+// dst[r * NC + j] = f(r, j, src[r * NC + j]) over an R x NC tile in global memory (dst may be
+// src: every element is read and written by the same thread); loads first, then stores.
+template <int R, int NC, typename F>
+__device__ __forceinline__ void cta_map(float *dst, const float *src, F f) {
+    constexpr int kVec = R * NC / 4, kIt = kVec / kBT;
+    static_assert(kVec % kBT == 0, "tile");
+    float4 v[kIt];
+#pragma unroll
+    for (int it = 0; it < kIt; ++it) v[it] = ld4(src + (threadIdx.x + it * kBT) * 4);
+#pragma unroll
+    for (int it = 0; it < kIt; ++it) {
+        const int e = (threadIdx.x + it * kBT) * 4, r = e / NC, j = e % NC;
+        st4(dst + e, make_float4(f(r, j, v[it].x), f(r, j + 1, v[it].y), f(r, j + 2, v[it].z), f(r, j + 3, v[it].w)));
+    }
+}
+
+// The CTA's tensor-core product context: the operand tiles in dynamic shared memory (aligned to
+// 1024 bytes), 128 TMEM columns for the accumulator (allocated by warp 0) and one mbarrier.
+__device__ tcg::Ctx tc_setup(uint8_t *dyn, uint64_t *bar, uint32_t *s_tmem, uint32_t *status) {
+    uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(dyn) + 1023) & ~uintptr_t(1023));
+    if (threadIdx.x < 32) {
+        ptx::tmem_alloc(s_tmem, 128);
+        ptx::tmem_relinquish();
+    }
+    if (threadIdx.x == 0) {
+        ptx::mbar_init(bar, 1);
+        ptx::fence_mbar_init();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    return tcg::Ctx{base, base + tcg::kTileA, bar, *s_tmem, 0u, status, DEV_ERR_TIMEOUT};
+}
+__device__ void tc_teardown(const tcg::Ctx &cx) {
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (threadIdx.x < 32) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(cx.tmem, 128);
+    }
 }
 
 // Record of one (chunk slot, head), in floats.
@@ -162,18 +167,16 @@ struct Scr {
                              kQb = kKh + kC * DK, kdQb = kQb + kC * DK, kdKb = kdQb + kC * DK,
                              kdKt = kdKb + kC * DK, kdKh = kdKt + kC * DK, kV = kdKh + kC * DK, kdO = kV + kC * DV,
                              kR = kdO + kC * DV, kU = kR + kC * DV, kdU = kU + kC * DV, kY = kdU + kC * DV,
-                             kMr = kY + kC * DV, kPr = kMr + kC * kC, kP = kPr + kC * kC, kTp = kP + kC * kC,
+                             kMr = kY + kC * DV, kP = kMr + kC * kC, kTp = kP + kC * kC,
                              kdP = kTp + kC * kC, kdTp = kdP + kC * kC, kX = kdTp + kC * kC, kdM = kX + kC * kC,
                              kTotal = kdM + kC * kC;
 };
 
-// Shared memory of the A and C kernels: the matrix-product slices, or the gate tile /
-// the two 64 x 64 matrices of the inverse / the gate-gradient tile (never live at once).
+// Shared memory of the A and C kernels besides the tensor-core tiles: the gate tile, or the two
+// 64 x 64 matrices of the inverse, or the gate-gradient tile (never live at once).
 template <int DK>
 struct SmemBuf {
-    static constexpr int kGemm = 16 * (128 + 4 + 128 + 4);
-    static constexpr int kTile = kC * DK > 2 * kC * kPad ? kC * DK : 2 * kC * kPad;
-    static constexpr int kFloats = kGemm > kTile ? kGemm : kTile;
+    static constexpr int kFloats = kC * DK > 2 * kC * kPad ? kC * DK : 2 * kC * kPad;
 };
 
 // Token range of sequence n; false (and the status bit) for an invalid partition.
@@ -225,9 +228,26 @@ __device__ void load_chunk(const BwdParams &p, int64_t t0, int Lc, int h, float 
     const Tin *G = static_cast<const Tin *>(p.g), *K = static_cast<const Tin *>(p.k);
     const Tin *Q = static_cast<const Tin *>(p.q), *V = static_cast<const Tin *>(p.v);
     const Tin *B = static_cast<const Tin *>(p.beta), *DO = static_cast<const Tin *>(p.d_o);
-    for (int e = tid; e < kC * DK; e += kBT) {
-        const int r = e / DK, i = e % DK;
-        s_buf[e] = r < Lc ? ld_in(G, ((t0 + r) * H + h) * DK + i) : 0.f;
+    // gate tile into shared memory, eight channels per load (q, k, v, g are 16-byte aligned and
+    // every row starts at a multiple of eight elements)
+    {
+        constexpr int kG = kC * DK / 8, kIt = kG / kBT;
+        static_assert(kG % kBT == 0, "gate tile");
+        float x[kIt][8];
+#pragma unroll
+        for (int it = 0; it < kIt; ++it) {
+            const int e = tid + it * kBT, r = e / (DK / 8), i = (e % (DK / 8)) * 8;
+            if (r < Lc) ld8(G, ((t0 + r) * H + h) * DK + i, true, x[it]);
+            else
+#pragma unroll
+                for (int t = 0; t < 8; ++t) x[it][t] = 0.f;
+        }
+#pragma unroll
+        for (int it = 0; it < kIt; ++it) {
+            const int e = tid + it * kBT, r = e / (DK / 8), i = (e % (DK / 8)) * 8;
+            *reinterpret_cast<float4 *>(s_buf + r * DK + i) = make_float4(x[it][0], x[it][1], x[it][2], x[it][3]);
+            *reinterpret_cast<float4 *>(s_buf + r * DK + i + 4) = make_float4(x[it][4], x[it][5], x[it][6], x[it][7]);
+        }
     }
     if (tid < kC) {
         float b = tid < Lc ? ld_in(B, (t0 + tid) * H + h) : 0.f;
@@ -252,63 +272,184 @@ __device__ void load_chunk(const BwdParams &p, int64_t t0, int Lc, int h, float 
         (is_q ? s_rq : s_rk)[r] = inv;
     }
     __syncthreads();
+    // in-chunk prefix products A_r of alpha, in place of the gate tile (and into the scratch)
     if (tid < DK) {
         const bool sig = (p.prep & PREP_SIGMOID_GATE) != 0;
         float a = 1.f;
         for (int r = 0; r < kC; ++r) {
             const float x = s_buf[r * DK + tid];
             if (r < Lc) a *= sig ? 1.f / (1.f + expf(-x)) : expf(x);  // padding rows: alpha = 1
+            s_buf[r * DK + tid] = a;
             W[S::kA + r * DK + tid] = a;
         }
         s_ac[tid] = a;
     }
     __syncthreads();
     const float sc = p.scale;
-    for (int e = tid; e < kC * DK; e += kBT) {
-        const int r = e / DK, i = e % DK;
-        const bool ok = r < Lc;
-        const float kk = ok ? ld_in(K, ((t0 + r) * H + h) * DK + i) * s_rk[r] : 0.f;
-        const float qq = ok ? ld_in(Q, ((t0 + r) * H + h) * DK + i) * s_rq[r] : 0.f;
-        const float a = W[S::kA + e];
-        W[S::kKb + e] = kk * a;
-        W[S::kKt + e] = kk / a;
-        W[S::kKh + e] = (kk / a) * s_ac[i];
-        W[S::kQb + e] = sc * qq * a;
+    {
+        constexpr int kG = kC * DK / 8, kIt = kG / kBT;
+        float kx[kIt][8], qx[kIt][8];
+#pragma unroll
+        for (int it = 0; it < kIt; ++it) {
+            const int e = tid + it * kBT, r = e / (DK / 8), i = (e % (DK / 8)) * 8;
+            if (r < Lc) {
+                ld8(K, ((t0 + r) * H + h) * DK + i, true, kx[it]);
+                ld8(Q, ((t0 + r) * H + h) * DK + i, true, qx[it]);
+            } else {
+#pragma unroll
+                for (int t = 0; t < 8; ++t) kx[it][t] = qx[it][t] = 0.f;
+            }
+        }
+#pragma unroll
+        for (int it = 0; it < kIt; ++it) {
+            const int e = tid + it * kBT, r = e / (DK / 8), i = (e % (DK / 8)) * 8;
+            const float rk = s_rk[r], rq = s_rq[r];
+            float kb[8], kt[8], kh[8], qb[8];
+#pragma unroll
+            for (int t = 0; t < 8; ++t) {
+                const float a = s_buf[r * DK + i + t], kk = kx[it][t] * rk, qq = qx[it][t] * rq;
+                kb[t] = kk * a;
+                kt[t] = kk / a;
+                kh[t] = (kk / a) * s_ac[i + t];
+                qb[t] = sc * qq * a;
+            }
+            const int o = r * DK + i;
+            st4(W + S::kKb + o, make_float4(kb[0], kb[1], kb[2], kb[3]));
+            st4(W + S::kKb + o + 4, make_float4(kb[4], kb[5], kb[6], kb[7]));
+            st4(W + S::kKt + o, make_float4(kt[0], kt[1], kt[2], kt[3]));
+            st4(W + S::kKt + o + 4, make_float4(kt[4], kt[5], kt[6], kt[7]));
+            st4(W + S::kKh + o, make_float4(kh[0], kh[1], kh[2], kh[3]));
+            st4(W + S::kKh + o + 4, make_float4(kh[4], kh[5], kh[6], kh[7]));
+            st4(W + S::kQb + o, make_float4(qb[0], qb[1], qb[2], qb[3]));
+            st4(W + S::kQb + o + 4, make_float4(qb[4], qb[5], qb[6], qb[7]));
+        }
     }
-    for (int e = tid; e < kC * DV; e += kBT) {
-        const int r = e / DV, j = e % DV;
-        const bool ok = r < Lc;
-        if (want_v) W[S::kV + e] = ok ? ld_in(V, ((t0 + r) * H + h) * DV + j) : 0.f;
-        W[S::kdO + e] = ok ? ld_in(DO, ((t0 + r) * H + h) * DV + j) : 0.f;
+    {
+        constexpr int kG = kC * DV / 8, kIt = kG / kBT;
+        static_assert(kG % kBT == 0, "value tile");
+        const bool vec_do = (reinterpret_cast<uintptr_t>(DO) & 15u) == 0;
+        float vx[kIt][8], dx[kIt][8];
+#pragma unroll
+        for (int it = 0; it < kIt; ++it) {
+            const int e = tid + it * kBT, r = e / (DV / 8), j = (e % (DV / 8)) * 8;
+            if (r < Lc) {
+                if (want_v) ld8(V, ((t0 + r) * H + h) * DV + j, true, vx[it]);
+                ld8(DO, ((t0 + r) * H + h) * DV + j, vec_do, dx[it]);
+            } else {
+#pragma unroll
+                for (int t = 0; t < 8; ++t) vx[it][t] = dx[it][t] = 0.f;
+            }
+        }
+#pragma unroll
+        for (int it = 0; it < kIt; ++it) {
+            const int e = tid + it * kBT, r = e / (DV / 8), j = (e % (DV / 8)) * 8;
+            const int o = r * DV + j;
+            if (want_v) {
+                st4(W + S::kV + o, make_float4(vx[it][0], vx[it][1], vx[it][2], vx[it][3]));
+                st4(W + S::kV + o + 4, make_float4(vx[it][4], vx[it][5], vx[it][6], vx[it][7]));
+            }
+            st4(W + S::kdO + o, make_float4(dx[it][0], dx[it][1], dx[it][2], dx[it][3]));
+            st4(W + S::kdO + o + 4, make_float4(dx[it][4], dx[it][5], dx[it][6], dx[it][7]));
+        }
     }
     __syncthreads();
 }
 
-// T = (I + M)^-1 for M = Diag(beta) strictly-lower(Mr) (64 x 64), by forward
-// substitution down each column: T_ij = -sum_{j <= k < i} M_ik T_kj.  Four threads per
-// column split each sum and combine it with two shuffles; a column never leaves its
-// warp, so the warp's own barrier orders its rows.  Writes T (row stride 64) to `Tout`.
-__device__ void tri_inverse(const float *Mr, const float *s_beta, float *s_buf, float *Tout) {
+// T = (I + M)^-1 for M = Diag(beta) strictly-lower(Mr) (64 x 64, unit lower triangular), by
+// blocks: the four 16 x 16 diagonal blocks by forward substitution down each column (four
+// threads per column split each sum; a column never leaves its warp), then twice the block
+// rule for a lower-triangular inverse, [[A, 0], [C, D]]^-1 = [[A^-1, 0], [-D^-1 C A^-1, D^-1]],
+// from 16 to 32 and from 32 to 64 rows.  Writes T (row stride 64) to `Tout` and T Diag(beta)
+// to `Tp_out` (if not null).
+__device__ void tri_inverse(const float *Mr, const float *s_beta, float *s_buf, float *Tout, float *Tp_out) {
     const int tid = threadIdx.x;
     float *sM = s_buf, *sT = s_buf + kC * kPad;
+    static_assert(kBT == 256 && kC == 64, "block layout");
+    {
+        constexpr int kIt = kC * kC / 4 / kBT;
+        float4 v[kIt];
+#pragma unroll
+        for (int it = 0; it < kIt; ++it) v[it] = ld4(Mr + (tid + it * kBT) * 4);
+#pragma unroll
+        for (int it = 0; it < kIt; ++it) {
+            const int e = (tid + it * kBT) * 4, i = e / kC, j = e % kC;
+            const float b = s_beta[i];
+            const float m[4] = {v[it].x, v[it].y, v[it].z, v[it].w};
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+                sM[i * kPad + j + t] = i > j + t ? b * m[t] : 0.f;
+                sT[i * kPad + j + t] = i == j + t ? 1.f : 0.f;
+            }
+        }
+    }
+    __syncthreads();
+    {  // diagonal blocks: block b = tid / 64 (two warps), column jl = (tid / 4) % 16, part = tid % 4
+        const int b = tid >> 6, jl = (tid >> 2) & 15, part = tid & 3, j = b * 16 + jl;
+        for (int il = 1; il < 16; ++il) {
+            const int i = b * 16 + il;
+            float acc = 0.f;
+            if (il > jl)
+                for (int k = j + part; k < i; k += 4) acc = fmaf(sM[i * kPad + k], sT[k * kPad + j], acc);
+            acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+            acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+            if (part == 0 && il > jl) sT[i * kPad + j] = -acc;
+            __syncwarp();
+        }
+    }
+    __syncthreads();
+    {  // 16 -> 32: in each 32-row block (o = 0, 32), C = M[o+16.., o..], A^-1 = T[o.., o..], D^-1 = T[o+16.., o+16..]
+        const int o = (tid >> 7) * 32, t = tid & 127, r = t >> 3, c = (t & 7) * 2;
+        float y0 = 0.f, y1 = 0.f;
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+            const float m = sM[(o + 16 + r) * kPad + o + k];
+            y0 = fmaf(m, sT[(o + k) * kPad + o + c], y0);
+            y1 = fmaf(m, sT[(o + k) * kPad + o + c + 1], y1);
+        }
+        sT[(o + 16 + r) * kPad + o + c] = y0;  // C A^-1, in place of the (zero) lower-left block
+        sT[(o + 16 + r) * kPad + o + c + 1] = y1;
+        __syncthreads();
+        float z0 = 0.f, z1 = 0.f;
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+            const float d = sT[(o + 16 + r) * kPad + o + 16 + k];
+            z0 = fmaf(d, sT[(o + 16 + k) * kPad + o + c], z0);
+            z1 = fmaf(d, sT[(o + 16 + k) * kPad + o + c + 1], z1);
+        }
+        __syncthreads();
+        sT[(o + 16 + r) * kPad + o + c] = -z0;
+        sT[(o + 16 + r) * kPad + o + c + 1] = -z1;
+    }
+    __syncthreads();
+    {  // 32 -> 64: C = M[32.., ..32], A^-1 = T[..32, ..32], D^-1 = T[32.., 32..]; four columns per thread
+        const int r = tid >> 3, c = (tid & 7) * 4;
+        float y[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 8
+        for (int k = 0; k < 32; ++k) {
+            const float m = sM[(32 + r) * kPad + k];
+#pragma unroll
+            for (int t = 0; t < 4; ++t) y[t] = fmaf(m, sT[k * kPad + c + t], y[t]);
+        }
+#pragma unroll
+        for (int t = 0; t < 4; ++t) sT[(32 + r) * kPad + c + t] = y[t];
+        __syncthreads();
+        float z[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 8
+        for (int k = 0; k < 32; ++k) {
+            const float d = sT[(32 + r) * kPad + 32 + k];
+#pragma unroll
+            for (int t = 0; t < 4; ++t) z[t] = fmaf(d, sT[(32 + k) * kPad + c + t], z[t]);
+        }
+        __syncthreads();
+#pragma unroll
+        for (int t = 0; t < 4; ++t) sT[(32 + r) * kPad + c + t] = -z[t];
+    }
+    __syncthreads();
     for (int e = tid; e < kC * kC; e += kBT) {
-        const int i = e / kC, j = e % kC;
-        sM[i * kPad + j] = i > j ? s_beta[i] * Mr[e] : 0.f;
+        const float t = sT[(e / kC) * kPad + e % kC];
+        Tout[e] = t;
+        if (Tp_out) Tp_out[e] = t * s_beta[e % kC];
     }
-    const int j = tid >> 2, part = tid & 3;
-    for (int i = part; i < kC; i += 4) sT[i * kPad + j] = (i == j) ? 1.f : 0.f;
-    __syncthreads();
-    for (int i = 1; i < kC; ++i) {
-        float acc = 0.f;
-        if (i > j)
-            for (int k = j + part; k < i; k += 4) acc = fmaf(sM[i * kPad + k], sT[k * kPad + j], acc);
-        acc += __shfl_xor_sync(0xffffffffu, acc, 1);
-        acc += __shfl_xor_sync(0xffffffffu, acc, 2);
-        if (part == 0 && i > j) sT[i * kPad + j] = -acc;
-        __syncwarp();
-    }
-    __syncthreads();
-    for (int e = tid; e < kC * kC; e += kBT) Tout[e] = sT[(e / kC) * kPad + e % kC];
     __syncthreads();
 }
 
@@ -319,6 +460,10 @@ __global__ void __launch_bounds__(kBT, 2) kda_bwd_chunk_kernel(BwdParams p) {
     using RC = Rec<DK, DV>;
     __shared__ __align__(16) float s_buf[SmemBuf<DK>::kFloats];
     __shared__ float s_beta[kC], s_ac[DK], s_rk[kC], s_rq[kC];
+    extern __shared__ uint8_t bwd_dyn[];
+    __shared__ uint64_t s_bar;
+    __shared__ uint32_t s_tmem;
+    tcg::Ctx cx = tc_setup(bwd_dyn, &s_bar, &s_tmem, p.status);
     float *W = p.scratch + static_cast<int64_t>(blockIdx.x) * S::kTotal;
     const int64_t items = p.nslots * p.H;
     for (int64_t item = blockIdx.x; item < items; item += gridDim.x) {
@@ -335,35 +480,50 @@ __global__ void __launch_bounds__(kBT, 2) kda_bwd_chunk_kernel(BwdParams p) {
             rec[RC::kAC + threadIdx.x] = s_ac[threadIdx.x];
             if (!(s_ac[threadIdx.x] >= kMinDecay)) atomicOr(p.status, DEV_ERR_GATE);
         }
-        cta_copy(rec + RC::kKb, W + S::kKb, kC * DK);
-        cta_gemm<kC, kC, DK, false, true>(W + S::kMr, kC, W + S::kKb, DK, W + S::kKt, DK, 1.f, false, 0, s_buf);
-        cta_gemm<kC, kC, DK, false, true>(W + S::kPr, kC, W + S::kQb, DK, W + S::kKt, DK, 1.f, false, 0, s_buf);
-        tri_inverse(W + S::kMr, s_beta, s_buf, rec + RC::kT);
-        for (int e = threadIdx.x; e < kC * kC; e += kBT) {
-            const int i = e / kC, j = e % kC;
-            W[S::kTp + e] = rec[RC::kT + e] * s_beta[j];
-            W[S::kP + e] = i >= j ? W[S::kPr + e] : 0.f;
-        }
-        __syncthreads();
+        cta_copy<kC, DK>(rec + RC::kKb, DK, W + S::kKb, DK);
+        tcg::gemm<kC, kC, DK, false, true, kBT>(cx, W + S::kMr, kC, W + S::kKb, DK, W + S::kKt, DK, 1.f, false, 0);
+        tcg::gemm<kC, kC, DK, false, true, kBT>(cx, W + S::kP, kC, W + S::kQb, DK, W + S::kKt, DK, 1.f, false, 1);
+        tri_inverse(W + S::kMr, s_beta, s_buf, rec + RC::kT, W + S::kTp);
         // G = T'^T Khat, F = T'^T (P^T dO), E = Qbar^T dO
-        cta_gemm<kC, DK, kC, true, false>(rec + RC::kG, DK, W + S::kTp, kC, W + S::kKh, DK, 1.f, false, 0, s_buf);
-        cta_gemm<kC, DV, kC, true, false>(W + S::kY, DV, W + S::kP, kC, W + S::kdO, DV, 1.f, false, 0, s_buf);
-        cta_gemm<kC, DV, kC, true, false>(rec + RC::kF, DV, W + S::kTp, kC, W + S::kY, DV, 1.f, false, 0, s_buf);
-        cta_gemm<DK, DV, kC, true, false>(rec + RC::kE, DV, W + S::kQb, DK, W + S::kdO, DV, 1.f, false, 0, s_buf);
+        tcg::gemm<kC, DK, kC, true, false, kBT>(cx, rec + RC::kG, DK, W + S::kTp, kC, W + S::kKh, DK, 1.f, false, 0);
+        tcg::gemm<kC, DV, kC, true, false, kBT>(cx, W + S::kY, DV, W + S::kP, kC, W + S::kdO, DV, 1.f, false, 0);
+        tcg::gemm<kC, DV, kC, true, false, kBT>(cx, rec + RC::kF, DV, W + S::kTp, kC, W + S::kY, DV, 1.f, false, 0);
+        tcg::gemm<DK, DV, kC, true, false, kBT>(cx, rec + RC::kE, DV, W + S::kQb, DK, W + S::kdO, DV, 1.f, false, 0);
     }
+    tc_teardown(cx);
 }
 
 // ---------------------------------------------------------------------------- phase B
 // The columns of dS follow independent recurrences (dR and the update of column j read
-// column j only), so each (sequence, head) chain is split into DV / kChainCols CTAs.
-constexpr int kChainCols = 32;
+// column j only), so each (sequence, head) chain is split into DV / kCB CTAs of kCB columns
+// (32 when that still fits the resident CTAs, else 64).  While one chunk is processed the
+// records of the next one back are prefetched into L2.
+
+// Prefetches the rows [0, rows) x [0, row_bytes) of a matrix with row stride `ld_bytes` into
+// L2, one 128-byte line per thread and round.
+__device__ __forceinline__ void prefetch_rows(const void *base, int rows, int row_bytes, int64_t ld_bytes) {
+    const int lines = row_bytes / 128;
+    for (int e = threadIdx.x; e < rows * lines; e += kBT) {
+        const char *a = static_cast<const char *>(base) + (e / lines) * ld_bytes + (e % lines) * 128;
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(a));
+    }
+}
 
 template <int DK, int DV>
-__global__ void __launch_bounds__(kBT, 1) kda_bwd_chain_kernel(BwdParams p) {
+__device__ __forceinline__ void prefetch_chain_record(const float *rec, int col0, int kCB) {
+    using RC = Rec<DK, DV>;
+    prefetch_rows(rec + RC::kG, 1, kC * DK * 4, 0);
+    prefetch_rows(rec + RC::kKb, 1, kC * DK * 4, 0);
+    prefetch_rows(rec + RC::kF + col0, kC, kCB * 4, DV * 4);
+    prefetch_rows(rec + RC::kE + col0, DK, kCB * 4, DV * 4);
+    prefetch_rows(rec + RC::kAC, 1, DK * 4, 0);
+}
+
+template <int DK, int DV, int kCB>
+__global__ void __launch_bounds__(kBT, 2) kda_bwd_chain_kernel(BwdParams p) {
     using S = Scr<DK, DV>;
     using RC = Rec<DK, DV>;
-    constexpr int kCB = kChainCols, kBlocks = DV / kCB;
-    __shared__ __align__(16) float s_buf[SmemBuf<DK>::kFloats];
+    constexpr int kBlocks = DV / kCB;
     const int tid = threadIdx.x;
     const int64_t pair = blockIdx.x / kBlocks;
     const int col0 = static_cast<int>(blockIdx.x % kBlocks) * kCB;
@@ -373,35 +533,50 @@ __global__ void __launch_bounds__(kBT, 1) kda_bwd_chain_kernel(BwdParams p) {
         if (tid == 0 && h == 0 && col0 == 0) atomicOr(p.status, DEV_ERR_SEQLENS);
         return;
     }
+    extern __shared__ uint8_t bwd_dyn[];
+    __shared__ uint64_t s_bar;
+    __shared__ uint32_t s_tmem;
+    tcg::Ctx cx = tc_setup(bwd_dyn, &s_bar, &s_tmem, p.status);
     // this CTA's columns of the chain's two DK x DV states (row stride DV)
     float *dS = p.scratch + static_cast<int64_t>(p.ctas) * S::kTotal + pair * 2 * DK * DV + col0;
     float *dSn = dS + DK * DV;
+    const int nch = static_cast<int>((eos - bos + kC - 1) / kC);
+    const int64_t base = ckpt_base(bos, n);
+    if (nch > 0) prefetch_chain_record<DK, DV>(p.rec + ((base + nch - 1) * p.H + h) * RC::kTotal, col0, kCB);
     for (int e = tid; e < DK * kCB; e += kBT) {
         const int i = e / kCB, j = e % kCB;
         dS[i * DV + j] = p.d_final ? p.d_final[pair * DK * DV + i * DV + col0 + j] : 0.f;
     }
     __syncthreads();
-    const int nch = static_cast<int>((eos - bos + kC - 1) / kC);
-    const int64_t base = ckpt_base(bos, n);
     for (int c = nch - 1; c >= 0; --c) {
         float *rec = p.rec + ((base + c) * p.H + h) * RC::kTotal;
-        for (int e = tid; e < DK * kCB; e += kBT) {
-            const int i = e / kCB, j = e % kCB;
-            rec[RC::kdSn + i * DV + col0 + j] = dS[i * DV + j];
-            dSn[i * DV + j] = rec[RC::kE + i * DV + col0 + j];
-        }
-        for (int e = tid; e < kC * kCB; e += kBT) {
-            const int r = e / kCB, j = e % kCB;
-            rec[RC::kdR + r * DV + col0 + j] = rec[RC::kF + r * DV + col0 + j];
-        }
+        if (c > 0) prefetch_chain_record<DK, DV>(p.rec + ((base + c - 1) * p.H + h) * RC::kTotal, col0, kCB);
+        cta_copy<DK, kCB>(rec + RC::kdSn + col0, DV, dS, DV);
+        cta_copy<DK, kCB>(dSn, DV, rec + RC::kE + col0, DV);
+        cta_copy<kC, kCB>(rec + RC::kdR + col0, DV, rec + RC::kF + col0, DV);
         __syncthreads();
         // dR = G dS_next + F;  dS = Diag(A_C) dS_next + E - Kbar^T dR   (this CTA's columns)
-        cta_gemm<kC, kCB, DK, false, false>(rec + RC::kdR + col0, DV, rec + RC::kG, DK, dS, DV, 1.f, true, 0, s_buf);
-        cta_gemm<DK, kCB, kC, true, false>(dSn, DV, rec + RC::kKb, DK, rec + RC::kdR + col0, DV, -1.f, true, 0,
-                                            s_buf);
-        for (int e = tid; e < DK * kCB; e += kBT) {
-            const int i = e / kCB, j = e % kCB;
-            dS[i * DV + j] = fmaf(rec[RC::kAC + i], dS[i * DV + j], dSn[i * DV + j]);
+        tcg::gemm<kC, kCB, DK, false, false, kBT>(cx, rec + RC::kdR + col0, DV, rec + RC::kG, DK, dS, DV, 1.f, true, 0);
+        tcg::gemm<DK, kCB, kC, true, false, kBT>(cx, dSn, DV, rec + RC::kKb, DK, rec + RC::kdR + col0, DV, -1.f, true, 0);
+        {
+            constexpr int kVec = DK * kCB / 4, kIt = kVec / kBT;
+            static_assert(kVec % kBT == 0, "chain block");
+            float4 a[kIt], b[kIt];
+            float ac[kIt];
+#pragma unroll
+            for (int it = 0; it < kIt; ++it) {
+                const int e = tid + it * kBT, i = e / (kCB / 4), j = (e % (kCB / 4)) * 4;
+                a[it] = __ldcg(reinterpret_cast<const float4 *>(dS + i * DV + j));
+                b[it] = __ldcg(reinterpret_cast<const float4 *>(dSn + i * DV + j));
+                ac[it] = __ldcg(rec + RC::kAC + i);
+            }
+#pragma unroll
+            for (int it = 0; it < kIt; ++it) {
+                const int e = tid + it * kBT, i = e / (kCB / 4), j = (e % (kCB / 4)) * 4;
+                const float4 r = make_float4(fmaf(ac[it], a[it].x, b[it].x), fmaf(ac[it], a[it].y, b[it].y),
+                                             fmaf(ac[it], a[it].z, b[it].z), fmaf(ac[it], a[it].w, b[it].w));
+                *reinterpret_cast<float4 *>(dS + i * DV + j) = r;
+            }
         }
         __syncthreads();
     }
@@ -410,6 +585,7 @@ __global__ void __launch_bounds__(kBT, 1) kda_bwd_chain_kernel(BwdParams p) {
             const int i = e / kCB, j = e % kCB;
             p.d_init[pair * DK * DV + i * DV + col0 + j] = dS[i * DV + j];
         }
+    tc_teardown(cx);
 }
 
 // ---------------------------------------------------------------------------- phase C
@@ -418,7 +594,11 @@ __global__ void __launch_bounds__(kBT, 2) kda_bwd_grad_kernel(BwdParams p) {
     using S = Scr<DK, DV>;
     using RC = Rec<DK, DV>;
     __shared__ __align__(16) float s_buf[SmemBuf<DK>::kFloats];
-    __shared__ float s_beta[kC], s_dbeta[kC], s_ac[DK], s_red[kBT], s_rk[kC], s_rq[kC];
+    __shared__ float s_beta[kC], s_dbeta[kC], s_ac[DK], s_red[kBT], s_rk[kC], s_rq[kC], s_rowdot[DK];
+    extern __shared__ uint8_t bwd_dyn[];
+    __shared__ uint64_t s_bar;
+    __shared__ uint32_t s_tmem;
+    tcg::Ctx cx = tc_setup(bwd_dyn, &s_bar, &s_tmem, p.status);
     const int tid = threadIdx.x;
     float *W = p.scratch + static_cast<int64_t>(blockIdx.x) * S::kTotal;
     const int64_t H = p.H;
@@ -443,35 +623,31 @@ __global__ void __launch_bounds__(kBT, 2) kda_bwd_grad_kernel(BwdParams p) {
         float *A_ = W + S::kA, *Kb = W + S::kKb, *Kt = W + S::kKt, *Kh = W + S::kKh, *Qb = W + S::kQb;
         float *dQb = W + S::kdQb, *dKb = W + S::kdKb, *dKt = W + S::kdKt, *dKh = W + S::kdKh;
         float *Vs = W + S::kV, *dOs = W + S::kdO, *R = W + S::kR, *U = W + S::kU, *dU = W + S::kdU;
-        float *Mr = W + S::kMr, *Pr = W + S::kPr, *P = W + S::kP, *Tp = W + S::kTp, *dP = W + S::kdP;
+        float *Mr = W + S::kMr, *P = W + S::kP, *Tp = W + S::kTp, *dP = W + S::kdP;
         float *dTp = W + S::kdTp, *X = W + S::kX, *dM = W + S::kdM;
 
         load_chunk<DK, DV, Tin>(p, t0, Lc, h, W, true, s_buf, s_beta, s_ac, s_rk, s_rq);
-        cta_gemm<kC, kC, DK, false, true>(Mr, kC, Kb, DK, Kt, DK, 1.f, false, 0, s_buf);
-        cta_gemm<kC, kC, DK, false, true>(Pr, kC, Qb, DK, Kt, DK, 1.f, false, 0, s_buf);
-        for (int e = tid; e < kC * kC; e += kBT) {
-            const int i = e / kC, j = e % kC;
-            Tp[e] = T[e] * s_beta[j];
-            P[e] = i >= j ? Pr[e] : 0.f;
-        }
-        cta_copy(R, Vs, kC * DV);
+        tcg::gemm<kC, kC, DK, false, true, kBT>(cx, Mr, kC, Kb, DK, Kt, DK, 1.f, false, 0);
+        tcg::gemm<kC, kC, DK, false, true, kBT>(cx, P, kC, Qb, DK, Kt, DK, 1.f, false, 1);
+        cta_map<kC, kC>(Tp, T, [&](int, int j, float x) { return x * s_beta[j]; });
+        cta_copy<kC, DV>(R, DV, Vs, DV);
         __syncthreads();
         // forward quantities of the chunk: R = V - Kbar S, U = T' R
-        if (Sc) cta_gemm<kC, DV, DK, false, false>(R, DV, Kb, DK, Sc, DV, -1.f, true, 0, s_buf);
-        cta_gemm<kC, DV, kC, false, false>(U, DV, Tp, kC, R, DV, 1.f, false, 0, s_buf);
+        if (Sc) tcg::gemm<kC, DV, DK, false, false, kBT>(cx, R, DV, Kb, DK, Sc, DV, -1.f, true, 0);
+        tcg::gemm<kC, DV, kC, false, false, kBT>(cx, U, DV, Tp, kC, R, DV, 1.f, false, 0);
         // reverse
-        cta_gemm<kC, DV, DK, false, false>(dU, DV, Kh, DK, dSx, DV, 1.f, false, 0, s_buf);
-        cta_gemm<kC, DV, kC, true, false>(dU, DV, P, kC, dOs, DV, 1.f, true, 0, s_buf);
-        cta_gemm<kC, kC, DV, false, true>(dP, kC, dOs, DV, U, DV, 1.f, false, 1, s_buf);
-        cta_gemm<kC, kC, DV, false, true>(dTp, kC, dU, DV, R, DV, 1.f, false, 0, s_buf);
-        cta_gemm<kC, DK, kC, false, false>(dQb, DK, dP, kC, Kt, DK, 1.f, false, 0, s_buf);
-        if (Sc) cta_gemm<kC, DK, DV, false, true>(dQb, DK, dOs, DV, Sc, DV, 1.f, true, 0, s_buf);
-        cta_gemm<kC, DK, DV, false, true>(dKh, DK, U, DV, dSx, DV, 1.f, false, 0, s_buf);
+        tcg::gemm<kC, DV, DK, false, false, kBT>(cx, dU, DV, Kh, DK, dSx, DV, 1.f, false, 0);
+        tcg::gemm<kC, DV, kC, true, false, kBT>(cx, dU, DV, P, kC, dOs, DV, 1.f, true, 0);
+        tcg::gemm<kC, kC, DV, false, true, kBT>(cx, dP, kC, dOs, DV, U, DV, 1.f, false, 1);
+        tcg::gemm<kC, kC, DV, false, true, kBT>(cx, dTp, kC, dU, DV, R, DV, 1.f, false, 0);
+        tcg::gemm<kC, DK, kC, false, false, kBT>(cx, dQb, DK, dP, kC, Kt, DK, 1.f, false, 0);
+        if (Sc) tcg::gemm<kC, DK, DV, false, true, kBT>(cx, dQb, DK, dOs, DV, Sc, DV, 1.f, true, 0);
+        tcg::gemm<kC, DK, DV, false, true, kBT>(cx, dKh, DK, U, DV, dSx, DV, 1.f, false, 0);
         if (Sc)
-            cta_gemm<kC, DK, DV, false, true>(dKb, DK, dR, DV, Sc, DV, -1.f, false, 0, s_buf);
+            tcg::gemm<kC, DK, DV, false, true, kBT>(cx, dKb, DK, dR, DV, Sc, DV, -1.f, false, 0);
         else
             for (int e = tid; e < kC * DK; e += kBT) dKb[e] = 0.f;
-        cta_gemm<kC, DK, kC, true, false>(dKt, DK, dP, kC, Qb, DK, 1.f, false, 0, s_buf);
+        tcg::gemm<kC, DK, kC, true, false, kBT>(cx, dKt, DK, dP, kC, Qb, DK, 1.f, false, 0);
         // beta through T' = T Diag(beta) (column sums over 4 row quarters); dT = dT' Diag(beta)
         {
             const int j = tid & 63, qr = tid >> 6;
@@ -481,11 +657,11 @@ __global__ void __launch_bounds__(kBT, 2) kda_bwd_grad_kernel(BwdParams p) {
         }
         __syncthreads();
         if (tid < kC) s_dbeta[tid] = (s_red[tid] + s_red[tid + 64]) + (s_red[tid + 128] + s_red[tid + 192]);
-        for (int e = tid; e < kC * kC; e += kBT) dTp[e] *= s_beta[e % kC];
+        cta_map<kC, kC>(dTp, dTp, [&](int, int j, float x) { return x * s_beta[j]; });
         __syncthreads();
         // through the inverse: dM = strictly-lower(-T^T dT T^T)
-        cta_gemm<kC, kC, kC, true, false>(X, kC, T, kC, dTp, kC, 1.f, false, 0, s_buf);
-        cta_gemm<kC, kC, kC, false, true>(dM, kC, X, kC, T, kC, -1.f, false, 2, s_buf);
+        tcg::gemm<kC, kC, kC, true, false, kBT>(cx, X, kC, T, kC, dTp, kC, 1.f, false, 0);
+        tcg::gemm<kC, kC, kC, false, true, kBT>(cx, dM, kC, X, kC, T, kC, -1.f, false, 2);
         // through M = Diag(beta) strictly-lower(Kbar Ktil^T): row sums, four threads per row
         {
             const int i = tid >> 2, part = tid & 3;
@@ -496,48 +672,115 @@ __global__ void __launch_bounds__(kBT, 2) kda_bwd_grad_kernel(BwdParams p) {
             if (part == 0) s_dbeta[i] += acc;
         }
         __syncthreads();
-        for (int e = tid; e < kC * kC; e += kBT) dM[e] *= s_beta[e / kC];
+        cta_map<kC, kC>(dM, dM, [&](int i, int, float x) { return x * s_beta[i]; });
         __syncthreads();
-        cta_gemm<kC, DK, kC, false, false>(dKb, DK, dM, kC, Kt, DK, 1.f, true, 0, s_buf);
-        cta_gemm<kC, DK, kC, true, false>(dKt, DK, dM, kC, Kb, DK, 1.f, true, 0, s_buf);
-        // gate gradients: dlogA_C = A_C sum_j dS_next S + sum_r dKhat Khat
+        tcg::gemm<kC, DK, kC, false, false, kBT>(cx, dKb, DK, dM, kC, Kt, DK, 1.f, true, 0);
+        tcg::gemm<kC, DK, kC, true, false, kBT>(cx, dKt, DK, dM, kC, Kb, DK, 1.f, true, 0);
+        // gate gradients: dlogA_C = A_C sum_j dS_next S + sum_r dKhat Khat.  The row sums of
+        // dS_next * S take one warp per group of rows, lanes across the columns (four rows'
+        // loads in flight); the column sums of dKhat * Khat one thread per column and part.
         {
+            constexpr int kWarps = kBT / 32, kRows = DK / kWarps, kPer = DV / 32;
+            static_assert(kRows % 4 == 0 && (kPer == 4 || kPer == 2), "row sums");
+            const int warp = tid >> 5, lane = tid & 31;
+#pragma unroll 1
+            for (int r0 = 0; r0 < kRows; r0 += 4) {
+                float part[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int row = warp * kRows + r0 + u;
+                    part[u] = 0.f;
+                    if (Sc) {
+                        const float *x = dSx + row * DV + lane * kPer, *y = Sc + row * DV + lane * kPer;
+                        if (kPer == 4) {
+                            const float4 a = ld4(x), b = ld4(y);
+                            part[u] = fmaf(a.x, b.x, fmaf(a.y, b.y, fmaf(a.z, b.z, a.w * b.w)));
+                        } else {
+                            const float2 a = __ldcg(reinterpret_cast<const float2 *>(x));
+                            const float2 b = __ldcg(reinterpret_cast<const float2 *>(y));
+                            part[u] = fmaf(a.x, b.x, a.y * b.y);
+                        }
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) part[u] += __shfl_xor_sync(0xffffffffu, part[u], o);
+                    if (lane == 0) s_rowdot[warp * kRows + r0 + u] = part[u] * s_ac[warp * kRows + r0 + u];
+                }
+            }
             constexpr int kGroups = kBT / DK;
             const int i = tid % DK, grp = tid / DK;
             float acc = 0.f;
-            if (Sc)
-                for (int j = grp; j < DV; j += kGroups) acc = fmaf(dSx[i * DV + j], Sc[i * DV + j], acc);
-            acc *= s_ac[i];
             for (int r = grp; r < kC; r += kGroups) acc = fmaf(dKh[r * DK + i], Kh[r * DK + i], acc);
             s_red[tid] = acc;
         }
         __syncthreads();
-        // per element: dK, dQ and dlogA_r (into shared memory for the reverse sums)
+        // per element: dK, dQ and dlogA_r (into shared memory for the reverse sums); four
+        // elements per thread and round, two rounds' loads in flight
         const bool norms = (p.prep & (PREP_L2NORM_K | PREP_L2NORM_Q)) != 0;
-        for (int e = tid; e < kC * DK; e += kBT) {
-            const int r = e / DK, i = e % DK;
-            const float a = A_[e];
-            const float gk = dKb[e] * a + dKt[e] / a + dKh[e] * (s_ac[i] / a);
-            const float gq = sc * dQb[e] * a;
-            s_buf[e] = dKb[e] * Kb[e] - dKt[e] * Kt[e] + dQb[e] * Qb[e] - dKh[e] * Kh[e];
-            if (norms) {  // gradients of the normalised rows, carried back below
-                dKb[e] = gk;
-                dQb[e] = gq;
-            } else if (r < Lc) {
-                const int64_t o = ((t0 + r) * H + h) * DK + i;
-                st_out(DK_, o, gk);
-                st_out(DQ, o, gq);
+        {
+            constexpr int kVec = kC * DK / 4, kRounds = kVec / kBT, kB = 2;
+            static_assert(kRounds % kB == 0, "rounds");
+#pragma unroll 1
+            for (int rb = 0; rb < kRounds; rb += kB) {
+                float4 a[kB], kb[kB], kt[kB], kh[kB], qb[kB], dkb[kB], dkt[kB], dkh[kB], dqb[kB];
+#pragma unroll
+                for (int u = 0; u < kB; ++u) {
+                    const int e = (tid + (rb + u) * kBT) * 4;
+                    a[u] = ld4(A_ + e); kb[u] = ld4(Kb + e); kt[u] = ld4(Kt + e); kh[u] = ld4(Kh + e);
+                    qb[u] = ld4(Qb + e); dkb[u] = ld4(dKb + e); dkt[u] = ld4(dKt + e); dkh[u] = ld4(dKh + e);
+                    dqb[u] = ld4(dQb + e);
+                }
+#pragma unroll
+                for (int u = 0; u < kB; ++u) {
+                    const int e = (tid + (rb + u) * kBT) * 4, r = e / DK, i = e % DK;
+                    const float *pa = &a[u].x, *pkb = &kb[u].x, *pkt = &kt[u].x, *pkh = &kh[u].x, *pqb = &qb[u].x;
+                    const float *pdkb = &dkb[u].x, *pdkt = &dkt[u].x, *pdkh = &dkh[u].x, *pdqb = &dqb[u].x;
+                    float gk[4], gq[4];
+#pragma unroll
+                    for (int t = 0; t < 4; ++t) {
+                        const float ra = 1.f / pa[t];
+                        gk[t] = pdkb[t] * pa[t] + pdkt[t] * ra + pdkh[t] * (s_ac[i + t] * ra);
+                        gq[t] = sc * pdqb[t] * pa[t];
+                        s_buf[e + t] = pdkb[t] * pkb[t] - pdkt[t] * pkt[t] + pdqb[t] * pqb[t] - pdkh[t] * pkh[t];
+                    }
+                    if (norms) {  // gradients of the normalised rows, carried back below
+                        st4(dKb + e, make_float4(gk[0], gk[1], gk[2], gk[3]));
+                        st4(dQb + e, make_float4(gq[0], gq[1], gq[2], gq[3]));
+                    } else if (r < Lc) {
+                        const int64_t o = ((t0 + r) * H + h) * DK + i;
+#pragma unroll
+                        for (int t = 0; t < 4; ++t) {
+                            st_out(DK_, o + t, gk[t]);
+                            st_out(DQ, o + t, gq[t]);
+                        }
+                    }
+                }
             }
         }
-        for (int e = tid; e < kC * DV; e += kBT) {
-            const int r = e / DV, j = e % DV;
-            if (r < Lc) st_out(DV_, ((t0 + r) * H + h) * DV + j, dR[e]);
+        {
+            constexpr int kVec = kC * DV / 4, kIt = kVec / kBT;
+            float4 d[kIt];
+#pragma unroll
+            for (int it = 0; it < kIt; ++it) d[it] = ld4(dR + (tid + it * kBT) * 4);
+#pragma unroll
+            for (int it = 0; it < kIt; ++it) {
+                const int e = (tid + it * kBT) * 4, r = e / DV, j = e % DV;
+                if (r < Lc) {
+                    const int64_t o = ((t0 + r) * H + h) * DV + j;
+                    st_out(DV_, o, d[it].x);
+                    st_out(DV_, o + 1, d[it].y);
+                    st_out(DV_, o + 2, d[it].z);
+                    st_out(DV_, o + 3, d[it].w);
+                }
+            }
         }
         __syncthreads();
         if (tid < DK) {  // dg_s = dlogA_C + sum_{r >= s} dlogA_r (raw gate x: times 1 - sigmoid(x))
             const bool sig = (p.prep & PREP_SIGMOID_GATE) != 0;
             const Tin *G = static_cast<const Tin *>(p.g);
-            float acc = 0.f;
+            float acc = s_rowdot[tid];
             for (int gi = 0; gi < kBT / DK; ++gi) acc += s_red[tid + gi * DK];
             for (int r = kC - 1; r >= 0; --r) {
                 acc += s_buf[r * DK + tid];
@@ -575,6 +818,7 @@ __global__ void __launch_bounds__(kBT, 2) kda_bwd_grad_kernel(BwdParams p) {
         }
         __syncthreads();
     }
+    tc_teardown(cx);
 }
 
 template <int DK, int DV, typename Tin>
@@ -582,9 +826,24 @@ cudaError_t launch_typed(const BwdParams &p, cudaStream_t stream) {
     const int64_t chains = static_cast<int64_t>(p.N) * p.H;
     if (chains <= 0) return cudaSuccess;
     if (chains > 0x7fffffffLL || p.ctas <= 0) return cudaErrorInvalidConfiguration;
-    kda_bwd_chunk_kernel<DK, DV, Tin><<<p.ctas, kBT, 0, stream>>>(p);
-    kda_bwd_chain_kernel<DK, DV><<<static_cast<unsigned>(chains * (DV / kChainCols)), kBT, 0, stream>>>(p);
-    kda_bwd_grad_kernel<DK, DV, Tin><<<p.ctas, kBT, 0, stream>>>(p);
+    // the tensor-core operand tiles are dynamic shared memory (a per-device function attribute,
+    // set on every launch)
+    const int dyn = static_cast<int>(tcg::kSmemBytes);
+    // chain blocks of 32 columns while they fit the resident CTAs (two per SM), else 64
+    const bool narrow = DV >= 64 && chains * (DV / 32) <= p.ctas;
+    const void *chain_fn = narrow ? reinterpret_cast<const void *>(kda_bwd_chain_kernel<DK, DV, 32>)
+                                  : reinterpret_cast<const void *>(kda_bwd_chain_kernel<DK, DV, 64>);
+    for (const void *fn : {reinterpret_cast<const void *>(kda_bwd_chunk_kernel<DK, DV, Tin>), chain_fn,
+                           reinterpret_cast<const void *>(kda_bwd_grad_kernel<DK, DV, Tin>)}) {
+        const cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn);
+        if (e != cudaSuccess) return e;
+    }
+    kda_bwd_chunk_kernel<DK, DV, Tin><<<p.ctas, kBT, dyn, stream>>>(p);
+    if (narrow)
+        kda_bwd_chain_kernel<DK, DV, 32><<<static_cast<unsigned>(chains * (DV / 32)), kBT, dyn, stream>>>(p);
+    else
+        kda_bwd_chain_kernel<DK, DV, 64><<<static_cast<unsigned>(chains * (DV / 64)), kBT, dyn, stream>>>(p);
+    kda_bwd_grad_kernel<DK, DV, Tin><<<p.ctas, kBT, dyn, stream>>>(p);
     return cudaGetLastError();
 }
 
