@@ -754,11 +754,12 @@ def run_gpu(args, world, rank, local):
                  "timing": "median per-step CUDA-event time of kda_chunk_fwd (includes the status-word memset"
                            " and the partial-chunk launch)"})
 
-    # the rest of the metric's 4K-128K range and the speculative rollout loop (default workload only)
+    # the rest of the metric's 4K-128K range, 64-wide heads and the speculative rollout loop
+    # (default workload only)
     workloads_sub = None
     if args.workload == "prefill_4k" and not (args.prep or args.no_sub_workloads):
         workloads_sub = {name: measure_workload(kda, name, dev, hbm_peak, tf_peak)
-                         for name in ("long_128k", "varlen_64")}
+                         for name in ("long_128k", "varlen_64", "prefill_4k_d64")}
         workloads_sub["spec_rollout"] = measure_spec_rollout(kda, dev, hbm_peak)
     state_kernels = measure_state_kernels(kda, dev, hbm_peak) if not args.no_state_kernels else None
     backward = measure_backward(kda, case, dev, hbm_peak) if not (args.no_backward or args.prep) else None

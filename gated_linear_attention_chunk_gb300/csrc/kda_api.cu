@@ -132,7 +132,7 @@ kda_status kda_chunk_fwd_prep(const void *q, const void *k, const void *v, const
         }
         kda::ChunkParams cp{};
         cp.q = q; cp.k = k; cp.v = v; cp.g = g; cp.beta = beta; cp.o = o;
-        cp.N = N; cp.H = H; cp.scale = scale;
+        cp.N = N; cp.H = H; cp.dk = dk; cp.dv = dv; cp.scale = scale;
         cp.cu = cu_seqlens; cp.T_total = T_total; cp.seq_len_fixed = fixed_len;
         cp.init_state = init_state; cp.state_out = chunk_state; cp.status = status;
         cp.prep = static_cast<int>(prep); cp.prep_eps = l2_eps;
@@ -418,11 +418,12 @@ kda_status kda_chunk_bwd_prep(const void *q, const void *k, const void *v, const
     const int64_t fixed_len = cu_seqlens ? 0 : T_total / N;
 
     // forward pass leaving the chunk-start states: the tensor-core kernel (no outputs) where
-    // it serves the shape, else the token-sequential kernel
-    if (kda::chunk_tc_supported(dk, dv, static_cast<int>(dtype)) && T_total <= 0x7fffffffLL) {
+    // it serves the shape (its checkpoints are laid out 128 x 128), else the token-sequential kernel
+    if (dk == 128 && dv == 128 && kda::chunk_tc_supported(dk, dv, static_cast<int>(dtype)) &&
+        T_total <= 0x7fffffffLL) {
         kda::ChunkParams cp{};
         cp.q = q; cp.k = k; cp.v = v; cp.g = g; cp.beta = beta; cp.o = nullptr;
-        cp.N = N; cp.H = H; cp.scale = scale; cp.cu = cu_seqlens; cp.T_total = T_total;
+        cp.N = N; cp.H = H; cp.dk = dk; cp.dv = dv; cp.scale = scale; cp.cu = cu_seqlens; cp.T_total = T_total;
         cp.seq_len_fixed = fixed_len; cp.init_state = init_state;
         cp.state_out = reinterpret_cast<float *>(ws + stage_off); cp.status = status; cp.split = 0;
         cp.ckpt = ckpt; cp.prep = static_cast<int>(prep); cp.prep_eps = l2_eps;

@@ -90,6 +90,7 @@ struct TcParams {
     float prep_eps;               // epsilon of the L2 normalisation
     int64_t T_total, seq_len_fixed;
     int N, H;
+    int dk, dv;                   // head dims of the tensors (64 or 128); the tiles are always 128 wide
     float scale;
 };
 
@@ -361,11 +362,13 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_tc_kernel(const __grid_
                     // warm L2 with the chunk that will reuse this stage, so its load is short
                     if (c + 2 < nfull) {
                         const int t2 = t0 + 2 * kC;
-                        for (int x = 0; x < 128; x += 64) {
-                            tma_prefetch_l2_3d(&p.tm_q, x, h, t2);
-                            tma_prefetch_l2_3d(&p.tm_k, x, h, t2);
-                            tma_prefetch_l2_3d(&p.tm_g, x, h, t2);
-                            if (!v_zero) tma_prefetch_l2_3d(&p.tm_v, x, h, t2);
+                        for (int x = 0; x < 128; x += 64) {  // (boxes beyond dk or dv hold no data)
+                            if (x < p.dk) {
+                                tma_prefetch_l2_3d(&p.tm_q, x, h, t2);
+                                tma_prefetch_l2_3d(&p.tm_k, x, h, t2);
+                                tma_prefetch_l2_3d(&p.tm_g, x, h, t2);
+                            }
+                            if (!v_zero && x < p.dv) tma_prefetch_l2_3d(&p.tm_v, x, h, t2);
                         }
                     }
                 }
@@ -496,14 +499,17 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_tc_kernel(const __grid_
         int gseq = 0;
         const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
         const uint32_t tS = tmem + lane_base + TM_S, tSB = tmem + lane_base + TM_SB;
-        const float *s0 = (role == 0 && p.init_state) ? p.init_state + pair * kD * kD : nullptr;
+        // states are dk x dv (row stride dv); channels >= dk and columns >= dv stay zero
+        const int sdk = p.dk, sdv = p.dv;
+        const float *s0 =
+            (role == 0 && p.init_state && j < sdv) ? p.init_state + pair * sdk * sdv : nullptr;
         __nv_bfloat16 *const obase = (role == 2) ? p.o_phi : p.o;
         for (int cc = 0; cc < kD; cc += 32) {
             uint32_t a[16], b[16], pk[16];
 #pragma unroll
             for (int e = 0; e < 16; ++e) {
-                a[e] = __float_as_uint(s0 ? s0[(cc + e) * kD + j] : 0.f);
-                b[e] = __float_as_uint(s0 ? s0[(cc + 16 + e) * kD + j] : 0.f);
+                a[e] = __float_as_uint(s0 && cc + e < sdk ? s0[(cc + e) * sdv + j] : 0.f);
+                b[e] = __float_as_uint(s0 && cc + 16 + e < sdk ? s0[(cc + 16 + e) * sdv + j] : 0.f);
             }
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
@@ -542,8 +548,9 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_tc_kernel(const __grid_
             if constexpr (kPrep) {
                 if (!obase) return;  // checkpoint-only forward
             }
-            __nv_bfloat16 *orow = obase + (t0 * H + h) * kD + j;
-            const int64_t rs = H * kD;
+            if (j >= sdv) return;  // column beyond dv: zero, not stored
+            __nv_bfloat16 *orow = obase + (t0 * H + h) * sdv + j;
+            const int64_t rs = H * sdv;
 #pragma unroll
             for (int e = 0; e < 32; ++e) {
                 const __nv_bfloat162 v = *reinterpret_cast<const __nv_bfloat162 *>(&opk[e]);
@@ -620,7 +627,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_tc_kernel(const __grid_
             }
             tc_fence_after();
             const bool last = (c == nfull - 1);
-            float *sout = (role == 0 ? p.state_out : role == 1 ? p.psi : p.phi) + pair * kD * kD;
+            float *sout = (role == 0 ? p.state_out : role == 1 ? p.psi : p.phi) + pair * sdk * sdv;
             for (int cc = 0; cc < kD; cc += 32) {
                 uint32_t a[16], b[16], pk[16];
                 tmem_ld16(tS + cc, a);
@@ -642,11 +649,11 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_tc_kernel(const __grid_
                 tmem_st16(tS + cc, a);
                 tmem_st16(tS + cc + 16, b);
                 tmem_st16(tSB + cc / 2, pk);
-                if (last) {
+                if (last && j < sdv) {
 #pragma unroll
                     for (int e = 0; e < 16; ++e) {
-                        sout[(cc + e) * kD + j] = __uint_as_float(a[e]);
-                        sout[(cc + 16 + e) * kD + j] = __uint_as_float(b[e]);
+                        if (cc + e < sdk) sout[(cc + e) * sdv + j] = __uint_as_float(a[e]);
+                        if (cc + 16 + e < sdk) sout[(cc + 16 + e) * sdv + j] = __uint_as_float(b[e]);
                     }
                 }
                 if constexpr (kPrep) {
@@ -1101,12 +1108,14 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encoder() {
     return fn;
 }
 
-// [T, H, 128] bf16 tensor, 64 x 64 boxes with the 128-byte swizzle.
-bool encode_tile_map(CUtensorMap *map, const void *base, int64_t T, int H) {
+// [T, H, D] bf16 tensor (D = 64 or 128), 64 x 64 boxes with the 128-byte swizzle.  The kernel
+// reads channels [0, 128) in two boxes; with D = 64 the second box lies wholly beyond the
+// tensor and arrives as zeros (its x coordinate, 64, keeps the 16-byte rule).
+bool encode_tile_map(CUtensorMap *map, const void *base, int64_t T, int H, int D) {
     auto enc = get_encoder();
     if (!enc) return false;
-    cuuint64_t dims[3] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(T)};
-    cuuint64_t strides[2] = {static_cast<cuuint64_t>(kD) * 2, static_cast<cuuint64_t>(H) * kD * 2};
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(T)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(H) * D * 2};
     cuuint32_t box[3] = {64, 1, 64};
     cuuint32_t es[3] = {1, 1, 1};
     return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, es,
@@ -1137,18 +1146,25 @@ cudaError_t launch_order(const int32_t *cu, int N, int32_t *order, cudaStream_t 
     return cudaGetLastError();
 }
 
-bool chunk_tc_supported(int dk, int dv, int dtype) { return dk == 128 && dv == 128 && dtype == 0; }
+bool chunk_tc_supported(int dk, int dv, int dtype) {
+    return (dk == 64 || dk == 128) && (dv == 64 || dv == 128) && dtype == 0;
+}
 
 cudaError_t launch_chunk_tc(const ChunkParams &cp, cudaStream_t stream) {
-    if (!chunk_tc_supported(128, 128, 0)) return cudaErrorNotSupported;
+    const int dk = cp.dk ? cp.dk : kD, dv = cp.dv ? cp.dv : kD;
+    if (!chunk_tc_supported(dk, dv, 0)) return cudaErrorNotSupported;
+    // the T-segment roles, their merge and the backward's checkpoints are laid out 128 x 128
+    if ((cp.split || cp.ckpt) && (dk != kD || dv != kD)) return cudaErrorNotSupported;
     const int64_t seqs = (cp.order && !cp.split) ? cp.n_active : cp.N;
     const int64_t blocks = seqs * cp.H * (cp.split ? 3 : 1);
     if (blocks <= 0 || cp.T_total <= 0) return cudaSuccess;
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     TcParams p{};
-    if (!encode_tile_map(&p.tm_q, cp.q, cp.T_total, cp.H) || !encode_tile_map(&p.tm_k, cp.k, cp.T_total, cp.H) ||
-        !encode_tile_map(&p.tm_g, cp.g, cp.T_total, cp.H) || !encode_tile_map(&p.tm_v, cp.v, cp.T_total, cp.H))
+    if (!encode_tile_map(&p.tm_q, cp.q, cp.T_total, cp.H, dk) || !encode_tile_map(&p.tm_k, cp.k, cp.T_total, cp.H, dk) ||
+        !encode_tile_map(&p.tm_g, cp.g, cp.T_total, cp.H, dk) || !encode_tile_map(&p.tm_v, cp.v, cp.T_total, cp.H, dv))
         return cudaErrorInvalidValue;
+    p.dk = dk;
+    p.dv = dv;
     p.beta = static_cast<const __nv_bfloat16 *>(cp.beta);
     p.o = static_cast<__nv_bfloat16 *>(cp.o);
     p.cu = cp.cu;

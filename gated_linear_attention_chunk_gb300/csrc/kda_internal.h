@@ -131,6 +131,10 @@ struct ChunkParams {
     const void *q, *k, *v, *g, *beta;
     void *o;
     int N, H;
+    // head dims, each 64 or 128 (0 is taken as 128): q, k, g rows have dk channels, v and o
+    // rows dv columns, the states are dk x dv; the kernel works at 128 x 128 with the missing
+    // channels and columns zero (TMA fills them), which leaves the result unchanged
+    int dk, dv;
     float scale;
     const int32_t *cu;          // may be null: equal lengths seq_len_fixed
     int64_t T_total;

@@ -133,9 +133,11 @@ size_t kda_chunk_fwd_workspace_size(int N, int64_t T_total, int H, int dk, int d
  *                init_state (in-place update).
  *   workspace    >= kda_chunk_fwd_workspace_size() bytes (see above), device.
  *
- * Full 64-token chunks run through the chunked WY kernel (bf16, dk=dv=128);
+ * Full 64-token chunks run through the chunked WY kernel (bf16; dk and dv each
+ * 64 or 128: the kernel's tiles are 128 wide and a 64-wide head arrives with
+ * zero channels and columns, which leave the result unchanged);
  * the last len % 64 tokens of each sequence, sequences shorter than 64, and
- * the other dtype/size combinations run through the token-sequential kernel,
+ * fp32 inputs run through the token-sequential kernel,
  * which is the same routine kda_decode_step and kda_replay use: a 1-token
  * sequence here gives the same bits as kda_decode_step on the same state.
  * An empty sequence copies init_state to final_state.  A chain whose chunk
