@@ -418,9 +418,8 @@ kda_status kda_chunk_bwd_prep(const void *q, const void *k, const void *v, const
     const int64_t fixed_len = cu_seqlens ? 0 : T_total / N;
 
     // forward pass leaving the chunk-start states: the tensor-core kernel (no outputs) where
-    // it serves the shape (its checkpoints are laid out 128 x 128), else the token-sequential kernel
-    if (dk == 128 && dv == 128 && kda::chunk_tc_supported(dk, dv, static_cast<int>(dtype)) &&
-        T_total <= 0x7fffffffLL) {
+    // it serves the shape, else the token-sequential kernel
+    if (kda::chunk_tc_supported(dk, dv, static_cast<int>(dtype)) && T_total <= 0x7fffffffLL) {
         kda::ChunkParams cp{};
         cp.q = q; cp.k = k; cp.v = v; cp.g = g; cp.beta = beta; cp.o = nullptr;
         cp.N = N; cp.H = H; cp.dk = dk; cp.dv = dv; cp.scale = scale; cp.cu = cu_seqlens; cp.T_total = T_total;

@@ -657,12 +657,12 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_tc_kernel(const __grid_
                     }
                 }
                 if constexpr (kPrep) {
-                    if (p.ckpt) {  // the state at the start of chunk c + 1 (slot c + 1 of the sequence)
-                        float *ck = p.ckpt + ((ckpt_base(bos, n) + c + 1) * H + h) * kD * kD;
+                    if (p.ckpt && j < sdv) {  // the state at the start of chunk c + 1 (slot c + 1 of the sequence)
+                        float *ck = p.ckpt + ((ckpt_base(bos, n) + c + 1) * H + h) * sdk * sdv;
 #pragma unroll
                         for (int e = 0; e < 16; ++e) {
-                            ck[(cc + e) * kD + j] = __uint_as_float(a[e]);
-                            ck[(cc + 16 + e) * kD + j] = __uint_as_float(b[e]);
+                            if (cc + e < sdk) ck[(cc + e) * sdv + j] = __uint_as_float(a[e]);
+                            if (cc + 16 + e < sdk) ck[(cc + 16 + e) * sdv + j] = __uint_as_float(b[e]);
                         }
                     }
                 }
@@ -1153,8 +1153,8 @@ bool chunk_tc_supported(int dk, int dv, int dtype) {
 cudaError_t launch_chunk_tc(const ChunkParams &cp, cudaStream_t stream) {
     const int dk = cp.dk ? cp.dk : kD, dv = cp.dv ? cp.dv : kD;
     if (!chunk_tc_supported(dk, dv, 0)) return cudaErrorNotSupported;
-    // the T-segment roles, their merge and the backward's checkpoints are laid out 128 x 128
-    if ((cp.split || cp.ckpt) && (dk != kD || dv != kD)) return cudaErrorNotSupported;
+    // the T-segment roles and their merge are laid out 128 x 128
+    if (cp.split && (dk != kD || dv != kD)) return cudaErrorNotSupported;
     const int64_t seqs = (cp.order && !cp.split) ? cp.n_active : cp.N;
     const int64_t blocks = seqs * cp.H * (cp.split ? 3 : 1);
     if (blocks <= 0 || cp.T_total <= 0) return cudaSuccess;

@@ -121,7 +121,7 @@ def test_bwd_full_size_prefill_4k_sampled_heads(kda):
         _check(got, ref, f" (sequence {n})")
 
 
-@pytest.mark.parametrize("dk,dv,dtype", [(128, 128, torch.bfloat16), (64, 64, torch.float32)])
+@pytest.mark.parametrize("dk,dv,dtype", [(128, 128, torch.bfloat16), (64, 64, torch.bfloat16), (64, 64, torch.float32)])
 def test_bwd_prep_matches_oracle(kda, dk, dv, dtype):
     """Raw inputs with every preprocessing flag: the gradients with respect to the raw
     q, k, gate and beta logits (and v, the initial state) equal the oracle's."""
