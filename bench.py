@@ -509,6 +509,28 @@ def _median_ms(call, reps: int, warm: int = 3) -> float:
     return ms[len(ms) // 2]
 
 
+def host_link_peak(dev, nbytes=512 << 20, reps=5):
+    """GB/s of one large pinned host -> device copy and of one device -> host copy (best of
+    ``reps``, CUDA events): the link bound the end-to-end pipeline is measured against."""
+    host = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    devb = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    out = {}
+    for name, dst, src in (("h2d", devb, host), ("d2h", host, devb)):
+        best = None
+        for _ in range(reps):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            dst.copy_(src, non_blocking=True)
+            b.record()
+            torch.cuda.synchronize()
+            ms = a.elapsed_time(b)
+            best = ms if best is None else min(best, ms)
+        out[name] = nbytes / (best / 1e3) / 1e9
+    del host, devb
+    torch.cuda.empty_cache()
+    return out
+
+
 def measure_workload(kda, name, dev, hbm_peak, tf_peak, reps=10):
     """kda_chunk_fwd tokens/s and roofline fraction on another named prefill workload (inputs
     drawn on the device with the same recipe; full workspace, so every path of the call is
@@ -728,7 +750,11 @@ def run_gpu(args, world, rank, local):
         e2e = {"value": world * T * e2e_steps / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
                "d2h_bytes_per_step": int(d2h), "steps": e2e_steps, "ms_per_step": e2e_ms / e2e_steps,
                "host_link_GBs": (h2d + d2h) * e2e_steps / (e2e_ms / 1e3) / 1e9,
+               "host_link_peak_GBs": host_link_peak(dev),
                "pipeline": f"{len(pipe.groups)} sequence groups; H2D, compute and D2H on three streams"}
+        # with the two directions overlapped, a step cannot be shorter than its larger copy
+        pk = e2e["host_link_peak_GBs"]
+        e2e["link_bound_ms_per_step"] = max(h2d / pk["h2d"], d2h / pk["d2h"]) / 1e6
         del pipe
         torch.cuda.empty_cache()
 

@@ -14,7 +14,7 @@ carries that call's accuracy.
 """
 from __future__ import annotations
 
-from typing import List, Optional
+from typing import List, Optional, Tuple
 
 import torch
 
@@ -23,6 +23,22 @@ from . import kda as _kda
 
 def _pinned(t: torch.Tensor) -> torch.Tensor:
     return t if t.is_pinned() else t.pin_memory()
+
+
+def plan_groups(cu: List[int], groups: int) -> List[Tuple[int, int]]:
+    """Cuts N sequences (token offsets ``cu``, N + 1 of them) into at most ``groups`` runs of
+    whole sequences [a, b) with about the same number of tokens each: boundary i is the
+    sequence offset nearest to i / groups of the tokens, kept strictly increasing so that no
+    group is empty (lengths of zero are allowed and go with their neighbours)."""
+    N = len(cu) - 1
+    groups = max(1, min(int(groups), N))
+    T = cu[N] - cu[0]
+    bounds: List[int] = [0]
+    for i in range(1, groups):
+        target = cu[0] + T * i / groups
+        bounds.append(min(range(bounds[-1] + 1, N - (groups - i) + 1), key=lambda m: abs(cu[m] - target)))
+    bounds.append(N)
+    return [(bounds[i], bounds[i + 1]) for i in range(groups) if bounds[i + 1] > bounds[i]]
 
 
 class HostPrefill:
@@ -46,14 +62,7 @@ class HostPrefill:
         T, H, dk = q.shape
         dv = v.shape[2]
         self.scale = float(scale)
-        groups = max(1, min(int(groups), N))
-        # group boundaries in sequences: about the same number of tokens per group
-        bounds: List[int] = [0]
-        for i in range(1, groups):
-            target = T * i / groups
-            bounds.append(min(range(bounds[-1] + 1, N - (groups - i) + 1), key=lambda m: abs(cu[m] - target)))
-        bounds.append(N)
-        self.groups = [(bounds[i], bounds[i + 1]) for i in range(groups) if bounds[i + 1] > bounds[i]]
+        self.groups = plan_groups(cu, groups)
         # per-group cu_seqlens, rebased to the group's first token (host side, pinned)
         self.host_cu = [_pinned(torch.tensor([c - cu[a] for c in cu[a:b + 1]], dtype=torch.int32))
                         for a, b in self.groups]
