@@ -224,7 +224,9 @@ __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, const 
 
 // kPrep: the extended instance -- it applies the input preprocessing of p.prep and
 // writes the chunk-end checkpoints of p.ckpt (the other instance carries none of that code).
-template <bool kPrep>
+// kNarrow: dk or dv is 64 (p.dk, p.dv); the instances for 128 x 128 heads use the constant
+// width, so they carry none of the narrow heads' strides and guards.
+template <bool kPrep, bool kNarrow>
 __global__ void __launch_bounds__(kThreads, 1) kda_chunk_tc_kernel(const __grid_constant__ TcParams p) {
     extern __shared__ uint8_t dsmem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(dsmem_raw) + 1023) & ~uintptr_t(1023));
@@ -363,12 +365,12 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_tc_kernel(const __grid_
                     if (c + 2 < nfull) {
                         const int t2 = t0 + 2 * kC;
                         for (int x = 0; x < 128; x += 64) {  // (boxes beyond dk or dv hold no data)
-                            if (x < p.dk) {
+                            if (!kNarrow || x < p.dk) {
                                 tma_prefetch_l2_3d(&p.tm_q, x, h, t2);
                                 tma_prefetch_l2_3d(&p.tm_k, x, h, t2);
                                 tma_prefetch_l2_3d(&p.tm_g, x, h, t2);
                             }
-                            if (!v_zero && x < p.dv) tma_prefetch_l2_3d(&p.tm_v, x, h, t2);
+                            if (!v_zero && (!kNarrow || x < p.dv)) tma_prefetch_l2_3d(&p.tm_v, x, h, t2);
                         }
                     }
                 }
@@ -500,7 +502,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_tc_kernel(const __grid_
         const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
         const uint32_t tS = tmem + lane_base + TM_S, tSB = tmem + lane_base + TM_SB;
         // states are dk x dv (row stride dv); channels >= dk and columns >= dv stay zero
-        const int sdk = p.dk, sdv = p.dv;
+        const int sdk = kNarrow ? p.dk : kD, sdv = kNarrow ? p.dv : kD;
         const float *s0 =
             (role == 0 && p.init_state && j < sdv) ? p.init_state + pair * sdk * sdv : nullptr;
         __nv_bfloat16 *const obase = (role == 2) ? p.o_phi : p.o;
@@ -1190,7 +1192,8 @@ cudaError_t launch_chunk_tc(const ChunkParams &cp, cudaStream_t stream) {
     // that is current when it is set, so it is set on every launch (a host-side call that
     // allocates nothing and does not synchronize).
     static std::atomic<int> regs_ok{0};  // 0 unknown, 1 as assumed, 2 not
-    for (auto fn : {kda_chunk_tc_kernel<false>, kda_chunk_tc_kernel<true>}) {
+    for (auto fn : {kda_chunk_tc_kernel<false, false>, kda_chunk_tc_kernel<true, false>,
+                    kda_chunk_tc_kernel<false, true>, kda_chunk_tc_kernel<true, true>}) {
         if (regs_ok.load(std::memory_order_acquire) == 0) {
             cudaFuncAttributes fa{};
             if (cudaFuncGetAttributes(&fa, fn) != cudaSuccess) return cudaErrorInvalidConfiguration;
@@ -1203,10 +1206,15 @@ cudaError_t launch_chunk_tc(const ChunkParams &cp, cudaStream_t stream) {
     }
     int unknown = 0;
     regs_ok.compare_exchange_strong(unknown, 1);
-    if (p.prep || p.ckpt)
-        kda_chunk_tc_kernel<true><<<static_cast<unsigned>(blocks), kThreads, kDynSmem, stream>>>(p);
-    else
-        kda_chunk_tc_kernel<false><<<static_cast<unsigned>(blocks), kThreads, kDynSmem, stream>>>(p);
+    const unsigned grid = static_cast<unsigned>(blocks);
+    const bool ext = p.prep || p.ckpt, narrow = dk != kD || dv != kD;
+    if (narrow) {
+        if (ext) kda_chunk_tc_kernel<true, true><<<grid, kThreads, kDynSmem, stream>>>(p);
+        else kda_chunk_tc_kernel<false, true><<<grid, kThreads, kDynSmem, stream>>>(p);
+    } else {
+        if (ext) kda_chunk_tc_kernel<true, false><<<grid, kThreads, kDynSmem, stream>>>(p);
+        else kda_chunk_tc_kernel<false, false><<<grid, kThreads, kDynSmem, stream>>>(p);
+    }
     return cudaGetLastError();
 }
 

@@ -168,6 +168,17 @@ __global__ void __launch_bounds__(kMoThreads, 1) merge_o_kernel(const __grid_con
 
     __nv_bfloat16 *O = static_cast<__nv_bfloat16 *>(p.o);
     const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    // this thread's o row of block i (orow), and of block i + 1 (onext), read one block ahead so
+    // that the read's latency overlaps the current block's products and epilogue
+    uint4 orow[16], onext[16];
+    {
+        const int64_t t = b1 + blk0 * kTB + tid;
+        if (t < e1) {
+            const __nv_bfloat16 *op = O + (t * H + h) * kD;
+#pragma unroll
+            for (int c = 0; c < 16; ++c) orow[c] = reinterpret_cast<const uint4 *>(op)[c];
+        }
+    }
     int i = 0;
     for (; i < nb && !*reinterpret_cast<volatile int *>(&s_stop); ++i) {  // read after the block's barrier
         if (tid == 0) {
@@ -183,6 +194,14 @@ __global__ void __launch_bounds__(kMoThreads, 1) merge_o_kernel(const __grid_con
                 atomicOr(p.status, DEV_ERR_TIMEOUT);
             }
         }
+        if (i + 1 < nb) {
+            const int64_t t = b1 + (blk0 + i + 1) * kTB + tid;
+            if (t < e1) {
+                const __nv_bfloat16 *op = O + (t * H + h) * kD;
+#pragma unroll
+                for (int c = 0; c < 16; ++c) onext[c] = reinterpret_cast<const uint4 *>(op)[c];
+            }
+        }
         // every thread: block i's accumulator row -> o row (this thread's token)
         const bool got = mbar_wait(&bar_d[i & 1], (i >> 1) & 1, globaltimer_ns() + kMoWaitNs);
         if (!got) {
@@ -192,12 +211,7 @@ __global__ void __launch_bounds__(kMoThreads, 1) merge_o_kernel(const __grid_con
         tc_fence_after();
         const int64_t t_begin = b1 + (blk0 + i) * kTB;
         const bool mine = got && (t_begin + tid < e1);
-        uint4 orow[16];
         __nv_bfloat16 *op = O + ((t_begin + tid) * H + h) * kD;
-        if (mine) {
-#pragma unroll
-            for (int c = 0; c < 16; ++c) orow[c] = reinterpret_cast<const uint4 *>(op)[c];
-        }
 #pragma unroll
         for (int cb = 0; cb < 4; ++cb) {
             uint32_t a[32];
@@ -222,6 +236,8 @@ __global__ void __launch_bounds__(kMoThreads, 1) merge_o_kernel(const __grid_con
 #pragma unroll
             for (int c = 0; c < 16; ++c) reinterpret_cast<uint4 *>(op)[c] = orow[c];
         }
+#pragma unroll
+        for (int c = 0; c < 16; ++c) orow[c] = onext[c];
         tc_fence_before();
         __syncthreads();
     }
