@@ -30,8 +30,6 @@ constexpr int kThreads = 256;
 
 __device__ __forceinline__ float ld_in(const float *p, int64_t i) { return p[i]; }
 __device__ __forceinline__ float ld_in(const __nv_bfloat16 *p, int64_t i) { return __bfloat162float(p[i]); }
-__device__ __forceinline__ void st_out(float *p, int64_t i, float x) { p[i] = x; }
-__device__ __forceinline__ void st_out(__nv_bfloat16 *p, int64_t i, float x) { p[i] = __float2bfloat16_rn(x); }
 
 // Sequence of token t: the largest n with first token <= t.
 __device__ __forceinline__ int seq_of(const ConvParams &p, int64_t t) {
@@ -75,48 +73,64 @@ __device__ __forceinline__ float conv_input(const ConvParams &p, int64_t src, in
     return p.state_in[((static_cast<int64_t>(n) * (kConvW - 1) + (kConvW - 1 - back)) * H + h) * Ct + c];
 }
 
-// Eight consecutive channels of one row as floats (16-byte aligned rows).
-__device__ __forceinline__ void ld8(const float *p, float (&x)[8]) {
-    const float4 a = *reinterpret_cast<const float4 *>(p), b = *reinterpret_cast<const float4 *>(p + 4);
-    x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w; x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
-}
-__device__ __forceinline__ void ld8(const __nv_bfloat16 *p, float (&x)[8]) {
-    const uint4 u = *reinterpret_cast<const uint4 *>(p);
-    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-        x[2 * e] = __uint_as_float(w[e] << 16);
-        x[2 * e + 1] = __uint_as_float(w[e] & 0xffff0000u);
+// Raw rows of 4 channels, kept undecoded until they are used (bf16: 8 bytes, fp32: 16).
+template <typename Tin>
+struct Raw4;
+template <>
+struct Raw4<__nv_bfloat16> {
+    uint2 u;
+    __device__ __forceinline__ void load(const __nv_bfloat16 *p) { u = *reinterpret_cast<const uint2 *>(p); }
+    __device__ __forceinline__ void get(float (&x)[4]) const {
+        x[0] = __uint_as_float(u.x << 16);
+        x[1] = __uint_as_float(u.x & 0xffff0000u);
+        x[2] = __uint_as_float(u.y << 16);
+        x[3] = __uint_as_float(u.y & 0xffff0000u);
     }
+};
+template <>
+struct Raw4<float> {
+    float4 a;
+    __device__ __forceinline__ void load(const float *p) { a = *reinterpret_cast<const float4 *>(p); }
+    __device__ __forceinline__ void get(float (&x)[4]) const {
+        x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+    }
+};
+__device__ __forceinline__ void ld4f(const float *p, float (&x)[4]) {
+    const float4 a = *reinterpret_cast<const float4 *>(p);
+    x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
 }
-__device__ __forceinline__ void st8(float *p, const float (&y)[8]) {
+__device__ __forceinline__ void ld4f(const __nv_bfloat16 *p, float (&x)[4]) {
+    Raw4<__nv_bfloat16> r;
+    r.load(p);
+    r.get(x);
+}
+__device__ __forceinline__ void st4(float *p, const float (&y)[4]) {
     *reinterpret_cast<float4 *>(p) = make_float4(y[0], y[1], y[2], y[3]);
-    *reinterpret_cast<float4 *>(p + 4) = make_float4(y[4], y[5], y[6], y[7]);
 }
-__device__ __forceinline__ void st8(__nv_bfloat16 *p, const float (&y)[8]) {
-    uint32_t w[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-        const __nv_bfloat162 v = __floats2bfloat162_rn(y[2 * e], y[2 * e + 1]);
-        w[e] = *reinterpret_cast<const uint32_t *>(&v);
-    }
-    *reinterpret_cast<uint4 *>(p) = make_uint4(w[0], w[1], w[2], w[3]);
+__device__ __forceinline__ void st4(__nv_bfloat16 *p, const float (&y)[4]) {
+    const __nv_bfloat162 a = __floats2bfloat162_rn(y[0], y[1]), b = __floats2bfloat162_rn(y[2], y[3]);
+    *reinterpret_cast<uint2 *>(p) = make_uint2(*reinterpret_cast<const uint32_t *>(&a), *reinterpret_cast<const uint32_t *>(&b));
 }
 
-// A thread owns 8 consecutive channels (all in one of q, k, v) of one head and slides the
-// width-4 window down a block of kConvBlock tokens, so every input is loaded once with
-// 16-byte loads (a warp reads 512 contiguous bytes per token).  The window restarts from
-// the sequence's state where a sequence begins inside the block.  Grid: token blocks x
-// groups of kConvThreads (head, channel group) pairs.
+// A thread owns 4 consecutive channels (all in one of q, k, v) of one head and slides the
+// width-4 window down a block of kConvBlock tokens, so every input is loaded once (a warp
+// reads 256 contiguous bytes of bf16 per token).  The rows are loaded 16 tokens at a time
+// before any is used, so a batch costs one memory latency instead of one per token, and few
+// enough registers stay live that two CTAs fit on an SM.  The window restarts from the
+// sequence's state where a sequence begins inside the block.  Grid: token blocks x groups of
+// kConvThreads (head, channel group) pairs.
 constexpr int kConvBlock = 64;
 constexpr int kConvThreads = 256;
+constexpr int kConvCh = 4;  // channels per thread
 
 template <typename Tin>
-__global__ void __launch_bounds__(kConvThreads) conv_out_kernel(ConvParams p) {
-    const int Ct = 2 * p.dk + p.dv, G = Ct / 8;
+__global__ void __launch_bounds__(kConvThreads, 2) conv_out_kernel(ConvParams p) {
+    constexpr int kBatch = 16;
+    static_assert(kConvBlock % kBatch == 0, "batch");
+    const int Ct = 2 * p.dk + p.dv, G = Ct / kConvCh;
     const int u = static_cast<int>(blockIdx.y) * kConvThreads + threadIdx.x;
     if (u >= p.H * G) return;
-    const int h = u / G, c0 = (u % G) * 8;
+    const int h = u / G, c0 = (u % G) * kConvCh;
     const int64_t H = p.H;
     // which tensor the group lies in, its channel offset there and row length
     const Tin *X;
@@ -125,9 +139,9 @@ __global__ void __launch_bounds__(kConvThreads) conv_out_kernel(ConvParams p) {
     if (c0 < p.dk) { X = static_cast<const Tin *>(p.q); Y = static_cast<Tin *>(p.q_out); cx = c0; d = p.dk; }
     else if (c0 < 2 * p.dk) { X = static_cast<const Tin *>(p.k); Y = static_cast<Tin *>(p.k_out); cx = c0 - p.dk; d = p.dk; }
     else { X = static_cast<const Tin *>(p.v); Y = static_cast<Tin *>(p.v_out); cx = c0 - 2 * p.dk; d = p.dv; }
-    float w[8][kConvW];
+    float w[kConvCh][kConvW];
 #pragma unroll
-    for (int e = 0; e < 8; ++e)
+    for (int e = 0; e < kConvCh; ++e)
 #pragma unroll
         for (int i = 0; i < kConvW; ++i) w[e][i] = p.weight[(static_cast<int64_t>(h) * Ct + c0 + e) * kConvW + i];
     const int64_t t_begin = static_cast<int64_t>(blockIdx.x) * kConvBlock;
@@ -138,54 +152,59 @@ __global__ void __launch_bounds__(kConvThreads) conv_out_kernel(ConvParams p) {
         if (u == 0) atomicOr(p.status, DEV_ERR_SEQLENS);
         return;
     }
-    float hw[kConvW - 1][8];  // the window: inputs t-3, t-2, t-1
+    float hw[kConvW - 1][kConvCh];  // the window: inputs t-3, t-2, t-1
     auto window_at = [&](int64_t t) {
 #pragma unroll
         for (int j = 0; j < kConvW - 1; ++j) {
             const int64_t src = t - (kConvW - 1) + j;
             if (src >= bos) {
-                ld8(X + (src * H + h) * d + cx, hw[j]);
+                ld4f(X + (src * H + h) * d + cx, hw[j]);
             } else if (p.state_in) {
                 const int64_t back = bos - src;
                 const float *sp = p.state_in + ((static_cast<int64_t>(n) * (kConvW - 1) + (kConvW - 1 - back)) * H + h) * Ct + c0;
 #pragma unroll
-                for (int e = 0; e < 8; ++e) hw[j][e] = sp[e];
+                for (int e = 0; e < kConvCh; ++e) hw[j][e] = sp[e];
             } else {
 #pragma unroll
-                for (int e = 0; e < 8; ++e) hw[j][e] = 0.f;
+                for (int e = 0; e < kConvCh; ++e) hw[j][e] = 0.f;
             }
         }
     };
     window_at(t_begin);
-    float xn[8];  // the next token's inputs, loaded one step ahead
-    ld8(X + (t_begin * H + h) * d + cx, xn);
-    for (int64_t t = t_begin; t < t_end; ++t) {
-        if (t >= eos) {  // the next sequence (skipping empty ones) starts here
-            while (n + 1 < p.N && t >= eos) {
-                ++n;
-                if (!seq_bounds(p, n, bos, eos)) {
-                    if (u == 0) atomicOr(p.status, DEV_ERR_SEQLENS);
-                    return;
+    for (int64_t tb = t_begin; tb < t_end; tb += kBatch) {
+        Raw4<Tin> r[kBatch];
+#pragma unroll
+        for (int b = 0; b < kBatch; ++b)
+            if (tb + b < t_end) r[b].load(X + ((tb + b) * H + h) * d + cx);
+#pragma unroll
+        for (int b = 0; b < kBatch; ++b) {
+            const int64_t t = tb + b;
+            if (t >= t_end) break;
+            if (t >= eos) {  // the next sequence (skipping empty ones) starts here
+                while (n + 1 < p.N && t >= eos) {
+                    ++n;
+                    if (!seq_bounds(p, n, bos, eos)) {
+                        if (u == 0) atomicOr(p.status, DEV_ERR_SEQLENS);
+                        return;
+                    }
                 }
+                window_at(t);
             }
-            window_at(t);
-        }
-        float x[8], y[8];
+            float x[kConvCh], y[kConvCh];
+            r[b].get(x);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) x[e] = xn[e];
-        if (t + 1 < t_end) ld8(X + ((t + 1) * H + h) * d + cx, xn);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            float pre = __fmaf_rn(w[e][0], hw[0][e], 0.f);
-            pre = __fmaf_rn(w[e][1], hw[1][e], pre);
-            pre = __fmaf_rn(w[e][2], hw[2][e], pre);
-            pre = __fmaf_rn(w[e][3], x[e], pre);
-            y[e] = __fdividef(pre, 1.f + __expf(-pre));  // SiLU (fast intrinsics; the outputs are rounded to Tin)
-            hw[0][e] = hw[1][e];
-            hw[1][e] = hw[2][e];
-            hw[2][e] = x[e];
+            for (int e = 0; e < kConvCh; ++e) {
+                float pre = __fmaf_rn(w[e][0], hw[0][e], 0.f);
+                pre = __fmaf_rn(w[e][1], hw[1][e], pre);
+                pre = __fmaf_rn(w[e][2], hw[2][e], pre);
+                pre = __fmaf_rn(w[e][3], x[e], pre);
+                y[e] = __fdividef(pre, 1.f + __expf(-pre));  // SiLU (fast intrinsics; the outputs are rounded to Tin)
+                hw[0][e] = hw[1][e];
+                hw[1][e] = hw[2][e];
+                hw[2][e] = x[e];
+            }
+            st4(Y + (t * H + h) * d + cx, y);
         }
-        st8(Y + (t * H + h) * d + cx, y);
     }
 }
 
@@ -213,7 +232,7 @@ cudaError_t launch_typed(const ConvParams &p, cudaStream_t s) {
     const int64_t Ct = 2 * p.dk + p.dv;
     const int64_t n_state = static_cast<int64_t>(p.N) * p.H * Ct;
     const int64_t b_out = (p.T_total + kConvBlock - 1) / kConvBlock, b_state = (n_state + kThreads - 1) / kThreads;
-    const int64_t b_grp = (static_cast<int64_t>(p.H) * (Ct / 8) + kConvThreads - 1) / kConvThreads;
+    const int64_t b_grp = (static_cast<int64_t>(p.H) * (Ct / kConvCh) + kConvThreads - 1) / kConvThreads;
     if (b_out > 0x7fffffffLL || b_state > 0x7fffffffLL || b_grp > 65535) return cudaErrorInvalidConfiguration;
     if (b_out > 0)
         conv_out_kernel<Tin><<<dim3(static_cast<unsigned>(b_out), static_cast<unsigned>(b_grp)), kConvThreads, 0, s>>>(p);
