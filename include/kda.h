@@ -315,7 +315,8 @@ kda_status kda_chunk_bwd_prep(const void *q, const void *k, const void *v, const
  *   previous raw inputs, oldest first (zeros for a new sequence).
  *
  * kda_conv_fwd: the prefill form.  q, k, v [T_total, H, d] raw -> q_out, k_out,
- * v_out (same dtype and layout; then call kda_chunk_fwd(_prep) on them);
+ * v_out (same dtype and layout, not overlapping the inputs, since a block's window
+ * reads the raw rows before it; then call kda_chunk_fwd(_prep) on them);
  * conv_state_in / conv_state_out [N, 3, H, 2dk+dv] (either NULL = zeros / not
  * written; they may be the same buffer).
  * kda_decode_step_conv / kda_replay_conv: the decode and replay forms, the
