@@ -214,6 +214,51 @@ __device__ bool slot_chunk(const BwdParams &p, int64_t slot, int &n, int &c, int
     return true;
 }
 
+// Prefetches the rows [0, rows) x [0, row_bytes) of a matrix with row stride `ld_bytes` into
+// L2, one 128-byte line per thread and round.
+__device__ __forceinline__ void prefetch_rows(const void *base, int rows, int row_bytes, int64_t ld_bytes) {
+    const int lines = row_bytes / 128;
+    for (int e = threadIdx.x; e < rows * lines; e += kBT) {
+        const char *a = static_cast<const char *>(base) + (e / lines) * ld_bytes + (e % lines) * 128;
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(a));
+    }
+}
+
+// Prefetches into L2 what (chunk, head) item `item` will read: its rows of q, k, g, v and dO,
+// and with `records` also its chunk-start state (a checkpoint, or the initial state) and the
+// parts of its record the gradient phase reads (T, dR, dS_next).  Items past the end, or of
+// an invalid partition, prefetch nothing.
+template <int DK, int DV, typename Tin>
+__device__ void prefetch_item(const BwdParams &p, int64_t item, bool records) {
+    if (item >= p.nslots * p.H) return;
+    const int64_t slot = item / p.H;
+    const int h = static_cast<int>(item % p.H);
+    int n, c;
+    int64_t bos, eos;
+    if (!slot_chunk(p, slot, n, c, bos, eos)) return;
+    const int64_t t0 = bos + static_cast<int64_t>(c) * kC;
+    const int Lc = static_cast<int>(eos - t0 < kC ? eos - t0 : kC);
+    const int64_t H = p.H, es = sizeof(Tin);
+    const char *q = static_cast<const char *>(p.q), *k = static_cast<const char *>(p.k);
+    const char *g = static_cast<const char *>(p.g), *v = static_cast<const char *>(p.v);
+    const char *d_o = static_cast<const char *>(p.d_o);
+    const int64_t rk = (t0 * H + h) * DK * es, rv = (t0 * H + h) * DV * es;
+    prefetch_rows(q + rk, Lc, DK * es, H * DK * es);
+    prefetch_rows(k + rk, Lc, DK * es, H * DK * es);
+    prefetch_rows(g + rk, Lc, DK * es, H * DK * es);
+    prefetch_rows(v + rv, Lc, DV * es, H * DV * es);
+    prefetch_rows(d_o + rv, Lc, DV * es, H * DV * es);  // (dO may be unaligned: a row's last line can be missed)
+    if (!records) return;
+    using RC = Rec<DK, DV>;
+    const float *rec = p.rec + item * RC::kTotal;
+    prefetch_rows(rec + RC::kT, 1, kC * kC * 4, 0);
+    prefetch_rows(rec + RC::kdR, 1, kC * DV * 4, 0);
+    prefetch_rows(rec + RC::kdSn, 1, DK * DV * 4, 0);
+    const float *Sc = c > 0 ? p.ckpt + (slot * H + h) * DK * DV
+                            : (p.init_state ? p.init_state + (static_cast<int64_t>(n) * H + h) * DK * DV : nullptr);
+    if (Sc) prefetch_rows(Sc, 1, DK * DV * 4, 0);
+}
+
 // Chunk inputs of (t0, Lc, h) into the CTA scratch: A, Kbar, Ktil, Khat, Qbar (C x DK),
 // V (optional) and dO (C x DV), beta and A_C into shared memory.  With preprocessing
 // (p.prep) the raw inputs are mapped as the forward maps them: alpha = sigmoid(x_g),
@@ -476,6 +521,7 @@ __global__ void __launch_bounds__(kBT, 2) kda_bwd_chunk_kernel(BwdParams p) {
         const int Lc = static_cast<int>(eos - t0 < kC ? eos - t0 : kC);
         float *rec = p.rec + item * RC::kTotal;
         load_chunk<DK, DV, Tin>(p, t0, Lc, h, W, false, s_buf, s_beta, s_ac, s_rk, s_rq);
+        prefetch_item<DK, DV, Tin>(p, item + gridDim.x, false);
         if (threadIdx.x < DK) {
             rec[RC::kAC + threadIdx.x] = s_ac[threadIdx.x];
             if (!(s_ac[threadIdx.x] >= kMinDecay)) atomicOr(p.status, DEV_ERR_GATE);
@@ -499,15 +545,6 @@ __global__ void __launch_bounds__(kBT, 2) kda_bwd_chunk_kernel(BwdParams p) {
 // (32 when that still fits the resident CTAs, else 64).  While one chunk is processed the
 // records of the next one back are prefetched into L2.
 
-// Prefetches the rows [0, rows) x [0, row_bytes) of a matrix with row stride `ld_bytes` into
-// L2, one 128-byte line per thread and round.
-__device__ __forceinline__ void prefetch_rows(const void *base, int rows, int row_bytes, int64_t ld_bytes) {
-    const int lines = row_bytes / 128;
-    for (int e = threadIdx.x; e < rows * lines; e += kBT) {
-        const char *a = static_cast<const char *>(base) + (e / lines) * ld_bytes + (e % lines) * 128;
-        asm volatile("prefetch.global.L2 [%0];" ::"l"(a));
-    }
-}
 
 template <int DK, int DV>
 __device__ __forceinline__ void prefetch_chain_record(const float *rec, int col0, int kCB) {
@@ -626,6 +663,7 @@ __global__ void __launch_bounds__(kBT, 2) kda_bwd_grad_kernel(BwdParams p) {
         float *Mr = W + S::kMr, *P = W + S::kP, *Tp = W + S::kTp, *dP = W + S::kdP;
         float *dTp = W + S::kdTp, *X = W + S::kX, *dM = W + S::kdM;
 
+        if (item == blockIdx.x) prefetch_item<DK, DV, Tin>(p, item, true);  // later items: one item ahead
         load_chunk<DK, DV, Tin>(p, t0, Lc, h, W, true, s_buf, s_beta, s_ac, s_rk, s_rq);
         tcg::gemm<kC, kC, DK, false, true, kBT>(cx, Mr, kC, Kb, DK, Kt, DK, 1.f, false, 0);
         tcg::gemm<kC, kC, DK, false, true, kBT>(cx, P, kC, Qb, DK, Kt, DK, 1.f, false, 1);
@@ -676,6 +714,7 @@ __global__ void __launch_bounds__(kBT, 2) kda_bwd_grad_kernel(BwdParams p) {
         __syncthreads();
         tcg::gemm<kC, DK, kC, false, false, kBT>(cx, dKb, DK, dM, kC, Kt, DK, 1.f, true, 0);
         tcg::gemm<kC, DK, kC, true, false, kBT>(cx, dKt, DK, dM, kC, Kb, DK, 1.f, true, 0);
+        prefetch_item<DK, DV, Tin>(p, item + gridDim.x, true);
         // gate gradients: dlogA_C = A_C sum_j dS_next S + sum_r dKhat Khat.  The row sums of
         // dS_next * S take one warp per group of rows, lanes across the columns (four rows'
         // loads in flight); the column sums of dKhat * Khat one thread per column and part.
