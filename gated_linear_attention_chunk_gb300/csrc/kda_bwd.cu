@@ -154,10 +154,12 @@ __device__ void tc_teardown(const tcg::Ctx &cx) {
     }
 }
 
-// Record of one (chunk slot, head), in floats.
+// Record of one (chunk slot, head), in floats.  Phase A writes F into the dR slot and E into
+// its own slot; the chain accumulates dR = F + G dS_next and E - Kbar^T dR onto them in place
+// and writes dS_next.
 template <int DK, int DV>
 struct Rec {
-    static constexpr int64_t kT = 0, kKb = kT + kC * kC, kG = kKb + kC * DK, kF = kG + kC * DK, kdR = kF + kC * DV,
+    static constexpr int64_t kT = 0, kKb = kT + kC * kC, kG = kKb + kC * DK, kdR = kG + kC * DK,
                              kE = kdR + kC * DV, kdSn = kE + DK * DV, kAC = kdSn + DK * DV, kTotal = kAC + DK;
 };
 // Scratch of one persistent CTA, in floats.
@@ -533,7 +535,7 @@ __global__ void __launch_bounds__(kBT, 2) kda_bwd_chunk_kernel(BwdParams p) {
         // G = T'^T Khat, F = T'^T (P^T dO), E = Qbar^T dO
         tcg::gemm<kC, DK, kC, true, false, kBT>(cx, rec + RC::kG, DK, W + S::kTp, kC, W + S::kKh, DK, 1.f, false, 0);
         tcg::gemm<kC, DV, kC, true, false, kBT>(cx, W + S::kY, DV, W + S::kP, kC, W + S::kdO, DV, 1.f, false, 0);
-        tcg::gemm<kC, DV, kC, true, false, kBT>(cx, rec + RC::kF, DV, W + S::kTp, kC, W + S::kY, DV, 1.f, false, 0);
+        tcg::gemm<kC, DV, kC, true, false, kBT>(cx, rec + RC::kdR, DV, W + S::kTp, kC, W + S::kY, DV, 1.f, false, 0);
         tcg::gemm<DK, DV, kC, true, false, kBT>(cx, rec + RC::kE, DV, W + S::kQb, DK, W + S::kdO, DV, 1.f, false, 0);
     }
     tc_teardown(cx);
@@ -551,7 +553,7 @@ __device__ __forceinline__ void prefetch_chain_record(const float *rec, int col0
     using RC = Rec<DK, DV>;
     prefetch_rows(rec + RC::kG, 1, kC * DK * 4, 0);
     prefetch_rows(rec + RC::kKb, 1, kC * DK * 4, 0);
-    prefetch_rows(rec + RC::kF + col0, kC, kCB * 4, DV * 4);
+    prefetch_rows(rec + RC::kdR + col0, kC, kCB * 4, DV * 4);
     prefetch_rows(rec + RC::kE + col0, DK, kCB * 4, DV * 4);
     prefetch_rows(rec + RC::kAC, 1, DK * 4, 0);
 }
@@ -574,27 +576,27 @@ __global__ void __launch_bounds__(kBT, 2) kda_bwd_chain_kernel(BwdParams p) {
     __shared__ uint64_t s_bar;
     __shared__ uint32_t s_tmem;
     tcg::Ctx cx = tc_setup(bwd_dyn, &s_bar, &s_tmem, p.status);
-    // this CTA's columns of the chain's two DK x DV states (row stride DV)
+    // this CTA's columns of the chain's DK x DV state dS (row stride DV)
     float *dS = p.scratch + static_cast<int64_t>(p.ctas) * S::kTotal + pair * 2 * DK * DV + col0;
-    float *dSn = dS + DK * DV;
     const int nch = static_cast<int>((eos - bos + kC - 1) / kC);
     const int64_t base = ckpt_base(bos, n);
-    if (nch > 0) prefetch_chain_record<DK, DV>(p.rec + ((base + nch - 1) * p.H + h) * RC::kTotal, col0, kCB);
+    auto rec_of = [&](int c) { return p.rec + ((base + c) * p.H + h) * RC::kTotal; };
+    if (nch > 0) prefetch_chain_record<DK, DV>(rec_of(nch - 1), col0, kCB);
     for (int e = tid; e < DK * kCB; e += kBT) {
         const int i = e / kCB, j = e % kCB;
-        dS[i * DV + j] = p.d_final ? p.d_final[pair * DK * DV + i * DV + col0 + j] : 0.f;
+        const float x = p.d_final ? p.d_final[pair * DK * DV + i * DV + col0 + j] : 0.f;
+        dS[i * DV + j] = x;
+        if (nch > 0) rec_of(nch - 1)[RC::kdSn + i * DV + col0 + j] = x;  // dS_next of the last chunk
     }
     __syncthreads();
     for (int c = nch - 1; c >= 0; --c) {
-        float *rec = p.rec + ((base + c) * p.H + h) * RC::kTotal;
-        if (c > 0) prefetch_chain_record<DK, DV>(p.rec + ((base + c - 1) * p.H + h) * RC::kTotal, col0, kCB);
-        cta_copy<DK, kCB>(rec + RC::kdSn + col0, DV, dS, DV);
-        cta_copy<DK, kCB>(dSn, DV, rec + RC::kE + col0, DV);
-        cta_copy<kC, kCB>(rec + RC::kdR + col0, DV, rec + RC::kF + col0, DV);
-        __syncthreads();
-        // dR = G dS_next + F;  dS = Diag(A_C) dS_next + E - Kbar^T dR   (this CTA's columns)
+        float *rec = rec_of(c);
+        if (c > 0) prefetch_chain_record<DK, DV>(rec_of(c - 1), col0, kCB);
+        // dR = F + G dS_next (onto F in the dR slot);  E' = E - Kbar^T dR (onto E);
+        // dS = Diag(A_C) dS_next + E', which is also the dS_next of chunk c - 1
         tcg::gemm<kC, kCB, DK, false, false, kBT>(cx, rec + RC::kdR + col0, DV, rec + RC::kG, DK, dS, DV, 1.f, true, 0);
-        tcg::gemm<DK, kCB, kC, true, false, kBT>(cx, dSn, DV, rec + RC::kKb, DK, rec + RC::kdR + col0, DV, -1.f, true, 0);
+        tcg::gemm<DK, kCB, kC, true, false, kBT>(cx, rec + RC::kE + col0, DV, rec + RC::kKb, DK, rec + RC::kdR + col0,
+                                                 DV, -1.f, true, 0);
         {
             constexpr int kVec = DK * kCB / 4, kIt = kVec / kBT;
             static_assert(kVec % kBT == 0, "chain block");
@@ -604,15 +606,17 @@ __global__ void __launch_bounds__(kBT, 2) kda_bwd_chain_kernel(BwdParams p) {
             for (int it = 0; it < kIt; ++it) {
                 const int e = tid + it * kBT, i = e / (kCB / 4), j = (e % (kCB / 4)) * 4;
                 a[it] = __ldcg(reinterpret_cast<const float4 *>(dS + i * DV + j));
-                b[it] = __ldcg(reinterpret_cast<const float4 *>(dSn + i * DV + j));
+                b[it] = __ldcg(reinterpret_cast<const float4 *>(rec + RC::kE + col0 + i * DV + j));
                 ac[it] = __ldcg(rec + RC::kAC + i);
             }
+            float *prev = c > 0 ? rec_of(c - 1) + RC::kdSn + col0 : nullptr;
 #pragma unroll
             for (int it = 0; it < kIt; ++it) {
                 const int e = tid + it * kBT, i = e / (kCB / 4), j = (e % (kCB / 4)) * 4;
                 const float4 r = make_float4(fmaf(ac[it], a[it].x, b[it].x), fmaf(ac[it], a[it].y, b[it].y),
                                              fmaf(ac[it], a[it].z, b[it].z), fmaf(ac[it], a[it].w, b[it].w));
                 *reinterpret_cast<float4 *>(dS + i * DV + j) = r;
+                if (prev) *reinterpret_cast<float4 *>(prev + i * DV + j) = r;
             }
         }
         __syncthreads();
