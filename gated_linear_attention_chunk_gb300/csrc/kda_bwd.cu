@@ -165,10 +165,12 @@ struct Rec {
 // Scratch of one persistent CTA, in floats.
 template <int DK, int DV>
 struct Scr {
-    static constexpr int64_t kA = 0, kKb = kA + kC * DK, kKt = kKb + kC * DK, kKh = kKt + kC * DK,
-                             kQb = kKh + kC * DK, kdQb = kQb + kC * DK, kdKb = kdQb + kC * DK,
-                             kdKt = kdKb + kC * DK, kdKh = kdKt + kC * DK, kV = kdKh + kC * DK, kdO = kV + kC * DV,
-                             kR = kdO + kC * DV, kU = kR + kC * DV, kdU = kU + kC * DV, kY = kdU + kC * DV,
+    // Kbar and Qbar are adjacent (one 128-row operand for [M; P]), as are M and P; V is loaded
+    // into R's slot, where R = V - Kbar S accumulates
+    static constexpr int64_t kA = 0, kKb = kA + kC * DK, kQb = kKb + kC * DK, kKt = kQb + kC * DK,
+                             kKh = kKt + kC * DK, kdQb = kKh + kC * DK, kdKb = kdQb + kC * DK,
+                             kdKt = kdKb + kC * DK, kdKh = kdKt + kC * DK, kR = kdKh + kC * DK, kdO = kR + kC * DV,
+                             kV = kR, kU = kdO + kC * DV, kdU = kU + kC * DV, kY = kdU + kC * DV,
                              kMr = kY + kC * DV, kP = kMr + kC * kC, kTp = kP + kC * kC,
                              kdP = kTp + kC * kC, kdTp = kdP + kC * kC, kX = kdTp + kC * kC, kdM = kX + kC * kC,
                              kTotal = kdM + kC * kC;
@@ -529,8 +531,8 @@ __global__ void __launch_bounds__(kBT, 2) kda_bwd_chunk_kernel(BwdParams p) {
             if (!(s_ac[threadIdx.x] >= kMinDecay)) atomicOr(p.status, DEV_ERR_GATE);
         }
         cta_copy<kC, DK>(rec + RC::kKb, DK, W + S::kKb, DK);
-        tcg::gemm<kC, kC, DK, false, true, kBT>(cx, W + S::kMr, kC, W + S::kKb, DK, W + S::kKt, DK, 1.f, false, 0);
-        tcg::gemm<kC, kC, DK, false, true, kBT>(cx, W + S::kP, kC, W + S::kQb, DK, W + S::kKt, DK, 1.f, false, 1);
+        // [Mr; P] = [Kbar; Qbar] Ktil^T in one product, P's rows masked to the lower triangle
+        tcg::gemm<2 * kC, kC, DK, false, true, kBT>(cx, W + S::kMr, kC, W + S::kKb, DK, W + S::kKt, DK, 1.f, false, 3);
         tri_inverse(W + S::kMr, s_beta, s_buf, rec + RC::kT, W + S::kTp);
         // G = T'^T Khat, F = T'^T (P^T dO), E = Qbar^T dO
         tcg::gemm<kC, DK, kC, true, false, kBT>(cx, rec + RC::kG, DK, W + S::kTp, kC, W + S::kKh, DK, 1.f, false, 0);
@@ -663,16 +665,14 @@ __global__ void __launch_bounds__(kBT, 2) kda_bwd_grad_kernel(BwdParams p) {
         const float *dSx = rec + RC::kdSn, *dR = rec + RC::kdR, *T = rec + RC::kT;
         float *A_ = W + S::kA, *Kb = W + S::kKb, *Kt = W + S::kKt, *Kh = W + S::kKh, *Qb = W + S::kQb;
         float *dQb = W + S::kdQb, *dKb = W + S::kdKb, *dKt = W + S::kdKt, *dKh = W + S::kdKh;
-        float *Vs = W + S::kV, *dOs = W + S::kdO, *R = W + S::kR, *U = W + S::kU, *dU = W + S::kdU;
+        float *dOs = W + S::kdO, *R = W + S::kR, *U = W + S::kU, *dU = W + S::kdU;
         float *Mr = W + S::kMr, *P = W + S::kP, *Tp = W + S::kTp, *dP = W + S::kdP;
         float *dTp = W + S::kdTp, *X = W + S::kX, *dM = W + S::kdM;
 
         if (item == blockIdx.x) prefetch_item<DK, DV, Tin>(p, item, true);  // later items: one item ahead
         load_chunk<DK, DV, Tin>(p, t0, Lc, h, W, true, s_buf, s_beta, s_ac, s_rk, s_rq);
-        tcg::gemm<kC, kC, DK, false, true, kBT>(cx, Mr, kC, Kb, DK, Kt, DK, 1.f, false, 0);
-        tcg::gemm<kC, kC, DK, false, true, kBT>(cx, P, kC, Qb, DK, Kt, DK, 1.f, false, 1);
+        tcg::gemm<2 * kC, kC, DK, false, true, kBT>(cx, Mr, kC, Kb, DK, Kt, DK, 1.f, false, 3);  // [Mr; P]
         cta_map<kC, kC>(Tp, T, [&](int, int j, float x) { return x * s_beta[j]; });
-        cta_copy<kC, DV>(R, DV, Vs, DV);
         __syncthreads();
         // forward quantities of the chunk: R = V - Kbar S, U = T' R
         if (Sc) tcg::gemm<kC, DV, DK, false, false, kBT>(cx, R, DV, Kb, DK, Sc, DV, -1.f, true, 0);

@@ -4,7 +4,8 @@
 // stores are seen after a barrier).
 //
 //   C (M x N, row stride ldc) = alpha op(A) op(B), or += when `acc`, with the optional triangular
-//   masks of the scalar version (1 keeps entries i >= j, 2 entries i > j).
+//   masks (1 keeps entries i >= j, 2 entries i > j, 3 rows i < 64 whole and rows i >= 64 where
+//   i - 64 >= j: two stacked 64-row results, the second lower-triangular).
 //
 // op(A) is staged as a 128-row, K-major tile with the 128-byte swizzle (rows M .. 127 are not
 // written: their results are never read), op(B) as an N-row K-major tile (row n holds column n of
@@ -168,7 +169,7 @@ __device__ bool gemm(Ctx &cx, float *C, int ldc, const float *A, int lda, const 
 #pragma unroll
                 for (int e = 0; e < kW; ++e) {
                     const int n = cc + e;
-                    const bool keep = mask == 0 || (mask == 1 ? m >= n : m > n);
+                    const bool keep = mask == 0 || (mask == 1 ? m >= n : mask == 2 ? m > n : (m < 64 || m - 64 >= n));
                     d[e] = keep ? alpha * __uint_as_float(v[e >> 4][e & 15]) : 0.f;
                 }
                 if (acc) {
