@@ -265,9 +265,14 @@ kda_status kda_replay_prep(float *state_pool, int64_t num_slots, const int32_t *
  * (d_final_state [N, H, dk, dv] fp32, or NULL = zero).  The KDA paragraph of
  * "Kimi K3 on Fireworks: Fast RL at frontier scale" quotes a backward kernel but
  * no formula; this is the reverse mode of the same recurrence, evaluated on the
- * 64-token chunked form: a forward pass stores the state at every chunk start
- * in the workspace, then one CTA per (sequence, head) walks the chunks in
- * reverse.
+ * 64-token chunked form in four launches: a forward pass stores the state at
+ * every chunk start in the workspace; every (chunk, head) computes its
+ * chunk-local terms in parallel; one CTA per (sequence, head, block of state
+ * columns) carries the state gradient back through the chunks; every (chunk,
+ * head) then computes its gradients in parallel.  The matrix products run on the
+ * tensor cores in tf32 with fp32 accumulation.  Gates whose 64-token decay falls
+ * below the chunked form's range are not recomputed token by token here (the
+ * forward call does that): the backward reports KDA_ERR_GATE_RANGE instead.
  *
  * Inputs as for kda_chunk_fwd (same dtype, layouts, cu_seqlens, init_state,
  * scale).  Outputs, all in the input dtype: d_q, d_k, d_g [T_total, H, dk],

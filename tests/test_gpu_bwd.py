@@ -149,3 +149,21 @@ def test_bwd_prep_zero_is_the_plain_call(kda):
     torch.cuda.synchronize()
     for key in ("dq", "dk", "dv", "dg", "dbeta", "d_init"):
         assert torch.equal(a[key], b[key]), key
+
+
+def test_bwd_strong_decay_reports_gate_range(kda):
+    """A chunk whose decay leaves the chunked form's range: the backward has no token-by-token
+    fallback, so it reports KDA_ERR_GATE_RANGE through the device status (and returns)."""
+    case = workloads.make_case([300, 130], H=2, dk=128, dv=128, seed=88)
+    g = case.g.clone()
+    g[70:134, 1, :] = -3.0  # a whole chunk of sequence 0, head 1: decay e^-192
+    d_o, d_fin = _grads_out(case, seed=9)
+    d = to_dev(case)
+    ws = kda.new_workspace(kda.kda_chunk_bwd_workspace_size(case.N, case.T_total, case.H, case.dk, case.dv), "cuda")
+    kda.kda_chunk_bwd(d["q"], d["k"], d["v"], g.cuda(), d["beta"], d_o.cuda(), cu_seqlens=d["cu_seqlens"],
+                      init_state=d["init_state"], d_final_state=d_fin.cuda(), scale=case.scale, workspace=ws)
+    assert kda.kda_device_status(ws) == kda.KDA_ERR_GATE_RANGE
+    # the same call on in-range gates is clean with the same workspace
+    kda.kda_chunk_bwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d_o.cuda(), cu_seqlens=d["cu_seqlens"],
+                      init_state=d["init_state"], d_final_state=d_fin.cuda(), scale=case.scale, workspace=ws)
+    assert kda.kda_device_status(ws) == kda.KDA_OK
