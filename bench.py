@@ -739,19 +739,25 @@ def run_gpu(args, world, rank, local):
             raise RuntimeError("e2e device status")
         if distributed:
             dist.barrier()
-        a, bb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        for _ in range(e2e_steps):
-            pipe.run()
-        bb.record(stream)
-        torch.cuda.synchronize()
-        e2e_ms = max_over_ranks(a.elapsed_time(bb), dev)
+        # three timed loops, the median one reported: the host link is shared with the node's
+        # other jobs, so a single loop can land in someone else's burst
+        loop_ms = []
+        for _ in range(3):
+            a, bb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for _ in range(e2e_steps):
+                pipe.run()
+            bb.record(stream)
+            torch.cuda.synchronize()
+            loop_ms.append(a.elapsed_time(bb))
+        e2e_ms = max_over_ranks(sorted(loop_ms)[1], dev)
         h2d, d2h = pipe.h2d_bytes, pipe.d2h_bytes
         e2e = {"value": world * T * e2e_steps / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
                "d2h_bytes_per_step": int(d2h), "steps": e2e_steps, "ms_per_step": e2e_ms / e2e_steps,
                "host_link_GBs": (h2d + d2h) * e2e_steps / (e2e_ms / 1e3) / 1e9,
                "host_link_peak_GBs": host_link_peak(dev),
-               "pipeline": f"{len(pipe.groups)} sequence groups; H2D, compute and D2H on three streams"}
+               "pipeline": f"{len(pipe.groups)} sequence groups; H2D, compute and D2H on three streams",
+               "loops_ms": loop_ms, "timing": "median of 3 timed loops"}
         # with the two directions overlapped, a step cannot be shorter than its larger copy
         pk = e2e["host_link_peak_GBs"]
         e2e["link_bound_ms_per_step"] = max(h2d / pk["h2d"], d2h / pk["d2h"]) / 1e6
