@@ -362,12 +362,14 @@ def measure_state_kernels(kda, dev, hbm_peak, n_seq=128, H=32, d=128, reps=50):
     # the same with the short convolution fused (raw projections, every preprocessing flag)
     cw = torch.randn(H, 3 * d, kda.KDA_CONV_WIDTH, device=dev) * 0.5
     cpool = torch.zeros(n_seq, kda.KDA_CONV_WIDTH - 1, H, 3 * d, device=dev)
-    for name in ("decode", "replay", "decode_conv", "replay_conv"):
+    for name in ("decode", "replay", "replay_prep", "decode_conv", "replay_conv"):
         def call():
             if name == "decode":
                 kda.kda_decode_step(q[:n_seq], k[:n_seq], v[:n_seq], g[:n_seq], b[:n_seq], pool, o=o, workspace=ws)
             elif name == "replay":
                 kda.kda_replay(pool, k, v, g, b, cu, workspace=ws)
+            elif name == "replay_prep":  # every preprocessing flag, no convolution
+                kda.kda_replay_prep(pool, k, v, g, b, cu, prep=15, workspace=ws)
             elif name == "decode_conv":
                 kda.kda_decode_step_conv(q[:n_seq], k[:n_seq], v[:n_seq], g[:n_seq], b[:n_seq], pool, cw, cpool,
                                          prep=15, o=o, workspace=ws)
