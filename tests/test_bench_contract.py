@@ -29,3 +29,20 @@ def test_warmup_below_three_is_refused():
     r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--warmup", "2"],
                        capture_output=True, text=True, timeout=120, cwd=ROOT)
     assert r.returncode != 0 and "warmup" in r.stderr
+
+
+def test_stored_traffic_is_reported_only_for_the_captured_source(tmp_path, monkeypatch):
+    """roofline.traffic comes from one ncu capture: bench.py reports it only while the kernel's
+    source hashes to the value stored with it, and null for any other source."""
+    sys.path.insert(0, ROOT)
+    import bench
+    nbytes, sha = bench.DOMINANT_TRAFFIC["prefill_4k"]
+    assert nbytes > 0 and len(sha) == 16
+    src = tmp_path / "kernel.cu"
+    src.write_bytes(open(bench.DOMINANT_SRC, "rb").read())
+    monkeypatch.setattr(bench, "DOMINANT_SRC", str(src))
+    expect = nbytes if bench.source_sha16(str(src)) == sha else None
+    assert bench.dominant_traffic("prefill_4k") == expect
+    src.write_bytes(open(bench.DOMINANT_SRC, "rb").read() + b"\n// changed\n")
+    assert bench.dominant_traffic("prefill_4k") is None
+    assert bench.dominant_traffic("varlen_64") is None
