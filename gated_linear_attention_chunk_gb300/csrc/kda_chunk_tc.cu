@@ -215,11 +215,11 @@ __device__ __forceinline__ bool group_wait(uint64_t *bar, uint32_t parity, const
     return *reinterpret_cast<volatile int *>(grp_fail) > w;
 }
 
-// Wait taken by lane 0 of a warp, result broadcast to the warp.
-__device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, const Ctl &ctl, int lane) {
-    int ok = 1;
-    if (lane == 0) ok = wait_bar(bar, parity, ctl) ? 1 : 0;
-    return __shfl_sync(0xffffffffu, ok, 0) != 0;
+// Wait taken by every lane of a warp, which then agrees on the outcome: all lanes go on or all
+// stop.  (Letting lane 0 wait alone while the rest of the warp waits at a shuffle was measured
+// markedly slower to resume than this converged wait.)
+__device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, const Ctl &ctl) {
+    return __all_sync(0xffffffffu, wait_bar(bar, parity, ctl)) != 0;
 }
 
 // kPrep: the extended instance -- it applies the input preprocessing of p.prep and
@@ -347,7 +347,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_tc_kernel(const __grid_
                         b_hi = 1.f / (1.f + __expf(-b_hi));
                     }
                 }
-                if (c >= 2 && !warp_wait(&bar_free[s], ((c >> 1) - 1) & 1, ctl, lane)) break;
+                if (c >= 2 && !warp_wait(&bar_free[s], ((c >> 1) - 1) & 1, ctl)) break;
                 uint8_t *st = sm + s * kStage;
                 if (lane == 0) {
                     mbar_arrive_expect_tx(&bar_full[s], v_zero ? kStage - 16384 : kStage);
@@ -390,13 +390,15 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_tc_kernel(const __grid_
                 }
         } else if (warp == 1) {
             // ------------------------------------------------------------------ chain MMA issuer
-            if (lane == 0) {
+            // The whole warp runs this loop and issues through one elected lane (warp-uniform
+            // operands: about half the issue time of a branch taken by lane 0 alone).
+            {
                 const uint32_t idU = idesc_bf16(128, 64, false, true, true);    // U -= S^T W  (W MN-major)
                 const uint32_t idO = idesc_bf16(128, 64, false, false);         // O  = S^T Qbar^T, += U^T P^T
                 const uint32_t idS = idesc_bf16(128, 128, false, true);         // S += U^T Ktil (Ktil MN-major)
                 for (int c = 0; c < nfull; ++c) {
                     const int s = c & 1;
-                    if (!wait_bar(&bar_ready, c & 1, ctl)) break;
+                    if (!warp_wait(&bar_ready, c & 1, ctl)) break;
                     tc_fence_after();
                     const uint32_t st = sm_base + s * kStage;
                     // descriptors built once per chunk; k-steps add constant start offsets
@@ -406,26 +408,26 @@ __global__ void __launch_bounds__(kThreads, 1) kda_chunk_tc_kernel(const __grid_
                     const uint64_t dG = sdesc_sw128(st + OFF_G, 8192, 1024);          // Ktil, MN-major
 #pragma unroll
                     for (int ks = 0; ks < 8; ++ks)
-                        mma_bf16_ts(tmem + TM_U, tmem + TM_SB + 8 * ks, dW + (((ks >> 2) * 16384 + (ks & 3) * 2048) >> 4),
+                        mma_bf16_ts_warp(tmem + TM_U, tmem + TM_SB + 8 * ks, dW + (((ks >> 2) * 16384 + (ks & 3) * 2048) >> 4),
                                     idU, 1u);
-                    mma_commit(&bar_c1);  // U is on the critical path: release its epilogue first
+                    mma_commit_warp(&bar_c1);  // U is on the critical path: release its epilogue first
 #pragma unroll
                     for (int ks = 0; ks < 8; ++ks)
-                        mma_bf16_ts(tmem + TM_O, tmem + TM_SB + 8 * ks, dQ + (((ks >> 2) * 16384 + (ks & 3) * 32) >> 4),
+                        mma_bf16_ts_warp(tmem + TM_O, tmem + TM_SB + 8 * ks, dQ + (((ks >> 2) * 16384 + (ks & 3) * 32) >> 4),
                                     idO, ks > 0 ? 1u : 0u);
-                    if (!wait_bar(&bar_uready, c & 1, ctl)) break;
+                    if (!warp_wait(&bar_uready, c & 1, ctl)) break;
                     tc_fence_after();
 #pragma unroll
                     for (int ks = 0; ks < 4; ++ks)
-                        mma_bf16_ts(tmem + TM_S, tmem + TM_UB + 8 * ks, dG + ((ks * 2048) >> 4), idS, 1u);
+                        mma_bf16_ts_warp(tmem + TM_S, tmem + TM_UB + 8 * ks, dG + ((ks * 2048) >> 4), idS, 1u);
 #pragma unroll
                     for (int ks = 0; ks < 4; ++ks)
-                        mma_bf16_ts(tmem + TM_O, tmem + TM_UB + 8 * ks, dP + ((ks * 32) >> 4), idO, 1u);
-                    mma_commit(&bar_c3);
-                    mma_commit(&bar_free[s]);
+                        mma_bf16_ts_warp(tmem + TM_O, tmem + TM_UB + 8 * ks, dP + ((ks * 32) >> 4), idO, 1u);
+                    mma_commit_warp(&bar_c3);
+                    mma_commit_warp(&bar_free[s]);
                 }
-                // drain: every MMA this thread issued completes before the TMEM is freed
-                mma_commit(&bar_drain[0]);
+                // drain: every MMA the elected lane issued completes before the TMEM is freed
+                mma_commit_warp(&bar_drain[0]);
                 const uint64_t deadline = globaltimer_ns() + kWaitNs;
                 while (!mbar_try_wait(&bar_drain[0], 0) && globaltimer_ns() < deadline) {
                 }
