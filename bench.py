@@ -818,7 +818,7 @@ def run_gpu(args, world, rank, local):
     workloads_sub = None
     if args.workload == "prefill_4k" and not (args.prep or args.no_sub_workloads):
         workloads_sub = {name: measure_workload(kda, name, dev, hbm_peak, tf_peak)
-                         for name in ("long_128k", "varlen_64", "prefill_4k_d64")}
+                         for name in ("long_128k", "varlen_64", "prefill_4k_d64", "prefill_4k_fp32")}
         workloads_sub["spec_rollout"] = measure_spec_rollout(kda, dev, hbm_peak)
     state_kernels = measure_state_kernels(kda, dev, hbm_peak) if not args.no_state_kernels else None
     backward = measure_backward(kda, case, dev, hbm_peak) if not (args.no_backward or args.prep) else None

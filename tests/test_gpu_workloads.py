@@ -105,6 +105,14 @@ def test_prefill_4k_full_size_sampled(kda):
     _check_chains(case, o, fs, [(0, 0), (0, 31), (1, 7), (1, 16), (2, 19), (2, 2), (3, 0), (3, 31)], "prefill_4k")
 
 
+def test_prefill_4k_fp32_full_size_sampled(kda):
+    """The 4 x 4096 batch with fp32 inputs (token-sequential kernel), four chains checked."""
+    case = workloads.named_case("prefill_4k_fp32")
+    assert not kda.kda_chunk_fwd_uses_tensor_cores(case.dk, case.dv, case.q.dtype)
+    o, fs = _run(kda, case)
+    _check_chains(case, o, fs, [(0, 0), (1, 13), (2, 22), (3, 31)], "prefill_4k_fp32")
+
+
 def test_varlen_64_full_size_sampled(kda):
     case = workloads.named_case("varlen_64")
     o, fs = _run(kda, case)

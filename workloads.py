@@ -149,6 +149,9 @@ NAMED_WORKLOADS = {
     "prefill_4k_d64": dict(desc="B=4 T=4096 H=32 dk=dv=64 bf16, N(0,0.02) initial state (config 1 with"
                                 " 64-wide heads)",
                            lengths=[4096] * 4, H=32, dk=64, dv=64, dtype="bf16", init=True, g_mu=3.0, seed=6),
+    "prefill_4k_fp32": dict(desc="B=4 T=4096 H=32 dk=dv=128 fp32, N(0,0.02) initial state (config 1 with fp32"
+                                 " inputs: the token-sequential kernel)",
+                            lengths=[4096] * 4, H=32, dk=128, dv=128, dtype="f32", init=True, g_mu=3.0, seed=7),
     "varlen_64": dict(desc="64 sequences, log-normal lengths (median 4096, sigma 0.5, clipped to"
                            " [1024, 20480]), H=32 dk=dv=128 bf16, random initial states",
                       lengths="lognormal", H=32, dk=128, dv=128, dtype="bf16", init=True, g_mu=3.0, seed=2),
