@@ -103,8 +103,12 @@ __device__ __forceinline__ float4 f4_shfl_xor(float4 a, int m) {
 
 // PREP: the extended instance -- it applies the input preprocessing of p.prep and
 // writes the chunk-start checkpoints of p.ckpt (the other one carries none of that code).
+// Six CTAs per SM, except the instances that preprocess and write o (decode with the fused
+// convolution or flags, the preprocessed prefill tail): they carry more live values and ran
+// faster with five CTAs' worth of registers each (decode with the convolution: 5274 against
+// 4924 GB/s), while the replay instances ran slower with fewer CTAs.
 template <int DK, int DV, typename Tin, bool WRITE_O, bool PREP>
-__global__ void __launch_bounds__(kSeqThreads, 6) kda_seq_kernel(SeqParams p) {
+__global__ void __launch_bounds__(kSeqThreads, (PREP && WRITE_O) ? 5 : 6) kda_seq_kernel(SeqParams p) {
     constexpr int CB = kColBlock;         // columns of this CTA
     constexpr int NCB = DV / CB;          // column blocks per state
     constexpr int LPR = CB / 4;           // lanes per state row (8)
