@@ -176,6 +176,12 @@ __global__ void __launch_bounds__(kConvThreads, 2) conv_out_kernel(ConvParams p)
 #pragma unroll
         for (int b = 0; b < kBatch; ++b)
             if (tb + b < t_end) r[b].load(X + ((tb + b) * H + h) * d + cx);
+        // the next batch's rows into L2 while this one is computed (no registers held)
+#pragma unroll
+        for (int b = 0; b < kBatch; ++b) {
+            const int64_t tn = tb + kBatch + b;
+            if (tn < t_end) asm volatile("prefetch.global.L2 [%0];" ::"l"(X + (tn * H + h) * d + cx));
+        }
 #pragma unroll
         for (int b = 0; b < kBatch; ++b) {
             const int64_t t = tb + b;
