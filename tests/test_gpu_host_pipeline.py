@@ -94,3 +94,28 @@ def test_host_prefill_graph_replay_matches_eager(kda):
                                    case.init_state, threads=0)
     assert_close(graph.host_o, o_ref, "graph replay o")
     assert_close(graph.host_final_state, fs_ref, "graph replay final_state")
+
+
+@pytest.mark.parametrize("dtype,dk,dv", [(torch.float32, 128, 128), (torch.bfloat16, 64, 64), (torch.bfloat16, 64, 128)])
+def test_host_prefill_parts_other_dtypes_and_head_dims(kda, dtype, dk, dv):
+    """Parts of a sequence continue bit for bit on the token-sequential path (fp32 inputs) and on
+    the 64-wide tensor-core instances, as within one call."""
+    from gated_linear_attention_chunk_gb300.host_pipeline import HostPrefill
+    case = workloads.make_case([1100, 40, 700], H=2, dk=dk, dv=dv, dtype=dtype, seed=34 + dk + dv)
+    pipe = HostPrefill(case.q, case.k, case.v, case.g, case.beta, case.cu_seqlens, case.init_state,
+                       scale=case.scale, groups=6, device="cuda")
+    assert any(b == a + 1 and (t0, t1) != (int(case.cu_seqlens[a]), int(case.cu_seqlens[b]))
+               for a, b, t0, t1 in pipe.groups)
+    pipe.run()
+    torch.cuda.synchronize()
+    assert pipe.status() == kda.KDA_OK
+    d = to_dev(case)
+    o, fs = kda.kda_chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], cu_seqlens=d["cu_seqlens"],
+                              init_state=d["init_state"], scale=case.scale)
+    torch.cuda.synchronize()
+    assert torch.equal(pipe.host_o, o.cpu())
+    assert torch.equal(pipe.host_final_state, fs.cpu())
+    o_ref, fs_ref = oracle.forward(case.q, case.k, case.v, case.g, case.beta, case.cu_seqlens, case.init_state,
+                                   threads=0)
+    assert_close(pipe.host_o, o_ref, f"parts {dtype} {dk}x{dv} o")
+    assert_close(pipe.host_final_state, fs_ref, f"parts {dtype} {dk}x{dv} final_state")
