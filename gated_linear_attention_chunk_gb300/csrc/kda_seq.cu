@@ -23,9 +23,12 @@
 // SM many small CTAs, whose state loads overlap the other CTAs' token steps.
 // Reductions over dk run in a fixed order (rows in order inside a thread, then
 // the four row groups of a warp as (0+1)+(2+3), then warps 0..3 in order), and
-// every floating-point step uses an explicit round-to-nearest intrinsic, so every
-// caller of this routine -- decode, replay and the prefill tail -- produces the
-// same bits for the same state and tokens.
+// every floating-point step of the recurrence uses an explicit round-to-nearest
+// intrinsic.  The optional preprocessing's sigmoid and SiLU use the fast exp and
+// divide intrinsics (deterministic, a few ulp; they sit on the token path, and the
+// accurate forms cost replay with the fused convolution 16% of its bandwidth).
+// Every caller of this routine -- decode, replay and the prefill tail -- runs the
+// same code, so it produces the same bits for the same state and tokens.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -211,7 +214,7 @@ __global__ void __launch_bounds__(kSeqThreads, (PREP && WRITE_O) ? 5 : 6) kda_se
     // inverse norms are applied where k and q are read.
     // Short convolution (extended instance, decode / replay with conv_w): each thread keeps
     // its channel's last kConvW - 1 raw inputs and the kConvW weights in registers; the sum
-    // runs oldest first with round-to-nearest multiply-adds, then SiLU.
+    // runs oldest first with round-to-nearest multiply-adds, then SiLU (fast intrinsics).
     constexpr int Ct = 2 * DK + DV;
     float hq[kConvW - 1], hk[kConvW - 1], hv[kConvW - 1], wq[kConvW], wk[kConvW], wv[kConvW];
     if constexpr (PREP) {
@@ -240,7 +243,7 @@ __global__ void __launch_bounds__(kSeqThreads, (PREP && WRITE_O) ? 5 : 6) kda_se
 #pragma unroll
         for (int i = 0; i < kConvW - 2; ++i) hist[i] = hist[i + 1];
         hist[kConvW - 2] = x;
-        return __fdiv_rn(pre, __fadd_rn(1.f, expf(-pre)));
+        return __fdividef(pre, 1.f + __expf(-pre));
     };
     auto stage = [&](int buf, float rg, float rk, float rq, float rv, float rb) {
         if constexpr (PREP) {
@@ -253,14 +256,13 @@ __global__ void __launch_bounds__(kSeqThreads, (PREP && WRITE_O) ? 5 : 6) kda_se
             }
         }
         if (tid < DK) {
-            tok_a[buf][tid] = (PREP && (p.prep & PREP_SIGMOID_GATE)) ? __fdiv_rn(1.f, __fadd_rn(1.f, expf(-rg)))
-                                                                       : expf(rg);
+            tok_a[buf][tid] = (PREP && (p.prep & PREP_SIGMOID_GATE)) ? __fdividef(1.f, 1.f + __expf(-rg)) : expf(rg);
             tok_k[buf][tid] = rk;
             if (WRITE_O) tok_q[buf][tid] = __fmul_rn(rq, p.scale);
         }
         if (tid < CB) tok_v[buf][tid] = rv;
         if (tid == kSeqThreads - 1)
-            tok_b[buf] = (PREP && (p.prep & PREP_SIGMOID_BETA)) ? __fdiv_rn(1.f, __fadd_rn(1.f, expf(-rb))) : rb;
+            tok_b[buf] = (PREP && (p.prep & PREP_SIGMOID_BETA)) ? __fdividef(1.f, 1.f + __expf(-rb)) : rb;
         if constexpr (PREP) {
             if (p.prep & (PREP_L2NORM_K | PREP_L2NORM_Q)) {
                 float sk = __fmul_rn(rk, rk), sq = __fmul_rn(rq, rq);  // 0 beyond dk
