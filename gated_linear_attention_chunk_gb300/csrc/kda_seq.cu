@@ -24,9 +24,10 @@
 // Reductions over dk run in a fixed order (rows in order inside a thread, then
 // the four row groups of a warp as (0+1)+(2+3), then warps 0..3 in order), and
 // every floating-point step of the recurrence uses an explicit round-to-nearest
-// intrinsic.  The optional preprocessing's sigmoid and SiLU use the fast exp and
-// divide intrinsics (deterministic, a few ulp; they sit on the token path, and the
-// accurate forms cost replay with the fused convolution 16% of its bandwidth).
+// intrinsic.  The optional preprocessing's sigmoid, SiLU and inverse row norm use the
+// fast exp, divide and reciprocal-square-root intrinsics (deterministic, a few ulp; they
+// sit on the token path, and the IEEE-rounded forms cost replay with the fused
+// convolution 18% of its bandwidth).
 // Every caller of this routine -- decode, replay and the prefill tail -- runs the
 // same code, so it produces the same bits for the same state and tokens.
 #include <cuda_bf16.h>
@@ -284,7 +285,7 @@ __global__ void __launch_bounds__(kSeqThreads, (PREP && WRITE_O) ? 5 : 6) kda_se
         float t = part[0];
 #pragma unroll
         for (int w = 1; w < kSeqWarps; ++w) t = __fadd_rn(t, part[w]);
-        return __frsqrt_rn(__fadd_rn(t, p.prep_eps));
+        return rsqrtf(__fadd_rn(t, p.prep_eps));
     };
 
     // Warm L2 with the next three tokens' rows (fire and forget): in a multi-token call
