@@ -158,7 +158,8 @@ kda_status kda_chunk_fwd(const void *q, const void *k, const void *v, const void
  *   KDA_PREP_L2NORM_Q     q_t <- q_t / sqrt(sum_i q_{t,i}^2 + l2_eps)   per (token, head)
  *   KDA_PREP_L2NORM_K     k_t <- k_t / sqrt(sum_i k_{t,i}^2 + l2_eps)
  *   KDA_PREP_SIGMOID_GATE g holds raw gates x: the log-gate is logsigmoid(x), so the
- *                         decay is alpha = sigmoid(x) (never exactly 0 for finite x)
+ *                         decay is alpha = sigmoid(x) (0 only where fp32 underflows,
+ *                         below about x = -88)
  *   KDA_PREP_SIGMOID_BETA beta <- sigmoid(beta)
  * scale still multiplies q after the normalisation.  Unknown flags or a
  * negative / non-finite l2_eps return KDA_ERR_INVALID_ARGUMENT.  With prep = 0
